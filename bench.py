@@ -1,0 +1,413 @@
+#!/usr/bin/env python3
+"""Benchmark of the packed/chunked prefill path with block selection on GB300.
+
+One step = one pass of the whole path over one batch: prefill attention ->
+block importance -> Top-p selection + index build -> gather of the kept
+tokens' hidden states, every call through the C ABI of libunip.
+
+Default workload: one 32768-token prompt, H_q 32, H_kv 8, D 128 (Llama-3.1-8B
+attention shape), heavy keys in 10 spans, block 64, p 0.95, hidden d 4096.
+
+Prints one JSON line.  ``value`` = useful attention TFLOP/s over the whole
+step (4*D*H_q*sum_s[n*P + n(n+1)/2] per step / step time), inputs resident
+in HBM, L2 flushed before every step.  ``e2e`` = the same metric with the
+inputs copied from pinned host memory and the results read back inside the
+timed region.  ``--impl reference`` times the fp64 CPU oracle instead.
+
+Multi-GPU (torchrun): every rank runs its own batch (segments are independent
+units, no collective on the data path); the timed region is bracketed by a
+barrier and the max over ranks is reported (weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "prefill attn useful TFLOP/s (% BF16 peak); select+gather GB/s (% HBM)"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 256 << 20
+
+
+def useful_attention_flops(wl) -> float:
+    """4*D*H_q*sum_s [n_s*P_s + n_s(n_s+1)/2]: unmasked (query, key) pairs only."""
+    n = wl.seq_lens.astype(np.float64)
+    P = wl.prefix_lens.astype(np.float64)
+    pairs = float(np.sum(n * P + n * (n + 1) / 2))
+    return 4.0 * wl.head_dim * wl.num_heads_q * pairs
+
+
+def rows_flops(wl, rows) -> float:
+    cu = wl.cu_seqlens
+    P = wl.prefix_lens
+    tot = 0.0
+    for t in rows:
+        s = int(np.searchsorted(cu, t, side="right") - 1)
+        tot += float(P[s] + (t - cu[s]) + 1)
+    return 4.0 * wl.head_dim * wl.num_heads_q * tot
+
+
+def select_gather_bytes(wl, n_blocks: int, n_kept: int, d_model: int) -> float:
+    """Algorithmic bytes of Top-p + index build + gather."""
+    S = wl.num_segs
+    return float(4 * n_blocks          # scores read
+                 + n_blocks            # keep mask written
+                 + 4 * n_kept          # gather_idx written
+                 + 4 * n_kept          # positions_kept written
+                 + 4 * n_kept          # positions read for kept tokens
+                 + 2 * d_model * n_kept  # hidden rows read
+                 + 2 * d_model * n_kept  # hidden rows written
+                 + 4 * (S + 1) * 3)    # cu_seqlens, blk_cu read, cu_seqlens_kept written
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            pk = json.load(f)
+        return pk, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def recorded_traffic(kernel_src: str, summary: str):
+    """DRAM bytes per launch from a committed ncu summary, if the kernel source is unchanged since."""
+    path = os.path.join(ROOT, "profiles", summary)
+    if not os.path.exists(path):
+        return None
+    sha = hashlib.sha1(open(kernel_src, "rb").read()).hexdigest()
+    rec = {}
+    for line in open(path):
+        if ":" in line and line.strip().startswith("- "):
+            k, v = line.strip()[2:].split(":", 1)
+            rec[k.strip()] = v.strip().strip("`")
+    if rec.get("kernel_source_sha1") != sha:
+        return None
+    try:
+        return float(rec["dram_bytes_per_launch_full_workload"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        for l in getattr(self, "lines", []):
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for name, val in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"),
+                                 f[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def build_workload(name: str, rank: int):
+    from sparsified_long_context_gb300 import workloads as W
+    if name == "long_single":
+        return W.long_single(seed=4 + 1000 * rank)
+    if name == "mixed_step":
+        return W.mixed_step(seed=5 + 1000 * rank)
+    if name == "prepacked":
+        return W.prepacked(seed=3 + 1000 * rank)
+    if name == "tiny_packed":
+        return W.tiny_packed(seed=1 + 1000 * rank)
+    raise SystemExit(f"unknown workload {name}")
+
+
+def describe(wl) -> str:
+    lens = wl.seq_lens
+    return (f"{wl.name}: {wl.num_segs} segment(s), {wl.num_tokens} tokens (max {int(lens.max())}), "
+            f"H_q {wl.num_heads_q}, H_kv {wl.num_heads_kv}, D {wl.head_dim}, block {wl.block_size}, "
+            f"p {wl.top_p}, d_model {wl.hidden.shape[1] if wl.hidden is not None else 0}")
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def run_reference(args):
+    """The fp64 CPU oracle, timed on the host cores on a bounded row sample per step."""
+    import oracle
+    world, rank, _ = dist_setup(args)
+    if rank != 0:
+        return 0
+    wl = build_workload(args.workload, 0)
+    cores = oracle.default_threads()
+    rng = np.random.default_rng(123)
+    # calibrate a per-step row sample of a few seconds
+    probe = np.sort(rng.choice(wl.num_tokens, 4, replace=False)).astype(np.int32)
+    t0 = time.perf_counter()
+    oracle.attention(wl.q, wl.k, wl.v, wl.cu_seqlens, wl.positions, wl.num_heads_q, wl.num_heads_kv, wl.head_dim,
+                     rows=probe, nthreads=cores)
+    dt = time.perf_counter() - t0
+    per_row = max(dt / 4, 1e-4)
+    target = max(1.0, min(args.ref_step_seconds, 120.0 / max(1, args.steps + args.warmup)))
+    n_rows = int(min(max(4, target / per_row), wl.num_tokens))
+    flops_total, secs = 0.0, 0.0
+    for it in range(args.warmup + args.steps):
+        rows = np.sort(rng.choice(wl.num_tokens, n_rows, replace=False)).astype(np.int32)
+        t0 = time.perf_counter()
+        oracle.attention(wl.q, wl.k, wl.v, wl.cu_seqlens, wl.positions, wl.num_heads_q, wl.num_heads_kv,
+                         wl.head_dim, rows=rows, nthreads=cores)
+        dt = time.perf_counter() - t0
+        if it >= args.warmup:
+            flops_total += rows_flops(wl, rows)
+            secs += dt
+    value = flops_total / secs / 1e12
+    sample = (f"fp64 oracle attention on {n_rows} uniformly sampled query rows (all {wl.num_heads_q} heads) "
+              f"of the workload per step; useful FLOPs of those rows / wall time")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": describe(wl), "l2": "n/a (CPU)"},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def cpu_baseline(wl, seconds: float):
+    """Oracle as it stands on the host cores, bounded sample of the same workload."""
+    import oracle
+    cores = oracle.default_threads()
+    rng = np.random.default_rng(7)
+    probe = np.sort(rng.choice(wl.num_tokens, 4, replace=False)).astype(np.int32)
+    t0 = time.perf_counter()
+    oracle.attention(wl.q, wl.k, wl.v, wl.cu_seqlens, wl.positions, wl.num_heads_q, wl.num_heads_kv, wl.head_dim,
+                     rows=probe, nthreads=cores)
+    per_row = max((time.perf_counter() - t0) / 4, 1e-4)
+    n_rows = int(min(max(4, seconds / per_row), wl.num_tokens))
+    rows = np.sort(rng.choice(wl.num_tokens, n_rows, replace=False)).astype(np.int32)
+    t0 = time.perf_counter()
+    oracle.attention(wl.q, wl.k, wl.v, wl.cu_seqlens, wl.positions, wl.num_heads_q, wl.num_heads_kv, wl.head_dim,
+                     rows=rows, nthreads=cores)
+    dt = time.perf_counter() - t0
+    return {"value": rows_flops(wl, rows) / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"fp64 oracle attention on {n_rows} uniformly sampled query rows x {wl.num_heads_q} heads "
+                      f"of the same workload ({dt:.1f} s); useful FLOPs of those rows / wall time"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="unip", choices=["unip", "reference"])
+    ap.add_argument("--workload", default="long_single",
+                    choices=["long_single", "mixed_step", "prepacked", "tiny_packed"])
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ref-step-seconds", type=float, default=6.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    from sparsified_long_context_gb300 import binding as B
+    from sparsified_long_context_gb300.pipeline import (DeviceInputs, StepBuffers, kernels_per_step, run_attention,
+                                                        run_importance, run_topp_gather)
+    world, rank, local = dist_setup(args)
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    B.load()
+    B.unip_get_device_status(clear=True)
+    wl = build_workload(args.workload, rank)
+    di = DeviceInputs.from_workload(wl, f"cuda:{local}")
+    bufs = StepBuffers(di)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=f"cuda:{local}")
+    stream = torch.cuda.current_stream()
+    flops_step = useful_attention_flops(wl)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        run_attention(di, bufs, stream)
+        if ev is not None:
+            ev[1].record(stream)
+        run_importance(di, bufs, stream)
+        if ev is not None:
+            ev[2].record(stream)
+        run_topp_gather(di, bufs, stream=stream)
+        if ev is not None:
+            ev[3].record(stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    st = B.unip_get_device_status(clear=True)
+    if st:
+        raise SystemExit(f"device status after warm-up: {B.describe_status(st)}")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        wall0 = time.perf_counter()
+        for i in range(args.steps):
+            flush.zero_()
+            step(evs[i])
+        torch.cuda.synchronize()
+        wall1 = time.perf_counter()
+    if dist is not None:
+        dist.barrier()
+    st = B.unip_get_device_status(clear=True)
+    if st:
+        raise SystemExit(f"device status after timed steps: {B.describe_status(st)}")
+    t_attn = [e[0].elapsed_time(e[1]) for e in evs]
+    t_imp = [e[1].elapsed_time(e[2]) for e in evs]
+    t_sel = [e[2].elapsed_time(e[3]) for e in evs]
+    t_step = [e[0].elapsed_time(e[3]) for e in evs]
+    step_ms = float(np.sum(t_step))
+    if dist is not None:
+        t = torch.tensor([step_ms], dtype=torch.float64, device=f"cuda:{local}")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        step_ms = float(t.item())
+    ms_per_step = step_ms / args.steps
+    value = flops_step * world / (ms_per_step * 1e-3) / 1e12
+
+    n_kept = int(bufs.n_kept.item())
+    n_blocks = int(bufs.blk_cu[-1].item())
+    d_model = di.hidden.shape[1]
+    sg_bytes = select_gather_bytes(wl, n_blocks, n_kept, d_model)
+    attn_ms = statistics.mean(t_attn)
+    sel_ms = statistics.mean(t_sel)
+    imp_ms = statistics.mean(t_imp)
+    attn_tflops = flops_step / (attn_ms * 1e-3) / 1e12
+    sg_gbs = sg_bytes / (sel_ms * 1e-3) / 1e9
+    peaks, peak_src = load_peaks()
+    bf16_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+
+    # ---- end to end through the C ABI with host buffers (pinned), copies inside the timed region
+    host = {}
+    for name in ("q", "k", "v", "hidden", "cu_seqlens", "positions", "seg_mask"):
+        t = getattr(di, name)
+        host[name] = t.cpu().pin_memory()
+    out_host = torch.empty(bufs.out.shape, dtype=bufs.out.dtype).pin_memory()
+    hid_host = torch.empty(bufs.hidden_out.shape, dtype=bufs.hidden_out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h_list = []
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    e2e_t0 = time.perf_counter()
+    for _ in range(args.e2e_steps):
+        for name, t in host.items():
+            getattr(di, name).copy_(t, non_blocking=True)
+        step()
+        out_host.copy_(bufs.out, non_blocking=True)
+        m = int(bufs.n_kept.item())  # result size lives on the device
+        hid_host[:m].copy_(bufs.hidden_out[:m], non_blocking=True)
+        torch.cuda.synchronize()
+        d2h_list.append(out_host.numel() * 2 + 4 + m * d_model * 2)
+    e2e_dt = time.perf_counter() - e2e_t0
+    if dist is not None:
+        t = torch.tensor([e2e_dt], dtype=torch.float64, device=f"cuda:{local}")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_dt = float(t.item())
+    e2e_value = flops_step * world * args.e2e_steps / e2e_dt / 1e12
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return 0
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        cpu = cpu_baseline(wl, args.cpu_seconds)
+    launches = kernels_per_step(True) * args.steps
+    traffic = recorded_traffic(os.path.join(ROOT, "sparsified_long_context_gb300", "csrc", "unip_attention.cu"),
+                               "attn_fwd_long_single.md")
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded, bf16 ~N(0,1), heavy keys x4)",
+        "config": {"workload": describe(wl), "l2": "flushed (256 MB write) before every step",
+                   "parallelism": f"replicas x{world} (independent batches, no collective)",
+                   "useful_attention_flops_per_step": flops_step},
+        "parts": {
+            "attention_ms": attn_ms, "attention_tflops": attn_tflops, "attention_frac_bf16": attn_tflops / bf16_peak,
+            "importance_ms": imp_ms,
+            "select_gather_ms": sel_ms, "select_gather_bytes": sg_bytes, "select_gather_gbs": sg_gbs,
+            "select_gather_frac_hbm": sg_gbs / hbm_peak, "n_kept": n_kept, "n_blocks": n_blocks,
+            "peaks": f"{peak_src}: bf16 {bf16_peak} TFLOP/s, HBM {hbm_peak} GB/s",
+        },
+        "roofline": {"bound": "tensor", "achieved": attn_tflops, "peak": bf16_peak, "unit": "TFLOP/s",
+                     "frac": attn_tflops / bf16_peak, "traffic": traffic,
+                     "kernel": "attn_fwd_kernel<128> (+ its one-CTA planner), CUDA events around the call",
+                     "peak_source": f"{peak_src} bf16_tflops (burst)"},
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": int(statistics.mean(d2h_list)),
+                "how": "pinned host inputs copied in, 4 C-ABI calls, out + n_kept + compacted hidden copied back"},
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
+        "wall_s_timed_region": wall1 - wall0,
+    }
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,214 @@
+/*
+ * unip.h -- C ABI of libunip: packed / chunked long-context prefill attention
+ * with block-wise dynamic sparsification, for NVIDIA GB300 (sm_103a).
+ *
+ * The path, in call order:
+ *   unip_prefill_attention  causal attention of a packed token stream whose
+ *                           segments may continue a cached prefix held in KV
+ *                           pages; writes the output and the row log-sum-exp.
+ *   unip_block_importance   per-block importance of each selected segment,
+ *                           from the last query rows and the stored row LSE.
+ *   unip_topp_select        fewest blocks per segment whose cumulative
+ *                           importance reaches p, plus the compaction indices.
+ *   unip_gather_tokens      copies the kept tokens' hidden-state rows into a
+ *                           compacted stream.
+ *
+ * Sources (page titles as given on the pages):
+ *   [CP]  "Chunked Prefill" (Ultralytics glossary).  Section "Como funciona o
+ *         pre-preenchimento segmentado": each chunk attends to the cached K/V
+ *         of all earlier chunks plus its own tokens with a causal mask over
+ *         absolute positions, giving the one-pass result; the page's example
+ *         calls scaled_dot_product_attention (softmax scale 1/sqrt(D)).
+ *         Section "Tecnicas de servico relacionadas": PagedAttention stores
+ *         the KV cache in fixed-size pages.
+ *   [PP]  "Prepacking: A Simple Method for Fast Prefilling and Increased
+ *         Throughput in Large Language Models" summary, sections "技术框架"
+ *         and "关键设计": prompts of varying length are packed into one
+ *         sequence; the attention mask and positional encoding are changed so
+ *         that each prompt only sees itself (block-diagonal causal mask,
+ *         positions restarting per prompt).
+ *   [UP]  "[논문리뷰] UniPrefill: Universal Long-Context Prefill Acceleration
+ *         via Block-wise Dynamic Sparsification" review.  Section 1 ("Top-p
+ *         Token Selection"): the fewest blocks whose cumulative importance
+ *         reaches a threshold p.  Section 3: the input is cut into blocks whose
+ *         importance is estimated at a full-attention layer, and dropped
+ *         tokens are left out of every later sub-layer.
+ *
+ * Conventions shared by every call
+ *   - Every data pointer is DEVICE memory owned by the caller; the library
+ *     never allocates, frees or keeps a pointer after the call returns.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t passed as void*,
+ *     NULL = legacy default stream) and never synchronise the host.
+ *   - Layout is token-major: q [N][H_q][D], k and v [N][H_kv][D], bf16
+ *     (passed as void*), rows contiguous.  Query head h reads kv head
+ *     h / (H_q / H_kv) (contiguous groups).
+ *   - Segment s holds tokens cu_seqlens[s] .. cu_seqlens[s+1]-1 (int32,
+ *     cu_seqlens[0] = 0, non-decreasing, cu_seqlens[S] = N).  Its positions
+ *     must be contiguous; its cached-prefix length is positions[cu_seqlens[s]].
+ *   - Return value: UNIP_OK, or a negative code for errors found on the host
+ *     before any launch (nothing is enqueued then).  Errors that need the
+ *     device's data (bad cu_seqlens, non-contiguous positions, bad page ids,
+ *     a device wait that ran out) are recorded as bits of a per-device status
+ *     word, read with unip_get_device_status; the affected call leaves its
+ *     outputs unspecified.
+ *   - A workspace buffer is not shared between calls that may overlap.
+ */
+#ifndef UNIP_H_
+#define UNIP_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define UNIP_API __attribute__((visibility("default")))
+
+/* Host-side return codes. */
+#define UNIP_OK 0
+#define UNIP_ERR_INVALID_ARGUMENT (-1) /* null pointer, negative size, bad enum */
+#define UNIP_ERR_UNSUPPORTED (-2)      /* shape the kernels do not cover */
+#define UNIP_ERR_WORKSPACE (-3)        /* workspace missing, too small or misaligned */
+#define UNIP_ERR_CUDA (-4)             /* CUDA runtime / launch failure */
+#define UNIP_ERR_ALIGNMENT (-5)        /* pointer or row stride not 16-byte aligned */
+
+/* Device status bits (unip_get_device_status). */
+#define UNIP_DEV_BAD_SEQLENS 0x1u    /* cu_seqlens not monotone / ends wrong */
+#define UNIP_DEV_BAD_POSITIONS 0x2u  /* positions not contiguous in a segment, or negative */
+#define UNIP_DEV_BAD_PAGES 0x4u      /* prefix needs pages the block table does not give */
+#define UNIP_DEV_TIMEOUT 0x8u        /* a bounded device wait ran out; kernel returned early */
+#define UNIP_DEV_BAD_SCORES 0x10u    /* an importance score is negative, NaN or above 1 */
+#define UNIP_DEV_TOO_MANY_BLOCKS 0x20u /* a segment has more blocks than Top-p supports */
+#define UNIP_DEV_BAD_INDEX 0x40u     /* gather index out of range or n_kept above capacity */
+#define UNIP_DEV_BAD_BLOCKS 0x80u    /* blk_cu does not match cu_seqlens and block_size */
+
+/* Top-p flags. */
+#define UNIP_KEEP_FIRST 0x1u /* always keep each segment's first block */
+#define UNIP_KEEP_LAST 0x2u  /* always keep each segment's last block */
+
+/* Largest number of blocks one segment may have in unip_topp_select. */
+#define UNIP_TOPP_MAX_BLOCKS 8192
+
+typedef struct unip_attn_params {
+  int32_t num_heads_q;  /* H_q >= 1 */
+  int32_t num_heads_kv; /* H_kv >= 1, divides H_q */
+  int32_t head_dim;     /* D: 64 or 128 */
+  float scale;          /* softmax scale; <= 0 selects 1/sqrt(D) */
+} unip_attn_params;
+
+/* Paged KV cache holding the cached prefixes ([CP], PagedAttention). */
+typedef struct unip_paged_kv {
+  const void *k_cache;          /* bf16 [num_pages][page_size][H_kv][D] */
+  const void *v_cache;          /* bf16 [num_pages][page_size][H_kv][D] */
+  int32_t num_pages;
+  int32_t page_size;            /* tokens per page: 16, 32, 64 or 128 */
+  const int32_t *block_table;   /* int32 [num_segs][max_pages_per_seq]; entry p of row s
+                                   is the physical page of prefix tokens [p*page, (p+1)*page) */
+  int32_t max_pages_per_seq;
+} unip_paged_kv;
+
+/* Library version string (static storage). */
+UNIP_API const char *unip_version(void);
+
+/* Text for a host return code (static storage). */
+UNIP_API const char *unip_status_string(int32_t code);
+
+/* Reads the current device's status word into *bits (synchronises that
+ * device), and clears it when clear != 0.  Returns UNIP_OK or UNIP_ERR_CUDA. */
+UNIP_API int32_t unip_get_device_status(uint32_t *bits, int32_t clear);
+
+/* ---------------------------------------------------------------------------
+ * Attention ([CP] causal mask over absolute positions with a cached prefix,
+ * [PP] block-diagonal mask and restarted positions).
+ *
+ * Token t of segment s (local index i, position P_s + i) with query head h
+ * attends to the P_s prefix keys of its segment, read through block_table row
+ * s, and to its segment's own tokens 0..i; nothing of other segments.
+ *   out[t][h][:] = sum_j softmax_j(scale * q.k_j) v_j     (bf16, RNE)
+ *   lse[h][t]    = ln sum_j exp(scale * q.k_j)            (fp32, may be NULL)
+ * paged may be NULL when every segment starts at position 0.
+ * Slots of a prefix's last page beyond the prefix must hold finite values.
+ * workspace: device memory of unip_attention_workspace_size() bytes, 256-byte
+ * aligned.  q, k, v, out, cache pointers: 16-byte aligned.
+ * ------------------------------------------------------------------------- */
+UNIP_API size_t unip_attention_workspace_size(int32_t total_tokens, int32_t num_segs,
+                                              const unip_attn_params *prm);
+
+UNIP_API int32_t unip_prefill_attention(const void *q, const void *k, const void *v,
+                                        const int32_t *cu_seqlens, int32_t num_segs,
+                                        const int32_t *positions, int32_t total_tokens,
+                                        const unip_paged_kv *paged,
+                                        const unip_attn_params *prm,
+                                        void *out, float *lse,
+                                        void *workspace, size_t workspace_bytes,
+                                        void *stream);
+
+/* ---------------------------------------------------------------------------
+ * Block importance ([UP] section 3; scoring reading fixed by this library):
+ * for each segment s with seg_mask[s] != 0 (all segments when seg_mask is
+ * NULL) and n_s > 0 tokens, block b covers local tokens [b*B, min((b+1)*B, n_s)).
+ * The last W = min(B, n_s) query rows score the segment's own keys:
+ *   M_b = sum_{h < H_q} sum_{t in window} sum_{j in block b, j <= t}
+ *         exp(scale * q_t^h . k_j - lse[h][t])
+ *   imp_b = M_b / sum_b' M_b'.
+ * lse is the row LSE written by unip_prefill_attention (prefix included).
+ * Outputs: imp (fp32, capacity imp_capacity >= unip_importance_capacity()),
+ * blk_cu (int32 [num_segs+1], block offsets; unscored segments own 0 blocks).
+ * block_size: 16, 32, 64 or 128.
+ * ------------------------------------------------------------------------- */
+UNIP_API int32_t unip_importance_capacity(int32_t total_tokens, int32_t num_segs, int32_t block_size);
+
+UNIP_API size_t unip_importance_workspace_size(int32_t total_tokens, int32_t num_segs,
+                                               int32_t block_size, const unip_attn_params *prm);
+
+UNIP_API int32_t unip_block_importance(const void *q, const void *k, const float *lse,
+                                       const int32_t *cu_seqlens, int32_t num_segs,
+                                       int32_t total_tokens, const uint8_t *seg_mask,
+                                       int32_t block_size, const unip_attn_params *prm,
+                                       float *imp, int32_t imp_capacity, int32_t *blk_cu,
+                                       void *workspace, size_t workspace_bytes, void *stream);
+
+/* ---------------------------------------------------------------------------
+ * Top-p block selection ([UP] section 1) and compaction indices ([UP]
+ * section 3).  Per segment with nb > 0 blocks, bit-exact and independent of
+ * summation order:
+ *   q_b = floor(imp_b * 2^32) (uint64), T = sum q_b, thr = p * (double)T;
+ *   F = {first block if UNIP_KEEP_FIRST, last block if UNIP_KEEP_LAST};
+ *   the other blocks ranked by imp descending, ties by lower index, are added
+ *   in rank order while (double)(sum of kept q) < thr.  T == 0 keeps all.
+ * Segments with zero blocks in blk_cu (not scored) keep every token.
+ * Outputs: keep (uint8 per block), gather_idx (int32, kept source tokens in
+ * original order, capacity total_tokens), cu_seqlens_kept (int32
+ * [num_segs+1]), positions_kept (int32, original positions, capacity
+ * total_tokens), n_kept (one int32, device).  0 <= p <= 1.
+ * ------------------------------------------------------------------------- */
+UNIP_API size_t unip_topp_workspace_size(int32_t total_tokens, int32_t num_segs, int32_t block_size);
+
+UNIP_API int32_t unip_topp_select(const float *imp, const int32_t *blk_cu,
+                                  const int32_t *cu_seqlens, const int32_t *positions,
+                                  int32_t num_segs, int32_t total_tokens, int32_t block_size,
+                                  double p, uint32_t flags,
+                                  uint8_t *keep, int32_t keep_capacity,
+                                  int32_t *gather_idx, int32_t *cu_seqlens_kept,
+                                  int32_t *positions_kept, int32_t *n_kept,
+                                  void *workspace, size_t workspace_bytes, void *stream);
+
+/* ---------------------------------------------------------------------------
+ * Row gather ([UP] section 3: the kept tokens' hidden states form the stream
+ * of the later layers):  out[i][:] = hidden[gather_idx[i]][:] for
+ * i < *n_kept (read on the device), bit for bit.  hidden holds num_rows rows
+ * of d_model bf16 values with row stride row_stride elements; out rows have
+ * stride out_row_stride elements; capacity bounds *n_kept.  Pointers and
+ * strides must be 16-byte aligned (d_model, strides multiples of 8).
+ * ------------------------------------------------------------------------- */
+UNIP_API int32_t unip_gather_tokens(const void *hidden, int32_t num_rows, int64_t row_stride,
+                                    int32_t d_model, const int32_t *gather_idx,
+                                    const int32_t *n_kept, int32_t capacity,
+                                    void *out, int64_t out_row_stride, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* UNIP_H_ */

@@ -1,0 +1,217 @@
+"""Thin ctypes binding of libunip (argument marshalling only).
+
+Each function carries the name of the C entry point it calls and forwards
+device pointers taken from torch tensors; every step of the path runs in the
+library's CUDA kernels.  There is no CPU fallback: when libunip.so cannot be
+loaded, or a tensor is not on a CUDA device, the call raises.
+
+torch serves only as the owner of device memory and streams.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+from . import native_build
+
+_lib = None
+_lock = threading.Lock()
+
+UNIP_OK = 0
+UNIP_KEEP_FIRST = 0x1
+UNIP_KEEP_LAST = 0x2
+UNIP_TOPP_MAX_BLOCKS = 8192
+
+DEV_STATUS_BITS = {
+    0x1: "bad cu_seqlens", 0x2: "bad positions", 0x4: "bad pages", 0x8: "device wait timeout",
+    0x10: "bad importance scores", 0x20: "too many blocks in a segment", 0x40: "bad gather index",
+    0x80: "blk_cu does not match cu_seqlens",
+}
+
+
+class UnipError(RuntimeError):
+    pass
+
+
+class _AttnParams(ctypes.Structure):
+    _fields_ = [("num_heads_q", ctypes.c_int32), ("num_heads_kv", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("scale", ctypes.c_float)]
+
+
+class _PagedKV(ctypes.Structure):
+    _fields_ = [("k_cache", ctypes.c_void_p), ("v_cache", ctypes.c_void_p), ("num_pages", ctypes.c_int32),
+                ("page_size", ctypes.c_int32), ("block_table", ctypes.c_void_p),
+                ("max_pages_per_seq", ctypes.c_int32)]
+
+
+def library_path() -> str:
+    return native_build.LIB_PATH
+
+
+def load(build_if_missing: bool = True):
+    """Load libunip.so (building it in-tree first when it is missing or stale)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = native_build.LIB_PATH
+        if build_if_missing and not native_build.up_to_date():
+            native_build.build()
+        if not os.path.exists(path):
+            raise UnipError(f"libunip.so not found at {path}; run native_build.build()")
+        lib = ctypes.CDLL(path)
+        P, i32, i64, u32, f64, sz = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_uint32,
+                                     ctypes.c_double, ctypes.c_size_t)
+        pp = ctypes.POINTER(_AttnParams)
+        lib.unip_version.restype = ctypes.c_char_p
+        lib.unip_status_string.restype = ctypes.c_char_p
+        lib.unip_status_string.argtypes = [i32]
+        lib.unip_get_device_status.restype = i32
+        lib.unip_get_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32]
+        lib.unip_attention_workspace_size.restype = sz
+        lib.unip_attention_workspace_size.argtypes = [i32, i32, pp]
+        lib.unip_prefill_attention.restype = i32
+        lib.unip_prefill_attention.argtypes = [P, P, P, P, i32, P, i32, ctypes.POINTER(_PagedKV), pp, P, P, P, sz, P]
+        lib.unip_importance_capacity.restype = i32
+        lib.unip_importance_capacity.argtypes = [i32, i32, i32]
+        lib.unip_importance_workspace_size.restype = sz
+        lib.unip_importance_workspace_size.argtypes = [i32, i32, i32, pp]
+        lib.unip_block_importance.restype = i32
+        lib.unip_block_importance.argtypes = [P, P, P, P, i32, i32, P, i32, pp, P, i32, P, P, sz, P]
+        lib.unip_topp_workspace_size.restype = sz
+        lib.unip_topp_workspace_size.argtypes = [i32, i32, i32]
+        lib.unip_topp_select.restype = i32
+        lib.unip_topp_select.argtypes = [P, P, P, P, i32, i32, i32, f64, u32, P, i32, P, P, P, P, P, sz, P]
+        lib.unip_gather_tokens.restype = i32
+        lib.unip_gather_tokens.argtypes = [P, i32, i64, i32, P, P, i32, P, i64, P]
+        _lib = lib
+        return lib
+
+
+def _check(rc: int, what: str):
+    if rc != UNIP_OK:
+        msg = load().unip_status_string(rc).decode()
+        raise UnipError(f"{what} failed: {msg} (code {rc})")
+
+
+def _ptr(t) -> Optional[int]:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise UnipError("libunip takes CUDA tensors only (no CPU fallback)")
+    if not t.is_contiguous():
+        raise UnipError("libunip takes contiguous tensors")
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def _params(hq, hkv, d, scale):
+    return _AttnParams(int(hq), int(hkv), int(d), float(scale or 0.0))
+
+
+def _workspace(nbytes: int, device):
+    import torch
+    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+def unip_version() -> str:
+    return load().unip_version().decode()
+
+
+def unip_get_device_status(clear: bool = True) -> int:
+    """Device status bits (synchronises the current device)."""
+    bits = ctypes.c_uint32(0)
+    _check(load().unip_get_device_status(ctypes.byref(bits), 1 if clear else 0), "unip_get_device_status")
+    return int(bits.value)
+
+
+def describe_status(bits: int) -> str:
+    return ", ".join(v for k, v in DEV_STATUS_BITS.items() if bits & k) or "ok"
+
+
+def unip_attention_workspace_size(total_tokens, num_segs, hq, hkv, d) -> int:
+    p = _params(hq, hkv, d, 0.0)
+    return int(load().unip_attention_workspace_size(int(total_tokens), int(num_segs), ctypes.byref(p)))
+
+
+def unip_prefill_attention(q, k, v, cu_seqlens, positions, out, lse=None, *, num_heads_q, num_heads_kv,
+                           head_dim, k_cache=None, v_cache=None, block_table=None, page_size=16,
+                           scale=None, workspace=None, stream=None):
+    """Packed / chunked causal attention: writes out [N,Hq,D] bf16 and lse [Hq,N] fp32."""
+    lib = load()
+    n = int(q.shape[0])
+    S = int(cu_seqlens.shape[0]) - 1
+    prm = _params(num_heads_q, num_heads_kv, head_dim, scale)
+    need = lib.unip_attention_workspace_size(n, S, ctypes.byref(prm))
+    if workspace is None:
+        workspace = _workspace(need, q.device)
+    paged_p = None
+    if k_cache is not None:
+        paged = _PagedKV(_ptr(k_cache), _ptr(v_cache), int(k_cache.shape[0]), int(page_size), _ptr(block_table),
+                         int(block_table.shape[1]))
+        paged_p = ctypes.byref(paged)
+    rc = lib.unip_prefill_attention(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), S, _ptr(positions), n, paged_p,
+                                    ctypes.byref(prm), _ptr(out), _ptr(lse), _ptr(workspace),
+                                    workspace.numel(), _stream(stream))
+    _check(rc, "unip_prefill_attention")
+    return out, lse
+
+
+def unip_importance_capacity(total_tokens, num_segs, block_size) -> int:
+    return int(load().unip_importance_capacity(int(total_tokens), int(num_segs), int(block_size)))
+
+
+def unip_block_importance(q, k, lse, cu_seqlens, imp, blk_cu, *, block_size, num_heads_q, num_heads_kv,
+                          head_dim, seg_mask=None, scale=None, workspace=None, stream=None):
+    """Per-block importance imp (fp32) and block offsets blk_cu (int32 [S+1])."""
+    lib = load()
+    n = int(q.shape[0])
+    S = int(cu_seqlens.shape[0]) - 1
+    prm = _params(num_heads_q, num_heads_kv, head_dim, scale)
+    need = lib.unip_importance_workspace_size(n, S, int(block_size), ctypes.byref(prm))
+    if workspace is None:
+        workspace = _workspace(need, q.device)
+    rc = lib.unip_block_importance(_ptr(q), _ptr(k), _ptr(lse), _ptr(cu_seqlens), S, n, _ptr(seg_mask),
+                                   int(block_size), ctypes.byref(prm), _ptr(imp), int(imp.numel()), _ptr(blk_cu),
+                                   _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(rc, "unip_block_importance")
+    return imp, blk_cu
+
+
+def unip_topp_workspace_size(total_tokens, num_segs, block_size) -> int:
+    return int(load().unip_topp_workspace_size(int(total_tokens), int(num_segs), int(block_size)))
+
+
+def unip_topp_select(imp, blk_cu, cu_seqlens, positions, keep, gather_idx, cu_seqlens_kept, positions_kept,
+                     n_kept, *, block_size, p, flags=UNIP_KEEP_FIRST | UNIP_KEEP_LAST, workspace=None,
+                     stream=None):
+    """Top-p keep mask and compaction indices; n_kept stays on the device."""
+    lib = load()
+    n = int(positions.shape[0])
+    S = int(cu_seqlens.shape[0]) - 1
+    need = lib.unip_topp_workspace_size(n, S, int(block_size))
+    if workspace is None:
+        workspace = _workspace(need, imp.device)
+    rc = lib.unip_topp_select(_ptr(imp), _ptr(blk_cu), _ptr(cu_seqlens), _ptr(positions), S, n, int(block_size),
+                              float(p), int(flags), _ptr(keep), int(keep.numel()), _ptr(gather_idx),
+                              _ptr(cu_seqlens_kept), _ptr(positions_kept), _ptr(n_kept), _ptr(workspace),
+                              workspace.numel(), _stream(stream))
+    _check(rc, "unip_topp_select")
+
+
+def unip_gather_tokens(hidden, gather_idx, n_kept, out, *, stream=None):
+    """out[i] = hidden[gather_idx[i]] for i < n_kept (device scalar)."""
+    lib = load()
+    rows, d = int(hidden.shape[0]), int(hidden.shape[1])
+    rc = lib.unip_gather_tokens(_ptr(hidden), rows, int(hidden.stride(0)), d, _ptr(gather_idx), _ptr(n_kept),
+                                int(out.shape[0]), _ptr(out), int(out.stride(0)), _stream(stream))
+    _check(rc, "unip_gather_tokens")
+    return out

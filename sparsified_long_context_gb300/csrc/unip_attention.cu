@@ -1,0 +1,609 @@
+// Packed / chunked causal prefill attention for sm_103a.
+//
+// Operation (see include/unip.h): token t of segment s, local index i, attends
+// to the segment's P_s cached prefix keys (paged) and to its own tokens
+// 0..i.  Sources: "Chunked Prefill" glossary page, section "Como funciona o
+// pre-preenchimento segmentado" (chunk = cached K/V of earlier chunks + own
+// tokens under a causal mask over absolute positions, SDPA softmax) and
+// section "Tecnicas de servico relacionadas" (fixed-size KV pages); the
+// Prepacking summary, sections "技术框架"/"关键设计" (block-diagonal mask,
+// per-prompt positions).
+//
+// Design
+//   * A device planner (one CTA) validates cu_seqlens / positions, cuts every
+//     segment into 128-row query tiles and orders the (segment, tile) pairs
+//     longest-first by their number of 128-key KV tiles.  The attention grid
+//     is launched with a host-side upper bound; surplus CTAs exit at once.
+//   * One CTA = one 128-row query tile of one query head.  A KV tile is
+//     either 128 prefix keys (read page by page through the block table) or
+//     128 of the segment's own keys; only the last prefix tile and the
+//     diagonal own tile need a mask, every fully masked tile is skipped.
+//   * Warp roles: warps 0-3 softmax + epilogue (one query row per thread,
+//     i.e. one TMEM lane each), warp 4 TMA producer, warp 5 tcgen05 issuer.
+//   * TMEM (512 columns): two S buffers (128 fp32 columns each) so QK^T of
+//     tile j+1 overlaps the softmax of tile j, and the O accumulator (D cols).
+//   * Online softmax in base 2 with a lazy rescale: the running maximum is
+//     only moved (and O rescaled in TMEM) when a row's maximum grows by more
+//     than 8 (log2 units), which bounds P by 2^8; the final O / l is exact.
+//   * P goes to shared memory as bf16 in the 128-byte-swizzled K-major layout
+//     the second MMA reads; V is read MN-major straight from its TMA tile.
+#include <cuda_bf16.h>
+
+#include "unip_internal.cuh"
+
+namespace unip {
+namespace {
+
+constexpr int kBlockM = 128;
+constexpr int kBlockN = 128;
+constexpr int kThreads = 192;
+constexpr int kHistBins = 4096;
+constexpr int kPlanThreads = 1024;
+constexpr int kWsHeaderBytes = 256;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmemO = 256;  // first TMEM column of the O accumulator
+constexpr float kRescaleThreshold = 8.0f;
+constexpr float kLn2 = 0.69314718055994530942f;
+constexpr float kLog2e = 1.44269504088896340736f;
+
+struct AttnArgs {
+  CUtensorMap tm_q, tm_k, tm_v, tm_kc, tm_vc;
+  const int32_t *cu;
+  const int32_t *pos;
+  const int32_t *block_table;
+  const int2 *pairs;
+  const int32_t *num_pairs;
+  __nv_bfloat16 *out;
+  float *lse;
+  uint32_t *status;
+  int32_t S, N, Hq, group, num_pages, page_size, max_pages;
+  float scale_log2;
+};
+
+// ---------------------------------------------------------------------------
+// Planner
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ int32_t block_exclusive_scan_1024(int32_t v, int32_t *sh, int32_t *total) {
+  const int tid = threadIdx.x;
+  sh[tid] = v;
+  __syncthreads();
+  for (int off = 1; off < kPlanThreads; off <<= 1) {
+    const int32_t add = tid >= off ? sh[tid - off] : 0;
+    __syncthreads();
+    sh[tid] += add;
+    __syncthreads();
+  }
+  const int32_t incl = sh[tid];
+  *total = sh[kPlanThreads - 1];
+  __syncthreads();
+  return incl - v;
+}
+
+__global__ void __launch_bounds__(kPlanThreads) attn_plan_kernel(const int32_t *__restrict__ cu,
+                                                                 const int32_t *__restrict__ pos, int32_t S,
+                                                                 int32_t N, int32_t has_cache, int32_t page_size,
+                                                                 int32_t max_pages, int32_t *__restrict__ header,
+                                                                 int2 *__restrict__ pairs, int32_t max_pairs,
+                                                                 uint32_t *__restrict__ status) {
+  __shared__ int32_t s_hist[kHistBins];
+  __shared__ int32_t s_scan[kPlanThreads];
+  __shared__ uint32_t s_err;
+  const int tid = threadIdx.x;
+  for (int b = tid; b < kHistBins; b += kPlanThreads) s_hist[b] = 0;
+  if (tid == 0) s_err = (cu[0] != 0 || cu[S] != N) ? UNIP_DEV_BAD_SEQLENS : 0u;
+  __syncthreads();
+
+  // Each thread owns a contiguous range of segments.
+  const int per = (S + kPlanThreads - 1) / kPlanThreads;
+  const int s0 = min(S, tid * per), s1 = min(S, s0 + per);
+  // Phase A: cu_seqlens must be non-decreasing (with cu[0] = 0, cu[S] = N every entry is then in range).
+  bool mono = true;
+  for (int s = s0; s < s1; ++s) mono &= cu[s + 1] >= cu[s];
+  if (!mono) atomicOr(&s_err, UNIP_DEV_BAD_SEQLENS);
+  __syncthreads();
+  if (s_err != 0) {
+    if (tid == 0) {
+      header[0] = 0;
+      atomicOr(status, s_err);
+    }
+    return;
+  }
+  // Phase B: prefixes, pages and positions; count query tiles.
+  int32_t my_pairs = 0;
+  uint32_t err = 0;
+  for (int s = s0; s < s1; ++s) {
+    const int32_t n = cu[s + 1] - cu[s];
+    if (n == 0) continue;
+    const int32_t P = pos[cu[s]];
+    if (P < 0) err |= UNIP_DEV_BAD_POSITIONS;
+    if (P > 0 && (!has_cache || (P + page_size - 1) / page_size > max_pages)) err |= UNIP_DEV_BAD_PAGES;
+    my_pairs += (n + kBlockM - 1) / kBlockM;
+  }
+  for (int t = tid; t < N; t += kPlanThreads) {
+    const int s = find_segment(cu, S, t);
+    if (pos[t] != pos[cu[s]] + (t - cu[s])) err |= UNIP_DEV_BAD_POSITIONS;
+  }
+  if (err) atomicOr(&s_err, err);
+  int32_t total_pairs;
+  block_exclusive_scan_1024(my_pairs, s_scan, &total_pairs);
+  if (s_err != 0 || total_pairs > max_pairs) {
+    if (tid == 0) {
+      header[0] = 0;
+      atomicOr(status, s_err ? s_err : UNIP_DEV_BAD_SEQLENS);
+    }
+    return;
+  }
+  // Histogram of pair costs (number of KV tiles).
+  for (int s = s0; s < s1; ++s) {
+    const int32_t n = cu[s + 1] - cu[s];
+    if (n <= 0) continue;
+    const int32_t pt = (pos[cu[s]] + kBlockN - 1) / kBlockN;
+    const int32_t nt = (n + kBlockM - 1) / kBlockM;
+    for (int m = 0; m < nt; ++m) atomicAdd(&s_hist[min(pt + m + 1, kHistBins - 1)], 1);
+  }
+  __syncthreads();
+  // Bin start offsets in decreasing cost order.
+  constexpr int kPer = kHistBins / kPlanThreads;
+  int32_t cnt[kPer];
+  int32_t local = 0;
+#pragma unroll
+  for (int r = 0; r < kPer; ++r) {
+    cnt[r] = s_hist[kHistBins - 1 - (tid * kPer + r)];
+    local += cnt[r];
+  }
+  int32_t dummy;
+  int32_t run = block_exclusive_scan_1024(local, s_scan, &dummy);
+#pragma unroll
+  for (int r = 0; r < kPer; ++r) {
+    s_hist[kHistBins - 1 - (tid * kPer + r)] = run;
+    run += cnt[r];
+  }
+  __syncthreads();
+  for (int s = s0; s < s1; ++s) {
+    const int32_t n = cu[s + 1] - cu[s];
+    if (n <= 0) continue;
+    const int32_t pt = (pos[cu[s]] + kBlockN - 1) / kBlockN;
+    const int32_t nt = (n + kBlockM - 1) / kBlockM;
+    for (int m = nt - 1; m >= 0; --m) {
+      const int32_t slot = atomicAdd(&s_hist[min(pt + m + 1, kHistBins - 1)], 1);
+      pairs[slot] = make_int2(s, m);
+    }
+  }
+  if (tid == 0) header[0] = total_pairs;
+}
+
+// ---------------------------------------------------------------------------
+// Attention kernel
+// ---------------------------------------------------------------------------
+template <int D>
+struct SmemLayout {
+  static constexpr uint32_t kHalfBytes = kBlockM * 128;       // 128 rows x 128 B (64 bf16)
+  static constexpr uint32_t kTileBytes = kBlockM * D * 2;     // one Q / K / V tile
+  static constexpr uint32_t kQ = 0;
+  static constexpr uint32_t kK0 = kQ + kTileBytes;
+  static constexpr uint32_t kV0 = kK0 + 2 * kTileBytes;
+  static constexpr uint32_t kP = kV0 + 2 * kTileBytes;
+  static constexpr uint32_t kBytes = kP + kBlockM * kBlockN * 2;
+  static constexpr uint32_t kDynamic = kBytes + 1024;         // slack for 1024-byte alignment
+};
+
+enum BarId {
+  kBarQFull = 0,
+  kBarKFull0 = 1,   // +stage
+  kBarVFull0 = 3,   // +stage
+  kBarKVEmpty0 = 5, // +stage
+  kBarSFull0 = 7,   // +buffer
+  kBarSEmpty0 = 9,  // +buffer
+  kBarPFull = 11,
+  kBarODone = 12,
+  kBarFinal = 13,
+  kNumBars = 14
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_constant__ AttnArgs a) {
+  using L = SmemLayout<D>;
+  constexpr int kHalves = D / 64;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t bars[kNumBars];
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int32_t pair_idx = blockIdx.x / a.Hq;
+  if (pair_idx >= *a.num_pairs) return;  // uniform over the CTA
+  const int2 pr = a.pairs[pair_idx];
+  const int32_t s = pr.x, m = pr.y;
+  const int32_t h = blockIdx.x % a.Hq;
+  const int32_t g = h / a.group;
+  const int32_t c0 = a.cu[s];
+  const int32_t n = a.cu[s + 1] - c0;
+  const int32_t P = a.pos[c0];
+  const int32_t row0 = m * kBlockM;
+  const int32_t rows_valid = min(kBlockM, n - row0);
+  const int32_t Tp = (P + kBlockN - 1) / kBlockN;  // prefix KV tiles
+  const int32_t T = Tp + m + 1;                    // + own tiles up to the diagonal
+
+  const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  const uint32_t sQ = sbase + L::kQ;
+  const uint32_t sP = sbase + L::kP;
+  auto sK = [&](int st) { return sbase + L::kK0 + st * L::kTileBytes; };
+  auto sV = [&](int st) { return sbase + L::kV0 + st * L::kTileBytes; };
+  auto bar = [&](int i) { return smem_u32(&bars[i]); };
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(kBarQFull), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(kBarKFull0 + i), 1);
+      mbar_init(bar(kBarVFull0 + i), 1);
+      mbar_init(bar(kBarKVEmpty0 + i), 1);
+      mbar_init(bar(kBarSFull0 + i), 1);
+      mbar_init(bar(kBarSEmpty0 + i), kBlockM);
+    }
+    mbar_init(bar(kBarPFull), kBlockM);
+    mbar_init(bar(kBarODone), 1);
+    mbar_init(bar(kBarFinal), 1);
+    s_abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(smem_u32(&s_tmem), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+  volatile int *abort_flag = &s_abort;
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&a.tm_q);
+      tma_prefetch_desc(&a.tm_k);
+      tma_prefetch_desc(&a.tm_v);
+      if (Tp > 0) {
+        tma_prefetch_desc(&a.tm_kc);
+        tma_prefetch_desc(&a.tm_vc);
+      }
+      mbar_arrive_expect_tx(bar(kBarQFull), L::kTileBytes);
+#pragma unroll
+      for (int hf = 0; hf < kHalves; ++hf)
+        tma_load_3d(sQ + hf * L::kHalfBytes, &a.tm_q, bar(kBarQFull), hf * 64, h, c0 + row0);
+      const int32_t pages_per_tile = kBlockN / a.page_size;
+      const uint32_t page_bytes = a.page_size * 128u;
+      int32_t issued = 0;
+      for (int32_t j = 0; j < T; ++j) {
+        const int st = j & 1;
+        if (j >= 2 && !mbar_wait(bar(kBarKVEmpty0 + st), ((j - 2) >> 1) & 1, abort_flag, a.status)) break;
+        mbar_arrive_expect_tx(bar(kBarKFull0 + st), L::kTileBytes);
+        if (j < Tp) {
+          const int32_t first_page = j * pages_per_tile;
+          for (int32_t pi = 0; pi < pages_per_tile; ++pi) {
+            const int32_t lp = first_page + pi;
+            int32_t phys = a.num_pages;  // out of range -> zero fill
+            if (lp * a.page_size < P) {
+              const int32_t e = a.block_table[(int64_t)s * a.max_pages + lp];
+              if (e >= 0 && e < a.num_pages) phys = e; else atomicOr(a.status, UNIP_DEV_BAD_PAGES);
+            }
+#pragma unroll
+            for (int hf = 0; hf < kHalves; ++hf)
+              tma_load_4d(sK(st) + hf * L::kHalfBytes + pi * page_bytes, &a.tm_kc, bar(kBarKFull0 + st), hf * 64,
+                          g, 0, phys);
+          }
+          mbar_arrive_expect_tx(bar(kBarVFull0 + st), L::kTileBytes);
+          for (int32_t pi = 0; pi < pages_per_tile; ++pi) {
+            const int32_t lp = first_page + pi;
+            int32_t phys = a.num_pages;
+            if (lp * a.page_size < P) {
+              const int32_t e = a.block_table[(int64_t)s * a.max_pages + lp];
+              if (e >= 0 && e < a.num_pages) phys = e;
+            }
+#pragma unroll
+            for (int hf = 0; hf < kHalves; ++hf)
+              tma_load_4d(sV(st) + hf * L::kHalfBytes + pi * page_bytes, &a.tm_vc, bar(kBarVFull0 + st), hf * 64,
+                          g, 0, phys);
+          }
+        } else {
+          const int32_t krow = c0 + (j - Tp) * kBlockN;
+#pragma unroll
+          for (int hf = 0; hf < kHalves; ++hf)
+            tma_load_3d(sK(st) + hf * L::kHalfBytes, &a.tm_k, bar(kBarKFull0 + st), hf * 64, g, krow);
+          mbar_arrive_expect_tx(bar(kBarVFull0 + st), L::kTileBytes);
+#pragma unroll
+          for (int hf = 0; hf < kHalves; ++hf)
+            tma_load_3d(sV(st) + hf * L::kHalfBytes, &a.tm_v, bar(kBarVFull0 + st), hf * 64, g, krow);
+        }
+        issued = j + 1;
+      }
+      if (*abort_flag) {
+        // Let copies already in flight land before the CTA's shared memory is released.
+        for (int32_t j = max(0, issued - 2); j < issued; ++j) {
+          const uint32_t par = (j >> 1) & 1;
+          const uint64_t t0 = globaltimer_ns();
+          while (!mbar_try_wait(bar(kBarKFull0 + (j & 1)), par) && globaltimer_ns() - t0 < kWaitLimitNs) {}
+          while (!mbar_try_wait(bar(kBarVFull0 + (j & 1)), par) && globaltimer_ns() - t0 < kWaitLimitNs) {}
+        }
+      }
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_qk = idesc_bf16_f32(kBlockM, kBlockN, false, false);
+      constexpr uint32_t idesc_pv = idesc_bf16_f32(kBlockM, D, false, true);
+      auto issue_pv = [&](int32_t i) -> bool {
+        if (!mbar_wait(bar(kBarPFull), i & 1, abort_flag, a.status)) return false;
+        if (!mbar_wait(bar(kBarVFull0 + (i & 1)), (i >> 1) & 1, abort_flag, a.status)) return false;
+        tc_fence_after();
+        const uint32_t vb = sV(i & 1);
+#pragma unroll
+        for (int kk = 0; kk < kBlockN / 16; ++kk) {
+          const uint64_t ad = sdesc_sw128(sP + (kk >> 2) * L::kHalfBytes + (kk & 3) * 32, 16, 1024);
+          const uint64_t bd = sdesc_sw128(vb + kk * 2048, L::kHalfBytes, 1024);
+          umma_bf16_ss(tmem + kTmemO, ad, bd, idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
+        }
+        umma_commit(bar(kBarODone));
+        umma_commit(bar(kBarKVEmpty0 + (i & 1)));
+        return true;
+      };
+      bool ok = mbar_wait(bar(kBarQFull), 0, abort_flag, a.status);
+      for (int32_t j = 0; ok && j < T; ++j) {
+        const int st = j & 1;
+        ok = mbar_wait(bar(kBarKFull0 + st), (j >> 1) & 1, abort_flag, a.status);
+        if (ok && j >= 2) ok = mbar_wait(bar(kBarSEmpty0 + st), ((j - 2) >> 1) & 1, abort_flag, a.status);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t kb = sK(st);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * L::kHalfBytes + (kk & 3) * 32;
+          umma_bf16_ss(tmem + st * kBlockN, sdesc_sw128(sQ + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024),
+                       idesc_qk, kk > 0 ? 1u : 0u);
+        }
+        umma_commit(bar(kBarSFull0 + st));
+        if (j >= 1) ok = issue_pv(j - 1);
+      }
+      if (ok) issue_pv(T - 1);
+      // Every tcgen05 op of this CTA has landed before TMEM is released.
+      umma_commit(bar(kBarFinal));
+      const uint64_t t0 = globaltimer_ns();
+      while (!mbar_try_wait(bar(kBarFinal), 0) && globaltimer_ns() - t0 < kWaitLimitNs) {}
+    }
+  } else {
+    // ------------------------------------------------------------ softmax + epilogue
+    const int row = threadIdx.x;  // TMEM lane == query row of the tile
+    const uint32_t tl = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const float c = a.scale_log2;
+    float m_used = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int32_t j = 0; j < T; ++j) {
+      const int b = j & 1;
+      if (!mbar_wait(bar(kBarSFull0 + b), (j >> 1) & 1, abort_flag, a.status)) { ok = false; break; }
+      tc_fence_after();
+      float sv[kBlockN];
+#pragma unroll
+      for (int q4 = 0; q4 < kBlockN / 32; ++q4) tmem_ld32(tl + b * kBlockN + q4 * 32, sv + q4 * 32);
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(bar(kBarSEmpty0 + b));
+      if (j < Tp) {
+        if (j == Tp - 1) {
+          const int lim = P - j * kBlockN;  // keys at or after the prefix end are not cached tokens
+#pragma unroll
+          for (int k = 0; k < kBlockN; ++k)
+            if (k >= lim) sv[k] = -INFINITY;
+        }
+      } else if (j == T - 1) {
+#pragma unroll
+        for (int k = 0; k < kBlockN; ++k)
+          if (k > row) sv[k] = -INFINITY;  // causal diagonal tile
+      }
+      float mx = sv[0];
+#pragma unroll
+      for (int k = 1; k < kBlockN; ++k) mx = fmaxf(mx, sv[k]);
+      const float m_new = fmaxf(m_used, mx * c);
+      const bool need = m_new > m_used + kRescaleThreshold;
+      float alpha = 1.f;
+      if (need) {
+        alpha = ex2_approx(m_used - m_new);
+        m_used = m_new;
+      }
+      const float mb = (m_used == -INFINITY) ? 0.f : m_used;
+      uint32_t pk[kBlockN / 2];
+      float rs = 0.f;
+#pragma unroll
+      for (int k = 0; k < kBlockN / 2; ++k) {
+        const float p0 = ex2_approx(fmaf(sv[2 * k], c, -mb));
+        const float p1 = ex2_approx(fmaf(sv[2 * k + 1], c, -mb));
+        rs += p0 + p1;
+        pk[k] = pack_bf16x2(p0, p1);
+      }
+      l = l * alpha + rs;
+      if (j >= 1) {
+        // PV of the previous tile must be done: it reads the P buffer and accumulates into O.
+        if (!mbar_wait(bar(kBarODone), (j - 1) & 1, abort_flag, a.status)) { ok = false; break; }
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, need)) {
+#pragma unroll
+          for (int q4 = 0; q4 < D / 32; ++q4) {
+            float o[32];
+            tmem_ld32(tl + kTmemO + q4 * 32, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int x = 0; x < 32; ++x) o[x] *= alpha;
+            tmem_st32(tl + kTmemO + q4 * 32, o);
+          }
+          tmem_wait_st();
+        }
+      }
+      // P row -> shared memory, 128-byte swizzle (16-byte chunk c of row r sits at chunk c ^ (r & 7)).
+#pragma unroll
+      for (int hk = 0; hk < 2; ++hk) {
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {
+          const uint32_t addr = sP + hk * L::kHalfBytes + row * 128 + ((ch ^ (row & 7)) << 4);
+          const int base = hk * 32 + ch * 4;
+          st_shared_v4(addr, pk[base], pk[base + 1], pk[base + 2], pk[base + 3]);
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(bar(kBarPFull));
+    }
+    if (ok && mbar_wait(bar(kBarODone), (T - 1) & 1, abort_flag, a.status)) {
+      tc_fence_after();
+      const float inv_l = 1.f / l;
+      const int32_t t = c0 + row0 + row;
+      const bool store = row < rows_valid;
+      __nv_bfloat16 *orow = a.out + ((int64_t)t * a.Hq + h) * D;
+#pragma unroll
+      for (int q4 = 0; q4 < D / 32; ++q4) {
+        float o[32];
+        tmem_ld32(tl + kTmemO + q4 * 32, o);
+        tmem_wait_ld();
+        if (store) {
+          uint4 *dst = reinterpret_cast<uint4 *>(orow + q4 * 32);
+#pragma unroll
+          for (int v4 = 0; v4 < 4; ++v4) {
+            uint4 w;
+            w.x = pack_bf16x2(o[v4 * 8 + 0] * inv_l, o[v4 * 8 + 1] * inv_l);
+            w.y = pack_bf16x2(o[v4 * 8 + 2] * inv_l, o[v4 * 8 + 3] * inv_l);
+            w.z = pack_bf16x2(o[v4 * 8 + 4] * inv_l, o[v4 * 8 + 5] * inv_l);
+            w.w = pack_bf16x2(o[v4 * 8 + 6] * inv_l, o[v4 * 8 + 7] * inv_l);
+            dst[v4] = w;
+          }
+        }
+      }
+      if (store && a.lse) a.lse[(int64_t)h * a.N + t] = (m_used + log2f(l)) * kLn2;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <int D>
+cudaError_t launch_attention(const AttnArgs &args, int grid, cudaStream_t stream) {
+  using L = SmemLayout<D>;
+  static bool configured[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !configured[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)L::kDynamic);
+    if (e != cudaSuccess) return e;
+    configured[dev] = true;
+  }
+  attn_fwd_kernel<D><<<grid, kThreads, L::kDynamic, stream>>>(args);
+  return cudaGetLastError();
+}
+
+int32_t max_pairs_for(int32_t total_tokens, int32_t num_segs) {
+  return (total_tokens + kBlockM - 1) / kBlockM + num_segs;
+}
+
+}  // namespace
+}  // namespace unip
+
+using namespace unip;
+
+extern "C" {
+
+UNIP_API size_t unip_attention_workspace_size(int32_t total_tokens, int32_t num_segs, const unip_attn_params *prm) {
+  (void)prm;
+  if (total_tokens < 0 || num_segs < 0) return 0;
+  return kWsHeaderBytes + align_up(sizeof(int2) * (size_t)max_pairs_for(total_tokens, num_segs), 256);
+}
+
+UNIP_API int32_t unip_prefill_attention(const void *q, const void *k, const void *v, const int32_t *cu_seqlens,
+                                        int32_t num_segs, const int32_t *positions, int32_t total_tokens,
+                                        const unip_paged_kv *paged, const unip_attn_params *prm, void *out,
+                                        float *lse, void *workspace, size_t workspace_bytes, void *stream) {
+  if (!prm || !cu_seqlens || num_segs < 0 || total_tokens < 0) return UNIP_ERR_INVALID_ARGUMENT;
+  const int32_t Hq = prm->num_heads_q, Hkv = prm->num_heads_kv, D = prm->head_dim;
+  if (Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0) return UNIP_ERR_INVALID_ARGUMENT;
+  if (D != 64 && D != 128) return UNIP_ERR_UNSUPPORTED;
+  if (total_tokens == 0) return UNIP_OK;
+  if (num_segs == 0 || !q || !k || !v || !positions || !out) return UNIP_ERR_INVALID_ARGUMENT;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return UNIP_ERR_ALIGNMENT;
+  const size_t need_ws = unip_attention_workspace_size(total_tokens, num_segs, prm);
+  if (!workspace || workspace_bytes < need_ws || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return UNIP_ERR_WORKSPACE;
+  const bool has_cache = paged && paged->k_cache && paged->v_cache && paged->block_table && paged->num_pages > 0;
+  if (has_cache) {
+    const int32_t ps = paged->page_size;
+    if (ps != 16 && ps != 32 && ps != 64 && ps != 128) return UNIP_ERR_UNSUPPORTED;
+    if (paged->max_pages_per_seq <= 0) return UNIP_ERR_INVALID_ARGUMENT;
+    if (!aligned16(paged->k_cache) || !aligned16(paged->v_cache)) return UNIP_ERR_ALIGNMENT;
+  }
+  uint32_t *status = device_status_ptr();
+  if (!status) return UNIP_ERR_CUDA;
+
+  AttnArgs args;
+  memset(&args, 0, sizeof(args));
+  const cuuint32_t box3[3] = {64, 1, kBlockM};
+  {
+    const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)Hq, (cuuint64_t)total_tokens};
+    const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)Hq * D * 2};
+    if (encode_tiled(&args.tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(q), dims, strides, box3,
+                     CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+      return UNIP_ERR_CUDA;
+  }
+  {
+    const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)Hkv, (cuuint64_t)total_tokens};
+    const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)Hkv * D * 2};
+    if (encode_tiled(&args.tm_k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(k), dims, strides, box3,
+                     CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS ||
+        encode_tiled(&args.tm_v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(v), dims, strides, box3,
+                     CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+      return UNIP_ERR_CUDA;
+  }
+  if (has_cache) {
+    const int32_t ps = paged->page_size;
+    const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)Hkv, (cuuint64_t)ps, (cuuint64_t)paged->num_pages};
+    const cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)Hkv * D * 2, (cuuint64_t)ps * Hkv * D * 2};
+    const cuuint32_t box4[4] = {64, 1, (cuuint32_t)ps, 1};
+    if (encode_tiled(&args.tm_kc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(paged->k_cache), dims,
+                     strides, box4, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS ||
+        encode_tiled(&args.tm_vc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(paged->v_cache), dims,
+                     strides, box4, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+      return UNIP_ERR_CUDA;
+  }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int32_t *header = static_cast<int32_t *>(workspace);
+  int2 *pairs = reinterpret_cast<int2 *>(static_cast<uint8_t *>(workspace) + kWsHeaderBytes);
+  const int32_t max_pairs = max_pairs_for(total_tokens, num_segs);
+  attn_plan_kernel<<<1, kPlanThreads, 0, st>>>(cu_seqlens, positions, num_segs, total_tokens, has_cache ? 1 : 0,
+                                               has_cache ? paged->page_size : 16,
+                                               has_cache ? paged->max_pages_per_seq : 0, header, pairs, max_pairs,
+                                               status);
+  if (cudaGetLastError() != cudaSuccess) return UNIP_ERR_CUDA;
+
+  args.cu = cu_seqlens;
+  args.pos = positions;
+  args.block_table = has_cache ? paged->block_table : nullptr;
+  args.pairs = pairs;
+  args.num_pairs = header;
+  args.out = static_cast<__nv_bfloat16 *>(out);
+  args.lse = lse;
+  args.status = status;
+  args.S = num_segs;
+  args.N = total_tokens;
+  args.Hq = Hq;
+  args.group = Hq / Hkv;
+  args.num_pages = has_cache ? paged->num_pages : 0;
+  args.page_size = has_cache ? paged->page_size : 16;
+  args.max_pages = has_cache ? paged->max_pages_per_seq : 0;
+  const float scale = prm->scale > 0.f ? prm->scale : 1.0f / sqrtf((float)D);
+  args.scale_log2 = scale * kLog2e;
+  const int64_t grid = (int64_t)max_pairs * Hq;
+  if (grid > 0x7FFFFFFF) return UNIP_ERR_UNSUPPORTED;
+  const cudaError_t e = D == 128 ? launch_attention<128>(args, (int)grid, st) : launch_attention<64>(args, (int)grid, st);
+  return e == cudaSuccess ? UNIP_OK : UNIP_ERR_CUDA;
+}
+
+}  // extern "C"

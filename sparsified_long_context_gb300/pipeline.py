@@ -1,0 +1,131 @@
+"""Device buffers and the four-call step of the path (marshalling only).
+
+A step is: prefill attention -> block importance -> Top-p selection ->
+gather of the kept tokens' hidden states.  Every call goes through the C ABI;
+this module only owns the torch tensors (device memory) and the workspaces.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+from typing import Optional
+
+import numpy as np
+
+from . import binding as B
+from .workloads import Workload
+
+
+def _to_dev(a: Optional[np.ndarray], device, bf16: bool = False):
+    import torch
+    if a is None:
+        return None
+    t = torch.from_numpy(np.ascontiguousarray(a))
+    if bf16:
+        t = t.view(torch.bfloat16)
+    return t.to(device)
+
+
+@dataclass
+class DeviceInputs:
+    """A workload's inputs resident in device memory."""
+    wl: Workload
+    q: object
+    k: object
+    v: object
+    cu_seqlens: object
+    positions: object
+    k_cache: object = None
+    v_cache: object = None
+    block_table: object = None
+    seg_mask: object = None
+    hidden: object = None
+
+    @classmethod
+    def from_workload(cls, wl: Workload, device="cuda", with_hidden: bool = True):
+        kc = vc = bt = None
+        if wl.cache is not None:
+            kc, vc = wl.cache.to_torch(device)
+            bt = _to_dev(wl.block_table, device)
+        return cls(wl, _to_dev(wl.q, device, True), _to_dev(wl.k, device, True), _to_dev(wl.v, device, True),
+                   _to_dev(wl.cu_seqlens, device), _to_dev(wl.positions, device), kc, vc, bt,
+                   _to_dev(wl.seg_mask, device),
+                   _to_dev(wl.hidden, device, True) if (with_hidden and wl.hidden is not None) else None)
+
+
+class StepBuffers:
+    """Outputs and workspaces of one step, allocated once (torch owns the memory)."""
+
+    def __init__(self, di: DeviceInputs, block_size: Optional[int] = None):
+        import torch
+        wl = di.wl
+        dev = di.q.device
+        n, S = wl.num_tokens, wl.num_segs
+        hq, hkv, d = wl.num_heads_q, wl.num_heads_kv, wl.head_dim
+        self.block_size = block_size or wl.block_size or 64
+        bs = self.block_size
+        self.out = torch.empty((n, hq, d), dtype=torch.bfloat16, device=dev)
+        self.lse = torch.empty((hq, n), dtype=torch.float32, device=dev)
+        cap = B.unip_importance_capacity(n, S, bs)
+        self.imp = torch.empty(cap, dtype=torch.float32, device=dev)
+        self.blk_cu = torch.empty(S + 1, dtype=torch.int32, device=dev)
+        self.keep = torch.empty(cap, dtype=torch.uint8, device=dev)
+        self.gather_idx = torch.empty(max(n, 1), dtype=torch.int32, device=dev)
+        self.positions_kept = torch.empty(max(n, 1), dtype=torch.int32, device=dev)
+        self.cu_seqlens_kept = torch.empty(S + 1, dtype=torch.int32, device=dev)
+        self.n_kept = torch.empty(1, dtype=torch.int32, device=dev)
+        self.hidden_out = None
+        if di.hidden is not None:
+            self.hidden_out = torch.empty_like(di.hidden)
+        self.ws_attn = torch.empty(max(B.unip_attention_workspace_size(n, S, hq, hkv, d), 256), dtype=torch.uint8,
+                                   device=dev)
+        lib = B.load()
+        prm = B._params(hq, hkv, d, 0.0)
+        import ctypes
+        self.ws_imp = torch.empty(max(int(lib.unip_importance_workspace_size(n, S, bs, ctypes.byref(prm))), 256),
+                                  dtype=torch.uint8, device=dev)
+        self.ws_topp = torch.empty(max(B.unip_topp_workspace_size(n, S, bs), 256), dtype=torch.uint8, device=dev)
+
+
+def run_attention(di: DeviceInputs, bufs: StepBuffers, stream=None):
+    wl = di.wl
+    B.unip_prefill_attention(di.q, di.k, di.v, di.cu_seqlens, di.positions, bufs.out, bufs.lse,
+                             num_heads_q=wl.num_heads_q, num_heads_kv=wl.num_heads_kv, head_dim=wl.head_dim,
+                             k_cache=di.k_cache, v_cache=di.v_cache, block_table=di.block_table,
+                             page_size=wl.cache.page_size if wl.cache is not None else 16,
+                             workspace=bufs.ws_attn, stream=stream)
+
+
+def run_importance(di: DeviceInputs, bufs: StepBuffers, stream=None):
+    wl = di.wl
+    B.unip_block_importance(di.q, di.k, bufs.lse, di.cu_seqlens, bufs.imp, bufs.blk_cu,
+                            block_size=bufs.block_size, num_heads_q=wl.num_heads_q,
+                            num_heads_kv=wl.num_heads_kv, head_dim=wl.head_dim, seg_mask=di.seg_mask,
+                            workspace=bufs.ws_imp, stream=stream)
+
+
+def run_topp_gather(di: DeviceInputs, bufs: StepBuffers, p: Optional[float] = None, stream=None,
+                    flags: int = B.UNIP_KEEP_FIRST | B.UNIP_KEEP_LAST):
+    wl = di.wl
+    B.unip_topp_select(bufs.imp, bufs.blk_cu, di.cu_seqlens, di.positions, bufs.keep, bufs.gather_idx,
+                       bufs.cu_seqlens_kept, bufs.positions_kept, bufs.n_kept, block_size=bufs.block_size,
+                       p=wl.top_p if p is None else p, flags=flags, workspace=bufs.ws_topp, stream=stream)
+    if di.hidden is not None:
+        B.unip_gather_tokens(di.hidden, bufs.gather_idx, bufs.n_kept, bufs.hidden_out, stream=stream)
+
+
+def run_select(di: DeviceInputs, bufs: StepBuffers, p: Optional[float] = None, stream=None,
+               flags: int = B.UNIP_KEEP_FIRST | B.UNIP_KEEP_LAST):
+    run_importance(di, bufs, stream)
+    run_topp_gather(di, bufs, p, stream, flags)
+
+
+def run_step(di: DeviceInputs, bufs: StepBuffers, stream=None):
+    """One pass of the whole path over one batch."""
+    run_attention(di, bufs, stream)
+    run_select(di, bufs, stream=stream)
+
+
+def kernels_per_step(has_hidden: bool = True) -> int:
+    """libunip kernels one run_step launches (the Top-p call also enqueues one 4-byte memset)."""
+    # attention: plan + attention; importance: plan + score + norm; Top-p: select + index; gather: 1
+    return 2 + 3 + 2 + (1 if has_hidden else 0)

@@ -1,0 +1,51 @@
+"""The C-ABI library builds for sm_103a, loads without a GPU and exports every
+entry point declared in include/unip.h (no compute calls here)."""
+import ctypes
+import os
+import re
+
+from sparsified_long_context_gb300 import binding, native_build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "unip.h")
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return re.findall(r"UNIP_API\s+[\w\s\*]+?\b(unip_\w+)\s*\(", text)
+
+
+def test_header_declares_the_four_calls():
+    names = set(declared_symbols())
+    for n in ("unip_prefill_attention", "unip_block_importance", "unip_topp_select", "unip_gather_tokens"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol():
+    path = native_build.build()
+    lib = ctypes.CDLL(path)
+    missing = [n for n in declared_symbols() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_host_side_helpers_without_gpu():
+    lib = binding.load()
+    assert binding.unip_version().startswith("unip")
+    assert lib.unip_status_string(-2).decode() == "unsupported shape"
+    assert binding.unip_importance_capacity(32768, 1, 64) >= 512
+    assert binding.unip_attention_workspace_size(32768, 1, 32, 8, 128) >= 256 + 8 * 257
+    assert binding.unip_topp_workspace_size(8192, 260, 64) > 0
+
+
+def test_host_rejects_bad_arguments_before_launch():
+    lib = binding.load()
+    prm = binding._params(32, 8, 96, 0.0)   # head_dim 96 is not covered
+    rc = lib.unip_prefill_attention(None, None, None, ctypes.c_void_p(16), 1, None, 10, None, ctypes.byref(prm),
+                                    None, None, None, 0, None)
+    assert rc == -2
+    prm = binding._params(32, 7, 128, 0.0)  # H_q not a multiple of H_kv
+    rc = lib.unip_prefill_attention(None, None, None, ctypes.c_void_p(16), 1, None, 10, None, ctypes.byref(prm),
+                                    None, None, None, 0, None)
+    assert rc == -1
+    rc = lib.unip_topp_select(None, None, None, None, 1, 10, 16, 1.5, 3, None, 0, None, None, None, None, None, 0,
+                              None)
+    assert rc == -1

@@ -1,0 +1,106 @@
+"""GPU parity of unip_prefill_attention (through the C ABI) against the fp64 oracle."""
+import numpy as np
+import pytest
+
+import oracle
+from sparsified_long_context_gb300 import workloads as W
+
+from gpu_harness import assert_close, bf16_tensor_to_f64, oracle_attention_rows, sample_rows, LSE_ABS
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+def _run(wl: W.Workload):
+    from sparsified_long_context_gb300 import binding as B
+    from sparsified_long_context_gb300.pipeline import DeviceInputs, StepBuffers, run_attention
+    B.unip_get_device_status(clear=True)
+    di = DeviceInputs.from_workload(wl, "cuda", with_hidden=False)
+    bufs = StepBuffers(di, block_size=wl.block_size or 64)
+    run_attention(di, bufs)
+    torch.cuda.synchronize()
+    st = B.unip_get_device_status(clear=True)
+    assert st == 0, B.describe_status(st)
+    return bf16_tensor_to_f64(bufs.out), bufs.lse.cpu().numpy().astype(np.float64)
+
+
+def _check(wl, rows=None):
+    out, lse = _run(wl)
+    ref_o, ref_l = oracle_attention_rows(wl, rows)
+    sel = slice(None) if rows is None else rows
+    e = assert_close(out[sel], ref_o, what=f"{wl.name} out")
+    assert_close(lse.T[sel], ref_l, max_abs=LSE_ABS, mean_abs=LSE_ABS, what=f"{wl.name} lse")
+    return e
+
+
+def test_tiny_packed_full():
+    _check(W.tiny_packed())
+
+
+@pytest.mark.parametrize("lengths,hq,hkv,d", [
+    ([1], 2, 1, 64), ([1, 1, 1], 4, 2, 128), ([127, 128, 129], 4, 4, 64), ([0, 300, 0, 5], 8, 2, 128),
+    ([256, 1, 383], 2, 2, 128), ([1000], 8, 1, 64)])
+def test_packed_edge_shapes(lengths, hq, hkv, d):
+    _check(W.packed(lengths, hq, hkv, d, seed=sum(lengths) + hq + d))
+
+
+def _chunk_with_prefix(P, n, hq, hkv, d, page, seed):
+    """One segment continuing a P-token prefix held in shuffled pages."""
+    rng = np.random.default_rng(seed)
+    tot = P + n
+    k_all = W.f32_to_bf16_bits(rng.standard_normal((tot, hkv, d), dtype=np.float32))
+    v_all = W.f32_to_bf16_bits(rng.standard_normal((tot, hkv, d), dtype=np.float32))
+    q = W.f32_to_bf16_bits(rng.standard_normal((n, hq, d), dtype=np.float32))
+    n_pages = max(1, -(-P // page))
+    perm = rng.permutation(n_pages + 2)[:n_pages].astype(np.int32)
+    kp = np.zeros((n_pages + 2, page, hkv, d), np.uint16)
+    vp = np.zeros_like(kp)
+    for p in range(n_pages):
+        a, b = p * page, min(P, (p + 1) * page)
+        kp[perm[p], : b - a], vp[perm[p], : b - a] = k_all[a:b], v_all[a:b]
+    cache = W.PagedCache(n_pages + 2, page, hkv, d, "array", kp, vp)
+    return W.Workload(f"prefix{P}_n{n}_p{page}", hq, hkv, d, np.array([0, n], np.int32),
+                      np.arange(P, P + n, dtype=np.int32), q, k_all[P:], v_all[P:], cache=cache,
+                      block_table=perm[None, :])
+
+
+@pytest.mark.parametrize("P,n,page,d", [(16, 10, 16, 64), (45, 70, 16, 128), (128, 128, 16, 128),
+                                        (300, 1, 32, 128), (1000, 257, 64, 64), (4096, 130, 128, 128),
+                                        (513, 512, 16, 128)])
+def test_prefix_from_pages(P, n, page, d):
+    _check(_chunk_with_prefix(P, n, 4, 2, d, page, seed=P + n))
+
+
+def test_chunked_equals_one_shot():
+    one, chunks = W.chunked()
+    outs = []
+    for wl in chunks:
+        o, _ = _run(wl)
+        outs.append(o)
+    chunked = np.concatenate(outs, 0)
+    full, _ = _run(one)
+    # GPU chunked vs GPU one-shot on every element, then both against the oracle on sampled rows
+    assert_close(chunked, full, what="chunked vs one-shot (GPU)")
+    rows = sample_rows(one, 160)
+    ref, _ = oracle.attention(one.q, one.k, one.v, one.cu_seqlens, one.positions, 32, 8, 128, rows=rows)
+    assert_close(chunked[rows], ref, what="chunked vs oracle")
+    assert_close(full[rows], ref, what="one-shot vs oracle")
+
+
+def test_prepacked_sampled():
+    wl = W.prepacked()
+    _check(wl, sample_rows(wl, 400))
+
+
+def test_long_single_sampled():
+    wl = W.long_single(d_model=0)
+    _check(wl, sample_rows(wl, 48))
+
+
+def test_mixed_step_sampled():
+    wl = W.mixed_step(d_model=0)
+    rows = sample_rows(wl, 96)
+    # keep the decode rows in the sample modest: each reads up to 32k cached keys
+    dec = rows[rows < 256][:8]
+    rows = np.concatenate([dec, rows[rows >= 256]]).astype(np.int32)
+    _check(wl, rows)

@@ -1,0 +1,173 @@
+"""GPU parity of block importance, Top-p selection, index build and gather.
+
+Importance is compared with the oracle within the attention tolerance;
+selection, indices and gathered rows are compared bit for bit with the oracle
+fed the GPU's own fp32 scores.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from sparsified_long_context_gb300 import workloads as W
+
+from gpu_harness import assert_close
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+def _step(wl):
+    from sparsified_long_context_gb300 import binding as B
+    from sparsified_long_context_gb300.pipeline import DeviceInputs, StepBuffers, run_step
+    B.unip_get_device_status(clear=True)
+    di = DeviceInputs.from_workload(wl, "cuda")
+    bufs = StepBuffers(di)
+    run_step(di, bufs)
+    torch.cuda.synchronize()
+    st = B.unip_get_device_status(clear=True)
+    assert st == 0, B.describe_status(st)
+    return di, bufs
+
+
+def _check_selection(wl, bufs):
+    blk_cu = bufs.blk_cu.cpu().numpy()
+    nblk = int(blk_cu[-1])
+    imp = bufs.imp[:nblk].cpu().numpy()
+    keep = bufs.keep[:nblk].cpu().numpy()
+    ref_keep = oracle.topp_select(imp, blk_cu, wl.top_p)
+    assert np.array_equal(keep, ref_keep)
+    gi, ck, pk, m = oracle.index_build(ref_keep, blk_cu, wl.cu_seqlens, wl.positions, wl.block_size)
+    n_kept = int(bufs.n_kept.cpu().item())
+    assert n_kept == m
+    assert np.array_equal(bufs.cu_seqlens_kept.cpu().numpy(), ck)
+    assert np.array_equal(bufs.gather_idx[:m].cpu().numpy(), gi)
+    assert np.array_equal(bufs.positions_kept[:m].cpu().numpy(), pk)
+    if wl.hidden is not None:
+        ref_h = oracle.gather(wl.hidden, gi)
+        got = bufs.hidden_out[:m].view(torch.int16).cpu().numpy().view(np.uint16)
+        assert np.array_equal(got, ref_h)
+    return imp, blk_cu, m
+
+
+def test_tiny_full_chain():
+    wl = W.tiny_packed()
+    di, bufs = _step(wl)
+    _, lse = oracle.attention(wl.q, wl.k, wl.v, wl.cu_seqlens, wl.positions, 4, 2, 64)
+    ref_imp, ref_bc = oracle.block_importance(wl.q, wl.k, lse, wl.cu_seqlens, 4, 2, 64, wl.block_size,
+                                              seg_mask=wl.seg_mask)
+    imp, blk_cu, m = _check_selection(wl, bufs)
+    assert np.array_equal(blk_cu, ref_bc)
+    assert_close(imp.astype(np.float64), ref_imp, what="importance")
+    assert 0 < m <= wl.num_tokens
+
+
+def _importance_vs_oracle_with_gpu_lse(wl, bufs):
+    """Oracle importance fed the GPU's row LSE (rows outside the windows are never read)."""
+    lse_gpu = bufs.lse.cpu().numpy().astype(np.float64).T.copy()
+    ref_imp, ref_bc = oracle.block_importance(wl.q, wl.k, lse_gpu, wl.cu_seqlens, wl.num_heads_q,
+                                              wl.num_heads_kv, wl.head_dim, wl.block_size, seg_mask=wl.seg_mask)
+    blk_cu = bufs.blk_cu.cpu().numpy()
+    assert np.array_equal(blk_cu, ref_bc)
+    imp = bufs.imp[: int(blk_cu[-1])].cpu().numpy().astype(np.float64)
+    assert_close(imp, ref_imp, what="importance")
+    for s in range(wl.num_segs):
+        a, b = blk_cu[s], blk_cu[s + 1]
+        if b > a:
+            assert abs(imp[a:b].sum() - 1.0) < 1e-4
+
+
+def test_long_single_chain():
+    wl = W.long_single()
+    di, bufs = _step(wl)
+    _importance_vs_oracle_with_gpu_lse(wl, bufs)
+    _, _, m = _check_selection(wl, bufs)
+    assert 0 < m < wl.num_tokens
+
+
+def test_mixed_step_chain():
+    wl = W.mixed_step()
+    di, bufs = _step(wl)
+    _importance_vs_oracle_with_gpu_lse(wl, bufs)
+    _, _, m = _check_selection(wl, bufs)
+    assert m >= 256  # decode tokens are never dropped
+
+
+def _topp_direct(imp_np, blk_cu_np, cu_np, B_, p, flags):
+    from sparsified_long_context_gb300 import binding as Bd
+    dev = "cuda"
+    n = int(cu_np[-1])
+    S = len(cu_np) - 1
+    pos = np.concatenate([np.arange(cu_np[s + 1] - cu_np[s]) for s in range(S)]).astype(np.int32)
+    cap = Bd.unip_importance_capacity(n, S, B_)
+    imp_t = torch.zeros(cap, dtype=torch.float32, device=dev)
+    imp_t[: len(imp_np)] = torch.from_numpy(imp_np)
+    keep = torch.full((cap,), 7, dtype=torch.uint8, device=dev)
+    gi = torch.full((n,), -1, dtype=torch.int32, device=dev)
+    pk = torch.full((n,), -1, dtype=torch.int32, device=dev)
+    ck = torch.empty(S + 1, dtype=torch.int32, device=dev)
+    nk = torch.empty(1, dtype=torch.int32, device=dev)
+    Bd.unip_topp_select(imp_t, torch.from_numpy(blk_cu_np).to(dev), torch.from_numpy(cu_np).to(dev),
+                        torch.from_numpy(pos).to(dev), keep, gi, ck, pk, nk, block_size=B_, p=p, flags=flags)
+    torch.cuda.synchronize()
+    m = int(nk.item())
+    return keep[: len(imp_np)].cpu().numpy(), gi[:m].cpu().numpy(), ck.cpu().numpy(), pk[:m].cpu().numpy(), pos
+
+
+@pytest.mark.parametrize("flags", [0, 1, 2, 3])
+def test_topp_edge_cases_bit_exact(flags):
+    rng = np.random.default_rng(50 + flags)
+    B_ = 16
+    lengths = [1, 16, 17, 300, 0, 5000, 64, 33]
+    scored = [1, 1, 1, 1, 1, 1, 0, 1]
+    nbs = [(-(-L // B_) if (sc and L > 0) else 0) for L, sc in zip(lengths, scored)]
+    cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+    bc = np.concatenate([[0], np.cumsum(nbs)]).astype(np.int32)
+    parts = []
+    for s, nb in enumerate(nbs):
+        if nb == 0:
+            continue
+        kind = s % 3
+        if kind == 0:
+            x = rng.random(nb) ** 4
+        elif kind == 1:
+            x = np.round(rng.random(nb) * 3) + 1.0    # many exact ties
+        else:
+            x = np.zeros(nb)
+            x[rng.integers(0, nb)] = 1.0
+        x = (x / x.sum()).astype(np.float32)
+        parts.append(x)
+    imp = np.concatenate(parts).astype(np.float32)
+    for p in (0.0, 0.5, 0.9, 0.95, 1.0):
+        keep, gi, ck, pk, pos = _topp_direct(imp, bc, cu, B_, p, flags)
+        ref = oracle.topp_select(imp, bc, p, flags)
+        assert np.array_equal(keep, ref), (p, flags)
+        rgi, rck, rpk, rm = oracle.index_build(ref, bc, cu, pos, B_)
+        assert np.array_equal(gi, rgi) and np.array_equal(ck, rck) and np.array_equal(pk, rpk)
+
+
+def test_topp_zero_mass_keeps_all():
+    imp = np.zeros(4, np.float32)
+    keep, gi, ck, pk, pos = _topp_direct(imp, np.array([0, 4], np.int32), np.array([0, 50], np.int32), 16, 0.5, 3)
+    assert keep.tolist() == [1, 1, 1, 1] and len(gi) == 50
+
+
+@pytest.mark.parametrize("n_rows,d,extra", [(37, 8, 0), (1000, 256, 0), (3000, 4096, 0), (64, 512, 64)])
+def test_gather_bit_exact_and_strides(n_rows, d, extra):
+    from sparsified_long_context_gb300 import binding as Bd
+    rng = np.random.default_rng(n_rows + d)
+    hid = W.f32_to_bf16_bits(rng.standard_normal((n_rows, d + extra), dtype=np.float32))
+    idx = np.sort(rng.choice(n_rows, n_rows // 2 + 1, replace=False)).astype(np.int32)
+    h_t = torch.from_numpy(hid).view(torch.bfloat16).cuda()[:, :d]
+    cap = n_rows
+    out = torch.zeros((cap, d + extra), dtype=torch.bfloat16, device="cuda")[:, :d]
+    gi = torch.zeros(cap, dtype=torch.int32, device="cuda")
+    gi[: len(idx)] = torch.from_numpy(idx).cuda()
+    nk = torch.tensor([len(idx)], dtype=torch.int32, device="cuda")
+    lib = Bd.load()
+    rc = lib.unip_gather_tokens(h_t.data_ptr(), n_rows, h_t.stride(0), d, gi.data_ptr(), nk.data_ptr(), cap,
+                                out.data_ptr(), out.stride(0), torch.cuda.current_stream().cuda_stream)
+    assert rc == 0
+    torch.cuda.synchronize()
+    got = out[: len(idx)].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+    assert np.array_equal(got, oracle.gather(np.ascontiguousarray(hid[:, :d]), idx))
+    assert Bd.unip_get_device_status() == 0
