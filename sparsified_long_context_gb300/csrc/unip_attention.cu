@@ -36,7 +36,6 @@ namespace {
 
 constexpr int kBlockM = 128;
 constexpr int kBlockN = 128;
-constexpr int kThreads = 192;
 constexpr int kHistBins = 4096;
 constexpr int kPlanThreads = 1024;
 constexpr int kWsHeaderBytes = 256;
@@ -56,7 +55,7 @@ struct AttnArgs {
   __nv_bfloat16 *out;
   float *lse;
   uint32_t *status;
-  int32_t S, N, Hq, group, num_pages, page_size, max_pages;
+  int32_t S, N, Hq, group, heads_per_pair, num_pages, page_size, max_pages;
   float scale_log2;
 };
 
@@ -175,31 +174,164 @@ __global__ void __launch_bounds__(kPlanThreads) attn_plan_kernel(const int32_t *
 // ---------------------------------------------------------------------------
 // Attention kernel
 // ---------------------------------------------------------------------------
+constexpr int kStages = 4;        // K/V ring slots (each holds one K or one V tile)
+constexpr int kThreads = 320;     // 2 softmax warpgroups + TMA warp + MMA warp
+constexpr int kWarpTma = 8;
+constexpr int kWarpMma = 9;
+
 template <int D>
 struct SmemLayout {
-  static constexpr uint32_t kHalfBytes = kBlockM * 128;       // 128 rows x 128 B (64 bf16)
-  static constexpr uint32_t kTileBytes = kBlockM * D * 2;     // one Q / K / V tile
-  static constexpr uint32_t kQ = 0;
-  static constexpr uint32_t kK0 = kQ + kTileBytes;
-  static constexpr uint32_t kV0 = kK0 + 2 * kTileBytes;
-  static constexpr uint32_t kP = kV0 + 2 * kTileBytes;
-  static constexpr uint32_t kBytes = kP + kBlockM * kBlockN * 2;
-  static constexpr uint32_t kDynamic = kBytes + 1024;         // slack for 1024-byte alignment
+  static constexpr uint32_t kHalfBytes = kBlockM * 128;    // 128 rows x 128 B (64 bf16)
+  static constexpr uint32_t kTileBytes = kBlockM * D * 2;  // one Q / K / V tile
+  static constexpr uint32_t kQ0 = 0;
+  static constexpr uint32_t kQ1 = kTileBytes;
+  static constexpr uint32_t kRing = 2 * kTileBytes;
+  static constexpr uint32_t kBytes = kRing + kStages * kTileBytes;
+  static constexpr uint32_t kDynamic = kBytes + 1024;      // slack for 1024-byte alignment
 };
 
 enum BarId {
   kBarQFull = 0,
-  kBarKFull0 = 1,   // +stage
-  kBarVFull0 = 3,   // +stage
-  kBarKVEmpty0 = 5, // +stage
-  kBarSFull0 = 7,   // +buffer
-  kBarSEmpty0 = 9,  // +buffer
-  kBarPFull = 11,
-  kBarODone = 12,
-  kBarFinal = 13,
-  kNumBars = 14
+  kBarSlotFull0 = 1,                   // + slot
+  kBarSlotEmpty0 = 1 + kStages,        // + slot
+  kBarSFull0 = 1 + 2 * kStages,        // + tile
+  kBarPFull0 = 3 + 2 * kStages,        // + tile
+  kBarODone0 = 5 + 2 * kStages,        // + tile
+  kBarFinal = 7 + 2 * kStages,
+  kNumBars = 8 + 2 * kStages
 };
 
+__device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                             uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// Softmax, P write-back and (when needed) O rescale for one query tile.
+// Runs on one warpgroup; thread r owns query row r = TMEM lane r.
+template <int D>
+__device__ __forceinline__ void softmax_role(const AttnArgs &a, int tile, int h, int32_t T, int32_t Tp, int32_t P,
+                                             int32_t c0, int32_t row0, int32_t rows_valid, uint32_t tmem,
+                                             uint64_t *bars, volatile int *abort_flag) {
+  const int warp = threadIdx.x >> 5;
+  const int row = threadIdx.x & 127;
+  const uint32_t tl = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+  const uint32_t s_col = tile * kBlockN;
+  const uint32_t o_col = kTmemO + tile * 128;
+  const uint32_t bar_s = smem_u32(&bars[kBarSFull0 + tile]);
+  const uint32_t bar_p = smem_u32(&bars[kBarPFull0 + tile]);
+  const uint32_t bar_o = smem_u32(&bars[kBarODone0 + tile]);
+  const float c = a.scale_log2;
+  float m_used = -INFINITY, l = 0.f;
+  bool ok = true;
+  for (int32_t j = 0; j < T; ++j) {
+    if (!mbar_wait(bar_s, j & 1, abort_flag, a.status)) { ok = false; break; }
+    tc_fence_after();
+    float sv[kBlockN];
+#pragma unroll
+    for (int q4 = 0; q4 < kBlockN / 32; ++q4) tmem_ld32(tl + s_col + q4 * 32, sv + q4 * 32);
+    tmem_wait_ld();
+    if (j < Tp) {
+      if (j == Tp - 1) {
+        const int lim = P - j * kBlockN;  // keys at or past the prefix end are not cached tokens
+#pragma unroll
+        for (int k = 0; k < kBlockN; ++k)
+          if (k >= lim) sv[k] = -INFINITY;
+      }
+    } else if (j == T - 1) {
+#pragma unroll
+      for (int k = 0; k < kBlockN; ++k)
+        if (k > row) sv[k] = -INFINITY;  // causal diagonal tile
+    }
+    float mx8[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) mx8[u] = fmaxf(sv[u], sv[u + 8]);
+#pragma unroll
+    for (int k = 16; k < kBlockN; k += 16) {
+#pragma unroll
+      for (int u = 0; u < 8; ++u) mx8[u] = fmax3(mx8[u], sv[k + u], sv[k + u + 8]);
+    }
+    const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
+    const float m_new = fmaxf(m_used, mx * c);
+    const bool need = m_new > m_used + kRescaleThreshold;
+    float alpha = 1.f;
+    if (need) {
+      alpha = ex2_approx(m_used - m_new);
+      m_used = m_new;
+    }
+    const float mb = (m_used == -INFINITY) ? 0.f : m_used;
+    uint32_t pk[kBlockN / 2];
+    float rs8[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) rs8[u] = 0.f;
+#pragma unroll
+    for (int k = 0; k < kBlockN / 2; ++k) {
+      const float p0 = ex2_approx(fmaf(sv[2 * k], c, -mb));
+      const float p1 = ex2_approx(fmaf(sv[2 * k + 1], c, -mb));
+      rs8[k & 7] += p0 + p1;
+      pk[k] = pack_bf16x2(p0, p1);
+    }
+    const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
+    l = l * alpha + rs;
+    // PV of the previous tile is complete here: S of this tile was committed after it.
+    if (j >= 1 && __any_sync(0xffffffffu, need)) {
+#pragma unroll
+      for (int q4 = 0; q4 < D / 32; ++q4) {
+        float o[32];
+        tmem_ld32(tl + o_col + q4 * 32, o);
+        tmem_wait_ld();
+#pragma unroll
+        for (int x = 0; x < 32; ++x) o[x] *= alpha;
+        tmem_st32(tl + o_col + q4 * 32, o);
+      }
+    }
+    // P (bf16 pairs) over the first 64 columns of this tile's S region: the A operand of PV.
+    tmem_st32(tl + s_col, reinterpret_cast<const float *>(pk));
+    tmem_st32(tl + s_col + 32, reinterpret_cast<const float *>(pk + 32));
+    tmem_wait_st();
+    tc_fence_before();
+    mbar_arrive(bar_p);
+  }
+  if (ok && mbar_wait(bar_o, 0, abort_flag, a.status)) {
+    tc_fence_after();
+    const float inv_l = 1.f / l;
+    const int32_t t = c0 + row0 + row;
+    const bool store = row < rows_valid;
+    __nv_bfloat16 *orow = a.out + ((int64_t)t * a.Hq + h) * D;
+#pragma unroll
+    for (int q4 = 0; q4 < D / 32; ++q4) {
+      float o[32];
+      tmem_ld32(tl + o_col + q4 * 32, o);
+      tmem_wait_ld();
+      if (store) {
+        uint4 *dst = reinterpret_cast<uint4 *>(orow + q4 * 32);
+#pragma unroll
+        for (int v4 = 0; v4 < 4; ++v4) {
+          uint4 w;
+          w.x = pack_bf16x2(o[v4 * 8 + 0] * inv_l, o[v4 * 8 + 1] * inv_l);
+          w.y = pack_bf16x2(o[v4 * 8 + 2] * inv_l, o[v4 * 8 + 3] * inv_l);
+          w.z = pack_bf16x2(o[v4 * 8 + 4] * inv_l, o[v4 * 8 + 5] * inv_l);
+          w.w = pack_bf16x2(o[v4 * 8 + 6] * inv_l, o[v4 * 8 + 7] * inv_l);
+          dst[v4] = w;
+        }
+      }
+    }
+    if (store && a.lse) a.lse[(int64_t)h * a.N + t] = (m_used + log2f(l)) * kLn2;
+  }
+}
+
+// One CTA = one 128-row query tile of a segment for the query heads h0 (and
+// h0 + 1 when the GQA group is even): both share every K/V tile.
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_constant__ AttnArgs a) {
   using L = SmemLayout<D>;
@@ -211,12 +343,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int32_t pair_idx = blockIdx.x / a.Hq;
+  const int32_t pair_idx = blockIdx.x / a.heads_per_pair;
   if (pair_idx >= *a.num_pairs) return;  // uniform over the CTA
   const int2 pr = a.pairs[pair_idx];
   const int32_t s = pr.x, m = pr.y;
-  const int32_t h = blockIdx.x % a.Hq;
-  const int32_t g = h / a.group;
+  const int32_t hsel = blockIdx.x % a.heads_per_pair;
+  const bool two = (a.group & 1) == 0;  // two query heads of one kv head per CTA
+  const int32_t h0 = two ? 2 * hsel : hsel;
+  const int32_t g = h0 / a.group;
   const int32_t c0 = a.cu[s];
   const int32_t n = a.cu[s + 1] - c0;
   const int32_t P = a.pos[c0];
@@ -226,28 +360,25 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   const int32_t T = Tp + m + 1;                    // + own tiles up to the diagonal
 
   const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
-  const uint32_t sQ = sbase + L::kQ;
-  const uint32_t sP = sbase + L::kP;
-  auto sK = [&](int st) { return sbase + L::kK0 + st * L::kTileBytes; };
-  auto sV = [&](int st) { return sbase + L::kV0 + st * L::kTileBytes; };
+  auto slot_addr = [&](int slot) { return sbase + L::kRing + slot * L::kTileBytes; };
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
   if (threadIdx.x == 0) {
     mbar_init(bar(kBarQFull), 1);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(bar(kBarKFull0 + i), 1);
-      mbar_init(bar(kBarVFull0 + i), 1);
-      mbar_init(bar(kBarKVEmpty0 + i), 1);
-      mbar_init(bar(kBarSFull0 + i), 1);
-      mbar_init(bar(kBarSEmpty0 + i), kBlockM);
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(bar(kBarSlotFull0 + i), 1);
+      mbar_init(bar(kBarSlotEmpty0 + i), 1);
     }
-    mbar_init(bar(kBarPFull), kBlockM);
-    mbar_init(bar(kBarODone), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(kBarSFull0 + i), 1);
+      mbar_init(bar(kBarPFull0 + i), kBlockM);
+      mbar_init(bar(kBarODone0 + i), 1);
+    }
     mbar_init(bar(kBarFinal), 1);
     s_abort = 0;
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == kWarpMma) {
     tmem_alloc(smem_u32(&s_tmem), kTmemCols);
     tmem_relinquish();
   }
@@ -257,7 +388,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   const uint32_t tmem = s_tmem;
   volatile int *abort_flag = &s_abort;
 
-  if (warp == 4) {
+  if (warp == kWarpTma) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       tma_prefetch_desc(&a.tm_q);
@@ -267,220 +398,126 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         tma_prefetch_desc(&a.tm_kc);
         tma_prefetch_desc(&a.tm_vc);
       }
-      mbar_arrive_expect_tx(bar(kBarQFull), L::kTileBytes);
+      mbar_arrive_expect_tx(bar(kBarQFull), (two ? 2 : 1) * L::kTileBytes);
 #pragma unroll
-      for (int hf = 0; hf < kHalves; ++hf)
-        tma_load_3d(sQ + hf * L::kHalfBytes, &a.tm_q, bar(kBarQFull), hf * 64, h, c0 + row0);
+      for (int hf = 0; hf < kHalves; ++hf) {
+        tma_load_3d(sbase + L::kQ0 + hf * L::kHalfBytes, &a.tm_q, bar(kBarQFull), hf * 64, h0, c0 + row0);
+        if (two)
+          tma_load_3d(sbase + L::kQ1 + hf * L::kHalfBytes, &a.tm_q, bar(kBarQFull), hf * 64, h0 + 1, c0 + row0);
+      }
       const int32_t pages_per_tile = kBlockN / a.page_size;
       const uint32_t page_bytes = a.page_size * 128u;
       int32_t issued = 0;
-      for (int32_t j = 0; j < T; ++j) {
-        const int st = j & 1;
-        if (j >= 2 && !mbar_wait(bar(kBarKVEmpty0 + st), ((j - 2) >> 1) & 1, abort_flag, a.status)) break;
-        mbar_arrive_expect_tx(bar(kBarKFull0 + st), L::kTileBytes);
+      for (int32_t ld = 0; ld < 2 * T; ++ld) {
+        const int slot = ld % kStages;
+        if (ld >= kStages &&
+            !mbar_wait(bar(kBarSlotEmpty0 + slot), ((ld / kStages) - 1) & 1, abort_flag, a.status))
+          break;
+        const int32_t j = ld >> 1;
+        const bool is_v = ld & 1;
+        const uint32_t dst = slot_addr(slot);
+        const uint32_t fb = bar(kBarSlotFull0 + slot);
+        mbar_arrive_expect_tx(fb, L::kTileBytes);
         if (j < Tp) {
+          const void *map = is_v ? static_cast<const void *>(&a.tm_vc) : static_cast<const void *>(&a.tm_kc);
           const int32_t first_page = j * pages_per_tile;
           for (int32_t pi = 0; pi < pages_per_tile; ++pi) {
             const int32_t lp = first_page + pi;
             int32_t phys = a.num_pages;  // out of range -> zero fill
             if (lp * a.page_size < P) {
               const int32_t e = a.block_table[(int64_t)s * a.max_pages + lp];
-              if (e >= 0 && e < a.num_pages) phys = e; else atomicOr(a.status, UNIP_DEV_BAD_PAGES);
-            }
-#pragma unroll
-            for (int hf = 0; hf < kHalves; ++hf)
-              tma_load_4d(sK(st) + hf * L::kHalfBytes + pi * page_bytes, &a.tm_kc, bar(kBarKFull0 + st), hf * 64,
-                          g, 0, phys);
-          }
-          mbar_arrive_expect_tx(bar(kBarVFull0 + st), L::kTileBytes);
-          for (int32_t pi = 0; pi < pages_per_tile; ++pi) {
-            const int32_t lp = first_page + pi;
-            int32_t phys = a.num_pages;
-            if (lp * a.page_size < P) {
-              const int32_t e = a.block_table[(int64_t)s * a.max_pages + lp];
               if (e >= 0 && e < a.num_pages) phys = e;
+              else if (!is_v) atomicOr(a.status, UNIP_DEV_BAD_PAGES);
             }
 #pragma unroll
             for (int hf = 0; hf < kHalves; ++hf)
-              tma_load_4d(sV(st) + hf * L::kHalfBytes + pi * page_bytes, &a.tm_vc, bar(kBarVFull0 + st), hf * 64,
-                          g, 0, phys);
+              tma_load_4d(dst + hf * L::kHalfBytes + pi * page_bytes, map, fb, hf * 64, g, 0, phys);
           }
         } else {
+          const void *map = is_v ? static_cast<const void *>(&a.tm_v) : static_cast<const void *>(&a.tm_k);
           const int32_t krow = c0 + (j - Tp) * kBlockN;
 #pragma unroll
-          for (int hf = 0; hf < kHalves; ++hf)
-            tma_load_3d(sK(st) + hf * L::kHalfBytes, &a.tm_k, bar(kBarKFull0 + st), hf * 64, g, krow);
-          mbar_arrive_expect_tx(bar(kBarVFull0 + st), L::kTileBytes);
-#pragma unroll
-          for (int hf = 0; hf < kHalves; ++hf)
-            tma_load_3d(sV(st) + hf * L::kHalfBytes, &a.tm_v, bar(kBarVFull0 + st), hf * 64, g, krow);
+          for (int hf = 0; hf < kHalves; ++hf) tma_load_3d(dst + hf * L::kHalfBytes, map, fb, hf * 64, g, krow);
         }
-        issued = j + 1;
+        issued = ld + 1;
       }
       if (*abort_flag) {
         // Let copies already in flight land before the CTA's shared memory is released.
-        for (int32_t j = max(0, issued - 2); j < issued; ++j) {
-          const uint32_t par = (j >> 1) & 1;
+        for (int32_t ld = max(0, issued - kStages); ld < issued; ++ld) {
           const uint64_t t0 = globaltimer_ns();
-          while (!mbar_try_wait(bar(kBarKFull0 + (j & 1)), par) && globaltimer_ns() - t0 < kWaitLimitNs) {}
-          while (!mbar_try_wait(bar(kBarVFull0 + (j & 1)), par) && globaltimer_ns() - t0 < kWaitLimitNs) {}
+          while (!mbar_try_wait(bar(kBarSlotFull0 + ld % kStages), (ld / kStages) & 1) &&
+                 globaltimer_ns() - t0 < kWaitLimitNs) {
+          }
         }
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(kBlockM, kBlockN, false, false);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(kBlockM, D, false, true);
-      auto issue_pv = [&](int32_t i) -> bool {
-        if (!mbar_wait(bar(kBarPFull), i & 1, abort_flag, a.status)) return false;
-        if (!mbar_wait(bar(kBarVFull0 + (i & 1)), (i >> 1) & 1, abort_flag, a.status)) return false;
-        tc_fence_after();
-        const uint32_t vb = sV(i & 1);
-#pragma unroll
-        for (int kk = 0; kk < kBlockN / 16; ++kk) {
-          const uint64_t ad = sdesc_sw128(sP + (kk >> 2) * L::kHalfBytes + (kk & 3) * 32, 16, 1024);
-          const uint64_t bd = sdesc_sw128(vb + kk * 2048, L::kHalfBytes, 1024);
-          umma_bf16_ss(tmem + kTmemO, ad, bd, idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
-        }
-        umma_commit(bar(kBarODone));
-        umma_commit(bar(kBarKVEmpty0 + (i & 1)));
-        return true;
+      const int ntiles = two ? 2 : 1;
+      auto wait_slot = [&](int32_t ld) {
+        return mbar_wait(bar(kBarSlotFull0 + ld % kStages), (ld / kStages) & 1, abort_flag, a.status);
       };
-      bool ok = mbar_wait(bar(kBarQFull), 0, abort_flag, a.status);
-      for (int32_t j = 0; ok && j < T; ++j) {
-        const int st = j & 1;
-        ok = mbar_wait(bar(kBarKFull0 + st), (j >> 1) & 1, abort_flag, a.status);
-        if (ok && j >= 2) ok = mbar_wait(bar(kBarSEmpty0 + st), ((j - 2) >> 1) & 1, abort_flag, a.status);
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t kb = sK(st);
+      auto issue_qk = [&](int tile, int32_t j) {
+        const uint32_t kb = slot_addr((2 * j) % kStages);
+        const uint32_t qb = sbase + (tile ? L::kQ1 : L::kQ0);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * L::kHalfBytes + (kk & 3) * 32;
-          umma_bf16_ss(tmem + st * kBlockN, sdesc_sw128(sQ + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024),
+          umma_bf16_ss(tmem + tile * kBlockN, sdesc_sw128(qb + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024),
                        idesc_qk, kk > 0 ? 1u : 0u);
         }
-        umma_commit(bar(kBarSFull0 + st));
-        if (j >= 1) ok = issue_pv(j - 1);
+      };
+      auto issue_pv = [&](int tile, int32_t j) {
+        const uint32_t vb = slot_addr((2 * j + 1) % kStages);
+#pragma unroll
+        for (int kk = 0; kk < kBlockN / 16; ++kk)
+          umma_bf16_ts(tmem + kTmemO + tile * 128, tmem + tile * kBlockN + kk * 8,
+                       sdesc_sw128(vb + kk * 2048, L::kHalfBytes, 1024), idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+      };
+      bool ok = mbar_wait(bar(kBarQFull), 0, abort_flag, a.status) && wait_slot(0);
+      if (ok) {
+        tc_fence_after();
+        for (int t = 0; t < ntiles; ++t) {
+          issue_qk(t, 0);
+          umma_commit(bar(kBarSFull0 + t));
+        }
+        umma_commit(bar(kBarSlotEmpty0 + 0));
       }
-      if (ok) issue_pv(T - 1);
+      for (int32_t j = 0; ok && j < T; ++j) {
+        const bool more = j + 1 < T;
+        for (int t = 0; t < ntiles; ++t) {
+          ok = mbar_wait(bar(kBarPFull0 + t), j & 1, abort_flag, a.status);
+          if (ok && t == 0) ok = wait_slot(2 * j + 1);  // V_j
+          if (!ok) break;
+          tc_fence_after();
+          issue_pv(t, j);
+          if (!more) umma_commit(bar(kBarODone0 + t));
+          if (t == ntiles - 1) umma_commit(bar(kBarSlotEmpty0 + (2 * j + 1) % kStages));
+          if (more) {
+            if (t == 0 && !(ok = wait_slot(2 * j + 2))) break;  // K_{j+1}
+            issue_qk(t, j + 1);
+            umma_commit(bar(kBarSFull0 + t));
+            if (t == ntiles - 1) umma_commit(bar(kBarSlotEmpty0 + (2 * j + 2) % kStages));
+          }
+        }
+      }
       // Every tcgen05 op of this CTA has landed before TMEM is released.
       umma_commit(bar(kBarFinal));
       const uint64_t t0 = globaltimer_ns();
-      while (!mbar_try_wait(bar(kBarFinal), 0) && globaltimer_ns() - t0 < kWaitLimitNs) {}
+      while (!mbar_try_wait(bar(kBarFinal), 0) && globaltimer_ns() - t0 < kWaitLimitNs) {
+      }
     }
-  } else {
+  } else if (warp < 4 || two) {
     // ------------------------------------------------------------ softmax + epilogue
-    const int row = threadIdx.x;  // TMEM lane == query row of the tile
-    const uint32_t tl = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-    const float c = a.scale_log2;
-    float m_used = -INFINITY, l = 0.f;
-    bool ok = true;
-    for (int32_t j = 0; j < T; ++j) {
-      const int b = j & 1;
-      if (!mbar_wait(bar(kBarSFull0 + b), (j >> 1) & 1, abort_flag, a.status)) { ok = false; break; }
-      tc_fence_after();
-      float sv[kBlockN];
-#pragma unroll
-      for (int q4 = 0; q4 < kBlockN / 32; ++q4) tmem_ld32(tl + b * kBlockN + q4 * 32, sv + q4 * 32);
-      tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(bar(kBarSEmpty0 + b));
-      if (j < Tp) {
-        if (j == Tp - 1) {
-          const int lim = P - j * kBlockN;  // keys at or after the prefix end are not cached tokens
-#pragma unroll
-          for (int k = 0; k < kBlockN; ++k)
-            if (k >= lim) sv[k] = -INFINITY;
-        }
-      } else if (j == T - 1) {
-#pragma unroll
-        for (int k = 0; k < kBlockN; ++k)
-          if (k > row) sv[k] = -INFINITY;  // causal diagonal tile
-      }
-      float mx = sv[0];
-#pragma unroll
-      for (int k = 1; k < kBlockN; ++k) mx = fmaxf(mx, sv[k]);
-      const float m_new = fmaxf(m_used, mx * c);
-      const bool need = m_new > m_used + kRescaleThreshold;
-      float alpha = 1.f;
-      if (need) {
-        alpha = ex2_approx(m_used - m_new);
-        m_used = m_new;
-      }
-      const float mb = (m_used == -INFINITY) ? 0.f : m_used;
-      uint32_t pk[kBlockN / 2];
-      float rs = 0.f;
-#pragma unroll
-      for (int k = 0; k < kBlockN / 2; ++k) {
-        const float p0 = ex2_approx(fmaf(sv[2 * k], c, -mb));
-        const float p1 = ex2_approx(fmaf(sv[2 * k + 1], c, -mb));
-        rs += p0 + p1;
-        pk[k] = pack_bf16x2(p0, p1);
-      }
-      l = l * alpha + rs;
-      if (j >= 1) {
-        // PV of the previous tile must be done: it reads the P buffer and accumulates into O.
-        if (!mbar_wait(bar(kBarODone), (j - 1) & 1, abort_flag, a.status)) { ok = false; break; }
-        tc_fence_after();
-        if (__any_sync(0xffffffffu, need)) {
-#pragma unroll
-          for (int q4 = 0; q4 < D / 32; ++q4) {
-            float o[32];
-            tmem_ld32(tl + kTmemO + q4 * 32, o);
-            tmem_wait_ld();
-#pragma unroll
-            for (int x = 0; x < 32; ++x) o[x] *= alpha;
-            tmem_st32(tl + kTmemO + q4 * 32, o);
-          }
-          tmem_wait_st();
-        }
-      }
-      // P row -> shared memory, 128-byte swizzle (16-byte chunk c of row r sits at chunk c ^ (r & 7)).
-#pragma unroll
-      for (int hk = 0; hk < 2; ++hk) {
-#pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-          const uint32_t addr = sP + hk * L::kHalfBytes + row * 128 + ((ch ^ (row & 7)) << 4);
-          const int base = hk * 32 + ch * 4;
-          st_shared_v4(addr, pk[base], pk[base + 1], pk[base + 2], pk[base + 3]);
-        }
-      }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(bar(kBarPFull));
-    }
-    if (ok && mbar_wait(bar(kBarODone), (T - 1) & 1, abort_flag, a.status)) {
-      tc_fence_after();
-      const float inv_l = 1.f / l;
-      const int32_t t = c0 + row0 + row;
-      const bool store = row < rows_valid;
-      __nv_bfloat16 *orow = a.out + ((int64_t)t * a.Hq + h) * D;
-#pragma unroll
-      for (int q4 = 0; q4 < D / 32; ++q4) {
-        float o[32];
-        tmem_ld32(tl + kTmemO + q4 * 32, o);
-        tmem_wait_ld();
-        if (store) {
-          uint4 *dst = reinterpret_cast<uint4 *>(orow + q4 * 32);
-#pragma unroll
-          for (int v4 = 0; v4 < 4; ++v4) {
-            uint4 w;
-            w.x = pack_bf16x2(o[v4 * 8 + 0] * inv_l, o[v4 * 8 + 1] * inv_l);
-            w.y = pack_bf16x2(o[v4 * 8 + 2] * inv_l, o[v4 * 8 + 3] * inv_l);
-            w.z = pack_bf16x2(o[v4 * 8 + 4] * inv_l, o[v4 * 8 + 5] * inv_l);
-            w.w = pack_bf16x2(o[v4 * 8 + 6] * inv_l, o[v4 * 8 + 7] * inv_l);
-            dst[v4] = w;
-          }
-        }
-      }
-      if (store && a.lse) a.lse[(int64_t)h * a.N + t] = (m_used + log2f(l)) * kLn2;
-    }
+    const int tile = warp >> 2;
+    softmax_role<D>(a, tile, h0 + tile, T, Tp, P, c0, row0, rows_valid, tmem, bars, abort_flag);
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == kWarpMma) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
@@ -595,12 +632,13 @@ UNIP_API int32_t unip_prefill_attention(const void *q, const void *k, const void
   args.N = total_tokens;
   args.Hq = Hq;
   args.group = Hq / Hkv;
+  args.heads_per_pair = (args.group % 2 == 0) ? Hq / 2 : Hq;
   args.num_pages = has_cache ? paged->num_pages : 0;
   args.page_size = has_cache ? paged->page_size : 16;
   args.max_pages = has_cache ? paged->max_pages_per_seq : 0;
   const float scale = prm->scale > 0.f ? prm->scale : 1.0f / sqrtf((float)D);
   args.scale_log2 = scale * kLog2e;
-  const int64_t grid = (int64_t)max_pairs * Hq;
+  const int64_t grid = (int64_t)max_pairs * args.heads_per_pair;
   if (grid > 0x7FFFFFFF) return UNIP_ERR_UNSUPPORTED;
   const cudaError_t e = D == 128 ? launch_attention<128>(args, (int)grid, st) : launch_attention<64>(args, (int)grid, st);
   return e == cudaSuccess ? UNIP_OK : UNIP_ERR_CUDA;
