@@ -10,14 +10,19 @@
 // Kernels
 //   imp_plan_kernel   one CTA: block offsets blk_cu, list of (segment, 128-key
 //                     chunk) work items of the scored segments.
-//   imp_score_kernel  one CTA per (work item, kv head): 128 threads, one key
-//                     each; the window rows of the kv head's query-head group
-//                     are staged in shared memory; per-block partial masses
-//                     are reduced in registers/shuffles and written without
-//                     atomics (deterministic).
+//   imp_score_tc_kernel  one CTA per (work item, kv head): TMA loads the
+//                     128-key tile and the window rows of the kv head's query
+//                     heads; one tcgen05 MMA chain computes S^T = K Q_w^T into
+//                     TMEM (keys on lanes, window rows x heads on columns);
+//                     128 threads, one key each, sum exp(s - lse) over their
+//                     visible columns; per-block partial masses are reduced
+//                     with shuffles and written without atomics (deterministic).
 //   imp_norm_kernel   one CTA per segment: sums the kv-head partials in a
 //                     fixed order and divides by the segment total.
 #include <cuda_bf16.h>
+
+#include <algorithm>
+#include <cstring>
 
 #include "unip_internal.cuh"
 
@@ -25,8 +30,6 @@ namespace unip {
 namespace {
 
 constexpr int kChunk = 128;        // keys per score CTA
-constexpr int kScoreThreads = 128;
-constexpr int kRowsPerPass = 16;   // window rows staged per pass
 constexpr int kPlanThreads = 1024;
 constexpr int kNormThreads = 256;
 constexpr int kWsHeaderBytes = 256;
@@ -97,93 +100,192 @@ __global__ void __launch_bounds__(kPlanThreads) imp_plan_kernel(const int32_t *_
   if (tid == 0) header[0] = tot_items;
 }
 
+struct ScoreArgs {
+  CUtensorMap tm_k;   // k  [N][H_kv][D], box 64 x 1 x 128
+  CUtensorMap tm_q;   // q  [N][H_q][D],  box 64 x 1 x B
+  const float *lse;   // [H_q][N]
+  const int32_t *cu;
+  const int32_t *blk_cu;
+  const int2 *items;
+  const int32_t *num_items;
+  float *partial;     // [blocks][H_kv]
+  uint32_t *status;
+  int32_t N, Hq, Hkv, B, heads_per_group;
+  float scale_log2;
+};
+
+constexpr int kScoreWarpTma = 4;
+constexpr int kScoreWarpMma = 5;
+constexpr int kScoreThreadsTc = 192;
+constexpr int kMaxCols = 256;  // columns of S^T per MMA group (window rows x heads)
+
 template <int D>
-__global__ void __launch_bounds__(kScoreThreads) imp_score_kernel(
-    const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k, const float *__restrict__ lse,
-    const int32_t *__restrict__ cu, const int32_t *__restrict__ blk_cu, const int2 *__restrict__ items,
-    const int32_t *__restrict__ num_items, int32_t N, int32_t Hq, int32_t Hkv, int32_t B, float scale_log2,
-    float *__restrict__ partial) {
-  __shared__ float sq[kRowsPerPass][D];
-  __shared__ float sl[kRowsPerPass];
-  __shared__ float sred[kScoreThreads / 32];
-  const int32_t item = blockIdx.x / Hkv;
-  if (item >= *num_items) return;
-  const int32_t g = blockIdx.x % Hkv;
-  const int2 it = items[item];
+struct ScoreSmem {
+  static constexpr uint32_t kHalf = 128 * 128;            // 128 rows x 128 B
+  static constexpr uint32_t kK = 0;                       // K tile: D/64 halves of 128 rows
+  static constexpr uint32_t kQ = (D / 64) * kHalf;        // Q window: D/64 halves of 256 rows
+  static constexpr uint32_t kQHalf = kMaxCols * 128;
+  static constexpr uint32_t kBytes = kQ + (D / 64) * kQHalf;
+  static constexpr uint32_t kDynamic = kBytes + 1024;
+};
+
+// One CTA per (segment, 128-key chunk, kv head).  S^T = K Q_w^T on the
+// tensor cores: M = 128 keys of the chunk (TMEM lanes), N = window rows of
+// the group's query heads (TMEM columns), K = D.  Each of 128 threads owns one
+// key and sums exp(s - lse) over its visible window columns.
+template <int D>
+__global__ void __launch_bounds__(kScoreThreadsTc) imp_score_tc_kernel(const __grid_constant__ ScoreArgs a) {
+  using L = ScoreSmem<D>;
+  constexpr int kHalves = D / 64;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t bars[6];  // k_full, q_full, s_full, s_empty, q_empty, final
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+  __shared__ float s_lse[kMaxCols];
+  __shared__ float s_red[4];
+
+  const int32_t item = blockIdx.x / a.Hkv;
+  if (item >= *a.num_items) return;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
+  const int32_t g = blockIdx.x % a.Hkv;
+  const int2 it = a.items[item];
   const int32_t s = it.x, c = it.y;
-  const int32_t c0 = cu[s], n = cu[s + 1] - c0;
+  const int32_t c0 = a.cu[s], n = a.cu[s + 1] - c0;
+  const int32_t B = a.B;
   const int32_t W = min(B, n);
-  const int32_t group = Hq / Hkv;
-  const int tid = threadIdx.x;
-  const int32_t j = c * kChunk + tid;  // segment-local key index
-  const bool valid = j < n;
-
-  float kf[D];
-  if (valid) {
-    const uint4 *src = reinterpret_cast<const uint4 *>(k + ((int64_t)(c0 + j) * Hkv + g) * D);
-#pragma unroll
-    for (int v = 0; v < D / 8; ++v) {
-      const uint4 w = src[v];
-      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        kf[v * 8 + 2 * e] = __uint_as_float(ws[e] << 16);
-        kf[v * 8 + 2 * e + 1] = __uint_as_float(ws[e] & 0xFFFF0000u);
-      }
-    }
-  } else {
-#pragma unroll
-    for (int d = 0; d < D; ++d) kf[d] = 0.f;
+  const int32_t wrow0 = n - W;               // first window row (segment-local)
+  const int32_t group = a.Hq / a.Hkv;
+  const int32_t hpg = a.heads_per_group;     // heads per MMA group
+  const int32_t ngroups = (group + hpg - 1) / hpg;
+  const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  const uint32_t bar_k = smem_u32(&bars[0]), bar_q = smem_u32(&bars[1]), bar_s = smem_u32(&bars[2]);
+  const uint32_t bar_se = smem_u32(&bars[3]), bar_qe = smem_u32(&bars[4]);
+  if (tid == 0) {
+    mbar_init(bar_k, 1);
+    mbar_init(bar_q, 1);
+    mbar_init(bar_s, 1);
+    mbar_init(bar_se, 128);
+    mbar_init(bar_qe, 1);
+    mbar_init(smem_u32(&bars[5]), 1);
+    s_abort = 0;
+    fence_mbar_init();
   }
+  if (warp == kScoreWarpMma) {
+    tmem_alloc(smem_u32(&s_tmem), 256);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+  volatile int *abort_flag = &s_abort;
 
-  float acc = 0.f;
-  for (int32_t hh = 0; hh < group; ++hh) {
-    const int32_t h = g * group + hh;
-    for (int32_t r0 = n - W; r0 < n; r0 += kRowsPerPass) {
-      const int32_t nr = min(kRowsPerPass, n - r0);
-      __syncthreads();
-      for (int e = tid; e < kRowsPerPass * D; e += kScoreThreads) {
-        const int r = e / D, d = e % D;
-        sq[r][d] = r < nr ? __bfloat162float(q[((int64_t)(c0 + r0 + r) * Hq + h) * D + d]) : 0.f;
-      }
-      if (tid < kRowsPerPass) sl[tid] = tid < nr ? lse[(int64_t)h * N + c0 + r0 + tid] * kLog2e : 0.f;
-      __syncthreads();
-      for (int r = 0; r < nr; ++r) {
-        float dot = 0.f;
+  if (warp == kScoreWarpTma) {
+    if (lane == 0) {
+      mbar_arrive_expect_tx(bar_k, kHalves * L::kHalf);
 #pragma unroll
-        for (int d = 0; d < D; d += 4) {
-          const float4 qv = *reinterpret_cast<const float4 *>(&sq[r][d]);
-          dot = fmaf(qv.x, kf[d], dot);
-          dot = fmaf(qv.y, kf[d + 1], dot);
-          dot = fmaf(qv.z, kf[d + 2], dot);
-          dot = fmaf(qv.w, kf[d + 3], dot);
+      for (int hf = 0; hf < kHalves; ++hf)
+        tma_load_3d(sbase + L::kK + hf * L::kHalf, &a.tm_k, bar_k, hf * 64, g, c0 + c * 128);
+      for (int32_t gi = 0; gi < ngroups; ++gi) {
+        if (gi > 0 && !mbar_wait(bar_qe, (gi - 1) & 1, abort_flag, a.status)) break;
+        const int32_t hn = min(hpg, group - gi * hpg);
+        mbar_arrive_expect_tx(bar_q, kHalves * hn * B * 128);
+        for (int32_t hh = 0; hh < hn; ++hh) {
+          const int32_t h = g * group + gi * hpg + hh;
+#pragma unroll
+          for (int hf = 0; hf < kHalves; ++hf)
+            tma_load_3d(sbase + L::kQ + hf * L::kQHalf + hh * B * 128, &a.tm_q, bar_q, hf * 64, h, c0 + wrow0);
         }
-        if (valid && j <= r0 + r) acc += ex2_approx(fmaf(dot, scale_log2, -sl[r]));
+      }
+    }
+  } else if (warp == kScoreWarpMma) {
+    if (lane == 0) {
+      bool ok = mbar_wait(bar_k, 0, abort_flag, a.status);
+      for (int32_t gi = 0; ok && gi < ngroups; ++gi) {
+        ok = mbar_wait(bar_q, gi & 1, abort_flag, a.status);
+        if (ok && gi > 0) ok = mbar_wait(bar_se, (gi - 1) & 1, abort_flag, a.status);
+        if (!ok) break;
+        tc_fence_after();
+        const int32_t hn = min(hpg, group - gi * hpg);
+        const uint32_t idesc = idesc_bf16_f32(128, hn * B, false, false);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t koff = (kk >> 2) * L::kHalf + (kk & 3) * 32;
+          const uint32_t qoff = (kk >> 2) * L::kQHalf + (kk & 3) * 32;
+          umma_bf16_ss(tmem, sdesc_sw128(sbase + L::kK + koff, 16, 1024), sdesc_sw128(sbase + L::kQ + qoff, 16, 1024),
+                       idesc, kk > 0 ? 1u : 0u);
+        }
+        umma_commit(bar_s);
+        umma_commit(bar_qe);
+      }
+      // Every tcgen05 op of this CTA has landed before TMEM is released.
+      umma_commit(smem_u32(&bars[5]));
+      const uint64_t t0 = globaltimer_ns();
+      while (!mbar_try_wait(smem_u32(&bars[5]), 0) && globaltimer_ns() - t0 < kWaitLimitNs) {
+      }
+    }
+  } else {
+    // 4 warps: thread tid owns key j = c*128 + tid (TMEM lane tid)
+    const int32_t j = c * 128 + tid;
+    const bool kvalid = j < n;
+    const uint32_t tl = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    float acc = 0.f;
+    for (int32_t gi = 0; gi < ngroups; ++gi) {
+      const int32_t hn = min(hpg, group - gi * hpg);
+      // stage this group's row normalisers (log2 domain); window slots past the segment are masked
+      for (int32_t col = tid; col < hn * B; col += 128) {
+        const int32_t hh = col / B, t = col % B;
+        const int32_t h = g * group + gi * hpg + hh;
+        s_lse[col] = t < W ? a.lse[(int64_t)h * a.N + c0 + wrow0 + t] * kLog2e : INFINITY;
+      }
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+      if (!mbar_wait(bar_s, gi & 1, abort_flag, a.status)) break;
+      tc_fence_after();
+      for (uint32_t col0 = 0; col0 < (uint32_t)(hn * B); col0 += 32) {
+        float sv[32];
+        tmem_ld32(tl + col0, sv);
+        tmem_wait_ld();
+#pragma unroll
+        for (int x = 0; x < 32; ++x) {
+          const int32_t col = col0 + x;
+          const int32_t t = col % B;             // window slot
+          // visible: window slot inside the segment and key j at or before row wrow0 + t
+          if (kvalid && col < hn * B && j <= wrow0 + t) acc += ex2_approx(fmaf(sv[x], a.scale_log2, -s_lse[col]));
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(bar_se);
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+    }
+    // per-block sums over the chunk's keys
+    const int32_t nb_seg = a.blk_cu[s + 1] - a.blk_cu[s];
+    const int32_t bpc = 128 / B;
+    if (B <= 32) {
+      float v = acc;
+      for (int off = B / 2; off >= 1; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+      if ((tid % B) == 0) {
+        const int32_t b = c * bpc + tid / B;
+        if (b < nb_seg) a.partial[(int64_t)(a.blk_cu[s] + b) * a.Hkv + g] = v;
+      }
+    } else {
+      float v = acc;
+      for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+      if (lane == 0) s_red[warp] = v;
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+      const int wpb = B / 32;
+      if (tid < bpc) {
+        float t = 0.f;
+        for (int w = 0; w < wpb; ++w) t += s_red[tid * wpb + w];
+        const int32_t b = c * bpc + tid;
+        if (b < nb_seg) a.partial[(int64_t)(a.blk_cu[s] + b) * a.Hkv + g] = t;
       }
     }
   }
-  // Per-block sums over the chunk's keys (block size divides the chunk).
-  const int32_t nb_seg = blk_cu[s + 1] - blk_cu[s];
-  const int32_t blocks_per_chunk = kChunk / B;
-  if (B <= 32) {
-    float v = acc;
-    for (int off = B / 2; off >= 1; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-    if ((tid % B) == 0) {
-      const int32_t b = c * blocks_per_chunk + tid / B;
-      if (b < nb_seg) partial[(int64_t)(blk_cu[s] + b) * Hkv + g] = v;
-    }
-  } else {
-    float v = acc;
-    for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-    if ((tid & 31) == 0) sred[tid >> 5] = v;
-    __syncthreads();
-    const int wpb = B / 32;
-    if (tid < blocks_per_chunk) {
-      float t = 0.f;
-      for (int w = 0; w < wpb; ++w) t += sred[tid * wpb + w];
-      const int32_t b = c * blocks_per_chunk + tid;
-      if (b < nb_seg) partial[(int64_t)(blk_cu[s] + b) * Hkv + g] = t;
-    }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kScoreWarpMma) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 256);
   }
 }
 
@@ -213,6 +315,22 @@ __global__ void __launch_bounds__(kNormThreads) imp_norm_kernel(const int32_t *_
     for (int32_t g = 0; g < Hkv; ++g) m += partial[(int64_t)(b0 + b) * Hkv + g];
     imp[b0 + b] = m * inv;
   }
+}
+
+template <int D>
+cudaError_t launch_score(const ScoreArgs &args, int grid, cudaStream_t stream) {
+  using L = ScoreSmem<D>;
+  static bool configured[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !configured[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(imp_score_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)L::kDynamic);
+    if (e != cudaSuccess) return e;
+    configured[dev] = true;
+  }
+  imp_score_tc_kernel<D><<<grid, kScoreThreadsTc, L::kDynamic, stream>>>(args);
+  return cudaGetLastError();
 }
 
 int32_t max_items_for(int32_t total_tokens, int32_t num_segs) {
@@ -273,17 +391,39 @@ UNIP_API int32_t unip_block_importance(const void *q, const void *k, const float
   const float scale = prm->scale > 0.f ? prm->scale : 1.0f / sqrtf((float)D);
   const int64_t grid = (int64_t)max_items * Hkv;
   if (grid > 0x7FFFFFFF) return UNIP_ERR_UNSUPPORTED;
-  const __nv_bfloat16 *qb = static_cast<const __nv_bfloat16 *>(q);
-  const __nv_bfloat16 *kb = static_cast<const __nv_bfloat16 *>(k);
-  if (D == 128)
-    imp_score_kernel<128><<<(int)grid, kScoreThreads, 0, st>>>(qb, kb, lse, cu_seqlens, blk_cu, items, header,
-                                                               total_tokens, Hq, Hkv, block_size, scale * kLog2e,
-                                                               partial);
-  else
-    imp_score_kernel<64><<<(int)grid, kScoreThreads, 0, st>>>(qb, kb, lse, cu_seqlens, blk_cu, items, header,
-                                                              total_tokens, Hq, Hkv, block_size, scale * kLog2e,
-                                                              partial);
-  if (cudaGetLastError() != cudaSuccess) return UNIP_ERR_CUDA;
+  ScoreArgs args;
+  memset(&args, 0, sizeof(args));
+  {
+    const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)Hkv, (cuuint64_t)total_tokens};
+    const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)Hkv * D * 2};
+    const cuuint32_t box[3] = {64, 1, 128};
+    if (encode_tiled(&args.tm_k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(k), dims, strides, box,
+                     CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+      return UNIP_ERR_CUDA;
+  }
+  {
+    const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)Hq, (cuuint64_t)total_tokens};
+    const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)Hq * D * 2};
+    const cuuint32_t box[3] = {64, 1, (cuuint32_t)block_size};
+    if (encode_tiled(&args.tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(q), dims, strides, box,
+                     CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+      return UNIP_ERR_CUDA;
+  }
+  args.lse = lse;
+  args.cu = cu_seqlens;
+  args.blk_cu = blk_cu;
+  args.items = items;
+  args.num_items = header;
+  args.partial = partial;
+  args.status = status;
+  args.N = total_tokens;
+  args.Hq = Hq;
+  args.Hkv = Hkv;
+  args.B = block_size;
+  args.heads_per_group = std::min(Hq / Hkv, kMaxCols / block_size);
+  args.scale_log2 = scale * kLog2e;
+  cudaError_t e = D == 128 ? launch_score<128>(args, (int)grid, st) : launch_score<64>(args, (int)grid, st);
+  if (e != cudaSuccess) return UNIP_ERR_CUDA;
   imp_norm_kernel<<<num_segs, kNormThreads, 0, st>>>(blk_cu, partial, Hkv, imp);
   if (cudaGetLastError() != cudaSuccess) return UNIP_ERR_CUDA;
   return UNIP_OK;

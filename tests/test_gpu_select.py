@@ -171,3 +171,25 @@ def test_gather_bit_exact_and_strides(n_rows, d, extra):
     got = out[: len(idx)].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
     assert np.array_equal(got, oracle.gather(np.ascontiguousarray(hid[:, :d]), idx))
     assert Bd.unip_get_device_status() == 0
+
+
+@pytest.mark.parametrize("lengths,hq,hkv,d,B", [
+    ([37, 100, 64, 255], 4, 2, 64, 16), ([5, 130, 300], 8, 2, 128, 32), ([1000, 64], 4, 1, 64, 128),
+    ([7, 260], 8, 8, 128, 64), ([513], 16, 2, 128, 64), ([129, 1, 0, 40], 2, 1, 128, 16)])
+def test_importance_shapes_vs_oracle(lengths, hq, hkv, d, B):
+    from sparsified_long_context_gb300 import binding as Bd
+    from sparsified_long_context_gb300.pipeline import DeviceInputs, StepBuffers, run_attention, run_importance
+    wl = W.packed(lengths, hq, hkv, d, seed=sum(lengths) + B, block_size=B, top_p=0.9)
+    Bd.unip_get_device_status(clear=True)
+    di = DeviceInputs.from_workload(wl, "cuda", with_hidden=False)
+    bufs = StepBuffers(di, block_size=B)
+    run_attention(di, bufs)
+    run_importance(di, bufs)
+    torch.cuda.synchronize()
+    assert Bd.unip_get_device_status() == 0
+    _, lse = oracle.attention(wl.q, wl.k, wl.v, wl.cu_seqlens, wl.positions, hq, hkv, d)
+    ref_imp, ref_bc = oracle.block_importance(wl.q, wl.k, lse, wl.cu_seqlens, hq, hkv, d, B, seg_mask=wl.seg_mask)
+    blk_cu = bufs.blk_cu.cpu().numpy()
+    assert np.array_equal(blk_cu, ref_bc)
+    imp = bufs.imp[: blk_cu[-1]].cpu().numpy().astype(np.float64)
+    assert_close(imp, ref_imp, what="importance")
