@@ -72,6 +72,7 @@ extern "C" {
 #define UNIP_ERR_WORKSPACE (-3)        /* workspace missing, too small or misaligned */
 #define UNIP_ERR_CUDA (-4)             /* CUDA runtime / launch failure */
 #define UNIP_ERR_ALIGNMENT (-5)        /* pointer or row stride not 16-byte aligned */
+#define UNIP_ERR_TOO_LARGE (-6)        /* problem exceeds the built-in scratch of unip_prefill_attention_noalloc */
 
 /* Device status bits (unip_get_device_status). */
 #define UNIP_DEV_BAD_SEQLENS 0x1u    /* cu_seqlens not monotone / ends wrong */
@@ -143,6 +144,38 @@ UNIP_API int32_t unip_prefill_attention(const void *q, const void *k, const void
                                         void *out, float *lse,
                                         void *workspace, size_t workspace_bytes,
                                         void *stream);
+
+/* ---------------------------------------------------------------------------
+ * Attention without caller-provided workspace.  The paper has no counterpart:
+ * this is a library convenience.  It computes exactly what
+ * unip_prefill_attention computes, but its scratch (the tile plan) lives in a
+ * fixed device array inside the library, so the call allocates nothing and
+ * needs no workspace pointer.  It is meant for callers that cannot call
+ * cudaMalloc or own a device allocator: a host that hands out only the
+ * tensors it already owns (a plugin or custom-operator interface without an
+ * allocator), code running inside CUDA stream capture, where allocation would
+ * break the capture, or a latency-critical path that must not pay for an
+ * allocation that may synchronise the device.
+ *
+ * Limit: ceil(total_tokens / 128) + num_segs <= UNIP_NOALLOC_MAX_TILES;
+ * larger problems return UNIP_ERR_TOO_LARGE without enqueuing anything.
+ * The array costs UNIP_NOALLOC_SCRATCH_BYTES of memory on every device that
+ * loads the library, until the process exits.
+ * The first call on a device looks up the array's device address (with that
+ * device current); make that first call before any stream capture begins.
+ * Every call shares the one array per device: calls that may overlap on the
+ * GPU (other streams, other host threads) race and must be serialised by the
+ * caller.  Arguments, outputs and errors are those of unip_prefill_attention.
+ * ------------------------------------------------------------------------- */
+#define UNIP_NOALLOC_MAX_TILES 32768
+#define UNIP_NOALLOC_SCRATCH_BYTES (256 + 8 * UNIP_NOALLOC_MAX_TILES)
+
+UNIP_API int32_t unip_prefill_attention_noalloc(const void *q, const void *k, const void *v,
+                                                const int32_t *cu_seqlens, int32_t num_segs,
+                                                const int32_t *positions, int32_t total_tokens,
+                                                const unip_paged_kv *paged,
+                                                const unip_attn_params *prm,
+                                                void *out, float *lse, void *stream);
 
 /* ---------------------------------------------------------------------------
  * Block importance ([UP] section 3; scoring reading fixed by this library):

@@ -74,6 +74,9 @@ def load(build_if_missing: bool = True):
         lib.unip_attention_workspace_size.argtypes = [i32, i32, pp]
         lib.unip_prefill_attention.restype = i32
         lib.unip_prefill_attention.argtypes = [P, P, P, P, i32, P, i32, ctypes.POINTER(_PagedKV), pp, P, P, P, sz, P]
+        lib.unip_prefill_attention_noalloc.restype = i32
+        lib.unip_prefill_attention_noalloc.argtypes = [P, P, P, P, i32, P, i32, ctypes.POINTER(_PagedKV), pp, P, P,
+                                                       P]
         lib.unip_importance_capacity.restype = i32
         lib.unip_importance_capacity.argtypes = [i32, i32, i32]
         lib.unip_importance_workspace_size.restype = sz
@@ -162,6 +165,32 @@ def unip_prefill_attention(q, k, v, cu_seqlens, positions, out, lse=None, *, num
                                     ctypes.byref(prm), _ptr(out), _ptr(lse), _ptr(workspace),
                                     workspace.numel(), _stream(stream))
     _check(rc, "unip_prefill_attention")
+    return out, lse
+
+
+def unip_prefill_attention_noalloc(q, k, v, cu_seqlens, positions, out, lse=None, *, num_heads_q, num_heads_kv,
+                                   head_dim, k_cache=None, v_cache=None, block_table=None, page_size=16,
+                                   scale=None, stream=None):
+    """Same result as unip_prefill_attention, with the library's built-in scratch.
+
+    For callers that cannot allocate device memory: nothing is allocated here
+    either (no workspace tensor).  The library's one scratch array per device
+    is shared by every call, so calls that may overlap on the GPU must be
+    serialised by the caller; the first call on a device should come before
+    any stream capture.
+    """
+    lib = load()
+    n = int(q.shape[0])
+    S = int(cu_seqlens.shape[0]) - 1
+    prm = _params(num_heads_q, num_heads_kv, head_dim, scale)
+    paged_p = None
+    if k_cache is not None:
+        paged = _PagedKV(_ptr(k_cache), _ptr(v_cache), int(k_cache.shape[0]), int(page_size), _ptr(block_table),
+                         int(block_table.shape[1]))
+        paged_p = ctypes.byref(paged)
+    rc = lib.unip_prefill_attention_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), S, _ptr(positions), n,
+                                            paged_p, ctypes.byref(prm), _ptr(out), _ptr(lse), _stream(stream))
+    _check(rc, "unip_prefill_attention_noalloc")
     return out, lse
 
 

@@ -29,6 +29,9 @@
 //     the second MMA reads; V is read MN-major straight from its TMA tile.
 #include <cuda_bf16.h>
 
+#include <cstring>
+#include <mutex>
+
 #include "unip_internal.cuh"
 
 namespace unip {
@@ -642,6 +645,55 @@ UNIP_API int32_t unip_prefill_attention(const void *q, const void *k, const void
   if (grid > 0x7FFFFFFF) return UNIP_ERR_UNSUPPORTED;
   const cudaError_t e = D == 128 ? launch_attention<128>(args, (int)grid, st) : launch_attention<64>(args, (int)grid, st);
   return e == cudaSuccess ? UNIP_OK : UNIP_ERR_CUDA;
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// No-allocation variant: the tile plan lives in a fixed device array.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr int kNoAllocMaxDevices = 64;
+
+// Scratch of unip_prefill_attention_noalloc (planner header + tile pairs).
+static __device__ __align__(256) uint8_t g_noalloc_scratch[UNIP_NOALLOC_SCRATCH_BYTES];
+
+std::mutex g_noalloc_mu;
+void *g_noalloc_addr[kNoAllocMaxDevices] = {nullptr};
+
+// Device address of the scratch array on the current device, looked up once
+// per device with that device current (host code cannot use the symbol itself).
+void *noalloc_scratch_address() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (!g_noalloc_addr[dev]) {
+    void *ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) return nullptr;
+    g_noalloc_addr[dev] = ptr;
+  }
+  return g_noalloc_addr[dev];
+}
+
+}  // namespace
+
+extern "C" {
+
+UNIP_API int32_t unip_prefill_attention_noalloc(const void *q, const void *k, const void *v,
+                                                const int32_t *cu_seqlens, int32_t num_segs,
+                                                const int32_t *positions, int32_t total_tokens,
+                                                const unip_paged_kv *paged, const unip_attn_params *prm,
+                                                void *out, float *lse, void *stream) {
+  if (!prm || num_segs < 0 || total_tokens < 0) return UNIP_ERR_INVALID_ARGUMENT;
+  const int64_t tiles = ((int64_t)total_tokens + kBlockM - 1) / kBlockM + num_segs;
+  if (tiles > UNIP_NOALLOC_MAX_TILES) return UNIP_ERR_TOO_LARGE;
+  const size_t need = unip_attention_workspace_size(total_tokens, num_segs, prm);
+  if (need > (size_t)UNIP_NOALLOC_SCRATCH_BYTES) return UNIP_ERR_TOO_LARGE;
+  void *scratch = noalloc_scratch_address();
+  if (!scratch) return UNIP_ERR_CUDA;
+  return unip_prefill_attention(q, k, v, cu_seqlens, num_segs, positions, total_tokens, paged, prm, out, lse,
+                                scratch, (size_t)UNIP_NOALLOC_SCRATCH_BYTES, stream);
 }
 
 }  // extern "C"
