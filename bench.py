@@ -149,10 +149,10 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def build_workload(name: str, rank: int):
+def build_workload(name: str, rank: int, tokens: int = 32768):
     from sparsified_long_context_gb300 import workloads as W
     if name == "long_single":
-        return W.long_single(seed=4 + 1000 * rank)
+        return W.long_single(seed=4 + 1000 * rank, n=tokens)
     if name == "mixed_step":
         return W.mixed_step(seed=5 + 1000 * rank)
     if name == "prepacked":
@@ -182,7 +182,7 @@ def run_reference(args):
     world, rank, _ = dist_setup(args)
     if rank != 0:
         return 0
-    wl = build_workload(args.workload, 0)
+    wl = build_workload(args.workload, 0, args.tokens)
     cores = oracle.default_threads()
     rng = np.random.default_rng(123)
     # calibrate a per-step row sample of a few seconds
@@ -247,6 +247,8 @@ def main():
     ap.add_argument("--impl", default="unip", choices=["unip", "reference"])
     ap.add_argument("--workload", default="long_single",
                     choices=["long_single", "mixed_step", "prepacked", "tiny_packed"])
+    ap.add_argument("--tokens", type=int, default=32768,
+                    help="prompt length of the long_single workload (profiling runs use a shorter one)")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-step-seconds", type=float, default=6.0)
@@ -269,7 +271,7 @@ def main():
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     B.load()
     B.unip_get_device_status(clear=True)
-    wl = build_workload(args.workload, rank)
+    wl = build_workload(args.workload, rank, args.tokens)
     di = DeviceInputs.from_workload(wl, f"cuda:{local}")
     bufs = StepBuffers(di)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=f"cuda:{local}")

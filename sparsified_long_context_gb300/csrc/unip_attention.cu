@@ -14,19 +14,27 @@
 //     segment into 128-row query tiles and orders the (segment, tile) pairs
 //     longest-first by their number of 128-key KV tiles.  The attention grid
 //     is launched with a host-side upper bound; surplus CTAs exit at once.
-//   * One CTA = one 128-row query tile of one query head.  A KV tile is
-//     either 128 prefix keys (read page by page through the block table) or
-//     128 of the segment's own keys; only the last prefix tile and the
+//   * One CTA = one 128-row query tile for the two query heads of a GQA pair
+//     (one head when the group is odd); both share every K/V tile.  A KV tile
+//     is either 128 prefix keys (read page by page through the block table)
+//     or 128 of the segment's own keys; only the last prefix tile and the
 //     diagonal own tile need a mask, every fully masked tile is skipped.
-//   * Warp roles: warps 0-3 softmax + epilogue (one query row per thread,
-//     i.e. one TMEM lane each), warp 4 TMA producer, warp 5 tcgen05 issuer.
-//   * TMEM (512 columns): two S buffers (128 fp32 columns each) so QK^T of
-//     tile j+1 overlaps the softmax of tile j, and the O accumulator (D cols).
+//   * Warp roles: warps 0-3 and 4-7 softmax + epilogue of the two query tiles
+//     (one query row per thread, i.e. one TMEM lane each), warp 8 TMA
+//     producer, warp 9 tcgen05 issuer; setmaxnreg moves registers from the
+//     control warpgroup to the softmax warpgroups.
+//   * K and V tiles stream through one 4-slot ring of 128-byte-swizzled TMA
+//     tiles; a slot is released by a tcgen05.commit after its last MMA.
+//   * TMEM (512 columns): S of each query tile (128 fp32 columns) and O of
+//     each query tile (D columns).  P is written back as bf16 pairs over the
+//     first 64 columns of its S region and read by the PV MMA from TMEM; V is
+//     the MN-major B operand straight from its TMA tile.  The MMA order
+//     PV0(j), QK0(j+1), PV1(j), QK1(j+1) lets one tile's softmax run while
+//     the other tile's MMAs execute.
 //   * Online softmax in base 2 with a lazy rescale: the running maximum is
 //     only moved (and O rescaled in TMEM) when a row's maximum grows by more
 //     than 8 (log2 units), which bounds P by 2^8; the final O / l is exact.
-//   * P goes to shared memory as bf16 in the 128-byte-swizzled K-major layout
-//     the second MMA reads; V is read MN-major straight from its TMA tile.
+//     P is published in two halves so PV starts on keys 0..63 early.
 #include <cuda_bf16.h>
 
 #include <cstring>
@@ -178,7 +186,11 @@ __global__ void __launch_bounds__(kPlanThreads) attn_plan_kernel(const int32_t *
 // Attention kernel
 // ---------------------------------------------------------------------------
 constexpr int kStages = 4;        // K/V ring slots (each holds one K or one V tile)
-constexpr int kThreads = 320;     // 2 softmax warpgroups + TMA warp + MMA warp
+constexpr int kThreads = 384;     // 2 softmax warpgroups + one warpgroup for the TMA and MMA warps
+// Register split after launch (384 threads x 168): softmax warpgroups grow to 216, the
+// TMA/MMA warpgroup shrinks to 72; 2 x 216 + 72 = 3 x 168, the launch's own budget.
+constexpr uint32_t kRegsSoftmax = 216;
+constexpr uint32_t kRegsControl = 72;
 constexpr int kWarpTma = 8;
 constexpr int kWarpMma = 9;
 
@@ -198,10 +210,11 @@ enum BarId {
   kBarSlotFull0 = 1,                   // + slot
   kBarSlotEmpty0 = 1 + kStages,        // + slot
   kBarSFull0 = 1 + 2 * kStages,        // + tile
-  kBarPFull0 = 3 + 2 * kStages,        // + tile
-  kBarODone0 = 5 + 2 * kStages,        // + tile
-  kBarFinal = 7 + 2 * kStages,
-  kNumBars = 8 + 2 * kStages
+  kBarPLo0 = 3 + 2 * kStages,          // + tile: P of keys 0..63 in TMEM (and O rescaled)
+  kBarPHi0 = 5 + 2 * kStages,          // + tile: P of keys 64..127 in TMEM
+  kBarODone0 = 7 + 2 * kStages,        // + tile
+  kBarFinal = 9 + 2 * kStages,
+  kNumBars = 10 + 2 * kStages
 };
 
 __device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
@@ -212,6 +225,24 @@ __device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, u
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
+}
+
+// (d0, d1) = (a0, a1) * (b0, b1) + (c0, c1) in one packed instruction.
+__device__ __forceinline__ void ffma2(float &d0, float &d1, float a0, float a1, float b0, float b1, float c0,
+                                      float c1) {
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+// (d0, d1) += (a0, a1) in one packed instruction.
+__device__ __forceinline__ void fadd2_acc(float &d0, float &d1, float a0, float a1) {
+  asm("{\n\t.reg .b64 ra, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rd, {%0, %1};\n\t"
+      "add.f32x2 rd, rd, ra;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "+f"(d0), "+f"(d1)
+      : "f"(a0), "f"(a1));
 }
 
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
@@ -232,7 +263,8 @@ __device__ __forceinline__ void softmax_role(const AttnArgs &a, int tile, int h,
   const uint32_t s_col = tile * kBlockN;
   const uint32_t o_col = kTmemO + tile * 128;
   const uint32_t bar_s = smem_u32(&bars[kBarSFull0 + tile]);
-  const uint32_t bar_p = smem_u32(&bars[kBarPFull0 + tile]);
+  const uint32_t bar_plo = smem_u32(&bars[kBarPLo0 + tile]);
+  const uint32_t bar_phi = smem_u32(&bars[kBarPHi0 + tile]);
   const uint32_t bar_o = smem_u32(&bars[kBarODone0 + tile]);
   const float c = a.scale_log2;
   float m_used = -INFINITY, l = 0.f;
@@ -273,37 +305,40 @@ __device__ __forceinline__ void softmax_role(const AttnArgs &a, int tile, int h,
       m_used = m_new;
     }
     const float mb = (m_used == -INFINITY) ? 0.f : m_used;
-    uint32_t pk[kBlockN / 2];
-    float rs8[8];
+    // P = exp2(s*c - m) as bf16 pairs over the first 64 columns of this tile's S region (the A
+    // operand of PV), written and published in two halves so PV can start on keys 0..63.
+    float rsa = 0.f, rsb = 0.f, rsc = 0.f, rsd = 0.f;
 #pragma unroll
-    for (int u = 0; u < 8; ++u) rs8[u] = 0.f;
+    for (int half = 0; half < 2; ++half) {
+      uint32_t pk[32];
 #pragma unroll
-    for (int k = 0; k < kBlockN / 2; ++k) {
-      const float p0 = ex2_approx(fmaf(sv[2 * k], c, -mb));
-      const float p1 = ex2_approx(fmaf(sv[2 * k + 1], c, -mb));
-      rs8[k & 7] += p0 + p1;
-      pk[k] = pack_bf16x2(p0, p1);
-    }
-    const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
-    l = l * alpha + rs;
-    // PV of the previous tile is complete here: S of this tile was committed after it.
-    if (j >= 1 && __any_sync(0xffffffffu, need)) {
-#pragma unroll
-      for (int q4 = 0; q4 < D / 32; ++q4) {
-        float o[32];
-        tmem_ld32(tl + o_col + q4 * 32, o);
-        tmem_wait_ld();
-#pragma unroll
-        for (int x = 0; x < 32; ++x) o[x] *= alpha;
-        tmem_st32(tl + o_col + q4 * 32, o);
+      for (int k = 0; k < 32; ++k) {
+        const int e = half * 64 + 2 * k;
+        float x0, x1;
+        ffma2(x0, x1, sv[e], sv[e + 1], c, c, -mb, -mb);
+        const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+        if (k & 1) fadd2_acc(rsc, rsd, p0, p1); else fadd2_acc(rsa, rsb, p0, p1);
+        pk[k] = pack_bf16x2(p0, p1);
       }
+      // O must be rescaled before the first PV of this tile accumulates into it; PV of the
+      // previous tile is complete here because S of this tile was committed after it.
+      if (half == 0 && j >= 1 && __any_sync(0xffffffffu, need)) {
+#pragma unroll
+        for (int q4 = 0; q4 < D / 32; ++q4) {
+          float o[32];
+          tmem_ld32(tl + o_col + q4 * 32, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int x = 0; x < 32; ++x) o[x] *= alpha;
+          tmem_st32(tl + o_col + q4 * 32, o);
+        }
+      }
+      tmem_st32(tl + s_col + half * 32, reinterpret_cast<const float *>(pk));
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(half ? bar_phi : bar_plo);
     }
-    // P (bf16 pairs) over the first 64 columns of this tile's S region: the A operand of PV.
-    tmem_st32(tl + s_col, reinterpret_cast<const float *>(pk));
-    tmem_st32(tl + s_col + 32, reinterpret_cast<const float *>(pk + 32));
-    tmem_wait_st();
-    tc_fence_before();
-    mbar_arrive(bar_p);
+    l = l * alpha + ((rsa + rsb) + (rsc + rsd));
   }
   if (ok && mbar_wait(bar_o, 0, abort_flag, a.status)) {
     tc_fence_after();
@@ -374,7 +409,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(kBarSFull0 + i), 1);
-      mbar_init(bar(kBarPFull0 + i), kBlockM);
+      mbar_init(bar(kBarPLo0 + i), kBlockM);
+      mbar_init(bar(kBarPHi0 + i), kBlockM);
       mbar_init(bar(kBarODone0 + i), 1);
     }
     mbar_init(bar(kBarFinal), 1);
@@ -391,7 +427,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   const uint32_t tmem = s_tmem;
   volatile int *abort_flag = &s_abort;
 
-  if (warp == kWarpTma) {
+  if (warp < 8) {
+    // ------------------------------------------------------------ softmax + epilogue
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
+    const int tile = warp >> 2;
+    if (tile == 0 || two) softmax_role<D>(a, tile, h0 + tile, T, Tp, P, c0, row0, rows_valid, tmem, bars, abort_flag);
+  } else if (warp == kWarpTma) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsControl));
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       tma_prefetch_desc(&a.tm_q);
@@ -456,6 +498,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     }
   } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA issuer
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsControl));
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(kBlockM, kBlockN, false, false);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(kBlockM, D, false, true);
@@ -473,12 +516,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                        idesc_qk, kk > 0 ? 1u : 0u);
         }
       };
-      auto issue_pv = [&](int tile, int32_t j) {
+      auto issue_pv_half = [&](int tile, int32_t j, int half) {
         const uint32_t vb = slot_addr((2 * j + 1) % kStages);
 #pragma unroll
-        for (int kk = 0; kk < kBlockN / 16; ++kk)
+        for (int k4 = 0; k4 < kBlockN / 32; ++k4) {
+          const int kk = half * (kBlockN / 32) + k4;
           umma_bf16_ts(tmem + kTmemO + tile * 128, tmem + tile * kBlockN + kk * 8,
                        sdesc_sw128(vb + kk * 2048, L::kHalfBytes, 1024), idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+        }
       };
       bool ok = mbar_wait(bar(kBarQFull), 0, abort_flag, a.status) && wait_slot(0);
       if (ok) {
@@ -492,11 +537,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       for (int32_t j = 0; ok && j < T; ++j) {
         const bool more = j + 1 < T;
         for (int t = 0; t < ntiles; ++t) {
-          ok = mbar_wait(bar(kBarPFull0 + t), j & 1, abort_flag, a.status);
+          ok = mbar_wait(bar(kBarPLo0 + t), j & 1, abort_flag, a.status);
           if (ok && t == 0) ok = wait_slot(2 * j + 1);  // V_j
           if (!ok) break;
           tc_fence_after();
-          issue_pv(t, j);
+          issue_pv_half(t, j, 0);
+          if (!(ok = mbar_wait(bar(kBarPHi0 + t), j & 1, abort_flag, a.status))) break;
+          tc_fence_after();
+          issue_pv_half(t, j, 1);
           if (!more) umma_commit(bar(kBarODone0 + t));
           if (t == ntiles - 1) umma_commit(bar(kBarSlotEmpty0 + (2 * j + 1) % kStages));
           if (more) {
@@ -513,10 +561,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       while (!mbar_try_wait(bar(kBarFinal), 0) && globaltimer_ns() - t0 < kWaitLimitNs) {
       }
     }
-  } else if (warp < 4 || two) {
-    // ------------------------------------------------------------ softmax + epilogue
-    const int tile = warp >> 2;
-    softmax_role<D>(a, tile, h0 + tile, T, Tp, P, c0, row0, rows_valid, tmem, bars, abort_flag);
+  } else {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsControl));
   }
   tc_fence_before();
   __syncthreads();
@@ -533,8 +579,13 @@ cudaError_t launch_attention(const AttnArgs &args, int grid, cudaStream_t stream
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)L::kDynamic);
+    // The in-kernel register split may only hand out what the launch reserved; refuse to
+    // launch a build whose register count would leave setmaxnreg.inc short.
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, attn_fwd_kernel<D>);
+    if (e != cudaSuccess) return e;
+    if ((uint32_t)fa.numRegs * kThreads < 2 * 128 * kRegsSoftmax + 128 * kRegsControl) return cudaErrorInvalidValue;
+    e = cudaFuncSetAttribute(attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::kDynamic);
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }

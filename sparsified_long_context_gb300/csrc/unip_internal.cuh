@@ -6,7 +6,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/unip.h"
+#include "unip.h"
 
 namespace unip {
 

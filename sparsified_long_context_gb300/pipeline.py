@@ -126,6 +126,6 @@ def run_step(di: DeviceInputs, bufs: StepBuffers, stream=None):
 
 
 def kernels_per_step(has_hidden: bool = True) -> int:
-    """libunip kernels one run_step launches (the Top-p call also enqueues one 4-byte memset)."""
+    """libunip kernels one run_step launches (up to 12000 segments)."""
     # attention: plan + attention; importance: plan + score + norm; Top-p: select + index; gather: 1
     return 2 + 3 + 2 + (1 if has_hidden else 0)
