@@ -19,10 +19,11 @@
 //     is either 128 prefix keys (read page by page through the block table)
 //     or 128 of the segment's own keys; only the last prefix tile and the
 //     diagonal own tile need a mask, every fully masked tile is skipped.
-//   * Warp roles: warps 0-3 and 4-7 softmax + epilogue of the two query tiles
-//     (one query row per thread, i.e. one TMEM lane each), warp 8 TMA
-//     producer, warp 9 tcgen05 issuer; setmaxnreg moves registers from the
-//     control warpgroup to the softmax warpgroups.
+//   * Warp roles: 8 softmax warps per query tile, each owning 16 TMEM lanes
+//     (16 query rows, all 128 columns) read with the 16x256b shape, so that
+//     4 threads share a row and its maximum and sum need only quad shuffles.
+//     Warp 16 is the TMA producer, warp 17 the tcgen05 issuer; setmaxnreg
+//     moves registers from this control warpgroup to the softmax warpgroups.
 //   * K and V tiles stream through one 4-slot ring of 128-byte-swizzled TMA
 //     tiles; a slot is released by a tcgen05.commit after its last MMA.
 //   * TMEM (512 columns): S of each query tile (128 fp32 columns) and O of
@@ -34,7 +35,8 @@
 //   * Online softmax in base 2 with a lazy rescale: the running maximum is
 //     only moved (and O rescaled in TMEM) when a row's maximum grows by more
 //     than 8 (log2 units), which bounds P by 2^8; the final O / l is exact.
-//     P is published in two halves so PV starts on keys 0..63 early.
+//     Spreading each tile over 8 warps halves the softmax latency that sits
+//     between a tile's QK^T completing and its PV being issued.
 #include <cuda_bf16.h>
 
 #include <cstring>
@@ -186,13 +188,17 @@ __global__ void __launch_bounds__(kPlanThreads) attn_plan_kernel(const int32_t *
 // Attention kernel
 // ---------------------------------------------------------------------------
 constexpr int kStages = 4;        // K/V ring slots (each holds one K or one V tile)
-constexpr int kThreads = 384;     // 2 softmax warpgroups + one warpgroup for the TMA and MMA warps
-// Register split after launch (384 threads x 168): softmax warpgroups grow to 216, the
-// TMA/MMA warpgroup shrinks to 72; 2 x 216 + 72 = 3 x 168, the launch's own budget.
-constexpr uint32_t kRegsSoftmax = 216;
-constexpr uint32_t kRegsControl = 72;
-constexpr int kWarpTma = 8;
-constexpr int kWarpMma = 9;
+// 4 softmax warpgroups (8 warps per query tile, 16 rows each) + one control
+// warpgroup (TMA warp, MMA warp, 2 idle warps).
+constexpr int kThreads = 640;
+// Register split after launch (640 threads x 96): softmax warpgroups grow to 104, the
+// control warpgroup shrinks to 56; 4 x 128 x 104 + 128 x 56 <= 640 x 96, the launch's budget.
+constexpr uint32_t kRegsLaunch = 96;
+constexpr uint32_t kRegsSoftmax = 104;
+constexpr uint32_t kRegsControl = 56;
+static_assert(4 * 128 * kRegsSoftmax + 128 * kRegsControl <= kThreads * kRegsLaunch, "register split over budget");
+constexpr int kWarpTma = 16;
+constexpr int kWarpMma = 17;
 
 template <int D>
 struct SmemLayout {
@@ -209,12 +215,12 @@ enum BarId {
   kBarQFull = 0,
   kBarSlotFull0 = 1,                   // + slot
   kBarSlotEmpty0 = 1 + kStages,        // + slot
-  kBarSFull0 = 1 + 2 * kStages,        // + tile
-  kBarPLo0 = 3 + 2 * kStages,          // + tile: P of keys 0..63 in TMEM (and O rescaled)
-  kBarPHi0 = 5 + 2 * kStages,          // + tile: P of keys 64..127 in TMEM
-  kBarODone0 = 7 + 2 * kStages,        // + tile
-  kBarFinal = 9 + 2 * kStages,
-  kNumBars = 10 + 2 * kStages
+  kBarSFull0 = 1 + 2 * kStages,        // + tile: S in TMEM
+  kBarPFull0 = 3 + 2 * kStages,        // + tile: P in TMEM and O rescaled (both column halves)
+  kBarODone0 = 5 + 2 * kStages,        // + tile: last PV done
+  kBarXchg0 = 7 + 2 * kStages,         // + tile: final row statistics in shared memory
+  kBarFinal = 11 + 2 * kStages,
+  kNumBars = 12 + 2 * kStages
 };
 
 __device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
@@ -251,121 +257,161 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return r;
 }
 
-// Softmax, P write-back and (when needed) O rescale for one query tile.
-// Runs on one warpgroup; thread r owns query row r = TMEM lane r.
+// Softmax, P write-back, O rescale and epilogue of one query tile, run by the
+// tile's 8 warps.  Warp (q, g) with q = warp % 4 and g = (warp / 4) % 2 owns the
+// 16 TMEM lanes 32q + 16g .. 32q + 16g + 15 (16 query rows, all 128 columns)
+// and reads them with the 16x256b shape: each thread holds two rows (r, r + 8)
+// and two adjacent columns of every 8-column chunk, so a row's maximum and sum
+// are completed with two shuffles inside a 4-thread quad.  P goes back into
+// the first 64 columns of the tile's S region with the 16x128b shape, in the
+// packed layout the PV MMA reads as its A operand.
+struct RowStats {
+  float m[2][128];  // [tile][row] final running maximum (log2 domain)
+  float l[2][128];  // [tile][row] final row sum
+};
+
 template <int D>
-__device__ __forceinline__ void softmax_role(const AttnArgs &a, int tile, int h, int32_t T, int32_t Tp, int32_t P,
-                                             int32_t c0, int32_t row0, int32_t rows_valid, uint32_t tmem,
-                                             uint64_t *bars, volatile int *abort_flag) {
-  const int warp = threadIdx.x >> 5;
-  const int row = threadIdx.x & 127;
-  const uint32_t tl = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+__device__ __forceinline__ void softmax_tile_role(const AttnArgs &a, int tile, int h, int32_t T, int32_t Tp,
+                                                  int32_t P, int32_t c0, int32_t row0, int32_t rows_valid,
+                                                  uint32_t tmem, uint64_t *bars, RowStats &rs,
+                                                  volatile int *abort_flag) {
+  const int wt = (threadIdx.x >> 5) & 7;
+  const int lane = threadIdx.x & 31;
+  const int q = wt & 3, g = wt >> 2;
+  const uint32_t lane_base = 32 * q + 16 * g;
+  const int R0 = lane_base + (lane >> 2), R1 = R0 + 8;  // tile rows held by this thread
+  const int cq = 2 * (lane & 3);                         // first column of this thread in a chunk
+  const uint32_t tw = tmem + (lane_base << 16);
   const uint32_t s_col = tile * kBlockN;
   const uint32_t o_col = kTmemO + tile * 128;
   const uint32_t bar_s = smem_u32(&bars[kBarSFull0 + tile]);
-  const uint32_t bar_plo = smem_u32(&bars[kBarPLo0 + tile]);
-  const uint32_t bar_phi = smem_u32(&bars[kBarPHi0 + tile]);
+  const uint32_t bar_p = smem_u32(&bars[kBarPFull0 + tile]);
   const uint32_t bar_o = smem_u32(&bars[kBarODone0 + tile]);
+  const uint32_t bar_x = smem_u32(&bars[kBarXchg0 + tile]);
   const float c = a.scale_log2;
-  float m_used = -INFINITY, l = 0.f;
-  bool ok = true;
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
   for (int32_t j = 0; j < T; ++j) {
-    if (!mbar_wait(bar_s, j & 1, abort_flag, a.status)) { ok = false; break; }
+    if (!mbar_wait(bar_s, j & 1, abort_flag, a.status)) return;
     tc_fence_after();
-    float sv[kBlockN];
-#pragma unroll
-    for (int q4 = 0; q4 < kBlockN / 32; ++q4) tmem_ld32(tl + s_col + q4 * 32, sv + q4 * 32);
+    float sv[64];  // sv[4k + {0,1}]: row R0, columns 8k + cq + {0,1}; sv[4k + {2,3}]: row R1
+    tmem_ld_16x256b_x8(tw + s_col, sv);
+    tmem_ld_16x256b_x8(tw + s_col + 64, sv + 32);
     tmem_wait_ld();
     if (j < Tp) {
       if (j == Tp - 1) {
         const int lim = P - j * kBlockN;  // keys at or past the prefix end are not cached tokens
 #pragma unroll
-        for (int k = 0; k < kBlockN; ++k)
-          if (k >= lim) sv[k] = -INFINITY;
+        for (int k = 0; k < 16; ++k) {
+          const int col = 8 * k + cq;
+          if (col >= lim) { sv[4 * k] = -INFINITY; sv[4 * k + 2] = -INFINITY; }
+          if (col + 1 >= lim) { sv[4 * k + 1] = -INFINITY; sv[4 * k + 3] = -INFINITY; }
+        }
       }
     } else if (j == T - 1) {
 #pragma unroll
-      for (int k = 0; k < kBlockN; ++k)
-        if (k > row) sv[k] = -INFINITY;  // causal diagonal tile
-    }
-    float mx8[8];
-#pragma unroll
-    for (int u = 0; u < 8; ++u) mx8[u] = fmaxf(sv[u], sv[u + 8]);
-#pragma unroll
-    for (int k = 16; k < kBlockN; k += 16) {
-#pragma unroll
-      for (int u = 0; u < 8; ++u) mx8[u] = fmax3(mx8[u], sv[k + u], sv[k + u + 8]);
-    }
-    const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
-    const float m_new = fmaxf(m_used, mx * c);
-    const bool need = m_new > m_used + kRescaleThreshold;
-    float alpha = 1.f;
-    if (need) {
-      alpha = ex2_approx(m_used - m_new);
-      m_used = m_new;
-    }
-    const float mb = (m_used == -INFINITY) ? 0.f : m_used;
-    // P = exp2(s*c - m) as bf16 pairs over the first 64 columns of this tile's S region (the A
-    // operand of PV), written and published in two halves so PV can start on keys 0..63.
-    float rsa = 0.f, rsb = 0.f, rsc = 0.f, rsd = 0.f;
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      uint32_t pk[32];
-#pragma unroll
-      for (int k = 0; k < 32; ++k) {
-        const int e = half * 64 + 2 * k;
-        float x0, x1;
-        ffma2(x0, x1, sv[e], sv[e + 1], c, c, -mb, -mb);
-        const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-        if (k & 1) fadd2_acc(rsc, rsd, p0, p1); else fadd2_acc(rsa, rsb, p0, p1);
-        pk[k] = pack_bf16x2(p0, p1);
+      for (int k = 0; k < 16; ++k) {  // causal diagonal tile: key column <= query row
+        const int col = 8 * k + cq;
+        if (col > R0) sv[4 * k] = -INFINITY;
+        if (col + 1 > R0) sv[4 * k + 1] = -INFINITY;
+        if (col > R1) sv[4 * k + 2] = -INFINITY;
+        if (col + 1 > R1) sv[4 * k + 3] = -INFINITY;
       }
-      // O must be rescaled before the first PV of this tile accumulates into it; PV of the
-      // previous tile is complete here because S of this tile was committed after it.
-      if (half == 0 && j >= 1 && __any_sync(0xffffffffu, need)) {
+    }
+    float a0 = fmaxf(sv[0], sv[1]), a1 = fmaxf(sv[4], sv[5]);
+    float b0 = fmaxf(sv[2], sv[3]), b1 = fmaxf(sv[6], sv[7]);
 #pragma unroll
-        for (int q4 = 0; q4 < D / 32; ++q4) {
-          float o[32];
-          tmem_ld32(tl + o_col + q4 * 32, o);
-          tmem_wait_ld();
+    for (int k = 2; k < 16; k += 2) {
+      a0 = fmax3(a0, sv[4 * k], sv[4 * k + 1]);
+      a1 = fmax3(a1, sv[4 * k + 4], sv[4 * k + 5]);
+      b0 = fmax3(b0, sv[4 * k + 2], sv[4 * k + 3]);
+      b1 = fmax3(b1, sv[4 * k + 6], sv[4 * k + 7]);
+    }
+    float mx0 = fmaxf(a0, a1), mx1 = fmaxf(b0, b1);
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+    const float n0 = fmaxf(m0, mx0 * c), n1 = fmaxf(m1, mx1 * c);
+    const bool need0 = n0 > m0 + kRescaleThreshold, need1 = n1 > m1 + kRescaleThreshold;
+    float al0 = 1.f, al1 = 1.f;
+    if (need0) { al0 = ex2_approx(m0 - n0); m0 = n0; }
+    if (need1) { al1 = ex2_approx(m1 - n1); m1 = n1; }
+    const float mb0 = (m0 == -INFINITY) ? 0.f : m0, mb1 = (m1 == -INFINITY) ? 0.f : m1;
+    float r00 = 0.f, r01 = 0.f, r10 = 0.f, r11 = 0.f;
+    uint32_t pk[32];  // pk[2k]: row R0, P column 4k + lane%4; pk[2k+1]: row R1
 #pragma unroll
-          for (int x = 0; x < 32; ++x) o[x] *= alpha;
-          tmem_st32(tl + o_col + q4 * 32, o);
+    for (int k = 0; k < 16; ++k) {
+      float x0, x1, y0, y1;
+      ffma2(x0, x1, sv[4 * k], sv[4 * k + 1], c, c, -mb0, -mb0);
+      ffma2(y0, y1, sv[4 * k + 2], sv[4 * k + 3], c, c, -mb1, -mb1);
+      const float p0 = ex2_approx(x0), p1 = ex2_approx(x1), p2 = ex2_approx(y0), p3 = ex2_approx(y1);
+      fadd2_acc(r00, r01, p0, p1);
+      fadd2_acc(r10, r11, p2, p3);
+      pk[2 * k] = pack_bf16x2(p0, p1);
+      pk[2 * k + 1] = pack_bf16x2(p2, p3);
+    }
+    l0 = l0 * al0 + (r00 + r01);
+    l1 = l1 * al1 + (r10 + r11);
+    // O is rescaled before the PV of this tile accumulates into it; PV of the previous tile is
+    // complete here because S of this tile was committed after it.
+    if (j >= 1 && __any_sync(0xffffffffu, need0 || need1)) {
+#pragma unroll 1
+      for (int part = 0; part < D / 32; ++part) {
+        float o[16];
+        tmem_ld_16x256b_x4(tw + o_col + part * 32, o);
+        tmem_wait_ld();
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          o[4 * k] *= al0; o[4 * k + 1] *= al0; o[4 * k + 2] *= al1; o[4 * k + 3] *= al1;
         }
-      }
-      tmem_st32(tl + s_col + half * 32, reinterpret_cast<const float *>(pk));
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(half ? bar_phi : bar_plo);
-    }
-    l = l * alpha + ((rsa + rsb) + (rsc + rsd));
-  }
-  if (ok && mbar_wait(bar_o, 0, abort_flag, a.status)) {
-    tc_fence_after();
-    const float inv_l = 1.f / l;
-    const int32_t t = c0 + row0 + row;
-    const bool store = row < rows_valid;
-    __nv_bfloat16 *orow = a.out + ((int64_t)t * a.Hq + h) * D;
-#pragma unroll
-    for (int q4 = 0; q4 < D / 32; ++q4) {
-      float o[32];
-      tmem_ld32(tl + o_col + q4 * 32, o);
-      tmem_wait_ld();
-      if (store) {
-        uint4 *dst = reinterpret_cast<uint4 *>(orow + q4 * 32);
-#pragma unroll
-        for (int v4 = 0; v4 < 4; ++v4) {
-          uint4 w;
-          w.x = pack_bf16x2(o[v4 * 8 + 0] * inv_l, o[v4 * 8 + 1] * inv_l);
-          w.y = pack_bf16x2(o[v4 * 8 + 2] * inv_l, o[v4 * 8 + 3] * inv_l);
-          w.z = pack_bf16x2(o[v4 * 8 + 4] * inv_l, o[v4 * 8 + 5] * inv_l);
-          w.w = pack_bf16x2(o[v4 * 8 + 6] * inv_l, o[v4 * 8 + 7] * inv_l);
-          dst[v4] = w;
-        }
+        tmem_st_16x256b_x4(tw + o_col + part * 32, o);
       }
     }
-    if (store && a.lse) a.lse[(int64_t)h * a.N + t] = (m_used + log2f(l)) * kLn2;
+    tmem_st_16x128b_x16(tw + s_col, pk);
+    tmem_wait_st();
+    tc_fence_before();
+    mbar_arrive(bar_p);
   }
+  // Row sums over the quad; row statistics to shared memory for the epilogue's row-per-thread layout.
+  l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+  l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+  l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+  l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+  if ((lane & 3) == 0) {
+    rs.m[tile][R0] = m0; rs.l[tile][R0] = l0;
+    rs.m[tile][R1] = m1; rs.l[tile][R1] = l1;
+  }
+  mbar_arrive(bar_x);
+  if (!mbar_wait(bar_x, 0, abort_flag, a.status)) return;
+  if (!mbar_wait(bar_o, 0, abort_flag, a.status)) return;
+  tc_fence_after();
+  // Epilogue with the 32x32b shape: warp (q, g) stores rows 32q .. 32q + 31, columns [g*D/2, (g+1)*D/2).
+  constexpr int kOCols = D / 2;
+  const int row = 32 * q + lane;
+  const float inv_l = 1.f / rs.l[tile][row];
+  const int32_t t = c0 + row0 + row;
+  const bool store = row < rows_valid;
+  const uint32_t tl = tmem + (static_cast<uint32_t>(32 * q) << 16);
+  __nv_bfloat16 *orow = a.out + ((int64_t)t * a.Hq + h) * D + g * kOCols;
+#pragma unroll
+  for (int q4 = 0; q4 < kOCols / 32; ++q4) {
+    float o[32];
+    tmem_ld32(tl + o_col + g * kOCols + q4 * 32, o);
+    tmem_wait_ld();
+    if (store) {
+      uint4 *dst = reinterpret_cast<uint4 *>(orow + q4 * 32);
+#pragma unroll
+      for (int v4 = 0; v4 < 4; ++v4) {
+        uint4 w;
+        w.x = pack_bf16x2(o[v4 * 8 + 0] * inv_l, o[v4 * 8 + 1] * inv_l);
+        w.y = pack_bf16x2(o[v4 * 8 + 2] * inv_l, o[v4 * 8 + 3] * inv_l);
+        w.z = pack_bf16x2(o[v4 * 8 + 4] * inv_l, o[v4 * 8 + 5] * inv_l);
+        w.w = pack_bf16x2(o[v4 * 8 + 6] * inv_l, o[v4 * 8 + 7] * inv_l);
+        dst[v4] = w;
+      }
+    }
+  }
+  if (g == 0 && store && a.lse) a.lse[(int64_t)h * a.N + t] = (rs.m[tile][row] + log2f(rs.l[tile][row])) * kLn2;
 }
 
 // One CTA = one 128-row query tile of a segment for the query heads h0 (and
@@ -378,6 +424,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   __shared__ __align__(8) uint64_t bars[kNumBars];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
+  __shared__ RowStats row_stats;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -409,10 +456,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(kBarSFull0 + i), 1);
-      mbar_init(bar(kBarPLo0 + i), kBlockM);
-      mbar_init(bar(kBarPHi0 + i), kBlockM);
+      mbar_init(bar(kBarPFull0 + i), 2 * kBlockM);
       mbar_init(bar(kBarODone0 + i), 1);
     }
+    for (int i = 0; i < 2; ++i) mbar_init(bar(kBarXchg0 + i), 2 * kBlockM);
     mbar_init(bar(kBarFinal), 1);
     s_abort = 0;
     fence_mbar_init();
@@ -427,11 +474,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   const uint32_t tmem = s_tmem;
   volatile int *abort_flag = &s_abort;
 
-  if (warp < 8) {
+  if (warp < 16) {
     // ------------------------------------------------------------ softmax + epilogue
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
-    const int tile = warp >> 2;
-    if (tile == 0 || two) softmax_role<D>(a, tile, h0 + tile, T, Tp, P, c0, row0, rows_valid, tmem, bars, abort_flag);
+    const int tile = warp >> 3;
+    if (tile == 0 || two)
+      softmax_tile_role<D>(a, tile, h0 + tile, T, Tp, P, c0, row0, rows_valid, tmem, bars, row_stats, abort_flag);
   } else if (warp == kWarpTma) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsControl));
     // ------------------------------------------------------------ TMA producer
@@ -516,14 +564,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                        idesc_qk, kk > 0 ? 1u : 0u);
         }
       };
-      auto issue_pv_half = [&](int tile, int32_t j, int half) {
+      auto issue_pv = [&](int tile, int32_t j) {
         const uint32_t vb = slot_addr((2 * j + 1) % kStages);
 #pragma unroll
-        for (int k4 = 0; k4 < kBlockN / 32; ++k4) {
-          const int kk = half * (kBlockN / 32) + k4;
+        for (int kk = 0; kk < kBlockN / 16; ++kk)
           umma_bf16_ts(tmem + kTmemO + tile * 128, tmem + tile * kBlockN + kk * 8,
                        sdesc_sw128(vb + kk * 2048, L::kHalfBytes, 1024), idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
-        }
       };
       bool ok = mbar_wait(bar(kBarQFull), 0, abort_flag, a.status) && wait_slot(0);
       if (ok) {
@@ -537,14 +583,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       for (int32_t j = 0; ok && j < T; ++j) {
         const bool more = j + 1 < T;
         for (int t = 0; t < ntiles; ++t) {
-          ok = mbar_wait(bar(kBarPLo0 + t), j & 1, abort_flag, a.status);
+          ok = mbar_wait(bar(kBarPFull0 + t), j & 1, abort_flag, a.status);
           if (ok && t == 0) ok = wait_slot(2 * j + 1);  // V_j
           if (!ok) break;
           tc_fence_after();
-          issue_pv_half(t, j, 0);
-          if (!(ok = mbar_wait(bar(kBarPHi0 + t), j & 1, abort_flag, a.status))) break;
-          tc_fence_after();
-          issue_pv_half(t, j, 1);
+          issue_pv(t, j);
           if (!more) umma_commit(bar(kBarODone0 + t));
           if (t == ntiles - 1) umma_commit(bar(kBarSlotEmpty0 + (2 * j + 1) % kStages));
           if (more) {
@@ -584,7 +627,7 @@ cudaError_t launch_attention(const AttnArgs &args, int grid, cudaStream_t stream
     cudaFuncAttributes fa;
     cudaError_t e = cudaFuncGetAttributes(&fa, attn_fwd_kernel<D>);
     if (e != cudaSuccess) return e;
-    if ((uint32_t)fa.numRegs * kThreads < 2 * 128 * kRegsSoftmax + 128 * kRegsControl) return cudaErrorInvalidValue;
+    if ((uint32_t)fa.numRegs * kThreads < 4 * 128 * kRegsSoftmax + 128 * kRegsControl) return cudaErrorInvalidValue;
     e = cudaFuncSetAttribute(attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::kDynamic);
     if (e != cudaSuccess) return e;
     configured[dev] = true;
