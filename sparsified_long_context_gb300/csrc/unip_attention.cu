@@ -22,8 +22,7 @@
 //   * Warp roles: 8 softmax warps per query tile, each owning 16 TMEM lanes
 //     (16 query rows, all 128 columns) read with the 16x256b shape, so that
 //     4 threads share a row and its maximum and sum need only quad shuffles.
-//     Warp 16 is the TMA producer, warp 17 the tcgen05 issuer; setmaxnreg
-//     moves registers from this control warpgroup to the softmax warpgroups.
+//     Warp 16 is the TMA producer, warp 17 the tcgen05 issuer.
 //   * K and V tiles stream through one 4-slot ring of 128-byte-swizzled TMA
 //     tiles; a slot is released by a tcgen05.commit after its last MMA.
 //   * TMEM (512 columns): S of each query tile (128 fp32 columns) and O of
@@ -189,14 +188,8 @@ __global__ void __launch_bounds__(kPlanThreads) attn_plan_kernel(const int32_t *
 // ---------------------------------------------------------------------------
 constexpr int kStages = 4;        // K/V ring slots (each holds one K or one V tile)
 // 4 softmax warpgroups (8 warps per query tile, 16 rows each) + one control
-// warpgroup (TMA warp, MMA warp, 2 idle warps).
+// warpgroup (TMA warp, MMA warp, 2 idle warps); 96 registers per thread.
 constexpr int kThreads = 640;
-// Register split after launch (640 threads x 96): softmax warpgroups grow to 104, the
-// control warpgroup shrinks to 56; 4 x 128 x 104 + 128 x 56 <= 640 x 96, the launch's budget.
-constexpr uint32_t kRegsLaunch = 96;
-constexpr uint32_t kRegsSoftmax = 104;
-constexpr uint32_t kRegsControl = 56;
-static_assert(4 * 128 * kRegsSoftmax + 128 * kRegsControl <= kThreads * kRegsLaunch, "register split over budget");
 constexpr int kWarpTma = 16;
 constexpr int kWarpMma = 17;
 
@@ -338,20 +331,6 @@ __device__ __forceinline__ void softmax_tile_role(const AttnArgs &a, int tile, i
     if (need1) { al1 = ex2_approx(m1 - n1); m1 = n1; }
     const float mb0 = (m0 == -INFINITY) ? 0.f : m0, mb1 = (m1 == -INFINITY) ? 0.f : m1;
     float r00 = 0.f, r01 = 0.f, r10 = 0.f, r11 = 0.f;
-    uint32_t pk[32];  // pk[2k]: row R0, P column 4k + lane%4; pk[2k+1]: row R1
-#pragma unroll
-    for (int k = 0; k < 16; ++k) {
-      float x0, x1, y0, y1;
-      ffma2(x0, x1, sv[4 * k], sv[4 * k + 1], c, c, -mb0, -mb0);
-      ffma2(y0, y1, sv[4 * k + 2], sv[4 * k + 3], c, c, -mb1, -mb1);
-      const float p0 = ex2_approx(x0), p1 = ex2_approx(x1), p2 = ex2_approx(y0), p3 = ex2_approx(y1);
-      fadd2_acc(r00, r01, p0, p1);
-      fadd2_acc(r10, r11, p2, p3);
-      pk[2 * k] = pack_bf16x2(p0, p1);
-      pk[2 * k + 1] = pack_bf16x2(p2, p3);
-    }
-    l0 = l0 * al0 + (r00 + r01);
-    l1 = l1 * al1 + (r10 + r11);
     // O is rescaled before the PV of this tile accumulates into it; PV of the previous tile is
     // complete here because S of this tile was committed after it.
     if (j >= 1 && __any_sync(0xffffffffu, need0 || need1)) {
@@ -367,7 +346,26 @@ __device__ __forceinline__ void softmax_tile_role(const AttnArgs &a, int tile, i
         tmem_st_16x256b_x4(tw + o_col + part * 32, o);
       }
     }
-    tmem_st_16x128b_x16(tw + s_col, pk);
+    // P in two halves of 64 keys; all of S is already in registers, so P may overwrite it.
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+      uint32_t pk[16];  // pk[2k]: row R0, P column 4(8hf+k) + lane%4; pk[2k+1]: row R1
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int e = 4 * (8 * hf + k);
+        float x0, x1, y0, y1;
+        ffma2(x0, x1, sv[e], sv[e + 1], c, c, -mb0, -mb0);
+        ffma2(y0, y1, sv[e + 2], sv[e + 3], c, c, -mb1, -mb1);
+        const float p0 = ex2_approx(x0), p1 = ex2_approx(x1), p2 = ex2_approx(y0), p3 = ex2_approx(y1);
+        fadd2_acc(r00, r01, p0, p1);
+        fadd2_acc(r10, r11, p2, p3);
+        pk[2 * k] = pack_bf16x2(p0, p1);
+        pk[2 * k + 1] = pack_bf16x2(p2, p3);
+      }
+      tmem_st_16x128b_x8(tw + s_col + 32 * hf, pk);
+    }
+    l0 = l0 * al0 + (r00 + r01);
+    l1 = l1 * al1 + (r10 + r11);
     tmem_wait_st();
     tc_fence_before();
     mbar_arrive(bar_p);
@@ -476,12 +474,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
 
   if (warp < 16) {
     // ------------------------------------------------------------ softmax + epilogue
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
     const int tile = warp >> 3;
     if (tile == 0 || two)
       softmax_tile_role<D>(a, tile, h0 + tile, T, Tp, P, c0, row0, rows_valid, tmem, bars, row_stats, abort_flag);
   } else if (warp == kWarpTma) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsControl));
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       tma_prefetch_desc(&a.tm_q);
@@ -546,56 +542,74 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     }
   } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA issuer
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsControl));
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(kBlockM, kBlockN, false, false);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(kBlockM, D, false, true);
-      const int ntiles = two ? 2 : 1;
-      auto wait_slot = [&](int32_t ld) {
-        return mbar_wait(bar(kBarSlotFull0 + ld % kStages), (ld / kStages) & 1, abort_flag, a.status);
-      };
-      auto issue_qk = [&](int tile, int32_t j) {
-        const uint32_t kb = slot_addr((2 * j) % kStages);
-        const uint32_t qb = sbase + (tile ? L::kQ1 : L::kQ0);
+      // Shared-memory descriptors are built once; a K step or another slot only adds an offset
+      // (in 16-byte units) to the start-address field.
+      const uint64_t dq0 = sdesc_sw128(sbase + L::kQ0, 16, 1024);
+      const uint64_t dq1 = sdesc_sw128(sbase + L::kQ1, 16, 1024);
+      const uint64_t dk = sdesc_sw128(sbase + L::kRing, 16, 1024);
+      const uint64_t dv = sdesc_sw128(sbase + L::kRing, L::kHalfBytes, 1024);
+      const uint32_t d_s0 = tmem, d_s1 = tmem + kBlockN;
+      const uint32_t d_o0 = tmem + kTmemO, d_o1 = tmem + kTmemO + 128;
+      // K_j sits in slot 2*(j&1), V_j in slot 2*(j&1)+1; both complete phase (j>>1)&1.
+      auto slot_desc = [&](uint64_t d, int slot) { return d + ((uint64_t)(slot * L::kTileBytes) >> 4); };
+      auto qk = [&](uint32_t d_s, uint64_t dq, uint64_t dkb) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * L::kHalfBytes + (kk & 3) * 32;
-          umma_bf16_ss(tmem + tile * kBlockN, sdesc_sw128(qb + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024),
-                       idesc_qk, kk > 0 ? 1u : 0u);
+          const uint64_t off = (uint64_t)(((kk >> 2) * L::kHalfBytes + (kk & 3) * 32) >> 4);
+          umma_bf16_ss(d_s, dq + off, dkb + off, idesc_qk, kk > 0 ? 1u : 0u);
         }
       };
-      auto issue_pv = [&](int tile, int32_t j) {
-        const uint32_t vb = slot_addr((2 * j + 1) % kStages);
+      auto pv = [&](uint32_t d_o, uint32_t p_tmem, uint64_t dvb, uint32_t acc_first) {
 #pragma unroll
         for (int kk = 0; kk < kBlockN / 16; ++kk)
-          umma_bf16_ts(tmem + kTmemO + tile * 128, tmem + tile * kBlockN + kk * 8,
-                       sdesc_sw128(vb + kk * 2048, L::kHalfBytes, 1024), idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+          umma_bf16_ts(d_o, p_tmem + kk * 8, dvb + (uint64_t)((kk * 2048) >> 4), idesc_pv, kk > 0 ? 1u : acc_first);
       };
-      bool ok = mbar_wait(bar(kBarQFull), 0, abort_flag, a.status) && wait_slot(0);
+      bool ok = mbar_wait(bar(kBarQFull), 0, abort_flag, a.status) &&
+                mbar_wait(bar(kBarSlotFull0 + 0), 0, abort_flag, a.status);
       if (ok) {
         tc_fence_after();
-        for (int t = 0; t < ntiles; ++t) {
-          issue_qk(t, 0);
-          umma_commit(bar(kBarSFull0 + t));
+        const uint64_t dk0 = slot_desc(dk, 0);
+        qk(d_s0, dq0, dk0);
+        umma_commit(bar(kBarSFull0 + 0));
+        if (two) {
+          qk(d_s1, dq1, dk0);
+          umma_commit(bar(kBarSFull0 + 1));
         }
         umma_commit(bar(kBarSlotEmpty0 + 0));
       }
       for (int32_t j = 0; ok && j < T; ++j) {
         const bool more = j + 1 < T;
-        for (int t = 0; t < ntiles; ++t) {
-          ok = mbar_wait(bar(kBarPFull0 + t), j & 1, abort_flag, a.status);
-          if (ok && t == 0) ok = wait_slot(2 * j + 1);  // V_j
-          if (!ok) break;
-          tc_fence_after();
-          issue_pv(t, j);
-          if (!more) umma_commit(bar(kBarODone0 + t));
-          if (t == ntiles - 1) umma_commit(bar(kBarSlotEmpty0 + (2 * j + 1) % kStages));
-          if (more) {
-            if (t == 0 && !(ok = wait_slot(2 * j + 2))) break;  // K_{j+1}
-            issue_qk(t, j + 1);
-            umma_commit(bar(kBarSFull0 + t));
-            if (t == ntiles - 1) umma_commit(bar(kBarSlotEmpty0 + (2 * j + 2) % kStages));
-          }
+        const int vslot = 2 * (j & 1) + 1, kslot = 2 * ((j + 1) & 1);
+        const uint64_t dvj = slot_desc(dv, vslot), dkn = slot_desc(dk, kslot);
+        const uint32_t acc = j > 0 ? 1u : 0u;
+        // tile 0: PV(j), then QK(j+1)
+        ok = mbar_wait(bar(kBarPFull0 + 0), j & 1, abort_flag, a.status) &&
+             mbar_wait(bar(kBarSlotFull0 + vslot), (j >> 1) & 1, abort_flag, a.status);
+        if (!ok) break;
+        tc_fence_after();
+        pv(d_o0, d_s0, dvj, acc);
+        if (!more) umma_commit(bar(kBarODone0 + 0));
+        if (!two) umma_commit(bar(kBarSlotEmpty0 + vslot));
+        if (more) {
+          if (!(ok = mbar_wait(bar(kBarSlotFull0 + kslot), ((j + 1) >> 1) & 1, abort_flag, a.status))) break;
+          qk(d_s0, dq0, dkn);
+          umma_commit(bar(kBarSFull0 + 0));
+          if (!two) umma_commit(bar(kBarSlotEmpty0 + kslot));
+        }
+        if (!two) continue;
+        // tile 1: PV(j), then QK(j+1)
+        if (!(ok = mbar_wait(bar(kBarPFull0 + 1), j & 1, abort_flag, a.status))) break;
+        tc_fence_after();
+        pv(d_o1, d_s1, dvj, acc);
+        if (!more) umma_commit(bar(kBarODone0 + 1));
+        umma_commit(bar(kBarSlotEmpty0 + vslot));
+        if (more) {
+          qk(d_s1, dq1, dkn);
+          umma_commit(bar(kBarSFull0 + 1));
+          umma_commit(bar(kBarSlotEmpty0 + kslot));
         }
       }
       // Every tcgen05 op of this CTA has landed before TMEM is released.
@@ -604,8 +618,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       while (!mbar_try_wait(bar(kBarFinal), 0) && globaltimer_ns() - t0 < kWaitLimitNs) {
       }
     }
-  } else {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsControl));
   }
   tc_fence_before();
   __syncthreads();
@@ -622,13 +634,8 @@ cudaError_t launch_attention(const AttnArgs &args, int grid, cudaStream_t stream
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !configured[dev]) {
-    // The in-kernel register split may only hand out what the launch reserved; refuse to
-    // launch a build whose register count would leave setmaxnreg.inc short.
-    cudaFuncAttributes fa;
-    cudaError_t e = cudaFuncGetAttributes(&fa, attn_fwd_kernel<D>);
-    if (e != cudaSuccess) return e;
-    if ((uint32_t)fa.numRegs * kThreads < 4 * 128 * kRegsSoftmax + 128 * kRegsControl) return cudaErrorInvalidValue;
-    e = cudaFuncSetAttribute(attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::kDynamic);
+    cudaError_t e =
+        cudaFuncSetAttribute(attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::kDynamic);
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
