@@ -176,6 +176,21 @@ def dist_setup(args):
     return world, rank, local
 
 
+def max_over_ranks(value: float, dist=None, device="cpu") -> float:
+    """Largest value over all ranks (the slowest rank's time); identity without a process group."""
+    if dist is None:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def rank_seed_workload(name: str, rank: int, tokens: int = 32768):
+    """Each rank prefills its own independent batch: same shape, seed offset by rank."""
+    return build_workload(name, rank, tokens)
+
+
 def run_reference(args):
     """The fp64 CPU oracle, timed on the host cores on a bounded row sample per step."""
     import oracle
@@ -271,7 +286,7 @@ def main():
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     B.load()
     B.unip_get_device_status(clear=True)
-    wl = build_workload(args.workload, rank, args.tokens)
+    wl = rank_seed_workload(args.workload, rank, args.tokens)
     di = DeviceInputs.from_workload(wl, f"cuda:{local}")
     bufs = StepBuffers(di)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=f"cuda:{local}")
@@ -319,11 +334,7 @@ def main():
     t_imp = [e[1].elapsed_time(e[2]) for e in evs]
     t_sel = [e[2].elapsed_time(e[3]) for e in evs]
     t_step = [e[0].elapsed_time(e[3]) for e in evs]
-    step_ms = float(np.sum(t_step))
-    if dist is not None:
-        t = torch.tensor([step_ms], dtype=torch.float64, device=f"cuda:{local}")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        step_ms = float(t.item())
+    step_ms = max_over_ranks(float(np.sum(t_step)), dist, f"cuda:{local}")
     ms_per_step = step_ms / args.steps
     value = flops_step * world / (ms_per_step * 1e-3) / 1e12
 
@@ -362,11 +373,7 @@ def main():
         hid_host[:m].copy_(bufs.hidden_out[:m], non_blocking=True)
         torch.cuda.synchronize()
         d2h_list.append(out_host.numel() * 2 + 4 + m * d_model * 2)
-    e2e_dt = time.perf_counter() - e2e_t0
-    if dist is not None:
-        t = torch.tensor([e2e_dt], dtype=torch.float64, device=f"cuda:{local}")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_dt = float(t.item())
+    e2e_dt = max_over_ranks(time.perf_counter() - e2e_t0, dist, f"cuda:{local}")
     e2e_value = flops_step * world * args.e2e_steps / e2e_dt / 1e12
 
     if rank != 0:
