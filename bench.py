@@ -277,7 +277,7 @@ def main():
     import torch
     from sparsified_long_context_gb300 import binding as B
     from sparsified_long_context_gb300.pipeline import (DeviceInputs, StepBuffers, kernels_per_step, run_attention,
-                                                        run_importance, run_topp_gather)
+                                                        run_importance, run_select_gather)
     world, rank, local = dist_setup(args)
     torch.cuda.set_device(local)
     dist = None
@@ -302,7 +302,7 @@ def main():
         run_importance(di, bufs, stream)
         if ev is not None:
             ev[2].record(stream)
-        run_topp_gather(di, bufs, stream=stream)
+        run_select_gather(di, bufs, stream=stream)
         if ev is not None:
             ev[3].record(stream)
 
@@ -383,7 +383,7 @@ def main():
     cpu = None
     if not args.no_cpu_baseline and world == 1:
         cpu = cpu_baseline(wl, args.cpu_seconds)
-    launches = kernels_per_step(True) * args.steps
+    launches = kernels_per_step(True, fused_select=True) * args.steps
     traffic = recorded_traffic(os.path.join(ROOT, "sparsified_long_context_gb300", "csrc", "unip_attention.cu"),
                                "attn_fwd_long_single.md")
     line = {

@@ -228,6 +228,26 @@ UNIP_API int32_t unip_topp_select(const float *imp, const int32_t *blk_cu,
                                   void *workspace, size_t workspace_bytes, void *stream);
 
 /* ---------------------------------------------------------------------------
+ * Top-p selection and compaction in one call ([UP] sections 1 and 3): the
+ * outputs of unip_topp_select plus hidden_out[i][:] = hidden[gather_idx[i]][:]
+ * (hidden: total_tokens rows with row stride row_stride; hidden_out: capacity
+ * total_tokens rows with row stride out_row_stride; 16-byte aligned, d_model
+ * and strides multiples of 8).  Same results as unip_topp_select followed by
+ * unip_gather_tokens, with the index build folded into the gather so that the
+ * call launches two kernels; the gather may start while Top-p finishes
+ * (programmatic dependent launch).  Workspace as unip_topp_select.
+ * ------------------------------------------------------------------------- */
+UNIP_API int32_t unip_select_gather(const float *imp, const int32_t *blk_cu, const int32_t *cu_seqlens,
+                                    const int32_t *positions, int32_t num_segs, int32_t total_tokens,
+                                    int32_t block_size, double p, uint32_t flags,
+                                    uint8_t *keep, int32_t keep_capacity,
+                                    int32_t *gather_idx, int32_t *cu_seqlens_kept,
+                                    int32_t *positions_kept, int32_t *n_kept,
+                                    const void *hidden, int64_t row_stride, int32_t d_model,
+                                    void *hidden_out, int64_t out_row_stride,
+                                    void *workspace, size_t workspace_bytes, void *stream);
+
+/* ---------------------------------------------------------------------------
  * Row gather ([UP] section 3: the kept tokens' hidden states form the stream
  * of the later layers):  out[i][:] = hidden[gather_idx[i]][:] for
  * i < *n_kept (read on the device), bit for bit.  hidden holds num_rows rows

@@ -87,6 +87,9 @@ def load(build_if_missing: bool = True):
         lib.unip_topp_workspace_size.argtypes = [i32, i32, i32]
         lib.unip_topp_select.restype = i32
         lib.unip_topp_select.argtypes = [P, P, P, P, i32, i32, i32, f64, u32, P, i32, P, P, P, P, P, sz, P]
+        lib.unip_select_gather.restype = i32
+        lib.unip_select_gather.argtypes = [P, P, P, P, i32, i32, i32, f64, u32, P, i32, P, P, P, P, P, i64, i32, P, i64,
+                                           P, sz, P]
         lib.unip_gather_tokens.restype = i32
         lib.unip_gather_tokens.argtypes = [P, i32, i64, i32, P, P, i32, P, i64, P]
         _lib = lib
@@ -234,6 +237,27 @@ def unip_topp_select(imp, blk_cu, cu_seqlens, positions, keep, gather_idx, cu_se
                               _ptr(cu_seqlens_kept), _ptr(positions_kept), _ptr(n_kept), _ptr(workspace),
                               workspace.numel(), _stream(stream))
     _check(rc, "unip_topp_select")
+
+
+def unip_select_gather(imp, blk_cu, cu_seqlens, positions, keep, gather_idx, cu_seqlens_kept, positions_kept,
+                       n_kept, hidden, hidden_out, *, block_size, p, flags=UNIP_KEEP_FIRST | UNIP_KEEP_LAST,
+                       workspace=None, stream=None):
+    """Top-p selection, compaction indices and the hidden-state gather in two kernel launches."""
+    lib = load()
+    n = int(positions.shape[0])
+    S = int(cu_seqlens.shape[0]) - 1
+    need = lib.unip_topp_workspace_size(n, S, int(block_size))
+    if workspace is None:
+        workspace = _workspace(need, imp.device)
+    for t in (hidden, hidden_out):
+        if not t.is_cuda:
+            raise UnipError("libunip takes CUDA tensors only (no CPU fallback)")
+    rc = lib.unip_select_gather(_ptr(imp), _ptr(blk_cu), _ptr(cu_seqlens), _ptr(positions), S, n, int(block_size),
+                                float(p), int(flags), _ptr(keep), int(keep.numel()), _ptr(gather_idx),
+                                _ptr(cu_seqlens_kept), _ptr(positions_kept), _ptr(n_kept), hidden.data_ptr(),
+                                int(hidden.stride(0)), int(hidden.shape[1]), hidden_out.data_ptr(),
+                                int(hidden_out.stride(0)), _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(rc, "unip_select_gather")
 
 
 def unip_gather_tokens(hidden, gather_idx, n_kept, out, *, stream=None):

@@ -74,22 +74,6 @@ struct AttnArgs {
 // ---------------------------------------------------------------------------
 // Planner
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ int32_t block_exclusive_scan_1024(int32_t v, int32_t *sh, int32_t *total) {
-  const int tid = threadIdx.x;
-  sh[tid] = v;
-  __syncthreads();
-  for (int off = 1; off < kPlanThreads; off <<= 1) {
-    const int32_t add = tid >= off ? sh[tid - off] : 0;
-    __syncthreads();
-    sh[tid] += add;
-    __syncthreads();
-  }
-  const int32_t incl = sh[tid];
-  *total = sh[kPlanThreads - 1];
-  __syncthreads();
-  return incl - v;
-}
-
 __global__ void __launch_bounds__(kPlanThreads) attn_plan_kernel(const int32_t *__restrict__ cu,
                                                                  const int32_t *__restrict__ pos, int32_t S,
                                                                  int32_t N, int32_t has_cache, int32_t page_size,
@@ -97,7 +81,7 @@ __global__ void __launch_bounds__(kPlanThreads) attn_plan_kernel(const int32_t *
                                                                  int2 *__restrict__ pairs, int32_t max_pairs,
                                                                  uint32_t *__restrict__ status) {
   __shared__ int32_t s_hist[kHistBins];
-  __shared__ int32_t s_scan[kPlanThreads];
+  __shared__ int32_t s_scan[32];
   __shared__ uint32_t s_err;
   const int tid = threadIdx.x;
   for (int b = tid; b < kHistBins; b += kPlanThreads) s_hist[b] = 0;
@@ -136,7 +120,7 @@ __global__ void __launch_bounds__(kPlanThreads) attn_plan_kernel(const int32_t *
   }
   if (err) atomicOr(&s_err, err);
   int32_t total_pairs;
-  block_exclusive_scan_1024(my_pairs, s_scan, &total_pairs);
+  block_excl_scan<int32_t>(my_pairs, s_scan, &total_pairs);
   if (s_err != 0 || total_pairs > max_pairs) {
     if (tid == 0) {
       header[0] = 0;
@@ -163,7 +147,7 @@ __global__ void __launch_bounds__(kPlanThreads) attn_plan_kernel(const int32_t *
     local += cnt[r];
   }
   int32_t dummy;
-  int32_t run = block_exclusive_scan_1024(local, s_scan, &dummy);
+  int32_t run = block_excl_scan<int32_t>(local, s_scan, &dummy);
 #pragma unroll
   for (int r = 0; r < kPer; ++r) {
     s_hist[kHistBins - 1 - (tid * kPer + r)] = run;

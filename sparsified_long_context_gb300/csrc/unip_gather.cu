@@ -15,19 +15,6 @@ namespace unip {
 namespace {
 
 constexpr int kGatherThreads = 256;
-constexpr int kUnroll = 8;
-
-__device__ __forceinline__ uint4 ld_stream(const uint4 *p) {
-  uint4 r;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-               : "l"(p));
-  return r;
-}
-__device__ __forceinline__ void st_stream(uint4 *p, const uint4 &v) {
-  asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
-               : "memory");
-}
 
 __global__ void __launch_bounds__(kGatherThreads) gather_rows_kernel(const uint4 *__restrict__ hidden,
                                                                      int32_t num_rows, int64_t stride16,
@@ -50,17 +37,7 @@ __global__ void __launch_bounds__(kGatherThreads) gather_rows_kernel(const uint4
       if (lane == 0) atomicOr(status, UNIP_DEV_BAD_INDEX);
       continue;
     }
-    const uint4 *s = hidden + (int64_t)src * stride16;
-    uint4 *d = out + row * out_stride16;
-    int v = lane;
-    for (; v + 32 * (kUnroll - 1) < vec_per_row; v += 32 * kUnroll) {
-      uint4 r[kUnroll];
-#pragma unroll
-      for (int u = 0; u < kUnroll; ++u) r[u] = ld_stream(s + v + 32 * u);
-#pragma unroll
-      for (int u = 0; u < kUnroll; ++u) st_stream(d + v + 32 * u, r[u]);
-    }
-    for (; v < vec_per_row; v += 32) st_stream(d + v, ld_stream(s + v));
+    warp_copy_row(hidden + (int64_t)src * stride16, out + row * out_stride16, vec_per_row, lane);
   }
 }
 

@@ -35,29 +35,13 @@ constexpr int kNormThreads = 256;
 constexpr int kWsHeaderBytes = 256;
 constexpr float kLog2e = 1.44269504088896340736f;
 
-__device__ __forceinline__ int32_t scan1024(int32_t v, int32_t *sh, int32_t *total) {
-  const int tid = threadIdx.x;
-  sh[tid] = v;
-  __syncthreads();
-  for (int off = 1; off < kPlanThreads; off <<= 1) {
-    const int32_t add = tid >= off ? sh[tid - off] : 0;
-    __syncthreads();
-    sh[tid] += add;
-    __syncthreads();
-  }
-  const int32_t incl = sh[tid];
-  *total = sh[kPlanThreads - 1];
-  __syncthreads();
-  return incl - v;
-}
-
 __global__ void __launch_bounds__(kPlanThreads) imp_plan_kernel(const int32_t *__restrict__ cu, int32_t S,
                                                                 int32_t N, const uint8_t *__restrict__ seg_mask,
                                                                 int32_t B, int32_t *__restrict__ blk_cu,
                                                                 int32_t imp_capacity, int32_t *__restrict__ header,
                                                                 int2 *__restrict__ items, int32_t max_items,
                                                                 uint32_t *__restrict__ status) {
-  __shared__ int32_t s_scan[kPlanThreads];
+  __shared__ int32_t s_scan[32];
   __shared__ uint32_t s_err;
   const int tid = threadIdx.x;
   const int per = (S + kPlanThreads - 1) / kPlanThreads;
@@ -76,8 +60,8 @@ __global__ void __launch_bounds__(kPlanThreads) imp_plan_kernel(const int32_t *_
   }
   if (bad) atomicOr(&s_err, UNIP_DEV_BAD_SEQLENS);
   int32_t tot_blocks, tot_items;
-  int32_t blk_base = scan1024(my_blocks, s_scan, &tot_blocks);
-  int32_t item_base = scan1024(my_items, s_scan, &tot_items);
+  int32_t blk_base = block_excl_scan<int32_t>(my_blocks, s_scan, &tot_blocks);
+  int32_t item_base = block_excl_scan<int32_t>(my_items, s_scan, &tot_items);
   if (s_err != 0 || tot_blocks > imp_capacity || tot_items > max_items) {
     for (int s = tid; s <= S; s += kPlanThreads) blk_cu[s] = 0;
     if (tid == 0) {

@@ -284,6 +284,65 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                : "memory");
 }
 
+template <typename T>
+__device__ __forceinline__ T warp_incl_scan(T v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const T o = __shfl_up_sync(0xffffffffu, v, off);
+    if (lane >= off) v += o;
+  }
+  return v;
+}
+
+// Exclusive scan of one value per thread over the CTA (blockDim a multiple of 32, at most 1024);
+// *total gets the sum.  sh_warp: 32 elements of shared memory.
+template <typename T>
+__device__ T block_excl_scan(T v, T *sh_warp, T *total) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int nw = blockDim.x >> 5;
+  const T incl = warp_incl_scan(v);
+  if (lane == 31) sh_warp[wid] = incl;
+  __syncthreads();
+  if (wid == 0) {
+    T w = lane < nw ? sh_warp[lane] : T(0);
+    w = warp_incl_scan(w);
+    if (lane < nw) sh_warp[lane] = w;
+  }
+  __syncthreads();
+  const T before = wid > 0 ? sh_warp[wid - 1] : T(0);
+  *total = sh_warp[nw - 1];
+  __syncthreads();
+  return before + incl - v;
+}
+
+// 16-byte global load that does not allocate in L1 / streaming store (row copies).
+__device__ __forceinline__ uint4 ld_stream(const uint4 *p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+__device__ __forceinline__ void st_stream(uint4 *p, const uint4 &v) {
+  asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+// One warp copies one row of vec_per_row 16-byte vectors, 8 loads in flight per lane.
+__device__ __forceinline__ void warp_copy_row(const uint4 *__restrict__ src, uint4 *__restrict__ dst,
+                                              int32_t vec_per_row, int lane) {
+  constexpr int kUnroll = 8;
+  int v = lane;
+  for (; v + 32 * (kUnroll - 1) < vec_per_row; v += 32 * kUnroll) {
+    uint4 r[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) r[u] = ld_stream(src + v + 32 * u);
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) st_stream(dst + v + 32 * u, r[u]);
+  }
+  for (; v < vec_per_row; v += 32) st_stream(dst + v, ld_stream(src + v));
+}
+
 // Segment holding token t: largest s with cu[s] <= t (cu non-decreasing, t < cu[S]).
 __device__ __forceinline__ int32_t find_segment(const int32_t *cu, int32_t S, int32_t t) {
   int32_t lo = 0, hi = S - 1;

@@ -31,39 +31,11 @@ namespace {
 constexpr int kToppThreads = 512;
 constexpr int kIndexThreads = 256;
 constexpr int kMaxBlocks = UNIP_TOPP_MAX_BLOCKS;
+constexpr int kRankCountMax = 1024;  // segments up to this many blocks rank by counting instead of sorting
 constexpr int kWsHeaderBytes = 256;
 constexpr int kIndexSmemSegs = 12000;  // segments whose offsets the index kernel keeps in shared memory
-
-template <typename T>
-__device__ __forceinline__ T warp_incl_scan(T v) {
-  const int lane = threadIdx.x & 31;
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const T o = __shfl_up_sync(0xffffffffu, v, off);
-    if (lane >= off) v += o;
-  }
-  return v;
-}
-
-// Exclusive scan of one value per thread over the CTA; *total gets the sum.
-template <typename T>
-__device__ T block_excl_scan(T v, T *sh_warp, T *total) {
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  const int nw = blockDim.x >> 5;
-  const T incl = warp_incl_scan(v);
-  if (lane == 31) sh_warp[wid] = incl;
-  __syncthreads();
-  if (wid == 0) {
-    T w = lane < nw ? sh_warp[lane] : T(0);
-    w = warp_incl_scan(w);
-    if (lane < nw) sh_warp[lane] = w;
-  }
-  __syncthreads();
-  const T before = wid > 0 ? sh_warp[wid - 1] : T(0);
-  *total = sh_warp[nw - 1];
-  __syncthreads();
-  return before + incl - v;
-}
+constexpr int kGatherCtasPerSm = 2;    // fused gather grid: 16 warps per SM, each with 4 KB of loads in flight
+constexpr int kGatherStageBytes = 48 * 1024;  // shared memory of the fused gather (no opt-in needed)
 
 __device__ __forceinline__ unsigned long long fixed_mass(float f) {
   return static_cast<unsigned long long>(floor(static_cast<double>(f) * 4294967296.0));
@@ -91,6 +63,8 @@ __global__ void __launch_bounds__(kToppThreads) topp_kernel(
   const int32_t s = blockIdx.x;
   const int32_t n = cu[s + 1] - cu[s];
   const int32_t b0 = blk_cu[s], nb = blk_cu[s + 1] - blk_cu[s];
+  // A gather launched as a programmatic dependent may start now; it waits for this grid's results.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   if (nb == 0) {  // not scored: every token is kept
     if (tid == 0) seg_kept[s] = n > 0 ? n : 0;
@@ -147,6 +121,58 @@ __global__ void __launch_bounds__(kToppThreads) topp_kernel(
   }
   if (T == 0) {
     for (int b = tid; b < nb; b += kToppThreads) skeep[b] = 1;
+  } else if (nb <= kRankCountMax) {
+    // Small segment: the rank of a block is the number of smaller keys (keys are unique), so
+    // no sort is needed.  Forced blocks and padding hold the largest key and are never counted.
+    const double thr = __dmul_rn(p, static_cast<double>(T));
+    constexpr int kPer = kRankCountMax / kToppThreads;
+    const int npad = (nb + 15) & ~15;  // keys past npow are padded with the largest key up to npad
+    for (int b = npow + tid; b < npad; b += kToppThreads) skeys[b] = ~0ull;
+    __syncthreads();
+    int rank[kPer];
+    unsigned long long mine[kPer];
+#pragma unroll
+    for (int e = 0; e < kPer; ++e) {
+      const int b = tid + e * kToppThreads;
+      rank[e] = -1;
+      mine[e] = b < nb ? skeys[b] : ~0ull;
+      if (mine[e] != ~0ull) {
+        const ulonglong2 *k2 = reinterpret_cast<const ulonglong2 *>(skeys);  // two keys per load
+        int r = 0;
+        for (int o = 0; o < npad / 2; o += 8) {
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const ulonglong2 kk = k2[o + u];
+            r += (kk.x < mine[e] ? 1 : 0) + (kk.y < mine[e] ? 1 : 0);
+          }
+        }
+        rank[e] = r;
+      }
+    }
+    __syncthreads();  // every key has been read; the key array now holds masses in rank order
+#pragma unroll
+    for (int e = 0; e < kPer; ++e)
+      if (rank[e] >= 0) skeys[rank[e]] = fixed_mass(key_score(mine[e]));
+    __syncthreads();
+    const int R = nb - (f_first ? 1 : 0) - ((f_last && !(f_first && nb == 1)) ? 1 : 0);
+    const int ipt = (R + kToppThreads - 1) / kToppThreads;
+    const int r0 = tid * ipt;
+    unsigned long long local = 0;
+    for (int e = 0; e < ipt; ++e)
+      if (r0 + e < R) local += skeys[r0 + e];
+    unsigned long long tot;
+    unsigned long long run = block_excl_scan<unsigned long long>(local, sh64, &tot);
+    for (int e = 0; e < ipt; ++e) {
+      if (r0 + e < R) {
+        const unsigned long long m = skeys[r0 + e];
+        skeys[r0 + e] = run;  // exclusive prefix of ranked masses, in place
+        run += m;
+      }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int e = 0; e < kPer; ++e)
+      if (rank[e] >= 0) skeep[tid + e * kToppThreads] = static_cast<double>(CF + skeys[rank[e]]) < thr ? 1 : 0;
   } else {
     const double thr = __dmul_rn(p, static_cast<double>(T));
     // 2. bitonic sort, ascending key = score descending, index ascending
@@ -299,6 +325,73 @@ __global__ void __launch_bounds__(kIndexThreads) index_global_kernel(
   pos_kept[dest] = pos[t];
 }
 
+// Fused index build + row gather: kept row r is found from the per-segment
+// counts (shared-memory scan) and the per-block kept offsets (binary search,
+// staged in shared memory when they fit); one warp writes gather_idx /
+// positions_kept and copies the hidden row.
+__global__ void __launch_bounds__(kIndexThreads) select_gather_kernel(
+    const uint4 *__restrict__ hidden, int32_t num_rows, int64_t stride16, int32_t vec_per_row,
+    const int32_t *__restrict__ cu, const int32_t *__restrict__ pos, const int32_t *__restrict__ blk_cu,
+    const uint8_t *__restrict__ keep, const int32_t *__restrict__ kept_off, const int32_t *__restrict__ seg_kept,
+    int32_t S, int32_t B, int32_t capacity, uint4 *__restrict__ out, int64_t out_stride16,
+    int32_t *__restrict__ cu_kept, int32_t *__restrict__ n_kept, int32_t *__restrict__ gather_idx,
+    int32_t *__restrict__ pos_kept, int32_t stage_blocks, uint32_t *__restrict__ status) {
+  extern __shared__ int32_t soff[];  // S + 1 kept-token offsets, then (optionally) per-block kept offsets
+  __shared__ int32_t sh32[32];
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // the Top-p grid's results are visible past here
+  const int32_t nblk = blk_cu[S];
+  int32_t *skoff = soff + S + 1;
+  const bool staged = nblk <= stage_blocks;
+  if (staged)
+    for (int32_t b = threadIdx.x; b < nblk; b += kIndexThreads) skoff[b] = kept_off[b];
+  segment_offsets(seg_kept, S, soff, sh32);
+  if (blockIdx.x == 0) {
+    for (int i = threadIdx.x; i <= S; i += kIndexThreads) cu_kept[i] = soff[i];
+    if (threadIdx.x == 0) *n_kept = soff[S];
+  }
+  int32_t total = soff[S];
+  if (total > capacity) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(status, UNIP_DEV_BAD_INDEX);
+    total = capacity;
+  }
+  const int lane = threadIdx.x & 31;
+  const int warps_per_block = kIndexThreads / 32;
+  const int32_t nwarps = gridDim.x * warps_per_block;
+  for (int32_t r = blockIdx.x * warps_per_block + (threadIdx.x >> 5); r < total; r += nwarps) {
+    int32_t lo = 0, hi = S - 1;  // segment: last s with soff[s] <= r
+    while (lo < hi) {
+      const int32_t mid = (lo + hi + 1) >> 1;
+      if (soff[mid] <= r) lo = mid; else hi = mid - 1;
+    }
+    const int32_t sg = lo, local = r - soff[sg], c0 = cu[sg];
+    const int32_t b0 = blk_cu[sg], nb = blk_cu[sg + 1] - b0;
+    int32_t src;
+    if (nb == 0) {
+      src = c0 + local;
+    } else {
+      // block: last b with kept_off[b] <= local.  kept_off is non-decreasing and a dropped block
+      // shares its offset with the next kept one, so the answer is always a kept block.
+      const int32_t *ko = staged ? skoff + b0 : kept_off + b0;
+      int32_t blo = 0, bhi = nb - 1;
+      while (blo < bhi) {
+        const int32_t mid = (blo + bhi + 1) >> 1;
+        if (ko[mid] <= local) blo = mid; else bhi = mid - 1;
+      }
+      if (!keep[b0 + blo]) continue;
+      src = c0 + blo * B + (local - ko[blo]);
+    }
+    if (src < 0 || src >= num_rows) {
+      if (lane == 0) atomicOr(status, UNIP_DEV_BAD_INDEX);
+      continue;
+    }
+    if (lane == 0) {
+      gather_idx[r] = src;
+      pos_kept[r] = pos[src];
+    }
+    warp_copy_row(hidden + (int64_t)src * stride16, out + (int64_t)r * out_stride16, vec_per_row, lane);
+  }
+}
+
 }  // namespace
 }  // namespace unip
 
@@ -367,6 +460,86 @@ UNIP_API int32_t unip_topp_select(const float *imp, const int32_t *blk_cu, const
   }
   if (cudaGetLastError() != cudaSuccess) return UNIP_ERR_CUDA;
   return UNIP_OK;
+}
+
+UNIP_API int32_t unip_select_gather(const float *imp, const int32_t *blk_cu, const int32_t *cu_seqlens,
+                                    const int32_t *positions, int32_t num_segs, int32_t total_tokens,
+                                    int32_t block_size, double p, uint32_t flags, uint8_t *keep,
+                                    int32_t keep_capacity, int32_t *gather_idx, int32_t *cu_seqlens_kept,
+                                    int32_t *positions_kept, int32_t *n_kept, const void *hidden,
+                                    int64_t row_stride, int32_t d_model, void *hidden_out, int64_t out_row_stride,
+                                    void *workspace, size_t workspace_bytes, void *stream) {
+  if (!hidden || !hidden_out || d_model <= 0 || row_stride < d_model || out_row_stride < d_model)
+    return UNIP_ERR_INVALID_ARGUMENT;
+  if (!aligned16(hidden) || !aligned16(hidden_out) || (d_model % 8) || (row_stride % 8) || (out_row_stride % 8))
+    return UNIP_ERR_ALIGNMENT;
+  if (num_segs >= kIndexSmemSegs) {  // very many segments: the two-call path
+    const int32_t rc = unip_topp_select(imp, blk_cu, cu_seqlens, positions, num_segs, total_tokens, block_size, p,
+                                        flags, keep, keep_capacity, gather_idx, cu_seqlens_kept, positions_kept,
+                                        n_kept, workspace, workspace_bytes, stream);
+    if (rc != UNIP_OK) return rc;
+    return unip_gather_tokens(hidden, total_tokens, row_stride, d_model, gather_idx, n_kept, total_tokens,
+                              hidden_out, out_row_stride, stream);
+  }
+  if (!blk_cu || !cu_seqlens || !cu_seqlens_kept || !n_kept || num_segs < 0 || total_tokens < 0)
+    return UNIP_ERR_INVALID_ARGUMENT;
+  if (block_size <= 0 || !(p >= 0.0 && p <= 1.0) || (flags & ~(UNIP_KEEP_FIRST | UNIP_KEEP_LAST)))
+    return UNIP_ERR_INVALID_ARGUMENT;
+  if (total_tokens > 0 && (!positions || !gather_idx || !positions_kept)) return UNIP_ERR_INVALID_ARGUMENT;
+  if (keep_capacity < unip_importance_capacity(total_tokens, num_segs, block_size)) return UNIP_ERR_INVALID_ARGUMENT;
+  if (!keep || !imp) return UNIP_ERR_INVALID_ARGUMENT;
+  const size_t need = unip_topp_workspace_size(total_tokens, num_segs, block_size);
+  if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return UNIP_ERR_WORKSPACE;
+  uint32_t *status = device_status_ptr();
+  if (!status) return UNIP_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (num_segs == 0) {
+    if (cudaMemsetAsync(cu_seqlens_kept, 0, sizeof(int32_t), st) != cudaSuccess ||
+        cudaMemsetAsync(n_kept, 0, sizeof(int32_t), st) != cudaSuccess)
+      return UNIP_ERR_CUDA;
+    return UNIP_OK;
+  }
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  int32_t *seg_kept = reinterpret_cast<int32_t *>(ws + kWsHeaderBytes);
+  int32_t *kept_off = reinterpret_cast<int32_t *>(ws + kWsHeaderBytes + align_up(sizeof(int32_t) * num_segs, 256));
+  static bool configured[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const int smem = kMaxBlocks * ((int)sizeof(unsigned long long) + 1);
+  if (dev >= 0 && dev < 64 && !configured[dev]) {
+    if (cudaFuncSetAttribute(topp_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+      return UNIP_ERR_CUDA;
+    configured[dev] = true;
+  }
+  topp_kernel<<<num_segs, kToppThreads, smem, st>>>(imp, blk_cu, cu_seqlens, block_size, p, flags, keep, kept_off,
+                                                    seg_kept, status);
+  if (cudaGetLastError() != cudaSuccess) return UNIP_ERR_CUDA;
+  const int sms = device_sm_count();
+  const int warps_per_block = kIndexThreads / 32;
+  int64_t blocks = ((int64_t)(total_tokens > 0 ? total_tokens : 1) + warps_per_block - 1) / warps_per_block;
+  const int64_t max_blocks = (int64_t)(sms > 0 ? sms : 1) * kGatherCtasPerSm;
+  if (blocks > max_blocks) blocks = max_blocks;
+  // per-block kept offsets are staged in shared memory when the upper bound on blocks fits
+  const int32_t blk_bound = unip_importance_capacity(total_tokens, num_segs, block_size);
+  const int32_t stage_blocks =
+      (int64_t)(num_segs + 1 + blk_bound) * 4 <= kGatherStageBytes ? blk_bound : 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)blocks);
+  cfg.blockDim = dim3(kIndexThreads);
+  cfg.dynamicSmemBytes = (size_t)(num_segs + 1 + stage_blocks) * sizeof(int32_t);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(
+      &cfg, select_gather_kernel, static_cast<const uint4 *>(hidden), total_tokens, (int64_t)(row_stride / 8),
+      (int32_t)(d_model / 8), cu_seqlens, positions, blk_cu, (const uint8_t *)keep, (const int32_t *)kept_off,
+      (const int32_t *)seg_kept, num_segs, block_size, total_tokens, static_cast<uint4 *>(hidden_out),
+      (int64_t)(out_row_stride / 8), cu_seqlens_kept, n_kept, gather_idx, positions_kept, stage_blocks, status);
+  return e == cudaSuccess ? UNIP_OK : UNIP_ERR_CUDA;
 }
 
 }  // extern "C"

@@ -113,6 +113,16 @@ def run_topp_gather(di: DeviceInputs, bufs: StepBuffers, p: Optional[float] = No
         B.unip_gather_tokens(di.hidden, bufs.gather_idx, bufs.n_kept, bufs.hidden_out, stream=stream)
 
 
+def run_select_gather(di: DeviceInputs, bufs: StepBuffers, p: Optional[float] = None, stream=None,
+                      flags: int = B.UNIP_KEEP_FIRST | B.UNIP_KEEP_LAST):
+    """Top-p + index build + gather through the fused entry point (two kernel launches)."""
+    wl = di.wl
+    B.unip_select_gather(bufs.imp, bufs.blk_cu, di.cu_seqlens, di.positions, bufs.keep, bufs.gather_idx,
+                         bufs.cu_seqlens_kept, bufs.positions_kept, bufs.n_kept, di.hidden, bufs.hidden_out,
+                         block_size=bufs.block_size, p=wl.top_p if p is None else p, flags=flags,
+                         workspace=bufs.ws_topp, stream=stream)
+
+
 def run_select(di: DeviceInputs, bufs: StepBuffers, p: Optional[float] = None, stream=None,
                flags: int = B.UNIP_KEEP_FIRST | B.UNIP_KEEP_LAST):
     run_importance(di, bufs, stream)
@@ -125,7 +135,10 @@ def run_step(di: DeviceInputs, bufs: StepBuffers, stream=None):
     run_select(di, bufs, stream=stream)
 
 
-def kernels_per_step(has_hidden: bool = True) -> int:
-    """libunip kernels one run_step launches (up to 12000 segments)."""
-    # attention: plan + attention; importance: plan + score + norm; Top-p: select + index; gather: 1
+def kernels_per_step(has_hidden: bool = True, fused_select: bool = False) -> int:
+    """libunip kernels one step launches (up to 12000 segments)."""
+    # attention: plan + attention; importance: plan + score + norm;
+    # Top-p: select + index, gather: 1  -- or the fused select + gather: 2
+    if fused_select:
+        return 2 + 3 + 2
     return 2 + 3 + 2 + (1 if has_hidden else 0)

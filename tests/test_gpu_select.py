@@ -117,8 +117,8 @@ def _topp_direct(imp_np, blk_cu_np, cu_np, B_, p, flags):
 def test_topp_edge_cases_bit_exact(flags):
     rng = np.random.default_rng(50 + flags)
     B_ = 16
-    lengths = [1, 16, 17, 300, 0, 5000, 64, 33]
-    scored = [1, 1, 1, 1, 1, 1, 0, 1]
+    lengths = [1, 16, 17, 300, 0, 5000, 64, 33, 20000]   # 20000 tokens = 1250 blocks: the sorting path
+    scored = [1, 1, 1, 1, 1, 1, 0, 1, 1]
     nbs = [(-(-L // B_) if (sc and L > 0) else 0) for L, sc in zip(lengths, scored)]
     cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
     bc = np.concatenate([[0], np.cumsum(nbs)]).astype(np.int32)
@@ -193,3 +193,22 @@ def test_importance_shapes_vs_oracle(lengths, hq, hkv, d, B):
     assert np.array_equal(blk_cu, ref_bc)
     imp = bufs.imp[: blk_cu[-1]].cpu().numpy().astype(np.float64)
     assert_close(imp, ref_imp, what="importance")
+
+
+@pytest.mark.parametrize("name", ["tiny_packed", "long_single", "mixed_step"])
+def test_fused_select_gather_matches_oracle(name):
+    """unip_select_gather against the oracle fed the same scores (and so against the two-call path)."""
+    from sparsified_long_context_gb300 import binding as Bd
+    from sparsified_long_context_gb300.pipeline import (DeviceInputs, StepBuffers, run_attention, run_importance,
+                                                        run_select_gather)
+    wl = W.workload_by_name(name)
+    Bd.unip_get_device_status(clear=True)
+    di = DeviceInputs.from_workload(wl, "cuda")
+    bufs = StepBuffers(di)
+    run_attention(di, bufs)
+    run_importance(di, bufs)
+    bufs.hidden_out.zero_()
+    run_select_gather(di, bufs)
+    torch.cuda.synchronize()
+    assert Bd.unip_get_device_status(clear=True) == 0
+    _check_selection(wl, bufs)
