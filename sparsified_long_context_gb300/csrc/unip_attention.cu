@@ -82,6 +82,7 @@ __global__ void __launch_bounds__(kPlanThreads) attn_plan_kernel(const int32_t *
                                                                  uint32_t *__restrict__ status) {
   __shared__ int32_t s_hist[kHistBins];
   __shared__ int32_t s_scan[32];
+  __shared__ int32_t s_base[kPlanThreads + 1];
   __shared__ uint32_t s_err;
   const int tid = threadIdx.x;
   for (int b = tid; b < kHistBins; b += kPlanThreads) s_hist[b] = 0;
@@ -114,13 +115,24 @@ __global__ void __launch_bounds__(kPlanThreads) attn_plan_kernel(const int32_t *
     if (P > 0 && (!has_cache || (P + page_size - 1) / page_size > max_pages)) err |= UNIP_DEV_BAD_PAGES;
     my_pairs += (n + kBlockM - 1) / kBlockM;
   }
-  for (int t = tid; t < N; t += kPlanThreads) {
-    const int s = find_segment(cu, S, t);
-    if (pos[t] != pos[cu[s]] + (t - cu[s])) err |= UNIP_DEV_BAD_POSITIONS;
+  // Positions contiguous inside each segment: pos[t] - pos[t-1] == 1 unless t starts a segment.
+  // Independent loads, four tokens per thread in flight.
+  {
+    int32_t s_cur = 0;
+#pragma unroll 4
+    for (int t = tid; t < N; t += kPlanThreads) {
+      if (t == 0) continue;
+      const int32_t prev = pos[t - 1], cur = pos[t];
+      if (cur != prev + 1) {
+        // allowed only at a segment start (some s with cu[s] == t)
+        s_cur = find_segment(cu, S, t);
+        if (cu[s_cur] != t) err |= UNIP_DEV_BAD_POSITIONS;
+      }
+    }
   }
   if (err) atomicOr(&s_err, err);
   int32_t total_pairs;
-  block_excl_scan<int32_t>(my_pairs, s_scan, &total_pairs);
+  const int32_t my_base = block_excl_scan<int32_t>(my_pairs, s_scan, &total_pairs);
   if (s_err != 0 || total_pairs > max_pairs) {
     if (tid == 0) {
       header[0] = 0;
@@ -128,13 +140,34 @@ __global__ void __launch_bounds__(kPlanThreads) attn_plan_kernel(const int32_t *
     }
     return;
   }
+  // Pairs are spread over all threads (one long segment would otherwise sit on one thread):
+  // pair p belongs to the thread j with s_base[j] <= p < s_base[j+1], and to one of j's segments.
+  s_base[tid] = my_base;
+  if (tid == 0) s_base[kPlanThreads] = total_pairs;
+  __syncthreads();
+  auto locate = [&](int32_t p, int32_t &seg, int32_t &m, int32_t &cost) {
+    int32_t lo = 0, hi = kPlanThreads - 1;
+    while (lo < hi) {
+      const int32_t mid = (lo + hi + 1) >> 1;
+      if (s_base[mid] <= p) lo = mid; else hi = mid - 1;
+    }
+    int32_t rem = p - s_base[lo];
+    for (int32_t sg = min(S, lo * per);; ++sg) {
+      const int32_t nt = (cu[sg + 1] - cu[sg] + kBlockM - 1) / kBlockM;
+      if (rem < nt) {
+        seg = sg;
+        m = rem;
+        cost = (pos[cu[sg]] + kBlockN - 1) / kBlockN + rem + 1;
+        return;
+      }
+      rem -= nt;
+    }
+  };
   // Histogram of pair costs (number of KV tiles).
-  for (int s = s0; s < s1; ++s) {
-    const int32_t n = cu[s + 1] - cu[s];
-    if (n <= 0) continue;
-    const int32_t pt = (pos[cu[s]] + kBlockN - 1) / kBlockN;
-    const int32_t nt = (n + kBlockM - 1) / kBlockM;
-    for (int m = 0; m < nt; ++m) atomicAdd(&s_hist[min(pt + m + 1, kHistBins - 1)], 1);
+  for (int32_t p = tid; p < total_pairs; p += kPlanThreads) {
+    int32_t sg, m, cost;
+    locate(p, sg, m, cost);
+    atomicAdd(&s_hist[min(cost, kHistBins - 1)], 1);
   }
   __syncthreads();
   // Bin start offsets in decreasing cost order.
@@ -154,15 +187,10 @@ __global__ void __launch_bounds__(kPlanThreads) attn_plan_kernel(const int32_t *
     run += cnt[r];
   }
   __syncthreads();
-  for (int s = s0; s < s1; ++s) {
-    const int32_t n = cu[s + 1] - cu[s];
-    if (n <= 0) continue;
-    const int32_t pt = (pos[cu[s]] + kBlockN - 1) / kBlockN;
-    const int32_t nt = (n + kBlockM - 1) / kBlockM;
-    for (int m = nt - 1; m >= 0; --m) {
-      const int32_t slot = atomicAdd(&s_hist[min(pt + m + 1, kHistBins - 1)], 1);
-      pairs[slot] = make_int2(s, m);
-    }
+  for (int32_t p = tid; p < total_pairs; p += kPlanThreads) {
+    int32_t sg, m, cost;
+    locate(p, sg, m, cost);
+    pairs[atomicAdd(&s_hist[min(cost, kHistBins - 1)], 1)] = make_int2(sg, m);
   }
   if (tid == 0) header[0] = total_pairs;
 }

@@ -328,10 +328,10 @@ __device__ __forceinline__ void st_stream(uint4 *p, const uint4 &v) {
   asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
                : "memory");
 }
-// One warp copies one row of vec_per_row 16-byte vectors, 8 loads in flight per lane.
+// One warp copies one row of vec_per_row 16-byte vectors, 16 loads in flight per lane.
 __device__ __forceinline__ void warp_copy_row(const uint4 *__restrict__ src, uint4 *__restrict__ dst,
                                               int32_t vec_per_row, int lane) {
-  constexpr int kUnroll = 8;
+  constexpr int kUnroll = 16;  // 16 x 16 B per lane: an 8 KB row in one round trip
   int v = lane;
   for (; v + 32 * (kUnroll - 1) < vec_per_row; v += 32 * kUnroll) {
     uint4 r[kUnroll];

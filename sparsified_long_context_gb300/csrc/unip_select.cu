@@ -121,6 +121,32 @@ __global__ void __launch_bounds__(kToppThreads) topp_kernel(
   }
   if (T == 0) {
     for (int b = tid; b < nb; b += kToppThreads) skeep[b] = 1;
+  } else if (npow <= kToppThreads) {
+    // Up to 512 blocks: bitonic sort with one key per thread, in registers; strides below 32
+    // exchange through warp shuffles, larger ones through shared memory.
+    const double thr = __dmul_rn(p, static_cast<double>(T));
+    unsigned long long key = tid < npow ? skeys[tid] : ~0ull;
+    for (int size = 2; size <= npow; size <<= 1) {
+      for (int stride = size >> 1; stride > 0; stride >>= 1) {
+        unsigned long long other;
+        if (stride >= 32) {
+          __syncthreads();
+          skeys[tid] = key;
+          __syncthreads();
+          other = skeys[tid ^ stride];
+        } else {
+          other = __shfl_xor_sync(0xffffffffu, key, stride);
+        }
+        const bool lower = (tid & stride) == 0, asc = (tid & size) == 0;
+        const bool take_min = lower == asc;
+        key = take_min ? (other < key ? other : key) : (other > key ? other : key);
+      }
+    }
+    // thread tid now holds the key of rank tid; forced blocks and padding sort last
+    const unsigned long long m = key != ~0ull ? fixed_mass(key_score(key)) : 0ull;
+    unsigned long long tot;
+    const unsigned long long ex = block_excl_scan<unsigned long long>(m, sh64, &tot);
+    if (key != ~0ull) skeep[key & 0xFFFFFFFFull] = static_cast<double>(CF + ex) < thr ? 1 : 0;
   } else if (nb <= kRankCountMax) {
     // Small segment: the rank of a block is the number of smaller keys (keys are unique), so
     // no sort is needed.  Forced blocks and padding hold the largest key and are never counted.
