@@ -340,7 +340,7 @@ def main():
 
     n_kept = int(bufs.n_kept.item())
     n_blocks = int(bufs.blk_cu[-1].item())
-    d_model = di.hidden.shape[1]
+    d_model = di.hidden.shape[1] if di.hidden is not None else 0
     sg_bytes = select_gather_bytes(wl, n_blocks, n_kept, d_model)
     attn_ms = statistics.mean(t_attn)
     sel_ms = statistics.mean(t_sel)
@@ -355,9 +355,12 @@ def main():
     host = {}
     for name in ("q", "k", "v", "hidden", "cu_seqlens", "positions", "seg_mask"):
         t = getattr(di, name)
-        host[name] = t.cpu().pin_memory()
+        if t is not None:
+            host[name] = t.cpu().pin_memory()
     out_host = torch.empty(bufs.out.shape, dtype=bufs.out.dtype).pin_memory()
-    hid_host = torch.empty(bufs.hidden_out.shape, dtype=bufs.hidden_out.dtype).pin_memory()
+    hid_host = None
+    if bufs.hidden_out is not None:
+        hid_host = torch.empty(bufs.hidden_out.shape, dtype=bufs.hidden_out.dtype).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h_list = []
     torch.cuda.synchronize()
@@ -370,7 +373,8 @@ def main():
         step()
         out_host.copy_(bufs.out, non_blocking=True)
         m = int(bufs.n_kept.item())  # result size lives on the device
-        hid_host[:m].copy_(bufs.hidden_out[:m], non_blocking=True)
+        if hid_host is not None:
+            hid_host[:m].copy_(bufs.hidden_out[:m], non_blocking=True)
         torch.cuda.synchronize()
         d2h_list.append(out_host.numel() * 2 + 4 + m * d_model * 2)
     e2e_dt = max_over_ranks(time.perf_counter() - e2e_t0, dist, f"cuda:{local}")
@@ -383,7 +387,7 @@ def main():
     cpu = None
     if not args.no_cpu_baseline and world == 1:
         cpu = cpu_baseline(wl, args.cpu_seconds)
-    launches = kernels_per_step(True, fused_select=True) * args.steps
+    launches = kernels_per_step(di.hidden is not None, fused_select=True) * args.steps
     traffic = recorded_traffic(os.path.join(ROOT, "sparsified_long_context_gb300", "csrc", "unip_attention.cu"),
                                "attn_fwd_long_single.md")
     line = {

@@ -249,14 +249,21 @@ def unip_select_gather(imp, blk_cu, cu_seqlens, positions, keep, gather_idx, cu_
     need = lib.unip_topp_workspace_size(n, S, int(block_size))
     if workspace is None:
         workspace = _workspace(need, imp.device)
-    for t in (hidden, hidden_out):
-        if not t.is_cuda:
-            raise UnipError("libunip takes CUDA tensors only (no CPU fallback)")
+    if (hidden is None) != (hidden_out is None):
+        raise UnipError("hidden and hidden_out are given together or not at all")
+    if hidden is None:  # selection and indices only
+        h_ptr = o_ptr = None
+        h_stride = o_stride = d_model = 0
+    else:
+        for t in (hidden, hidden_out):
+            if not t.is_cuda:
+                raise UnipError("libunip takes CUDA tensors only (no CPU fallback)")
+        h_ptr, o_ptr = hidden.data_ptr(), hidden_out.data_ptr()
+        h_stride, o_stride, d_model = int(hidden.stride(0)), int(hidden_out.stride(0)), int(hidden.shape[1])
     rc = lib.unip_select_gather(_ptr(imp), _ptr(blk_cu), _ptr(cu_seqlens), _ptr(positions), S, n, int(block_size),
                                 float(p), int(flags), _ptr(keep), int(keep.numel()), _ptr(gather_idx),
-                                _ptr(cu_seqlens_kept), _ptr(positions_kept), _ptr(n_kept), hidden.data_ptr(),
-                                int(hidden.stride(0)), int(hidden.shape[1]), hidden_out.data_ptr(),
-                                int(hidden_out.stride(0)), _ptr(workspace), workspace.numel(), _stream(stream))
+                                _ptr(cu_seqlens_kept), _ptr(positions_kept), _ptr(n_kept), h_ptr, h_stride,
+                                d_model, o_ptr, o_stride, _ptr(workspace), workspace.numel(), _stream(stream))
     _check(rc, "unip_select_gather")
 
 

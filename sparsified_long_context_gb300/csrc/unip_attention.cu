@@ -58,7 +58,7 @@ constexpr float kLn2 = 0.69314718055994530942f;
 constexpr float kLog2e = 1.44269504088896340736f;
 
 struct AttnArgs {
-  CUtensorMap tm_q, tm_k, tm_v, tm_kc, tm_vc;
+  CUtensorMap tm_q, tm_qp, tm_k, tm_v, tm_kc, tm_vc;
   const int32_t *cu;
   const int32_t *pos;
   const int32_t *block_table;
@@ -68,7 +68,14 @@ struct AttnArgs {
   float *lse;
   uint32_t *status;
   int32_t S, N, Hq, group, heads_per_pair, num_pages, page_size, max_pages;
+  int32_t lg;  // 0: a tile's rows are 128 tokens of one head; log2(group): rows are (token, head of the group)
   float scale_log2;
+};
+
+// Rows of one query tile: row R is token tok0 + (R >> lg) (segment-local) and
+// query head head0 + (R & (2^lg - 1)); rows at or past rows_valid are not stored.
+struct TileRows {
+  int32_t tok0, head0, lg, rows_valid;
 };
 
 // ---------------------------------------------------------------------------
@@ -276,10 +283,9 @@ struct RowStats {
 };
 
 template <int D>
-__device__ __forceinline__ void softmax_tile_role(const AttnArgs &a, int tile, int h, int32_t T, int32_t Tp,
-                                                  int32_t P, int32_t c0, int32_t row0, int32_t rows_valid,
-                                                  uint32_t tmem, uint64_t *bars, RowStats &rs,
-                                                  volatile int *abort_flag) {
+__device__ __forceinline__ void softmax_tile_role(const AttnArgs &a, int tile, const TileRows tr, int32_t T,
+                                                  int32_t Tp, int32_t P, int32_t c0, uint32_t tmem, uint64_t *bars,
+                                                  RowStats &rs, volatile int *abort_flag) {
   const int wt = (threadIdx.x >> 5) & 7;
   const int lane = threadIdx.x & 31;
   const int q = wt & 3, g = wt >> 2;
@@ -294,9 +300,16 @@ __device__ __forceinline__ void softmax_tile_role(const AttnArgs &a, int tile, i
   const uint32_t bar_o = smem_u32(&bars[kBarODone0 + tile]);
   const uint32_t bar_x = smem_u32(&bars[kBarXchg0 + tile]);
   const float c = a.scale_log2;
+  const int32_t tok_r0 = tr.tok0 + (R0 >> tr.lg), tok_r1 = tr.tok0 + (R1 >> tr.lg);
+  // A warp whose 16 rows are all past the tile's valid rows only keeps the barrier protocol.
+  const bool active = static_cast<int32_t>(lane_base) < tr.rows_valid;
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
   for (int32_t j = 0; j < T; ++j) {
     if (!mbar_wait(bar_s, j & 1, abort_flag, a.status)) return;
+    if (!active) {
+      mbar_arrive(bar_p);
+      continue;
+    }
     tc_fence_after();
     float sv[64];  // sv[4k + {0,1}]: row R0, columns 8k + cq + {0,1}; sv[4k + {2,3}]: row R1
     tmem_ld_16x256b_x8(tw + s_col, sv);
@@ -312,14 +325,18 @@ __device__ __forceinline__ void softmax_tile_role(const AttnArgs &a, int tile, i
           if (col + 1 >= lim) { sv[4 * k + 1] = -INFINITY; sv[4 * k + 3] = -INFINITY; }
         }
       }
-    } else if (j == T - 1) {
+    } else {
+      // own keys: key (j - Tp) * 128 + col is visible to a row whose token index is at least that
+      const int32_t lim0 = tok_r0 - (j - Tp) * kBlockN, lim1 = tok_r1 - (j - Tp) * kBlockN;
+      if (min(lim0, lim1) < kBlockN - 1) {
 #pragma unroll
-      for (int k = 0; k < 16; ++k) {  // causal diagonal tile: key column <= query row
-        const int col = 8 * k + cq;
-        if (col > R0) sv[4 * k] = -INFINITY;
-        if (col + 1 > R0) sv[4 * k + 1] = -INFINITY;
-        if (col > R1) sv[4 * k + 2] = -INFINITY;
-        if (col + 1 > R1) sv[4 * k + 3] = -INFINITY;
+        for (int k = 0; k < 16; ++k) {
+          const int col = 8 * k + cq;
+          if (col > lim0) sv[4 * k] = -INFINITY;
+          if (col + 1 > lim0) sv[4 * k + 1] = -INFINITY;
+          if (col > lim1) sv[4 * k + 2] = -INFINITY;
+          if (col + 1 > lim1) sv[4 * k + 3] = -INFINITY;
+        }
       }
     }
     float a0 = fmaxf(sv[0], sv[1]), a1 = fmaxf(sv[4], sv[5]);
@@ -393,14 +410,16 @@ __device__ __forceinline__ void softmax_tile_role(const AttnArgs &a, int tile, i
   }
   mbar_arrive(bar_x);
   if (!mbar_wait(bar_x, 0, abort_flag, a.status)) return;
+  if (32 * q >= tr.rows_valid) return;  // no valid row in this warp's 32 epilogue rows (warp-uniform)
   if (!mbar_wait(bar_o, 0, abort_flag, a.status)) return;
   tc_fence_after();
   // Epilogue with the 32x32b shape: warp (q, g) stores rows 32q .. 32q + 31, columns [g*D/2, (g+1)*D/2).
   constexpr int kOCols = D / 2;
   const int row = 32 * q + lane;
   const float inv_l = 1.f / rs.l[tile][row];
-  const int32_t t = c0 + row0 + row;
-  const bool store = row < rows_valid;
+  const int32_t t = c0 + tr.tok0 + (row >> tr.lg);
+  const int32_t h = tr.head0 + (row & ((1 << tr.lg) - 1));
+  const bool store = row < tr.rows_valid;
   const uint32_t tl = tmem + (static_cast<uint32_t>(32 * q) << 16);
   __nv_bfloat16 *orow = a.out + ((int64_t)t * a.Hq + h) * D + g * kOCols;
 #pragma unroll
@@ -424,8 +443,12 @@ __device__ __forceinline__ void softmax_tile_role(const AttnArgs &a, int tile, i
   if (g == 0 && store && a.lse) a.lse[(int64_t)h * a.N + t] = (rs.m[tile][row] + log2f(rs.l[tile][row])) * kLn2;
 }
 
-// One CTA = one 128-row query tile of a segment for the query heads h0 (and
-// h0 + 1 when the GQA group is even): both share every K/V tile.
+// One CTA = two 128-row query tiles of one segment that share every K/V tile
+// (one tile when the second would hold no valid row).  With lg = 0 (odd or
+// non-dividing GQA group) the tiles are 128 tokens of the query heads h0 and
+// h0 + 1 of one kv head; with lg = log2(G) each row is a (token, head) pair of
+// the G query heads of kv head g, so a tile covers 128 / G tokens and a
+// single decode token still fills G rows.
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_constant__ AttnArgs a) {
   using L = SmemLayout<D>;
@@ -443,16 +466,38 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   const int2 pr = a.pairs[pair_idx];
   const int32_t s = pr.x, m = pr.y;
   const int32_t hsel = blockIdx.x % a.heads_per_pair;
-  const bool two = (a.group & 1) == 0;  // two query heads of one kv head per CTA
-  const int32_t h0 = two ? 2 * hsel : hsel;
-  const int32_t g = h0 / a.group;
   const int32_t c0 = a.cu[s];
   const int32_t n = a.cu[s + 1] - c0;
   const int32_t P = a.pos[c0];
-  const int32_t row0 = m * kBlockM;
-  const int32_t rows_valid = min(kBlockM, n - row0);
+  TileRows tr0, tr1;
+  int32_t g;
+  bool two;
+  if (a.lg > 0) {
+    const int32_t subs = a.group >> 1;  // CTAs per kv head for one 128-token item
+    g = hsel / subs;
+    const int32_t tpt = kBlockM >> a.lg;
+    tr0.tok0 = m * kBlockM + (hsel - g * subs) * 2 * tpt;
+    tr1.tok0 = tr0.tok0 + tpt;
+    tr0.head0 = tr1.head0 = g * a.group;
+    tr0.lg = tr1.lg = a.lg;
+    tr0.rows_valid = min(kBlockM, max(0, n - tr0.tok0) << a.lg);
+    tr1.rows_valid = min(kBlockM, max(0, n - tr1.tok0) << a.lg);
+    if (tr0.rows_valid == 0) return;  // every token of this CTA lies past the segment (uniform)
+    two = tr1.rows_valid > 0;
+  } else {
+    two = (a.group & 1) == 0;  // two query heads of one kv head per CTA
+    const int32_t h0 = two ? 2 * hsel : hsel;
+    g = h0 / a.group;
+    tr0.tok0 = tr1.tok0 = m * kBlockM;
+    tr0.head0 = h0;
+    tr1.head0 = h0 + 1;
+    tr0.lg = tr1.lg = 0;
+    tr0.rows_valid = tr1.rows_valid = min(kBlockM, n - m * kBlockM);
+  }
+  const TileRows &trl = two ? tr1 : tr0;  // the tile holding the CTA's last token
+  const int32_t end_tok = trl.tok0 + (trl.rows_valid >> trl.lg);
   const int32_t Tp = (P + kBlockN - 1) / kBlockN;  // prefix KV tiles
-  const int32_t T = Tp + m + 1;                    // + own tiles up to the diagonal
+  const int32_t T = Tp + (end_tok - 1) / kBlockN + 1;  // + own tiles up to the last token's
 
   const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
   auto slot_addr = [&](int slot) { return sbase + L::kRing + slot * L::kTileBytes; };
@@ -488,7 +533,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     // ------------------------------------------------------------ softmax + epilogue
     const int tile = warp >> 3;
     if (tile == 0 || two)
-      softmax_tile_role<D>(a, tile, h0 + tile, T, Tp, P, c0, row0, rows_valid, tmem, bars, row_stats, abort_flag);
+      softmax_tile_role<D>(a, tile, tile ? tr1 : tr0, T, Tp, P, c0, tmem, bars, row_stats, abort_flag);
   } else if (warp == kWarpTma) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
@@ -500,11 +545,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         tma_prefetch_desc(&a.tm_vc);
       }
       mbar_arrive_expect_tx(bar(kBarQFull), (two ? 2 : 1) * L::kTileBytes);
+      // box {64, 1, 128} of tm_q, or {64, G, 128 / G} of tm_qp: 128 rows of 128 bytes either way
+      const void *qmap = a.lg > 0 ? static_cast<const void *>(&a.tm_qp) : static_cast<const void *>(&a.tm_q);
 #pragma unroll
       for (int hf = 0; hf < kHalves; ++hf) {
-        tma_load_3d(sbase + L::kQ0 + hf * L::kHalfBytes, &a.tm_q, bar(kBarQFull), hf * 64, h0, c0 + row0);
+        tma_load_3d(sbase + L::kQ0 + hf * L::kHalfBytes, qmap, bar(kBarQFull), hf * 64, tr0.head0, c0 + tr0.tok0);
         if (two)
-          tma_load_3d(sbase + L::kQ1 + hf * L::kHalfBytes, &a.tm_q, bar(kBarQFull), hf * 64, h0 + 1, c0 + row0);
+          tma_load_3d(sbase + L::kQ1 + hf * L::kHalfBytes, qmap, bar(kBarQFull), hf * 64, tr1.head0,
+                      c0 + tr1.tok0);
       }
       const int32_t pages_per_tile = kBlockN / a.page_size;
       const uint32_t page_bytes = a.page_size * 128u;
@@ -699,11 +747,20 @@ UNIP_API int32_t unip_prefill_attention(const void *q, const void *k, const void
   AttnArgs args;
   memset(&args, 0, sizeof(args));
   const cuuint32_t box3[3] = {64, 1, kBlockM};
+  // Even groups that divide 128 put (token, head) pairs on a tile's rows.
+  const int32_t G = Hq / Hkv;
+  int32_t lg = 0;
+  if (G % 2 == 0 && kBlockM % G == 0)
+    while ((1 << lg) < G) ++lg;
   {
     const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)Hq, (cuuint64_t)total_tokens};
     const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)Hq * D * 2};
     if (encode_tiled(&args.tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(q), dims, strides, box3,
                      CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+      return UNIP_ERR_CUDA;
+    const cuuint32_t boxp[3] = {64, (cuuint32_t)G, (cuuint32_t)(kBlockM / G)};
+    if (lg > 0 && encode_tiled(&args.tm_qp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(q), dims,
+                               strides, boxp, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
       return UNIP_ERR_CUDA;
   }
   {
@@ -747,7 +804,8 @@ UNIP_API int32_t unip_prefill_attention(const void *q, const void *k, const void
   args.S = num_segs;
   args.N = total_tokens;
   args.Hq = Hq;
-  args.group = Hq / Hkv;
+  args.group = G;
+  args.lg = lg;
   args.heads_per_pair = (args.group % 2 == 0) ? Hq / 2 : Hq;
   args.num_pages = has_cache ? paged->num_pages : 0;
   args.page_size = has_cache ? paged->page_size : 16;

@@ -495,15 +495,19 @@ UNIP_API int32_t unip_select_gather(const float *imp, const int32_t *blk_cu, con
                                     int32_t *positions_kept, int32_t *n_kept, const void *hidden,
                                     int64_t row_stride, int32_t d_model, void *hidden_out, int64_t out_row_stride,
                                     void *workspace, size_t workspace_bytes, void *stream) {
-  if (!hidden || !hidden_out || d_model <= 0 || row_stride < d_model || out_row_stride < d_model)
-    return UNIP_ERR_INVALID_ARGUMENT;
-  if (!aligned16(hidden) || !aligned16(hidden_out) || (d_model % 8) || (row_stride % 8) || (out_row_stride % 8))
-    return UNIP_ERR_ALIGNMENT;
+  // d_model == 0 with both row pointers NULL: selection and indices only, no rows copied.
+  const bool rows = d_model != 0 || hidden || hidden_out;
+  if (rows) {
+    if (!hidden || !hidden_out || d_model <= 0 || row_stride < d_model || out_row_stride < d_model)
+      return UNIP_ERR_INVALID_ARGUMENT;
+    if (!aligned16(hidden) || !aligned16(hidden_out) || (d_model % 8) || (row_stride % 8) || (out_row_stride % 8))
+      return UNIP_ERR_ALIGNMENT;
+  }
   if (num_segs >= kIndexSmemSegs) {  // very many segments: the two-call path
     const int32_t rc = unip_topp_select(imp, blk_cu, cu_seqlens, positions, num_segs, total_tokens, block_size, p,
                                         flags, keep, keep_capacity, gather_idx, cu_seqlens_kept, positions_kept,
                                         n_kept, workspace, workspace_bytes, stream);
-    if (rc != UNIP_OK) return rc;
+    if (rc != UNIP_OK || !rows) return rc;
     return unip_gather_tokens(hidden, total_tokens, row_stride, d_model, gather_idx, n_kept, total_tokens,
                               hidden_out, out_row_stride, stream);
   }
@@ -561,10 +565,10 @@ UNIP_API int32_t unip_select_gather(const float *imp, const int32_t *blk_cu, con
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   const cudaError_t e = cudaLaunchKernelEx(
-      &cfg, select_gather_kernel, static_cast<const uint4 *>(hidden), total_tokens, (int64_t)(row_stride / 8),
+      &cfg, select_gather_kernel, static_cast<const uint4 *>(hidden), total_tokens, rows ? (int64_t)(row_stride / 8) : 0,
       (int32_t)(d_model / 8), cu_seqlens, positions, blk_cu, (const uint8_t *)keep, (const int32_t *)kept_off,
       (const int32_t *)seg_kept, num_segs, block_size, total_tokens, static_cast<uint4 *>(hidden_out),
-      (int64_t)(out_row_stride / 8), cu_seqlens_kept, n_kept, gather_idx, positions_kept, stage_blocks, status);
+      rows ? (int64_t)(out_row_stride / 8) : 0, cu_seqlens_kept, n_kept, gather_idx, positions_kept, stage_blocks, status);
   return e == cudaSuccess ? UNIP_OK : UNIP_ERR_CUDA;
 }
 

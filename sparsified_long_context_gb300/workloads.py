@@ -310,6 +310,7 @@ def prepacked(seed: int = 3, num_prompts: int = 64, bin_tokens: int = 16384,
     v = _normal_bf16(rng, (n, num_heads_kv, head_dim))
     return Workload("prepacked", num_heads_q, num_heads_kv, head_dim, _cu(packed_lengths),
                     _positions_for(packed_lengths, [0] * num_prompts), q, k, v,
+                    block_size=64, top_p=0.95,  # selection settings of the long-context layer
                     seg_mask=np.ones(num_prompts, np.uint8),
                     meta={"lengths": packed_lengths, "prompt_order": order, "bins": bins,
                           "bin_tokens": bin_tokens, "heavy_rows": heavy})

@@ -39,7 +39,9 @@ def test_tiny_packed_full():
 
 @pytest.mark.parametrize("lengths,hq,hkv,d", [
     ([1], 2, 1, 64), ([1, 1, 1], 4, 2, 128), ([127, 128, 129], 4, 4, 64), ([0, 300, 0, 5], 8, 2, 128),
-    ([256, 1, 383], 2, 2, 128), ([1000], 8, 1, 64)])
+    ([256, 1, 383], 2, 2, 128), ([1000], 8, 1, 64),
+    # groups of 16 and 32 heads (8 and 4 tokens per tile), an even group that does not divide 128, an odd one
+    ([1, 37, 200], 16, 1, 64), ([3, 40, 129], 32, 1, 128), ([5, 70, 131], 12, 2, 64), ([9, 130], 6, 2, 128)])
 def test_packed_edge_shapes(lengths, hq, hkv, d):
     _check(W.packed(lengths, hq, hkv, d, seed=sum(lengths) + hq + d))
 
@@ -69,6 +71,44 @@ def _chunk_with_prefix(P, n, hq, hkv, d, page, seed):
                                         (513, 512, 16, 128)])
 def test_prefix_from_pages(P, n, page, d):
     _check(_chunk_with_prefix(P, n, 4, 2, d, page, seed=P + n))
+
+
+def _batch_with_prefixes(Ps, ns, hq, hkv, d, page, seed):
+    """Several segments, each continuing its own prefix; all prefixes share one shuffled page pool."""
+    rng = np.random.default_rng(seed)
+    pages = [max(0, -(-P // page)) for P in Ps]
+    total = sum(pages)
+    perm = rng.permutation(total + 3).astype(np.int32)
+    kp = np.zeros((total + 3, page, hkv, d), np.uint16)
+    vp = np.zeros_like(kp)
+    bt = np.full((len(Ps), max(max(pages), 1)), -1, np.int32)
+    qs, ks, vs = [], [], []
+    off = 0
+    for s, (P, n) in enumerate(zip(Ps, ns)):
+        k_all = W.f32_to_bf16_bits(rng.standard_normal((P + n, hkv, d), dtype=np.float32))
+        v_all = W.f32_to_bf16_bits(rng.standard_normal((P + n, hkv, d), dtype=np.float32))
+        for p in range(pages[s]):
+            a, b = p * page, min(P, (p + 1) * page)
+            phys = perm[off + p]
+            kp[phys, : b - a], vp[phys, : b - a] = k_all[a:b], v_all[a:b]
+            bt[s, p] = phys
+        off += pages[s]
+        qs.append(W.f32_to_bf16_bits(rng.standard_normal((n, hq, d), dtype=np.float32)))
+        ks.append(k_all[P:])
+        vs.append(v_all[P:])
+    cu = np.concatenate([[0], np.cumsum(ns)]).astype(np.int32)
+    pos = np.concatenate([np.arange(P, P + n) for P, n in zip(Ps, ns)]).astype(np.int32)
+    cache = W.PagedCache(total + 3, page, hkv, d, "array", kp, vp)
+    return W.Workload(f"decode_batch_g{hq // hkv}", hq, hkv, d, cu, pos, np.concatenate(qs), np.concatenate(ks),
+                      np.concatenate(vs), cache=cache, block_table=bt)
+
+
+@pytest.mark.parametrize("hq,hkv,d", [(32, 8, 128), (8, 1, 64), (4, 2, 128), (6, 2, 64)])
+def test_decode_batch_with_prefixes(hq, hkv, d):
+    """Decode tokens and short chunks behind cached prefixes, as in a continuous-batching step."""
+    Ps = [1000, 17, 300, 2048, 5, 64, 129, 0]
+    ns = [1, 1, 2, 5, 33, 65, 1, 3]
+    _check(_batch_with_prefixes(Ps, ns, hq, hkv, d, 16, seed=hq * 100 + d))
 
 
 def test_chunked_equals_one_shot():
