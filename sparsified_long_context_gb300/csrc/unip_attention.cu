@@ -535,9 +535,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     if (tile == 0 || two)
       softmax_tile_role<D>(a, tile, tile ? tr1 : tr0, T, Tp, P, c0, tmem, bars, row_stats, abort_flag);
   } else if (warp == kWarpTma) {
-    // ------------------------------------------------------------ TMA producer
+    // ------------------------------------------------------------ TMA producer (whole warp)
     if (lane == 0) {
-      tma_prefetch_desc(&a.tm_q);
+      tma_prefetch_desc(a.lg > 0 ? &a.tm_qp : &a.tm_q);
       tma_prefetch_desc(&a.tm_k);
       tma_prefetch_desc(&a.tm_v);
       if (Tp > 0) {
@@ -554,49 +554,63 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           tma_load_3d(sbase + L::kQ1 + hf * L::kHalfBytes, qmap, bar(kBarQFull), hf * 64, tr1.head0,
                       c0 + tr1.tok0);
       }
-      const int32_t pages_per_tile = kBlockN / a.page_size;
-      const uint32_t page_bytes = a.page_size * 128u;
-      int32_t issued = 0;
-      for (int32_t ld = 0; ld < 2 * T; ++ld) {
-        const int slot = ld % kStages;
-        if (ld >= kStages &&
-            !mbar_wait(bar(kBarSlotEmpty0 + slot), ((ld / kStages) - 1) & 1, abort_flag, a.status))
-          break;
-        const int32_t j = ld >> 1;
-        const bool is_v = ld & 1;
-        const uint32_t dst = slot_addr(slot);
-        const uint32_t fb = bar(kBarSlotFull0 + slot);
-        mbar_arrive_expect_tx(fb, L::kTileBytes);
-        if (j < Tp) {
-          const void *map = is_v ? static_cast<const void *>(&a.tm_vc) : static_cast<const void *>(&a.tm_kc);
-          const int32_t first_page = j * pages_per_tile;
-          for (int32_t pi = 0; pi < pages_per_tile; ++pi) {
-            const int32_t lp = first_page + pi;
-            int32_t phys = a.num_pages;  // out of range -> zero fill
-            if (lp * a.page_size < P) {
-              const int32_t e = a.block_table[(int64_t)s * a.max_pages + lp];
-              if (e >= 0 && e < a.num_pages) phys = e;
-              else if (!is_v) atomicOr(a.status, UNIP_DEV_BAD_PAGES);
-            }
-#pragma unroll
-            for (int hf = 0; hf < kHalves; ++hf)
-              tma_load_4d(dst + hf * L::kHalfBytes + pi * page_bytes, map, fb, hf * 64, g, 0, phys);
-          }
-        } else {
-          const void *map = is_v ? static_cast<const void *>(&a.tm_v) : static_cast<const void *>(&a.tm_k);
-          const int32_t krow = c0 + (j - Tp) * kBlockN;
-#pragma unroll
-          for (int hf = 0; hf < kHalves; ++hf) tma_load_3d(dst + hf * L::kHalfBytes, map, fb, hf * 64, g, krow);
+    }
+    // Lane pi (< pages per tile) copies page pi of every prefix tile.  Its block-table entry is
+    // read two tiles ahead, so that the read overlaps earlier copies instead of stalling each one.
+    const int32_t pages_per_tile = kBlockN / a.page_size;
+    const uint32_t page_bytes = a.page_size * 128u;
+    const int64_t bt_row = (int64_t)s * a.max_pages;
+    auto lookup = [&](int32_t j) -> int32_t {
+      int32_t phys = a.num_pages;  // out of range -> zero fill
+      if (j < Tp && lane < pages_per_tile) {
+        const int32_t lp = j * pages_per_tile + lane;
+        if (lp * a.page_size < P) {
+          const int32_t e = a.block_table[bt_row + lp];
+          if (e >= 0 && e < a.num_pages) phys = e;
+          else atomicOr(a.status, UNIP_DEV_BAD_PAGES);
         }
-        issued = ld + 1;
       }
-      if (*abort_flag) {
-        // Let copies already in flight land before the CTA's shared memory is released.
-        for (int32_t ld = max(0, issued - kStages); ld < issued; ++ld) {
-          const uint64_t t0 = globaltimer_ns();
-          while (!mbar_try_wait(bar(kBarSlotFull0 + ld % kStages), (ld / kStages) & 1) &&
-                 globaltimer_ns() - t0 < kWaitLimitNs) {
-          }
+      return phys;
+    };
+    int32_t phys_cur = lookup(0), phys_next = lookup(1);
+    int32_t issued = 0;
+    for (int32_t ld = 0; ld < 2 * T; ++ld) {
+      const int slot = ld % kStages;
+      int ok = 1;
+      if (lane == 0 && ld >= kStages)
+        ok = mbar_wait(bar(kBarSlotEmpty0 + slot), ((ld / kStages) - 1) & 1, abort_flag, a.status);
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      const int32_t j = ld >> 1;
+      const bool is_v = ld & 1;
+      const uint32_t dst = slot_addr(slot);
+      const uint32_t fb = bar(kBarSlotFull0 + slot);
+      if (lane == 0) mbar_arrive_expect_tx(fb, L::kTileBytes);
+      __syncwarp();
+      if (j < Tp) {
+        const void *map = is_v ? static_cast<const void *>(&a.tm_vc) : static_cast<const void *>(&a.tm_kc);
+        if (lane < pages_per_tile) {
+#pragma unroll
+          for (int hf = 0; hf < kHalves; ++hf)
+            tma_load_4d(dst + hf * L::kHalfBytes + lane * page_bytes, map, fb, hf * 64, g, 0, phys_cur);
+        }
+        if (is_v) {
+          phys_cur = phys_next;
+          phys_next = lookup(j + 2);
+        }
+      } else if (lane == 0) {
+        const void *map = is_v ? static_cast<const void *>(&a.tm_v) : static_cast<const void *>(&a.tm_k);
+        const int32_t krow = c0 + (j - Tp) * kBlockN;
+#pragma unroll
+        for (int hf = 0; hf < kHalves; ++hf) tma_load_3d(dst + hf * L::kHalfBytes, map, fb, hf * 64, g, krow);
+      }
+      issued = ld + 1;
+    }
+    if (lane == 0 && *abort_flag) {
+      // Let copies already in flight land before the CTA's shared memory is released.
+      for (int32_t ld = max(0, issued - kStages); ld < issued; ++ld) {
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(bar(kBarSlotFull0 + ld % kStages), (ld / kStages) & 1) &&
+               globaltimer_ns() - t0 < kWaitLimitNs) {
         }
       }
     }
