@@ -84,15 +84,17 @@ struct TileRows {
 __global__ void __launch_bounds__(kPlanThreads) attn_plan_kernel(const int32_t *__restrict__ cu,
                                                                  const int32_t *__restrict__ pos, int32_t S,
                                                                  int32_t N, int32_t has_cache, int32_t page_size,
-                                                                 int32_t max_pages, int32_t *__restrict__ header,
+                                                                 int32_t max_pages, int32_t lg,
+                                                                 int32_t *__restrict__ header,
                                                                  int2 *__restrict__ pairs, int32_t max_pairs,
                                                                  uint32_t *__restrict__ status) {
-  __shared__ int32_t s_hist[kHistBins];
+  // [0]: heavy pairs (every tile row valid, or no cached prefix), [1]: light ones
+  __shared__ int32_t s_hist[2][kHistBins];
   __shared__ int32_t s_scan[32];
   __shared__ int32_t s_base[kPlanThreads + 1];
   __shared__ uint32_t s_err;
   const int tid = threadIdx.x;
-  for (int b = tid; b < kHistBins; b += kPlanThreads) s_hist[b] = 0;
+  for (int b = tid; b < 2 * kHistBins; b += kPlanThreads) (&s_hist[0][0])[b] = 0;
   if (tid == 0) s_err = (cu[0] != 0 || cu[S] != N) ? UNIP_DEV_BAD_SEQLENS : 0u;
   __syncthreads();
 
@@ -152,7 +154,10 @@ __global__ void __launch_bounds__(kPlanThreads) attn_plan_kernel(const int32_t *
   s_base[tid] = my_base;
   if (tid == 0) s_base[kPlanThreads] = total_pairs;
   __syncthreads();
-  auto locate = [&](int32_t p, int32_t &seg, int32_t &m, int32_t &cost) {
+  // A pair is light when the first query tile of its CTAs has fewer than 128 valid rows and its
+  // keys include a cached prefix (a decode token, a short chunk): such CTAs stream the prefix at
+  // HBM speed with an idle tensor pipe.
+  auto locate = [&](int32_t p, int32_t &seg, int32_t &m, int32_t &cost, int32_t &light) {
     int32_t lo = 0, hi = kPlanThreads - 1;
     while (lo < hi) {
       const int32_t mid = (lo + hi + 1) >> 1;
@@ -160,44 +165,58 @@ __global__ void __launch_bounds__(kPlanThreads) attn_plan_kernel(const int32_t *
     }
     int32_t rem = p - s_base[lo];
     for (int32_t sg = min(S, lo * per);; ++sg) {
-      const int32_t nt = (cu[sg + 1] - cu[sg] + kBlockM - 1) / kBlockM;
+      const int32_t len = cu[sg + 1] - cu[sg];
+      const int32_t nt = (len + kBlockM - 1) / kBlockM;
       if (rem < nt) {
         seg = sg;
         m = rem;
-        cost = (pos[cu[sg]] + kBlockN - 1) / kBlockN + rem + 1;
+        const int32_t P = pos[cu[sg]];
+        cost = (P + kBlockN - 1) / kBlockN + rem + 1;
+        const int32_t tok = len - rem * kBlockM;
+        light = (P > 0 && tok < (kBlockM >> lg)) ? 1 : 0;
         return;
       }
       rem -= nt;
     }
   };
-  // Histogram of pair costs (number of KV tiles).
+  // Histograms of pair costs (number of KV tiles), per class.
   for (int32_t p = tid; p < total_pairs; p += kPlanThreads) {
-    int32_t sg, m, cost;
-    locate(p, sg, m, cost);
-    atomicAdd(&s_hist[min(cost, kHistBins - 1)], 1);
+    int32_t sg, m, cost, light;
+    locate(p, sg, m, cost, light);
+    atomicAdd(&s_hist[light][min(cost, kHistBins - 1)], 1);
   }
   __syncthreads();
-  // Bin start offsets in decreasing cost order.
+  // Bin start offsets in decreasing cost order: ranks inside each class.
   constexpr int kPer = kHistBins / kPlanThreads;
-  int32_t cnt[kPer];
-  int32_t local = 0;
+  int32_t class_total[2];
 #pragma unroll
-  for (int r = 0; r < kPer; ++r) {
-    cnt[r] = s_hist[kHistBins - 1 - (tid * kPer + r)];
-    local += cnt[r];
-  }
-  int32_t dummy;
-  int32_t run = block_excl_scan<int32_t>(local, s_scan, &dummy);
+  for (int c = 0; c < 2; ++c) {
+    int32_t cnt[kPer];
+    int32_t local = 0;
 #pragma unroll
-  for (int r = 0; r < kPer; ++r) {
-    s_hist[kHistBins - 1 - (tid * kPer + r)] = run;
-    run += cnt[r];
+    for (int r = 0; r < kPer; ++r) {
+      cnt[r] = s_hist[c][kHistBins - 1 - (tid * kPer + r)];
+      local += cnt[r];
+    }
+    int32_t run = block_excl_scan<int32_t>(local, s_scan, &class_total[c]);
+#pragma unroll
+    for (int r = 0; r < kPer; ++r) {
+      s_hist[c][kHistBins - 1 - (tid * kPer + r)] = run;
+      run += cnt[r];
+    }
   }
   __syncthreads();
+  // Merge the two longest-first lists so that both advance at the same rate: heavy rank i sits
+  // at fraction i / H of the order and light rank k at k / L (heavy first on ties), so the
+  // prefix streaming of light pairs overlaps the tensor work of heavy ones.
+  const int64_t H = class_total[0], Lc = class_total[1];
   for (int32_t p = tid; p < total_pairs; p += kPlanThreads) {
-    int32_t sg, m, cost;
-    locate(p, sg, m, cost);
-    pairs[atomicAdd(&s_hist[min(cost, kHistBins - 1)], 1)] = make_int2(sg, m);
+    int32_t sg, m, cost, light;
+    locate(p, sg, m, cost, light);
+    const int64_t r = atomicAdd(&s_hist[light][min(cost, kHistBins - 1)], 1);
+    int64_t at = r;
+    if (H > 0 && Lc > 0) at = light ? r + (r * H) / Lc + 1 : r + (r * Lc + H - 1) / H;
+    pairs[at] = make_int2(sg, m);
   }
   if (tid == 0) header[0] = total_pairs;
 }
@@ -205,7 +224,8 @@ __global__ void __launch_bounds__(kPlanThreads) attn_plan_kernel(const int32_t *
 // ---------------------------------------------------------------------------
 // Attention kernel
 // ---------------------------------------------------------------------------
-constexpr int kStages = 4;        // K/V ring slots (each holds one K or one V tile)
+constexpr int kStages = 4;        // K/V ring slots (each holds one K or one V tile) with two query tiles
+constexpr int kStagesMax = 5;     // with one query tile the second Q buffer becomes a fifth slot
 // 4 softmax warpgroups (8 warps per query tile, 16 rows each) + one control
 // warpgroup (TMA warp, MMA warp, 2 idle warps); 96 registers per thread.
 constexpr int kThreads = 640;
@@ -225,14 +245,15 @@ struct SmemLayout {
 
 enum BarId {
   kBarQFull = 0,
-  kBarSlotFull0 = 1,                   // + slot
-  kBarSlotEmpty0 = 1 + kStages,        // + slot
-  kBarSFull0 = 1 + 2 * kStages,        // + tile: S in TMEM
-  kBarPFull0 = 3 + 2 * kStages,        // + tile: P in TMEM and O rescaled (both column halves)
-  kBarODone0 = 5 + 2 * kStages,        // + tile: last PV done
-  kBarXchg0 = 7 + 2 * kStages,         // + tile: final row statistics in shared memory
-  kBarFinal = 11 + 2 * kStages,
-  kNumBars = 12 + 2 * kStages
+  kBarSlotFull0 = 1,                      // + slot
+  kBarSlotEmpty0 = 1 + kStagesMax,        // + slot
+  kBarSFull0 = 1 + 2 * kStagesMax,        // + tile: S in TMEM
+  kBarPFull0 = 3 + 2 * kStagesMax,        // + tile: P in TMEM and O rescaled (both column halves)
+  kBarODone0 = 5 + 2 * kStagesMax,        // + tile: last PV done
+  kBarXchg0 = 7 + 2 * kStagesMax,         // + tile: final row statistics in shared memory
+  kBarFinal = 11 + 2 * kStagesMax,
+  kBarPVDone = 12 + 2 * kStagesMax,       // one query tile: each PV done (O may be rescaled)
+  kNumBars = 13 + 2 * kStagesMax
 };
 
 __device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
@@ -282,10 +303,10 @@ struct RowStats {
   float l[2][128];  // [tile][row] final row sum
 };
 
-template <int D>
+template <int D, bool db>
 __device__ __forceinline__ void softmax_tile_role(const AttnArgs &a, int tile, const TileRows tr, int32_t T,
-                                                  int32_t Tp, int32_t P, int32_t c0, uint32_t tmem, uint64_t *bars,
-                                                  RowStats &rs, volatile int *abort_flag) {
+                                                  int32_t Tp, int32_t P, int32_t c0, uint32_t tmem,
+                                                  uint64_t *bars, RowStats &rs, volatile int *abort_flag) {
   const int wt = (threadIdx.x >> 5) & 7;
   const int lane = threadIdx.x & 31;
   const int q = wt & 3, g = wt >> 2;
@@ -293,10 +314,8 @@ __device__ __forceinline__ void softmax_tile_role(const AttnArgs &a, int tile, c
   const int R0 = lane_base + (lane >> 2), R1 = R0 + 8;  // tile rows held by this thread
   const int cq = 2 * (lane & 3);                         // first column of this thread in a chunk
   const uint32_t tw = tmem + (lane_base << 16);
-  const uint32_t s_col = tile * kBlockN;
+  // db (one query tile): S and P of KV tile j alternate between the two S regions and their barriers.
   const uint32_t o_col = kTmemO + tile * 128;
-  const uint32_t bar_s = smem_u32(&bars[kBarSFull0 + tile]);
-  const uint32_t bar_p = smem_u32(&bars[kBarPFull0 + tile]);
   const uint32_t bar_o = smem_u32(&bars[kBarODone0 + tile]);
   const uint32_t bar_x = smem_u32(&bars[kBarXchg0 + tile]);
   const float c = a.scale_log2;
@@ -305,7 +324,11 @@ __device__ __forceinline__ void softmax_tile_role(const AttnArgs &a, int tile, c
   const bool active = static_cast<int32_t>(lane_base) < tr.rows_valid;
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
   for (int32_t j = 0; j < T; ++j) {
-    if (!mbar_wait(bar_s, j & 1, abort_flag, a.status)) return;
+    const int buf = db ? (j & 1) : tile;
+    const uint32_t par = db ? ((j >> 1) & 1) : (j & 1);
+    const uint32_t s_col = buf * kBlockN;
+    const uint32_t bar_p = smem_u32(&bars[kBarPFull0 + buf]);
+    if (!mbar_wait(smem_u32(&bars[kBarSFull0 + buf]), par, abort_flag, a.status)) return;
     if (!active) {
       mbar_arrive(bar_p);
       continue;
@@ -360,9 +383,12 @@ __device__ __forceinline__ void softmax_tile_role(const AttnArgs &a, int tile, c
     if (need1) { al1 = ex2_approx(m1 - n1); m1 = n1; }
     const float mb0 = (m0 == -INFINITY) ? 0.f : m0, mb1 = (m1 == -INFINITY) ? 0.f : m1;
     float r00 = 0.f, r01 = 0.f, r10 = 0.f, r11 = 0.f;
-    // O is rescaled before the PV of this tile accumulates into it; PV of the previous tile is
-    // complete here because S of this tile was committed after it.
+    // O is rescaled before the PV of this tile accumulates into it.  With two query tiles the PV of
+    // the previous KV tile is complete here because S of this one was committed after it; with
+    // one (db) S runs ahead, so that PV is waited for.
     if (j >= 1 && __any_sync(0xffffffffu, need0 || need1)) {
+      if (db && !mbar_wait(smem_u32(&bars[kBarPVDone]), (j - 1) & 1, abort_flag, a.status)) return;
+      tc_fence_after();
 #pragma unroll 1
       for (int part = 0; part < D / 32; ++part) {
         float o[16];
@@ -500,12 +526,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   const int32_t T = Tp + (end_tok - 1) / kBlockN + 1;  // + own tiles up to the last token's
 
   const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
-  auto slot_addr = [&](int slot) { return sbase + L::kRing + slot * L::kTileBytes; };
+  // K/V ring: four slots after both Q buffers, or five from the second Q buffer on when it is unused.
+  const int ns = two ? kStages : kStagesMax;
+  const uint32_t ring = two ? L::kRing : L::kQ1;
+  auto slot_addr = [&](int slot) { return sbase + ring + slot * L::kTileBytes; };
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
   if (threadIdx.x == 0) {
     mbar_init(bar(kBarQFull), 1);
-    for (int i = 0; i < kStages; ++i) {
+    for (int i = 0; i < kStagesMax; ++i) {
       mbar_init(bar(kBarSlotFull0 + i), 1);
       mbar_init(bar(kBarSlotEmpty0 + i), 1);
     }
@@ -516,6 +545,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     }
     for (int i = 0; i < 2; ++i) mbar_init(bar(kBarXchg0 + i), 2 * kBlockM);
     mbar_init(bar(kBarFinal), 1);
+    mbar_init(bar(kBarPVDone), 1);
     s_abort = 0;
     fence_mbar_init();
   }
@@ -532,8 +562,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   if (warp < 16) {
     // ------------------------------------------------------------ softmax + epilogue
     const int tile = warp >> 3;
-    if (tile == 0 || two)
-      softmax_tile_role<D>(a, tile, tile ? tr1 : tr0, T, Tp, P, c0, tmem, bars, row_stats, abort_flag);
+    if (two)
+      softmax_tile_role<D, false>(a, tile, tile ? tr1 : tr0, T, Tp, P, c0, tmem, bars, row_stats, abort_flag);
+    else if (tile == 0)
+      softmax_tile_role<D, true>(a, 0, tr0, T, Tp, P, c0, tmem, bars, row_stats, abort_flag);
   } else if (warp == kWarpTma) {
     // ------------------------------------------------------------ TMA producer (whole warp)
     if (lane == 0) {
@@ -555,30 +587,29 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                       c0 + tr1.tok0);
       }
     }
-    // Lane pi (< pages per tile) copies page pi of every prefix tile.  Its block-table entry is
-    // read two tiles ahead, so that the read overlaps earlier copies instead of stalling each one.
-    const int32_t pages_per_tile = kBlockN / a.page_size;
+    // Lane pi (< pages per tile) copies page pi of every prefix tile.  Block-table entries come in
+    // batches of 32 (one per lane, covering 32 / pages-per-tile tiles), fetched two batches ahead
+    // and validated only when used, so no copy waits on a block-table read.
+    const int32_t ppt = kBlockN / a.page_size;  // 1, 2, 4 or 8
+    const int32_t tpb = 32 / ppt;               // tiles per batch (a power of two)
     const uint32_t page_bytes = a.page_size * 128u;
     const int64_t bt_row = (int64_t)s * a.max_pages;
-    auto lookup = [&](int32_t j) -> int32_t {
-      int32_t phys = a.num_pages;  // out of range -> zero fill
-      if (j < Tp && lane < pages_per_tile) {
-        const int32_t lp = j * pages_per_tile + lane;
-        if (lp * a.page_size < P) {
-          const int32_t e = a.block_table[bt_row + lp];
-          if (e >= 0 && e < a.num_pages) phys = e;
-          else atomicOr(a.status, UNIP_DEV_BAD_PAGES);
-        }
-      }
-      return phys;
+    auto fetch = [&](int32_t j0) -> int32_t {  // raw entry of logical page j0 * ppt + lane, or -1
+      const int32_t lp = j0 * ppt + lane;
+      return (j0 < Tp && lp * a.page_size < P) ? __ldg(&a.block_table[bt_row + lp]) : -1;
     };
-    int32_t phys_cur = lookup(0), phys_next = lookup(1);
+    int32_t bt_cur = fetch(0), bt_nxt = fetch(tpb), bt_nx2 = fetch(2 * tpb);
     int32_t issued = 0;
+    int slot = -1;
+    uint32_t round = 0;  // load ld fills slot ld % ns for the (ld / ns)-th time
     for (int32_t ld = 0; ld < 2 * T; ++ld) {
-      const int slot = ld % kStages;
+      if (++slot == ns) {
+        slot = 0;
+        ++round;
+      }
       int ok = 1;
-      if (lane == 0 && ld >= kStages)
-        ok = mbar_wait(bar(kBarSlotEmpty0 + slot), ((ld / kStages) - 1) & 1, abort_flag, a.status);
+      if (lane == 0 && round > 0)
+        ok = mbar_wait(bar(kBarSlotEmpty0 + slot), (round - 1) & 1, abort_flag, a.status);
       if (!__shfl_sync(0xffffffffu, ok, 0)) break;
       const int32_t j = ld >> 1;
       const bool is_v = ld & 1;
@@ -587,15 +618,22 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       if (lane == 0) mbar_arrive_expect_tx(fb, L::kTileBytes);
       __syncwarp();
       if (j < Tp) {
+        if (!is_v && j > 0 && (j & (tpb - 1)) == 0) {
+          bt_cur = bt_nxt;
+          bt_nxt = bt_nx2;
+          bt_nx2 = fetch(j + 2 * tpb);
+        }
+        const int32_t e = __shfl_sync(0xffffffffu, bt_cur, (j & (tpb - 1)) * ppt + (lane & (ppt - 1)));
         const void *map = is_v ? static_cast<const void *>(&a.tm_vc) : static_cast<const void *>(&a.tm_kc);
-        if (lane < pages_per_tile) {
+        if (lane < ppt) {
+          int32_t phys = a.num_pages;  // past the prefix end, or a bad entry: zero fill
+          if ((j * ppt + lane) * a.page_size < P) {
+            if (e >= 0 && e < a.num_pages) phys = e;
+            else if (!is_v) atomicOr(a.status, UNIP_DEV_BAD_PAGES);
+          }
 #pragma unroll
           for (int hf = 0; hf < kHalves; ++hf)
-            tma_load_4d(dst + hf * L::kHalfBytes + lane * page_bytes, map, fb, hf * 64, g, 0, phys_cur);
-        }
-        if (is_v) {
-          phys_cur = phys_next;
-          phys_next = lookup(j + 2);
+            tma_load_4d(dst + hf * L::kHalfBytes + lane * page_bytes, map, fb, hf * 64, g, 0, phys);
         }
       } else if (lane == 0) {
         const void *map = is_v ? static_cast<const void *>(&a.tm_v) : static_cast<const void *>(&a.tm_k);
@@ -607,9 +645,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     }
     if (lane == 0 && *abort_flag) {
       // Let copies already in flight land before the CTA's shared memory is released.
-      for (int32_t ld = max(0, issued - kStages); ld < issued; ++ld) {
+      for (int32_t ld = max(0, issued - ns); ld < issued; ++ld) {
         const uint64_t t0 = globaltimer_ns();
-        while (!mbar_try_wait(bar(kBarSlotFull0 + ld % kStages), (ld / kStages) & 1) &&
+        while (!mbar_try_wait(bar(kBarSlotFull0 + ld % ns), (ld / ns) & 1) &&
                globaltimer_ns() - t0 < kWaitLimitNs) {
         }
       }
@@ -623,11 +661,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       // (in 16-byte units) to the start-address field.
       const uint64_t dq0 = sdesc_sw128(sbase + L::kQ0, 16, 1024);
       const uint64_t dq1 = sdesc_sw128(sbase + L::kQ1, 16, 1024);
-      const uint64_t dk = sdesc_sw128(sbase + L::kRing, 16, 1024);
-      const uint64_t dv = sdesc_sw128(sbase + L::kRing, L::kHalfBytes, 1024);
+      const uint64_t dk = sdesc_sw128(sbase + ring, 16, 1024);
+      const uint64_t dv = sdesc_sw128(sbase + ring, L::kHalfBytes, 1024);
       const uint32_t d_s0 = tmem, d_s1 = tmem + kBlockN;
       const uint32_t d_o0 = tmem + kTmemO, d_o1 = tmem + kTmemO + 128;
-      // K_j sits in slot 2*(j&1), V_j in slot 2*(j&1)+1; both complete phase (j>>1)&1.
+      // K_j is load 2j and V_j load 2j+1 of the ring: slot ld % ns, phase (ld / ns) & 1.
       auto slot_desc = [&](uint64_t d, int slot) { return d + ((uint64_t)(slot * L::kTileBytes) >> 4); };
       auto qk = [&](uint32_t d_s, uint64_t dq, uint64_t dkb) {
 #pragma unroll
@@ -643,6 +681,46 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       };
       bool ok = mbar_wait(bar(kBarQFull), 0, abort_flag, a.status) &&
                 mbar_wait(bar(kBarSlotFull0 + 0), 0, abort_flag, a.status);
+      if (!two) {
+        // One query tile: S is double-buffered over both S regions, so QK(j+2) runs while the
+        // softmax of KV tile j does.  Order: QK(0), QK(1), then PV(j), QK(j+2) for each j.
+        if (ok) {
+          tc_fence_after();
+          qk(d_s0, dq0, slot_desc(dk, 0));
+          umma_commit(bar(kBarSFull0 + 0));
+          umma_commit(bar(kBarSlotEmpty0 + 0));
+          if (T > 1) {
+            if ((ok = mbar_wait(bar(kBarSlotFull0 + 2), 0, abort_flag, a.status))) {  // K_1 = load 2
+              qk(d_s1, dq0, slot_desc(dk, 2));
+              umma_commit(bar(kBarSFull0 + 1));
+              umma_commit(bar(kBarSlotEmpty0 + 2));
+            }
+          }
+        }
+        int vslot = 1, kslot = 4 % ns;  // V_0 = load 1, K_2 = load 4
+        uint32_t vphase = 0, kphase = 4 / ns;
+        for (int32_t j = 0; ok && j < T; ++j) {
+          const int buf = j & 1;
+          const uint32_t d_s = tmem + buf * kBlockN;
+          ok = mbar_wait(bar(kBarPFull0 + buf), (j >> 1) & 1, abort_flag, a.status) &&
+               mbar_wait(bar(kBarSlotFull0 + vslot), vphase, abort_flag, a.status);
+          if (!ok) break;
+          tc_fence_after();
+          pv(d_o0, d_s, slot_desc(dv, vslot), j > 0 ? 1u : 0u);
+          umma_commit(bar(kBarPVDone));
+          umma_commit(bar(kBarSlotEmpty0 + vslot));
+          if (j + 1 == T) umma_commit(bar(kBarODone0 + 0));
+          if (j + 2 < T) {
+            if (!(ok = mbar_wait(bar(kBarSlotFull0 + kslot), kphase, abort_flag, a.status))) break;
+            qk(d_s, dq0, slot_desc(dk, kslot));
+            umma_commit(bar(kBarSFull0 + buf));
+            umma_commit(bar(kBarSlotEmpty0 + kslot));
+          }
+          if ((vslot += 2) >= ns) { vslot -= ns; vphase ^= 1u; }
+          if ((kslot += 2) >= ns) { kslot -= ns; kphase ^= 1u; }
+        }
+        ok = false;  // the two-tile schedule below is skipped
+      }
       if (ok) {
         tc_fence_after();
         const uint64_t dk0 = slot_desc(dk, 0);
@@ -654,37 +732,41 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         }
         umma_commit(bar(kBarSlotEmpty0 + 0));
       }
+      int vslot = 1, kslot = 2;            // V_0 = load 1, K_1 = load 2 (ns >= 4)
+      uint32_t vphase = 0, kphase = 0;
       for (int32_t j = 0; ok && j < T; ++j) {
         const bool more = j + 1 < T;
-        const int vslot = 2 * (j & 1) + 1, kslot = 2 * ((j + 1) & 1);
         const uint64_t dvj = slot_desc(dv, vslot), dkn = slot_desc(dk, kslot);
         const uint32_t acc = j > 0 ? 1u : 0u;
         // tile 0: PV(j), then QK(j+1)
         ok = mbar_wait(bar(kBarPFull0 + 0), j & 1, abort_flag, a.status) &&
-             mbar_wait(bar(kBarSlotFull0 + vslot), (j >> 1) & 1, abort_flag, a.status);
+             mbar_wait(bar(kBarSlotFull0 + vslot), vphase, abort_flag, a.status);
         if (!ok) break;
         tc_fence_after();
         pv(d_o0, d_s0, dvj, acc);
         if (!more) umma_commit(bar(kBarODone0 + 0));
         if (!two) umma_commit(bar(kBarSlotEmpty0 + vslot));
         if (more) {
-          if (!(ok = mbar_wait(bar(kBarSlotFull0 + kslot), ((j + 1) >> 1) & 1, abort_flag, a.status))) break;
+          if (!(ok = mbar_wait(bar(kBarSlotFull0 + kslot), kphase, abort_flag, a.status))) break;
           qk(d_s0, dq0, dkn);
           umma_commit(bar(kBarSFull0 + 0));
           if (!two) umma_commit(bar(kBarSlotEmpty0 + kslot));
         }
-        if (!two) continue;
-        // tile 1: PV(j), then QK(j+1)
-        if (!(ok = mbar_wait(bar(kBarPFull0 + 1), j & 1, abort_flag, a.status))) break;
-        tc_fence_after();
-        pv(d_o1, d_s1, dvj, acc);
-        if (!more) umma_commit(bar(kBarODone0 + 1));
-        umma_commit(bar(kBarSlotEmpty0 + vslot));
-        if (more) {
-          qk(d_s1, dq1, dkn);
-          umma_commit(bar(kBarSFull0 + 1));
-          umma_commit(bar(kBarSlotEmpty0 + kslot));
+        if (two) {
+          // tile 1: PV(j), then QK(j+1)
+          if (!(ok = mbar_wait(bar(kBarPFull0 + 1), j & 1, abort_flag, a.status))) break;
+          tc_fence_after();
+          pv(d_o1, d_s1, dvj, acc);
+          if (!more) umma_commit(bar(kBarODone0 + 1));
+          umma_commit(bar(kBarSlotEmpty0 + vslot));
+          if (more) {
+            qk(d_s1, dq1, dkn);
+            umma_commit(bar(kBarSFull0 + 1));
+            umma_commit(bar(kBarSlotEmpty0 + kslot));
+          }
         }
+        if ((vslot += 2) >= ns) { vslot -= ns; vphase ^= 1u; }
+        if ((kslot += 2) >= ns) { kslot -= ns; kphase ^= 1u; }
       }
       // Every tcgen05 op of this CTA has landed before TMEM is released.
       umma_commit(bar(kBarFinal));
@@ -803,8 +885,8 @@ UNIP_API int32_t unip_prefill_attention(const void *q, const void *k, const void
   const int32_t max_pairs = max_pairs_for(total_tokens, num_segs);
   attn_plan_kernel<<<1, kPlanThreads, 0, st>>>(cu_seqlens, positions, num_segs, total_tokens, has_cache ? 1 : 0,
                                                has_cache ? paged->page_size : 16,
-                                               has_cache ? paged->max_pages_per_seq : 0, header, pairs, max_pairs,
-                                               status);
+                                               has_cache ? paged->max_pages_per_seq : 0, lg, header, pairs,
+                                               max_pairs, status);
   if (cudaGetLastError() != cudaSuccess) return UNIP_ERR_CUDA;
 
   args.cu = cu_seqlens;
