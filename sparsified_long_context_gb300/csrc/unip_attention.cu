@@ -231,6 +231,8 @@ constexpr int kStagesMax = 5;     // with one query tile the second Q buffer bec
 constexpr int kThreads = 640;
 constexpr int kWarpTma = 16;
 constexpr int kWarpMma = 17;
+constexpr int kWarpAux0 = 18;     // warps 18, 19: extra issuers of paged K/V copies
+constexpr int kPageIssuers = 3;   // TMA copies issue one at a time per warp: pages go to 3 warps
 
 template <int D>
 struct SmemLayout {
@@ -566,9 +568,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       softmax_tile_role<D, false>(a, tile, tile ? tr1 : tr0, T, Tp, P, c0, tmem, bars, row_stats, abort_flag);
     else if (tile == 0)
       softmax_tile_role<D, true>(a, 0, tr0, T, Tp, P, c0, tmem, bars, row_stats, abort_flag);
-  } else if (warp == kWarpTma) {
-    // ------------------------------------------------------------ TMA producer (whole warp)
-    if (lane == 0) {
+  } else if (warp == kWarpTma || warp >= kWarpAux0) {
+    // ------------------------------------------------------------ TMA producers
+    // Warp 16 loads Q and the segment's own K/V tiles and arms every slot; the page copies of a
+    // prefix tile are split over warps 16, 18 and 19 (page pi by warp pi mod 3), since one
+    // warp issues its TMA copies one after another.  All three follow the same load sequence
+    // and slot waits.
+    const int pw = warp == kWarpTma ? 0 : warp - kWarpAux0 + 1;
+    if (pw == 0 && lane == 0) {
       tma_prefetch_desc(a.lg > 0 ? &a.tm_qp : &a.tm_q);
       tma_prefetch_desc(&a.tm_k);
       tma_prefetch_desc(&a.tm_v);
@@ -599,6 +606,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       return (j0 < Tp && lp * a.page_size < P) ? __ldg(&a.block_table[bt_row + lp]) : -1;
     };
     int32_t bt_cur = fetch(0), bt_nxt = fetch(tpb), bt_nx2 = fetch(2 * tpb);
+    int32_t ph0 = a.num_pages, ph1 = a.num_pages;  // this lane's page of the last two K tiles
+    int32_t last_k = -1;
     int32_t issued = 0;
     int slot = -1;
     uint32_t round = 0;  // load ld fills slot ld % ns for the (ld / ns)-th time
@@ -611,31 +620,58 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       if (lane == 0 && round > 0)
         ok = mbar_wait(bar(kBarSlotEmpty0 + slot), (round - 1) & 1, abort_flag, a.status);
       if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-      const int32_t j = ld >> 1;
-      const bool is_v = ld & 1;
+      // Loads follow the order the MMAs consume them: K_j, V_j alternating with two query tiles;
+      // with one, K runs two tiles ahead of V: K0, K1, V0, K2, V1, ..., K(T-1), V(T-2), V(T-1).
+      int32_t j;
+      bool is_v;
+      if (two) {
+        j = ld >> 1;
+        is_v = ld & 1;
+      } else if (ld < 2) {
+        is_v = ld == 1 && T == 1;
+        j = is_v ? 0 : ld;
+      } else {
+        const int32_t t = ld - 2;
+        if (t < 2 * (T - 2)) {
+          is_v = (t & 1) == 0;
+          j = is_v ? (t >> 1) : (t >> 1) + 2;
+        } else {
+          is_v = true;
+          j = t - T + 2;
+        }
+      }
       const uint32_t dst = slot_addr(slot);
       const uint32_t fb = bar(kBarSlotFull0 + slot);
-      if (lane == 0) mbar_arrive_expect_tx(fb, L::kTileBytes);
+      if (pw == 0 && lane == 0) mbar_arrive_expect_tx(fb, L::kTileBytes);
       __syncwarp();
-      if (j < Tp) {
-        if (!is_v && j > 0 && (j & (tpb - 1)) == 0) {
-          bt_cur = bt_nxt;
-          bt_nxt = bt_nx2;
-          bt_nx2 = fetch(j + 2 * tpb);
-        }
-        const int32_t e = __shfl_sync(0xffffffffu, bt_cur, (j & (tpb - 1)) * ppt + (lane & (ppt - 1)));
-        const void *map = is_v ? static_cast<const void *>(&a.tm_vc) : static_cast<const void *>(&a.tm_kc);
-        if (lane < ppt) {
-          int32_t phys = a.num_pages;  // past the prefix end, or a bad entry: zero fill
-          if ((j * ppt + lane) * a.page_size < P) {
-            if (e >= 0 && e < a.num_pages) phys = e;
-            else if (!is_v) atomicOr(a.status, UNIP_DEV_BAD_PAGES);
+      int32_t phys = a.num_pages;  // past the prefix end, or a bad entry: zero fill
+      if (!is_v) {
+        if (j < Tp) {
+          if (j > 0 && (j & (tpb - 1)) == 0) {
+            bt_cur = bt_nxt;
+            bt_nxt = bt_nx2;
+            bt_nx2 = fetch(j + 2 * tpb);
           }
+          const int32_t e = __shfl_sync(0xffffffffu, bt_cur, (j & (tpb - 1)) * ppt + (lane & (ppt - 1)));
+          if (lane < ppt && (j * ppt + lane) * a.page_size < P) {
+            if (e >= 0 && e < a.num_pages) phys = e;
+            else if (lane % kPageIssuers == pw) atomicOr(a.status, UNIP_DEV_BAD_PAGES);
+          }
+        }
+        ph1 = ph0;
+        ph0 = phys;
+        last_k = j;
+      } else {
+        phys = last_k == j ? ph0 : ph1;  // V_j follows K_j or K_(j+1)
+      }
+      if (j < Tp) {
+        const void *map = is_v ? static_cast<const void *>(&a.tm_vc) : static_cast<const void *>(&a.tm_kc);
+        if (lane < ppt && lane % kPageIssuers == pw) {
 #pragma unroll
           for (int hf = 0; hf < kHalves; ++hf)
             tma_load_4d(dst + hf * L::kHalfBytes + lane * page_bytes, map, fb, hf * 64, g, 0, phys);
         }
-      } else if (lane == 0) {
+      } else if (pw == 0 && lane == 0) {
         const void *map = is_v ? static_cast<const void *>(&a.tm_v) : static_cast<const void *>(&a.tm_k);
         const int32_t krow = c0 + (j - Tp) * kBlockN;
 #pragma unroll
@@ -690,16 +726,18 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           umma_commit(bar(kBarSFull0 + 0));
           umma_commit(bar(kBarSlotEmpty0 + 0));
           if (T > 1) {
-            if ((ok = mbar_wait(bar(kBarSlotFull0 + 2), 0, abort_flag, a.status))) {  // K_1 = load 2
-              qk(d_s1, dq0, slot_desc(dk, 2));
+            if ((ok = mbar_wait(bar(kBarSlotFull0 + 1), 0, abort_flag, a.status))) {  // K_1 = load 1
+              qk(d_s1, dq0, slot_desc(dk, 1));
               umma_commit(bar(kBarSFull0 + 1));
-              umma_commit(bar(kBarSlotEmpty0 + 2));
+              umma_commit(bar(kBarSlotEmpty0 + 1));
             }
           }
         }
-        int vslot = 1, kslot = 4 % ns;  // V_0 = load 1, K_2 = load 4
-        uint32_t vphase = 0, kphase = 4 / ns;
+        // Load index of V_j: 2j + 2 while K still runs ahead (j < T - 2), then j + T; of K_m: 2m - 1.
         for (int32_t j = 0; ok && j < T; ++j) {
+          const int32_t iv = j < T - 2 ? 2 * j + 2 : j + T, ik = 2 * j + 3;
+          const int vslot = iv % ns, kslot = ik % ns;
+          const uint32_t vphase = (iv / ns) & 1, kphase = (ik / ns) & 1;
           const int buf = j & 1;
           const uint32_t d_s = tmem + buf * kBlockN;
           ok = mbar_wait(bar(kBarPFull0 + buf), (j >> 1) & 1, abort_flag, a.status) &&
@@ -716,8 +754,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             umma_commit(bar(kBarSFull0 + buf));
             umma_commit(bar(kBarSlotEmpty0 + kslot));
           }
-          if ((vslot += 2) >= ns) { vslot -= ns; vphase ^= 1u; }
-          if ((kslot += 2) >= ns) { kslot -= ns; kphase ^= 1u; }
         }
         ok = false;  // the two-tile schedule below is skipped
       }
