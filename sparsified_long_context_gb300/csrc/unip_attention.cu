@@ -608,10 +608,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     int32_t bt_cur = fetch(0), bt_nxt = fetch(tpb), bt_nx2 = fetch(2 * tpb);
     int32_t ph0 = a.num_pages, ph1 = a.num_pages;  // this lane's page of the last two K tiles
     int32_t last_k = -1;
+    // The helper warps stop after the last prefix copy: V_(Tp-1), load 2Tp - 1 with two query
+    // tiles, else 2Tp while K runs ahead (Tp - 1 < T - 2) and Tp - 1 + T after.
+    const int32_t n_loads =
+        pw == 0 ? 2 * T : (Tp == 0 ? 0 : (two ? 2 * Tp : (Tp - 1 < T - 2 ? 2 * Tp + 1 : Tp + T)));
     int32_t issued = 0;
     int slot = -1;
     uint32_t round = 0;  // load ld fills slot ld % ns for the (ld / ns)-th time
-    for (int32_t ld = 0; ld < 2 * T; ++ld) {
+    for (int32_t ld = 0; ld < n_loads; ++ld) {
       if (++slot == ns) {
         slot = 0;
         ++round;
