@@ -224,8 +224,8 @@ __global__ void __launch_bounds__(kPlanThreads) attn_plan_kernel(const int32_t *
 // ---------------------------------------------------------------------------
 // Attention kernel
 // ---------------------------------------------------------------------------
-constexpr int kStages = 4;        // K/V ring slots (each holds one K or one V tile) with two query tiles
-constexpr int kStagesMax = 5;     // with one query tile the second Q buffer becomes a fifth slot
+constexpr int kStages = 5;        // K/V ring slots (each holds one K or one V tile) with two query tiles
+constexpr int kStagesMax = 6;     // with one query tile the second Q buffer becomes a sixth slot
 // 4 softmax warpgroups (8 warps per query tile, 16 rows each) + one control
 // warpgroup (TMA warp, MMA warp, 2 idle warps); 96 registers per thread.
 constexpr int kThreads = 640;
@@ -252,10 +252,9 @@ enum BarId {
   kBarSFull0 = 1 + 2 * kStagesMax,        // + tile: S in TMEM
   kBarPFull0 = 3 + 2 * kStagesMax,        // + tile: P in TMEM and O rescaled (both column halves)
   kBarODone0 = 5 + 2 * kStagesMax,        // + tile: last PV done
-  kBarXchg0 = 7 + 2 * kStagesMax,         // + tile: final row statistics in shared memory
-  kBarFinal = 11 + 2 * kStagesMax,
-  kBarPVDone = 12 + 2 * kStagesMax,       // one query tile: each PV done (O may be rescaled)
-  kNumBars = 13 + 2 * kStagesMax
+  kBarFinal = 7 + 2 * kStagesMax,
+  kBarPVDone = 8 + 2 * kStagesMax,        // one query tile: each PV done (O may be rescaled)
+  kNumBars = 9 + 2 * kStagesMax
 };
 
 __device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
@@ -299,16 +298,13 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
 // and two adjacent columns of every 8-column chunk, so a row's maximum and sum
 // are completed with two shuffles inside a 4-thread quad.  P goes back into
 // the first 64 columns of the tile's S region with the 16x128b shape, in the
-// packed layout the PV MMA reads as its A operand.
-struct RowStats {
-  float m[2][128];  // [tile][row] final running maximum (log2 domain)
-  float l[2][128];  // [tile][row] final row sum
-};
+// packed layout the PV MMA reads as its A operand.  The epilogue reads O in
+// the same layout, so each thread already holds its rows' maximum and sum.
 
 template <int D, bool db>
 __device__ __forceinline__ void softmax_tile_role(const AttnArgs &a, int tile, const TileRows tr, int32_t T,
                                                   int32_t Tp, int32_t P, int32_t c0, uint32_t tmem,
-                                                  uint64_t *bars, RowStats &rs, volatile int *abort_flag) {
+                                                  uint64_t *bars, volatile int *abort_flag) {
   const int wt = (threadIdx.x >> 5) & 7;
   const int lane = threadIdx.x & 31;
   const int q = wt & 3, g = wt >> 2;
@@ -319,7 +315,6 @@ __device__ __forceinline__ void softmax_tile_role(const AttnArgs &a, int tile, c
   // db (one query tile): S and P of KV tile j alternate between the two S regions and their barriers.
   const uint32_t o_col = kTmemO + tile * 128;
   const uint32_t bar_o = smem_u32(&bars[kBarODone0 + tile]);
-  const uint32_t bar_x = smem_u32(&bars[kBarXchg0 + tile]);
   const float c = a.scale_log2;
   const int32_t tok_r0 = tr.tok0 + (R0 >> tr.lg), tok_r1 = tr.tok0 + (R1 >> tr.lg);
   // A warp whose 16 rows are all past the tile's valid rows only keeps the barrier protocol.
@@ -427,48 +422,39 @@ __device__ __forceinline__ void softmax_tile_role(const AttnArgs &a, int tile, c
     tc_fence_before();
     mbar_arrive(bar_p);
   }
-  // Row sums over the quad; row statistics to shared memory for the epilogue's row-per-thread layout.
+  // Row sums over the quad: all four threads of a quad then hold their two rows' m and l.
   l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
   l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
   l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
   l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-  if ((lane & 3) == 0) {
-    rs.m[tile][R0] = m0; rs.l[tile][R0] = l0;
-    rs.m[tile][R1] = m1; rs.l[tile][R1] = l1;
-  }
-  mbar_arrive(bar_x);
-  if (!mbar_wait(bar_x, 0, abort_flag, a.status)) return;
-  if (32 * q >= tr.rows_valid) return;  // no valid row in this warp's 32 epilogue rows (warp-uniform)
+  if (!active) return;  // warp-uniform
   if (!mbar_wait(bar_o, 0, abort_flag, a.status)) return;
   tc_fence_after();
-  // Epilogue with the 32x32b shape: warp (q, g) stores rows 32q .. 32q + 31, columns [g*D/2, (g+1)*D/2).
-  constexpr int kOCols = D / 2;
-  const int row = 32 * q + lane;
-  const float inv_l = 1.f / rs.l[tile][row];
-  const int32_t t = c0 + tr.tok0 + (row >> tr.lg);
-  const int32_t h = tr.head0 + (row & ((1 << tr.lg) - 1));
-  const bool store = row < tr.rows_valid;
-  const uint32_t tl = tmem + (static_cast<uint32_t>(32 * q) << 16);
-  __nv_bfloat16 *orow = a.out + ((int64_t)t * a.Hq + h) * D + g * kOCols;
+  // Epilogue in the softmax layout: O of rows R0, R1 in 32-column parts (16x256b), each thread
+  // writing two adjacent bf16 per 8-column chunk; a quad covers 16 contiguous bytes of a row.
+  const float inv0 = 1.f / l0, inv1 = 1.f / l1;
+  const int32_t t0 = c0 + tok_r0, t1 = c0 + tok_r1;
+  const int32_t hm = (1 << tr.lg) - 1;
+  const int32_t h0 = tr.head0 + (R0 & hm), h1 = tr.head0 + (R1 & hm);
+  const bool st0 = R0 < tr.rows_valid, st1 = R1 < tr.rows_valid;
+  __nv_bfloat16 *o0 = a.out + ((int64_t)t0 * a.Hq + h0) * D + cq;
+  __nv_bfloat16 *o1 = a.out + ((int64_t)t1 * a.Hq + h1) * D + cq;
 #pragma unroll
-  for (int q4 = 0; q4 < kOCols / 32; ++q4) {
-    float o[32];
-    tmem_ld32(tl + o_col + g * kOCols + q4 * 32, o);
+  for (int part = 0; part < D / 32; ++part) {
+    float o[16];  // o[4k + {0,1}]: row R0, columns 32 part + 8k + cq + {0,1}; o[4k + {2,3}]: row R1
+    tmem_ld_16x256b_x4(tw + o_col + part * 32, o);
     tmem_wait_ld();
-    if (store) {
-      uint4 *dst = reinterpret_cast<uint4 *>(orow + q4 * 32);
 #pragma unroll
-      for (int v4 = 0; v4 < 4; ++v4) {
-        uint4 w;
-        w.x = pack_bf16x2(o[v4 * 8 + 0] * inv_l, o[v4 * 8 + 1] * inv_l);
-        w.y = pack_bf16x2(o[v4 * 8 + 2] * inv_l, o[v4 * 8 + 3] * inv_l);
-        w.z = pack_bf16x2(o[v4 * 8 + 4] * inv_l, o[v4 * 8 + 5] * inv_l);
-        w.w = pack_bf16x2(o[v4 * 8 + 6] * inv_l, o[v4 * 8 + 7] * inv_l);
-        dst[v4] = w;
-      }
+    for (int k = 0; k < 4; ++k) {
+      const int col = part * 32 + 8 * k;
+      if (st0) *reinterpret_cast<uint32_t *>(o0 + col) = pack_bf16x2(o[4 * k] * inv0, o[4 * k + 1] * inv0);
+      if (st1) *reinterpret_cast<uint32_t *>(o1 + col) = pack_bf16x2(o[4 * k + 2] * inv1, o[4 * k + 3] * inv1);
     }
   }
-  if (g == 0 && store && a.lse) a.lse[(int64_t)h * a.N + t] = (rs.m[tile][row] + log2f(rs.l[tile][row])) * kLn2;
+  if ((lane & 3) == 0 && a.lse) {
+    if (st0) a.lse[(int64_t)h0 * a.N + t0] = (m0 + log2f(l0)) * kLn2;
+    if (st1) a.lse[(int64_t)h1 * a.N + t1] = (m1 + log2f(l1)) * kLn2;
+  }
 }
 
 // One CTA = two 128-row query tiles of one segment that share every K/V tile
@@ -485,7 +471,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   __shared__ __align__(8) uint64_t bars[kNumBars];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
-  __shared__ RowStats row_stats;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -545,7 +530,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       mbar_init(bar(kBarPFull0 + i), 2 * kBlockM);
       mbar_init(bar(kBarODone0 + i), 1);
     }
-    for (int i = 0; i < 2; ++i) mbar_init(bar(kBarXchg0 + i), 2 * kBlockM);
     mbar_init(bar(kBarFinal), 1);
     mbar_init(bar(kBarPVDone), 1);
     s_abort = 0;
@@ -565,9 +549,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     // ------------------------------------------------------------ softmax + epilogue
     const int tile = warp >> 3;
     if (two)
-      softmax_tile_role<D, false>(a, tile, tile ? tr1 : tr0, T, Tp, P, c0, tmem, bars, row_stats, abort_flag);
+      softmax_tile_role<D, false>(a, tile, tile ? tr1 : tr0, T, Tp, P, c0, tmem, bars, abort_flag);
     else if (tile == 0)
-      softmax_tile_role<D, true>(a, 0, tr0, T, Tp, P, c0, tmem, bars, row_stats, abort_flag);
+      softmax_tile_role<D, true>(a, 0, tr0, T, Tp, P, c0, tmem, bars, abort_flag);
   } else if (warp == kWarpTma || warp >= kWarpAux0) {
     // ------------------------------------------------------------ TMA producers
     // Warp 16 loads Q and the segment's own K/V tiles and arms every slot; the page copies of a
@@ -778,16 +762,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         const bool more = j + 1 < T;
         const uint64_t dvj = slot_desc(dv, vslot), dkn = slot_desc(dk, kslot);
         const uint32_t acc = j > 0 ? 1u : 0u;
-        // tile 0: PV(j), then QK(j+1)
-        ok = mbar_wait(bar(kBarPFull0 + 0), j & 1, abort_flag, a.status) &&
-             mbar_wait(bar(kBarSlotFull0 + vslot), vphase, abort_flag, a.status);
+        // tile 0: PV(j), then QK(j+1); K_(j+1) is waited for first so that both go out back to back
+        ok = mbar_wait(bar(kBarSlotFull0 + vslot), vphase, abort_flag, a.status) &&
+             (!more || mbar_wait(bar(kBarSlotFull0 + kslot), kphase, abort_flag, a.status)) &&
+             mbar_wait(bar(kBarPFull0 + 0), j & 1, abort_flag, a.status);
         if (!ok) break;
         tc_fence_after();
         pv(d_o0, d_s0, dvj, acc);
         if (!more) umma_commit(bar(kBarODone0 + 0));
         if (!two) umma_commit(bar(kBarSlotEmpty0 + vslot));
         if (more) {
-          if (!(ok = mbar_wait(bar(kBarSlotFull0 + kslot), kphase, abort_flag, a.status))) break;
           qk(d_s0, dq0, dkn);
           umma_commit(bar(kBarSFull0 + 0));
           if (!two) umma_commit(bar(kBarSlotEmpty0 + kslot));
@@ -798,12 +782,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           tc_fence_after();
           pv(d_o1, d_s1, dvj, acc);
           if (!more) umma_commit(bar(kBarODone0 + 1));
-          umma_commit(bar(kBarSlotEmpty0 + vslot));
           if (more) {
             qk(d_s1, dq1, dkn);
-            umma_commit(bar(kBarSFull0 + 1));
+            umma_commit(bar(kBarSFull0 + 1));  // first: the softmax of tile 1 waits on it
             umma_commit(bar(kBarSlotEmpty0 + kslot));
           }
+          umma_commit(bar(kBarSlotEmpty0 + vslot));
         }
         if ((vslot += 2) >= ns) { vslot -= ns; vphase ^= 1u; }
         if ((kslot += 2) >= ns) { kslot -= ns; kphase ^= 1u; }
