@@ -98,64 +98,72 @@ struct ScoreArgs {
   float scale_log2;
 };
 
-constexpr int kScoreWarpTma = 4;
-constexpr int kScoreWarpMma = 5;
-constexpr int kScoreThreadsTc = 192;
+constexpr int kScoreWarpTma = 8;
+constexpr int kScoreWarpMma = 9;
+constexpr int kScoreThreadsTc = 320;  // 8 score warps (two per TMEM lane quarter), TMA warp, MMA warp
+constexpr int kScoreCompute = 256;
 constexpr int kMaxCols = 256;  // columns of S^T per MMA group (window rows x heads)
 
 template <int D>
 struct ScoreSmem {
   static constexpr uint32_t kHalf = 128 * 128;            // 128 rows x 128 B
-  static constexpr uint32_t kK = 0;                       // K tile: D/64 halves of 128 rows
-  static constexpr uint32_t kQ = (D / 64) * kHalf;        // Q window: D/64 halves of 256 rows
+  static constexpr uint32_t kKTile = (D / 64) * kHalf;     // one K tile: D/64 halves of 128 rows
+  static constexpr uint32_t kQ = 2 * kKTile;               // after two K slots: Q window, D/64 halves of 256 rows
   static constexpr uint32_t kQHalf = kMaxCols * 128;
   static constexpr uint32_t kBytes = kQ + (D / 64) * kQHalf;
   static constexpr uint32_t kDynamic = kBytes + 1024;
 };
 
-// One CTA per (segment, 128-key chunk, kv head).  S^T = K Q_w^T on the
-// tensor cores: M = 128 keys of the chunk (TMEM lanes), N = window rows of
-// the group's query heads (TMEM columns), K = D.  Each of 128 threads owns one
-// key and sums exp(s - lse) over its visible window columns.
+enum ScoreBar {
+  kSbQFull = 0,
+  kSbQEmpty = 1,
+  kSbKFull0 = 2,   // + slot
+  kSbKEmpty0 = 4,  // + slot
+  kSbSFull0 = 6,   // + TMEM buffer
+  kSbSEmpty0 = 8,  // + TMEM buffer
+  kSbFinal = 10,
+  kSbNum = 11
+};
+
+// Persistent: CTA b walks a contiguous range of units (kv head g, 128-key
+// chunk c of segment s), ordered head-major so that consecutive units mostly
+// share a segment's window.  Per unit and query-head group: S^T = K Q_w^T on
+// the tensor cores (M = 128 keys on TMEM lanes, N = window rows x heads on
+// columns, K = D).  The window Q is loaded once per (segment, g, group); K
+// tiles and S buffers are double-buffered so the next MMA runs while the
+// score warps sum exp(s - lse) of the current one (warp w: lane quarter w % 4,
+// column half w / 4).
 template <int D>
-__global__ void __launch_bounds__(kScoreThreadsTc) imp_score_tc_kernel(const __grid_constant__ ScoreArgs a) {
+__global__ void __launch_bounds__(kScoreThreadsTc, 1) imp_score_tc_kernel(const __grid_constant__ ScoreArgs a) {
   using L = ScoreSmem<D>;
   constexpr int kHalves = D / 64;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t bars[6];  // k_full, q_full, s_full, s_empty, q_empty, final
+  __shared__ __align__(8) uint64_t bars[kSbNum];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
   __shared__ float s_lse[kMaxCols];
+  __shared__ float s_key[128];
   __shared__ float s_red[4];
 
-  const int32_t item = blockIdx.x / a.Hkv;
-  if (item >= *a.num_items) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
-  const int32_t g = blockIdx.x % a.Hkv;
-  const int2 it = a.items[item];
-  const int32_t s = it.x, c = it.y;
-  const int32_t c0 = a.cu[s], n = a.cu[s + 1] - c0;
+  const int32_t n_items = *a.num_items;
+  const int64_t U = (int64_t)n_items * a.Hkv;
+  const int64_t u0 = U * blockIdx.x / gridDim.x, u1 = U * (blockIdx.x + 1) / gridDim.x;
+  if (u0 >= u1) return;  // uniform over the CTA
   const int32_t B = a.B;
-  const int32_t W = min(B, n);
-  const int32_t wrow0 = n - W;               // first window row (segment-local)
   const int32_t group = a.Hq / a.Hkv;
   const int32_t hpg = a.heads_per_group;     // heads per MMA group
   const int32_t ngroups = (group + hpg - 1) / hpg;
+  const int64_t n_iter = (u1 - u0) * ngroups;  // iteration i: unit u0 + i / ngroups, group i % ngroups
   const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
-  const uint32_t bar_k = smem_u32(&bars[0]), bar_q = smem_u32(&bars[1]), bar_s = smem_u32(&bars[2]);
-  const uint32_t bar_se = smem_u32(&bars[3]), bar_qe = smem_u32(&bars[4]);
+  auto bar = [&](int k) { return smem_u32(&bars[k]); };
   if (tid == 0) {
-    mbar_init(bar_k, 1);
-    mbar_init(bar_q, 1);
-    mbar_init(bar_s, 1);
-    mbar_init(bar_se, 128);
-    mbar_init(bar_qe, 1);
-    mbar_init(smem_u32(&bars[5]), 1);
+    for (int k = 0; k < kSbNum; ++k) mbar_init(bar(k), (k == kSbSEmpty0 || k == kSbSEmpty0 + 1) ? kScoreCompute : 1);
     s_abort = 0;
     fence_mbar_init();
   }
   if (warp == kScoreWarpMma) {
-    tmem_alloc(smem_u32(&s_tmem), 256);
+    tmem_alloc(smem_u32(&s_tmem), 512);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -163,105 +171,187 @@ __global__ void __launch_bounds__(kScoreThreadsTc) imp_score_tc_kernel(const __g
   tc_fence_after();
   const uint32_t tmem = s_tmem;
   volatile int *abort_flag = &s_abort;
+  struct It {
+    int32_t g, s, c, gi;
+  };
+  auto decode = [&](int64_t i) {
+    It r;
+    const int64_t u = u0 + i / ngroups;
+    r.gi = (int32_t)(i % ngroups);
+    r.g = (int32_t)(u / n_items);
+    const int2 item = a.items[u % n_items];
+    r.s = item.x;
+    r.c = item.y;
+    return r;
+  };
+  auto same_q = [](const It &x, const It &y) { return x.s == y.s && x.g == y.g && x.gi == y.gi; };
 
   if (warp == kScoreWarpTma) {
     if (lane == 0) {
-      mbar_arrive_expect_tx(bar_k, kHalves * L::kHalf);
+      It prev = {-1, -1, -1, -1};
+      uint32_t qn = 0;
+      int64_t issued = 0;
+      for (int64_t i = 0; i < n_iter; ++i) {
+        const It it = decode(i);
+        const int32_t c0 = a.cu[it.s], n = a.cu[it.s + 1] - c0;
+        if (!same_q(it, prev)) {
+          if (qn > 0 && !mbar_wait(bar(kSbQEmpty), (qn - 1) & 1, abort_flag, a.status)) break;
+          const int32_t W = min(B, n), hn = min(hpg, group - it.gi * hpg);
+          mbar_arrive_expect_tx(bar(kSbQFull), kHalves * hn * B * 128);
+          for (int32_t hh = 0; hh < hn; ++hh) {
+            const int32_t h = it.g * group + it.gi * hpg + hh;
 #pragma unroll
-      for (int hf = 0; hf < kHalves; ++hf)
-        tma_load_3d(sbase + L::kK + hf * L::kHalf, &a.tm_k, bar_k, hf * 64, g, c0 + c * 128);
-      for (int32_t gi = 0; gi < ngroups; ++gi) {
-        if (gi > 0 && !mbar_wait(bar_qe, (gi - 1) & 1, abort_flag, a.status)) break;
-        const int32_t hn = min(hpg, group - gi * hpg);
-        mbar_arrive_expect_tx(bar_q, kHalves * hn * B * 128);
-        for (int32_t hh = 0; hh < hn; ++hh) {
-          const int32_t h = g * group + gi * hpg + hh;
+            for (int hf = 0; hf < kHalves; ++hf)
+              tma_load_3d(sbase + L::kQ + hf * L::kQHalf + hh * B * 128, &a.tm_q, bar(kSbQFull), hf * 64, h,
+                          c0 + n - W);
+          }
+          ++qn;
+          prev = it;
+        }
+        const int slot = (int)(i & 1);
+        if (i >= 2 && !mbar_wait(bar(kSbKEmpty0 + slot), ((i >> 1) - 1) & 1, abort_flag, a.status)) break;
+        mbar_arrive_expect_tx(bar(kSbKFull0 + slot), L::kKTile);
 #pragma unroll
-          for (int hf = 0; hf < kHalves; ++hf)
-            tma_load_3d(sbase + L::kQ + hf * L::kQHalf + hh * B * 128, &a.tm_q, bar_q, hf * 64, h, c0 + wrow0);
+        for (int hf = 0; hf < kHalves; ++hf)
+          tma_load_3d(sbase + slot * L::kKTile + hf * L::kHalf, &a.tm_k, bar(kSbKFull0 + slot), hf * 64, it.g,
+                      c0 + it.c * 128);
+        issued = i + 1;
+      }
+      if (*abort_flag) {  // copies in flight land before the CTA's shared memory is released
+        for (int64_t i = max((int64_t)0, issued - 2); i < issued; ++i) {
+          const uint64_t t0 = globaltimer_ns();
+          while (!mbar_try_wait(bar(kSbKFull0 + (int)(i & 1)), (i >> 1) & 1) && globaltimer_ns() - t0 < kWaitLimitNs) {
+          }
+        }
+        if (qn > 0) {
+          const uint64_t t0 = globaltimer_ns();
+          while (!mbar_try_wait(bar(kSbQFull), (qn - 1) & 1) && globaltimer_ns() - t0 < kWaitLimitNs) {
+          }
         }
       }
     }
   } else if (warp == kScoreWarpMma) {
     if (lane == 0) {
-      bool ok = mbar_wait(bar_k, 0, abort_flag, a.status);
-      for (int32_t gi = 0; ok && gi < ngroups; ++gi) {
-        ok = mbar_wait(bar_q, gi & 1, abort_flag, a.status);
-        if (ok && gi > 0) ok = mbar_wait(bar_se, (gi - 1) & 1, abort_flag, a.status);
+      It prev = {-1, -1, -1, -1};
+      uint32_t qn = 0;
+      bool ok = true;
+      for (int64_t i = 0; ok && i < n_iter; ++i) {
+        const It it = decode(i);
+        if (!same_q(it, prev)) {
+          ok = mbar_wait(bar(kSbQFull), qn & 1, abort_flag, a.status);
+          ++qn;
+          prev = it;
+        }
+        const int slot = (int)(i & 1);
+        ok = ok && mbar_wait(bar(kSbKFull0 + slot), (i >> 1) & 1, abort_flag, a.status) &&
+             (i < 2 || mbar_wait(bar(kSbSEmpty0 + slot), ((i >> 1) - 1) & 1, abort_flag, a.status));
         if (!ok) break;
         tc_fence_after();
-        const int32_t hn = min(hpg, group - gi * hpg);
+        const int32_t hn = min(hpg, group - it.gi * hpg);
         const uint32_t idesc = idesc_bf16_f32(128, hn * B, false, false);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t koff = (kk >> 2) * L::kHalf + (kk & 3) * 32;
-          const uint32_t qoff = (kk >> 2) * L::kQHalf + (kk & 3) * 32;
-          umma_bf16_ss(tmem, sdesc_sw128(sbase + L::kK + koff, 16, 1024), sdesc_sw128(sbase + L::kQ + qoff, 16, 1024),
+          const uint32_t koff = slot * L::kKTile + (kk >> 2) * L::kHalf + (kk & 3) * 32;
+          const uint32_t qoff = L::kQ + (kk >> 2) * L::kQHalf + (kk & 3) * 32;
+          umma_bf16_ss(tmem + slot * kMaxCols, sdesc_sw128(sbase + koff, 16, 1024), sdesc_sw128(sbase + qoff, 16, 1024),
                        idesc, kk > 0 ? 1u : 0u);
         }
-        umma_commit(bar_s);
-        umma_commit(bar_qe);
+        umma_commit(bar(kSbSFull0 + slot));
+        umma_commit(bar(kSbKEmpty0 + slot));
+        if (i + 1 == n_iter || !same_q(decode(i + 1), it)) umma_commit(bar(kSbQEmpty));  // last MMA on this Q
       }
       // Every tcgen05 op of this CTA has landed before TMEM is released.
-      umma_commit(smem_u32(&bars[5]));
+      umma_commit(bar(kSbFinal));
       const uint64_t t0 = globaltimer_ns();
-      while (!mbar_try_wait(smem_u32(&bars[5]), 0) && globaltimer_ns() - t0 < kWaitLimitNs) {
+      while (!mbar_try_wait(bar(kSbFinal), 0) && globaltimer_ns() - t0 < kWaitLimitNs) {
       }
     }
   } else {
-    // 4 warps: thread tid owns key j = c*128 + tid (TMEM lane tid)
-    const int32_t j = c * 128 + tid;
-    const bool kvalid = j < n;
-    const uint32_t tl = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-    float acc = 0.f;
-    for (int32_t gi = 0; gi < ngroups; ++gi) {
-      const int32_t hn = min(hpg, group - gi * hpg);
-      // stage this group's row normalisers (log2 domain); window slots past the segment are masked
-      for (int32_t col = tid; col < hn * B; col += 128) {
-        const int32_t hh = col / B, t = col % B;
-        const int32_t h = g * group + gi * hpg + hh;
-        s_lse[col] = t < W ? a.lse[(int64_t)h * a.N + c0 + wrow0 + t] * kLog2e : INFINITY;
-      }
-      asm volatile("bar.sync 1, 128;" ::: "memory");
-      if (!mbar_wait(bar_s, gi & 1, abort_flag, a.status)) break;
-      tc_fence_after();
-      for (uint32_t col0 = 0; col0 < (uint32_t)(hn * B); col0 += 32) {
-        float sv[32];
-        tmem_ld32(tl + col0, sv);
-        tmem_wait_ld();
-#pragma unroll
-        for (int x = 0; x < 32; ++x) {
-          const int32_t col = col0 + x;
-          const int32_t t = col % B;             // window slot
-          // visible: window slot inside the segment and key j at or before row wrow0 + t
-          if (kvalid && col < hn * B && j <= wrow0 + t) acc += ex2_approx(fmaf(sv[x], a.scale_log2, -s_lse[col]));
-        }
-      }
-      tc_fence_before();
-      mbar_arrive(bar_se);
-      asm volatile("bar.sync 1, 128;" ::: "memory");
-    }
-    // per-block sums over the chunk's keys
-    const int32_t nb_seg = a.blk_cu[s + 1] - a.blk_cu[s];
+    // Score warps.  Every one of them runs all n_iter iterations and every named barrier, also
+    // after a timed-out wait (live = false then skips the work), so none is left at a barrier.
+    const int qd = warp & 3, ch = warp >> 2;
+    const int key = 32 * qd + lane;
+    const uint32_t tl = tmem + (static_cast<uint32_t>(32 * qd) << 16);
     const int32_t bpc = 128 / B;
-    if (B <= 32) {
-      float v = acc;
-      for (int off = B / 2; off >= 1; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-      if ((tid % B) == 0) {
-        const int32_t b = c * bpc + tid / B;
-        if (b < nb_seg) a.partial[(int64_t)(a.blk_cu[s] + b) * a.Hkv + g] = v;
+    bool live = true;
+    It prev = {-1, -1, -1, -1};
+    float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
+    for (int64_t i = 0; i < n_iter; ++i) {
+      const It it = decode(i);
+      const int32_t c0 = a.cu[it.s], n = a.cu[it.s + 1] - c0;
+      const int32_t W = min(B, n), wrow0 = n - W;
+      const int32_t hn = min(hpg, group - it.gi * hpg), ncols = hn * B;
+      if (!same_q(it, prev)) {
+        // row normalisers of this window (log2 domain); window slots past the segment are masked
+        asm volatile("bar.sync 1, 256;" ::: "memory");
+        if (tid < ncols) {
+          const int32_t hh = tid / B, t = tid & (B - 1);
+          const int32_t h = it.g * group + it.gi * hpg + hh;
+          s_lse[tid] = t < W ? a.lse[(int64_t)h * a.N + c0 + wrow0 + t] * kLog2e : INFINITY;
+        }
+        asm volatile("bar.sync 1, 256;" ::: "memory");
+        prev = it;
       }
-    } else {
-      float v = acc;
-      for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-      if (lane == 0) s_red[warp] = v;
-      asm volatile("bar.sync 1, 128;" ::: "memory");
-      const int wpb = B / 32;
-      if (tid < bpc) {
-        float t = 0.f;
-        for (int w = 0; w < wpb; ++w) t += s_red[tid * wpb + w];
-        const int32_t b = c * bpc + tid;
-        if (b < nb_seg) a.partial[(int64_t)(a.blk_cu[s] + b) * a.Hkv + g] = t;
+      const int slot = (int)(i & 1);
+      live = live && mbar_wait(bar(kSbSFull0 + slot), (i >> 1) & 1, abort_flag, a.status);
+      const int32_t j = it.c * 128 + key;
+      const bool kvalid = j < n;
+      if (live) {
+        tc_fence_after();
+        // this warp's columns: [128 ch, 128 ch + 128) of the group's hn * B (a multiple of 16)
+        for (int32_t col0 = 128 * ch; col0 < min(128 * ch + 128, ncols); col0 += 64) {
+          float sv[64];
+          tmem_ld32(tl + slot * kMaxCols + col0, sv);
+          tmem_ld32(tl + slot * kMaxCols + col0 + 32, sv + 32);
+          tmem_wait_ld();
+#pragma unroll
+          for (int x = 0; x < 64; x += 4) {
+            float e[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int32_t col = col0 + x + u;
+              // visible: window slot inside the segment and key j at or before row wrow0 + slot
+              const bool vis = kvalid && col < ncols && j <= wrow0 + (col & (B - 1));
+              e[u] = vis ? ex2_approx(fmaf(sv[x + u], a.scale_log2, -s_lse[col])) : 0.f;
+            }
+            acc0 += e[0];
+            acc1 += e[1];
+            acc2 += e[2];
+            acc3 += e[3];
+          }
+        }
+        tc_fence_before();
+      }
+      mbar_arrive(bar(kSbSEmpty0 + slot));
+      if (it.gi != ngroups - 1) continue;  // the unit's mass sums over all head groups
+      // unit done: key masses of both column halves, then per-block sums over the chunk's keys
+      float v = (acc0 + acc1) + (acc2 + acc3);
+      acc0 = acc1 = acc2 = acc3 = 0.f;
+      asm volatile("bar.sync 1, 256;" ::: "memory");
+      if (ch == 1) s_key[key] = v;
+      asm volatile("bar.sync 1, 256;" ::: "memory");
+      if (ch == 0) {
+        v += s_key[key];
+        const int32_t nb_seg = a.blk_cu[it.s + 1] - a.blk_cu[it.s];
+        const int64_t pbase = (int64_t)a.blk_cu[it.s] + it.c * bpc;
+        if (B <= 32) {
+          for (int off = B / 2; off >= 1; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+          if ((key & (B - 1)) == 0) {
+            const int32_t b = key / B;
+            if (it.c * bpc + b < nb_seg && live) a.partial[(pbase + b) * a.Hkv + it.g] = v;
+          }
+        } else {
+          for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+          if (lane == 0) s_red[qd] = v;
+          asm volatile("bar.sync 2, 128;" ::: "memory");
+          const int wpb = B / 32;
+          if (key < bpc) {
+            float t = 0.f;
+            for (int w = 0; w < wpb; ++w) t += s_red[key * wpb + w];
+            if (it.c * bpc + key < nb_seg && live) a.partial[(pbase + key) * a.Hkv + it.g] = t;
+          }
+          asm volatile("bar.sync 2, 128;" ::: "memory");
+        }
       }
     }
   }
@@ -269,7 +359,7 @@ __global__ void __launch_bounds__(kScoreThreadsTc) imp_score_tc_kernel(const __g
   __syncthreads();
   if (warp == kScoreWarpMma) {
     tc_fence_after();
-    tmem_dealloc(tmem, 256);
+    tmem_dealloc(tmem, 512);
   }
 }
 
@@ -373,8 +463,10 @@ UNIP_API int32_t unip_block_importance(const void *q, const void *k, const float
   if (cudaGetLastError() != cudaSuccess) return UNIP_ERR_CUDA;
   if (total_tokens == 0) return UNIP_OK;
   const float scale = prm->scale > 0.f ? prm->scale : 1.0f / sqrtf((float)D);
-  const int64_t grid = (int64_t)max_items * Hkv;
-  if (grid > 0x7FFFFFFF) return UNIP_ERR_UNSUPPORTED;
+  // persistent score grid: one CTA per SM (each takes a contiguous range of (kv head, chunk) units)
+  const int64_t units_bound = (int64_t)max_items * Hkv;
+  const int sms = device_sm_count();
+  const int64_t grid = std::min<int64_t>(units_bound, sms > 0 ? sms : 1);
   ScoreArgs args;
   memset(&args, 0, sizeof(args));
   {
