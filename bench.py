@@ -254,6 +254,49 @@ def cpu_baseline(wl, seconds: float):
                       f"of the same workload ({dt:.1f} s); useful FLOPs of those rows / wall time"}
 
 
+def incremental_select_ms(di, bufs, flush, stream, reps: int = 10, trials: int = 5) -> float:
+    """Incremental device time of select+gather in the step: CUDA-graph replays of
+    [L2 flush, importance, select+gather] minus [L2 flush, importance], per step.
+
+    CUDA events recorded between the importance and the Top-p launches would break the
+    programmatic-dependent launch between them and add their own latency, so the in-step
+    event pair overstates this part; both are reported.
+    """
+    import torch
+    from sparsified_long_context_gb300.pipeline import run_importance, run_select_gather
+
+    cs = torch.cuda.Stream()  # graphs are captured on a side stream
+
+    def capture(with_select):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cs):
+            for _ in range(reps):
+                flush.zero_()
+                run_importance(di, bufs, cs)
+                if with_select:
+                    run_select_gather(di, bufs, stream=cs)
+        return g
+
+    def replay_ms(g):
+        ts = []
+        for _ in range(trials):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1) / reps)
+        return statistics.median(ts)
+
+    torch.cuda.synchronize()
+    g_imp, g_all = capture(False), capture(True)
+    torch.cuda.synchronize()
+    d = replay_ms(g_all) - replay_ms(g_imp)
+    del g_imp, g_all
+    return max(d, 1e-6)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -343,7 +386,8 @@ def main():
     d_model = di.hidden.shape[1] if di.hidden is not None else 0
     sg_bytes = select_gather_bytes(wl, n_blocks, n_kept, d_model)
     attn_ms = statistics.mean(t_attn)
-    sel_ms = statistics.mean(t_sel)
+    sel_ms_events = statistics.mean(t_sel)
+    sel_ms = incremental_select_ms(di, bufs, flush, stream)
     imp_ms = statistics.mean(t_imp)
     attn_tflops = flops_step / (attn_ms * 1e-3) / 1e12
     sg_gbs = sg_bytes / (sel_ms * 1e-3) / 1e9
@@ -400,7 +444,10 @@ def main():
         "parts": {
             "attention_ms": attn_ms, "attention_tflops": attn_tflops, "attention_frac_bf16": attn_tflops / bf16_peak,
             "importance_ms": imp_ms,
-            "select_gather_ms": sel_ms, "select_gather_bytes": sg_bytes, "select_gather_gbs": sg_gbs,
+            "select_gather_ms": sel_ms, "select_gather_ms_in_step_events": sel_ms_events,
+            "select_gather_timing": "incremental: graph replays of [L2 flush, importance, select+gather] minus "
+                                    "[L2 flush, importance]",
+            "select_gather_bytes": sg_bytes, "select_gather_gbs": sg_gbs,
             "select_gather_frac_hbm": sg_gbs / hbm_peak, "n_kept": n_kept, "n_blocks": n_blocks,
             "peaks": f"{peak_src}: bf16 {bf16_peak} TFLOP/s, HBM {hbm_peak} GB/s",
         },

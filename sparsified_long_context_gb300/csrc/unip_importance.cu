@@ -367,6 +367,8 @@ __global__ void __launch_bounds__(kNormThreads) imp_norm_kernel(const int32_t *_
                                                                  const float *__restrict__ partial, int32_t Hkv,
                                                                  float *__restrict__ imp) {
   __shared__ float sred[kNormThreads];
+  // a Top-p grid launched as a programmatic dependent may be scheduled now; it waits for this one
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int32_t s = blockIdx.x;
   const int32_t b0 = blk_cu[s], nb = blk_cu[s + 1] - b0;
   if (nb <= 0) return;

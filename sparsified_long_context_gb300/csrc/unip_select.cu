@@ -37,8 +37,22 @@ constexpr int kIndexSmemSegs = 12000;  // segments whose offsets the index kerne
 constexpr int kGatherCtasPerSm = 2;    // fused gather grid: 16 warps per SM, each with 4 KB of loads in flight
 constexpr int kGatherStageBytes = 48 * 1024;  // shared memory of the fused gather (no opt-in needed)
 
+// floor(f * 2^32) for 0 <= f <= 1, exactly and without FP64 arithmetic (a slow pipe on this
+// part): f = m * 2^(e - 150) with the 24-bit significand m and biased exponent e, so
+// f * 2^32 = m * 2^(e - 118).  Zero and subnormal scores are below 2^-126 and give 0.
 __device__ __forceinline__ unsigned long long fixed_mass(float f) {
-  return static_cast<unsigned long long>(floor(static_cast<double>(f) * 4294967296.0));
+  const uint32_t u = __float_as_uint(f);
+  const int e = static_cast<int>(u >> 23);  // f >= 0: no sign bit
+  if (e == 0) return 0ull;
+  const unsigned long long m = (u & 0x7FFFFFu) | 0x800000u;
+  const int sh = e - 118;
+  return sh >= 0 ? (m << sh) : (sh > -24 ? (m >> -sh) : 0ull);
+}
+
+// Keep test in integers: for an integer mass x below 2^53 (exact in fp64), x < thr holds exactly
+// when x < ceil(thr), with thr = p * T the one IEEE multiply of the selection rule.
+__device__ __forceinline__ unsigned long long mass_threshold(double p, unsigned long long T) {
+  return static_cast<unsigned long long>(ceil(__dmul_rn(p, static_cast<double>(T))));
 }
 
 // Rank key of a non-forced block: score descending (bits of a non-negative
@@ -50,27 +64,55 @@ __device__ __forceinline__ float key_score(unsigned long long key) {
   return __uint_as_float(~static_cast<uint32_t>(key >> 32));
 }
 
+// Bitonic sort of NPOW keys, one per thread (threads past NPOW hold padding): strides below 32
+// exchange through warp shuffles, larger ones through shared memory.  Every loop is unrolled, so
+// each stage is a shuffle (or a shared-memory swap) and a compare with constant lane masks.
+template <int NPOW>
+__device__ __forceinline__ void bitonic_sort_regs(unsigned long long &key, unsigned long long *skeys, int tid) {
+#pragma unroll
+  for (int size = 2; size <= NPOW; size <<= 1) {
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      unsigned long long other;
+      if (stride >= 32) {
+        __syncthreads();
+        if (tid < NPOW) skeys[tid] = key;
+        __syncthreads();
+        other = tid < NPOW ? skeys[tid ^ stride] : key;
+      } else {
+        other = __shfl_xor_sync(0xffffffffu, key, stride);
+      }
+      const bool take_min = ((tid & stride) == 0) == ((tid & size) == 0);
+      key = take_min ? (other < key ? other : key) : (other > key ? other : key);
+    }
+  }
+}
+
 __global__ void __launch_bounds__(kToppThreads) topp_kernel(
     const float *__restrict__ imp, const int32_t *__restrict__ blk_cu, const int32_t *__restrict__ cu, int32_t B,
     double p, uint32_t flags, uint8_t *__restrict__ keep, int32_t *__restrict__ kept_off,
-    int32_t *__restrict__ seg_kept, uint32_t *__restrict__ status) {
-  extern __shared__ unsigned long long skeys[];  // kMaxBlocks rank keys, then kMaxBlocks keep flags
-  uint8_t *skeep = reinterpret_cast<uint8_t *>(skeys + kMaxBlocks);
+    int32_t *__restrict__ seg_kept, int32_t cap, uint32_t *__restrict__ status) {
+  extern __shared__ unsigned long long skeys[];  // cap rank keys, then cap keep flags
+  uint8_t *skeep = reinterpret_cast<uint8_t *>(skeys + cap);
   __shared__ unsigned long long sh64[32];
   __shared__ int32_t sh32[32];
   __shared__ uint32_t s_bad;
   const int tid = threadIdx.x;
+  // A gather launched as a programmatic dependent may start now; it waits for this grid's results.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // This grid may itself run as a programmatic dependent of the importance kernels: no memory is
+  // touched before their results are visible.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int32_t s = blockIdx.x;
   const int32_t n = cu[s + 1] - cu[s];
   const int32_t b0 = blk_cu[s], nb = blk_cu[s + 1] - blk_cu[s];
-  // A gather launched as a programmatic dependent may start now; it waits for this grid's results.
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   if (nb == 0) {  // not scored: every token is kept
     if (tid == 0) seg_kept[s] = n > 0 ? n : 0;
     return;
   }
-  if (nb > kMaxBlocks || n <= 0 || nb != (n + B - 1) / B) {
+  // cap (a power of two) bounds the padded sort of every segment that fits the call's token count
+  if (nb > kMaxBlocks || nb > cap || n <= 0 || nb != (n + B - 1) / B) {
     if (tid == 0) {
       atomicOr(status, nb > kMaxBlocks ? UNIP_DEV_TOO_MANY_BLOCKS : UNIP_DEV_BAD_BLOCKS);
       seg_kept[s] = 0;
@@ -124,33 +166,29 @@ __global__ void __launch_bounds__(kToppThreads) topp_kernel(
   } else if (npow <= kToppThreads) {
     // Up to 512 blocks: bitonic sort with one key per thread, in registers; strides below 32
     // exchange through warp shuffles, larger ones through shared memory.
-    const double thr = __dmul_rn(p, static_cast<double>(T));
+    const unsigned long long kthr = mass_threshold(p, T);
     unsigned long long key = tid < npow ? skeys[tid] : ~0ull;
-    for (int size = 2; size <= npow; size <<= 1) {
-      for (int stride = size >> 1; stride > 0; stride >>= 1) {
-        unsigned long long other;
-        if (stride >= 32) {
-          __syncthreads();
-          skeys[tid] = key;
-          __syncthreads();
-          other = skeys[tid ^ stride];
-        } else {
-          other = __shfl_xor_sync(0xffffffffu, key, stride);
-        }
-        const bool lower = (tid & stride) == 0, asc = (tid & size) == 0;
-        const bool take_min = lower == asc;
-        key = take_min ? (other < key ? other : key) : (other > key ? other : key);
-      }
+    switch (npow) {  // fully unrolled network for the padded size
+      case 1: break;
+      case 2: bitonic_sort_regs<2>(key, skeys, tid); break;
+      case 4: bitonic_sort_regs<4>(key, skeys, tid); break;
+      case 8: bitonic_sort_regs<8>(key, skeys, tid); break;
+      case 16: bitonic_sort_regs<16>(key, skeys, tid); break;
+      case 32: bitonic_sort_regs<32>(key, skeys, tid); break;
+      case 64: bitonic_sort_regs<64>(key, skeys, tid); break;
+      case 128: bitonic_sort_regs<128>(key, skeys, tid); break;
+      case 256: bitonic_sort_regs<256>(key, skeys, tid); break;
+      default: bitonic_sort_regs<512>(key, skeys, tid); break;
     }
     // thread tid now holds the key of rank tid; forced blocks and padding sort last
     const unsigned long long m = key != ~0ull ? fixed_mass(key_score(key)) : 0ull;
     unsigned long long tot;
     const unsigned long long ex = block_excl_scan<unsigned long long>(m, sh64, &tot);
-    if (key != ~0ull) skeep[key & 0xFFFFFFFFull] = static_cast<double>(CF + ex) < thr ? 1 : 0;
+    if (key != ~0ull) skeep[key & 0xFFFFFFFFull] = CF + ex < kthr ? 1 : 0;
   } else if (nb <= kRankCountMax) {
     // Small segment: the rank of a block is the number of smaller keys (keys are unique), so
     // no sort is needed.  Forced blocks and padding hold the largest key and are never counted.
-    const double thr = __dmul_rn(p, static_cast<double>(T));
+    const unsigned long long kthr = mass_threshold(p, T);
     constexpr int kPer = kRankCountMax / kToppThreads;
     const int npad = (nb + 15) & ~15;  // keys past npow are padded with the largest key up to npad
     for (int b = npow + tid; b < npad; b += kToppThreads) skeys[b] = ~0ull;
@@ -198,9 +236,9 @@ __global__ void __launch_bounds__(kToppThreads) topp_kernel(
     __syncthreads();
 #pragma unroll
     for (int e = 0; e < kPer; ++e)
-      if (rank[e] >= 0) skeep[tid + e * kToppThreads] = static_cast<double>(CF + skeys[rank[e]]) < thr ? 1 : 0;
+      if (rank[e] >= 0) skeep[tid + e * kToppThreads] = CF + skeys[rank[e]] < kthr ? 1 : 0;
   } else {
-    const double thr = __dmul_rn(p, static_cast<double>(T));
+    const unsigned long long kthr = mass_threshold(p, T);
     // 2. bitonic sort, ascending key = score descending, index ascending
     for (int size = 2; size <= npow; size <<= 1) {
       for (int stride = size >> 1; stride > 0; stride >>= 1) {
@@ -217,7 +255,7 @@ __global__ void __launch_bounds__(kToppThreads) topp_kernel(
         __syncthreads();
       }
     }
-    // 3. ranked masses (recovered from the keys), exclusive scan, keep while below thr
+    // 3. ranked masses (recovered from the keys), exclusive scan, keep while below the threshold
     const int R = nb - (f_first ? 1 : 0) - ((f_last && !(f_first && nb == 1)) ? 1 : 0);
     const int ipt = (R + kToppThreads - 1) / kToppThreads;  // contiguous ranks per thread
     const int r0 = tid * ipt;
@@ -232,7 +270,7 @@ __global__ void __launch_bounds__(kToppThreads) topp_kernel(
       const int r = r0 + e;
       if (r < R) {
         const unsigned long long key = skeys[r];
-        skeep[key & 0xFFFFFFFFull] = static_cast<double>(CF + run) < thr ? 1 : 0;
+        skeep[key & 0xFFFFFFFFull] = CF + run < kthr ? 1 : 0;
         run += fixed_mass(key_score(key));
       }
     }
@@ -418,6 +456,37 @@ __global__ void __launch_bounds__(kIndexThreads) select_gather_kernel(
   }
 }
 
+// Top-p launch: shared memory for the padded sort of the largest segment the call can hold
+// (a power of two of at least total_tokens / B + 2 blocks, at most UNIP_TOPP_MAX_BLOCKS).
+cudaError_t launch_topp(const float *imp, const int32_t *blk_cu, const int32_t *cu_seqlens, int32_t num_segs,
+                        int32_t total_tokens, int32_t block_size, double p, uint32_t flags, uint8_t *keep,
+                        int32_t *kept_off, int32_t *seg_kept, uint32_t *status, cudaStream_t st) {
+  static bool configured[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !configured[dev]) {
+    const cudaError_t e = cudaFuncSetAttribute(topp_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               kMaxBlocks * ((int)sizeof(unsigned long long) + 1));
+    if (e != cudaSuccess) return e;
+    configured[dev] = true;
+  }
+  int32_t cap = 16;
+  const int64_t need = (int64_t)total_tokens / block_size + 2;
+  while (cap < need && cap < kMaxBlocks) cap <<= 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)num_segs);
+  cfg.blockDim = dim3(kToppThreads);
+  cfg.dynamicSmemBytes = (size_t)cap * (sizeof(unsigned long long) + 1);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, topp_kernel, imp, blk_cu, cu_seqlens, block_size, p, flags, keep, kept_off,
+                            seg_kept, cap, status);
+}
+
 }  // namespace
 }  // namespace unip
 
@@ -459,18 +528,9 @@ UNIP_API int32_t unip_topp_select(const float *imp, const int32_t *blk_cu, const
   uint8_t *ws = static_cast<uint8_t *>(workspace);
   int32_t *seg_kept = reinterpret_cast<int32_t *>(ws + kWsHeaderBytes);
   int32_t *kept_off = reinterpret_cast<int32_t *>(ws + kWsHeaderBytes + align_up(sizeof(int32_t) * num_segs, 256));
-  static bool configured[64] = {false};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  const int smem = kMaxBlocks * ((int)sizeof(unsigned long long) + 1);
-  if (dev >= 0 && dev < 64 && !configured[dev]) {
-    if (cudaFuncSetAttribute(topp_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-      return UNIP_ERR_CUDA;
-    configured[dev] = true;
-  }
-  topp_kernel<<<num_segs, kToppThreads, smem, st>>>(imp, blk_cu, cu_seqlens, block_size, p, flags, keep, kept_off,
-                                                    seg_kept, status);
-  if (cudaGetLastError() != cudaSuccess) return UNIP_ERR_CUDA;
+  if (launch_topp(imp, blk_cu, cu_seqlens, num_segs, total_tokens, block_size, p, flags, keep, kept_off, seg_kept,
+                  status, st) != cudaSuccess)
+    return UNIP_ERR_CUDA;
   const int grid = total_tokens > 0 ? (total_tokens + kIndexThreads - 1) / kIndexThreads : 1;
   if (num_segs < kIndexSmemSegs) {
     index_kernel<<<grid, kIndexThreads, (num_segs + 1) * sizeof(int32_t), st>>>(
@@ -533,18 +593,9 @@ UNIP_API int32_t unip_select_gather(const float *imp, const int32_t *blk_cu, con
   uint8_t *ws = static_cast<uint8_t *>(workspace);
   int32_t *seg_kept = reinterpret_cast<int32_t *>(ws + kWsHeaderBytes);
   int32_t *kept_off = reinterpret_cast<int32_t *>(ws + kWsHeaderBytes + align_up(sizeof(int32_t) * num_segs, 256));
-  static bool configured[64] = {false};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  const int smem = kMaxBlocks * ((int)sizeof(unsigned long long) + 1);
-  if (dev >= 0 && dev < 64 && !configured[dev]) {
-    if (cudaFuncSetAttribute(topp_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-      return UNIP_ERR_CUDA;
-    configured[dev] = true;
-  }
-  topp_kernel<<<num_segs, kToppThreads, smem, st>>>(imp, blk_cu, cu_seqlens, block_size, p, flags, keep, kept_off,
-                                                    seg_kept, status);
-  if (cudaGetLastError() != cudaSuccess) return UNIP_ERR_CUDA;
+  if (launch_topp(imp, blk_cu, cu_seqlens, num_segs, total_tokens, block_size, p, flags, keep, kept_off, seg_kept,
+                  status, st) != cudaSuccess)
+    return UNIP_ERR_CUDA;
   const int sms = device_sm_count();
   const int warps_per_block = kIndexThreads / 32;
   int64_t blocks = ((int64_t)(total_tokens > 0 ? total_tokens : 1) + warps_per_block - 1) / warps_per_block;
