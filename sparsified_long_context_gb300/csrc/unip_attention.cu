@@ -11,31 +11,39 @@
 //
 // Design
 //   * A device planner (one CTA) validates cu_seqlens / positions, cuts every
-//     segment into 128-row query tiles and orders the (segment, tile) pairs
-//     longest-first by their number of 128-key KV tiles.  The attention grid
-//     is launched with a host-side upper bound; surplus CTAs exit at once.
-//   * One CTA = one 128-row query tile for the two query heads of a GQA pair
-//     (one head when the group is odd); both share every K/V tile.  A KV tile
-//     is either 128 prefix keys (read page by page through the block table)
-//     or 128 of the segment's own keys; only the last prefix tile and the
-//     diagonal own tile need a mask, every fully masked tile is skipped.
+//     segment into 128-token items and orders them longest-first by their
+//     number of 128-key KV tiles, with light items (prefix-streaming tiles of
+//     fewer than 128 valid rows) spread evenly among the heavy ones.  The
+//     attention grid is launched with a host-side upper bound; surplus CTAs
+//     exit at once.
+//   * One CTA = two 128-row query tiles that share every K/V tile.  With an
+//     even GQA group G dividing 128, a tile's rows are (token, head) pairs of
+//     the G query heads of one kv head (128 / G tokens per tile, so a decode
+//     token fills G rows); otherwise 128 tokens of query heads h0 and h0 + 1.
+//     A KV tile is either 128 prefix keys (read page by page through the
+//     block table) or 128 of the segment's own keys; masks only where a tile
+//     crosses the prefix end or a row's own token.
 //   * Warp roles: 8 softmax warps per query tile, each owning 16 TMEM lanes
 //     (16 query rows, all 128 columns) read with the 16x256b shape, so that
 //     4 threads share a row and its maximum and sum need only quad shuffles.
-//     Warp 16 is the TMA producer, warp 17 the tcgen05 issuer.
-//   * K and V tiles stream through one 4-slot ring of 128-byte-swizzled TMA
-//     tiles; a slot is released by a tcgen05.commit after its last MMA.
+//     Warp 16 is the TMA producer, warp 17 the tcgen05 issuer, warps 18-19
+//     share the page copies of prefix tiles with warp 16 (TMA copies issue
+//     one after another within a warp).
+//   * K and V tiles stream through a ring of 128-byte-swizzled TMA tiles: 5
+//     slots with two query tiles, 6 with one (the second Q buffer joins);
+//     a slot is released by a tcgen05.commit after its last MMA.
 //   * TMEM (512 columns): S of each query tile (128 fp32 columns) and O of
 //     each query tile (D columns).  P is written back as bf16 pairs over the
 //     first 64 columns of its S region and read by the PV MMA from TMEM; V is
-//     the MN-major B operand straight from its TMA tile.  The MMA order
-//     PV0(j), QK0(j+1), PV1(j), QK1(j+1) lets one tile's softmax run while
-//     the other tile's MMAs execute.
+//     the MN-major B operand straight from its TMA tile.  Two tiles: the MMA
+//     order PV0(j), QK0(j+1), PV1(j), QK1(j+1) lets one tile's softmax run
+//     while the other tile's MMAs execute.  One tile: S is double-buffered
+//     over both S regions and QK(j+2) runs during the softmax of j.
 //   * Online softmax in base 2 with a lazy rescale: the running maximum is
 //     only moved (and O rescaled in TMEM) when a row's maximum grows by more
 //     than 8 (log2 units), which bounds P by 2^8; the final O / l is exact.
-//     Spreading each tile over 8 warps halves the softmax latency that sits
-//     between a tile's QK^T completing and its PV being issued.
+//     The epilogue reads O in the same 16x256b layout, so each thread holds
+//     its rows' statistics and no shared-memory exchange is needed.
 #include <cuda_bf16.h>
 
 #include <cstring>
