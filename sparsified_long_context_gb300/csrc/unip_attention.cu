@@ -46,6 +46,7 @@
 //     its rows' statistics and no shared-memory exchange is needed.
 #include <cuda_bf16.h>
 
+#include <algorithm>
 #include <cstring>
 #include <mutex>
 
@@ -72,6 +73,7 @@ struct AttnArgs {
   const int32_t *block_table;
   const int2 *pairs;
   const int32_t *num_pairs;
+  int32_t *work_counter;  // next unclaimed work item (set to 0 by the planner)
   __nv_bfloat16 *out;
   float *lse;
   uint32_t *status;
@@ -117,6 +119,7 @@ __global__ void __launch_bounds__(kPlanThreads) attn_plan_kernel(const int32_t *
   if (s_err != 0) {
     if (tid == 0) {
       header[0] = 0;
+      header[1] = 0;
       atomicOr(status, s_err);
     }
     return;
@@ -153,6 +156,7 @@ __global__ void __launch_bounds__(kPlanThreads) attn_plan_kernel(const int32_t *
   if (s_err != 0 || total_pairs > max_pairs) {
     if (tid == 0) {
       header[0] = 0;
+      header[1] = 0;
       atomicOr(status, s_err ? s_err : UNIP_DEV_BAD_SEQLENS);
     }
     return;
@@ -226,7 +230,10 @@ __global__ void __launch_bounds__(kPlanThreads) attn_plan_kernel(const int32_t *
     if (H > 0 && Lc > 0) at = light ? r + (r * H) / Lc + 1 : r + (r * Lc + H - 1) / H;
     pairs[at] = make_int2(sg, m);
   }
-  if (tid == 0) header[0] = total_pairs;
+  if (tid == 0) {
+    header[0] = total_pairs;
+    header[1] = 0;  // work counter of the attention grid
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -241,6 +248,7 @@ constexpr int kWarpTma = 16;
 constexpr int kWarpMma = 17;
 constexpr int kWarpAux0 = 18;     // warps 18, 19: extra issuers of paged K/V copies
 constexpr int kPageIssuers = 3;   // TMA copies issue one at a time per warp: pages go to 3 warps
+constexpr int kUnitReaders = 19;  // warps that read a published work item: 16 softmax, MMA, 2 helpers
 
 template <int D>
 struct SmemLayout {
@@ -262,7 +270,12 @@ enum BarId {
   kBarODone0 = 5 + 2 * kStagesMax,        // + tile: last PV done
   kBarFinal = 7 + 2 * kStagesMax,
   kBarPVDone = 8 + 2 * kStagesMax,        // one query tile: each PV done (O may be rescaled)
-  kNumBars = 9 + 2 * kStagesMax
+  kBarQEmpty = 9 + 2 * kStagesMax,        // last QK of a work item done: Q buffers may be reloaded
+  kBarOFree0 = 10 + 2 * kStagesMax,       // + tile: epilogue read O (count 256)
+  kBarSlotGo0 = 12 + 2 * kStagesMax,      // + slot: a prefix fill of the slot may be issued (helpers)
+  kBarUnitFull0 = 12 + 3 * kStagesMax,    // + k: work item i (k = i & 1) published in s_unit[k]
+  kBarUnitEmpty0 = 14 + 3 * kStagesMax,   // + k: every consumer warp has read s_unit[k]
+  kNumBars = 16 + 3 * kStagesMax
 };
 
 __device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
@@ -309,10 +322,13 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
 // packed layout the PV MMA reads as its A operand.  The epilogue reads O in
 // the same layout, so each thread already holds its rows' maximum and sum.
 
+// sb0 / sb1, pvb and ob: completions of S-full 0 / 1, PV-done and this tile's O-done before this
+// work item (the barriers run on across the items of a persistent CTA).  Returns false on a timeout.
 template <int D, bool db>
-__device__ __forceinline__ void softmax_tile_role(const AttnArgs &a, int tile, const TileRows tr, int32_t T,
+__device__ __forceinline__ bool softmax_tile_role(const AttnArgs &a, int tile, const TileRows tr, int32_t T,
                                                   int32_t Tp, int32_t P, int32_t c0, uint32_t tmem,
-                                                  uint64_t *bars, volatile int *abort_flag) {
+                                                  uint64_t *bars, volatile int *abort_flag, uint32_t sb0,
+                                                  uint32_t sb1, uint32_t pvb, uint32_t ob) {
   const int wt = (threadIdx.x >> 5) & 7;
   const int lane = threadIdx.x & 31;
   const int q = wt & 3, g = wt >> 2;
@@ -330,10 +346,10 @@ __device__ __forceinline__ void softmax_tile_role(const AttnArgs &a, int tile, c
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
   for (int32_t j = 0; j < T; ++j) {
     const int buf = db ? (j & 1) : tile;
-    const uint32_t par = db ? ((j >> 1) & 1) : (j & 1);
+    const uint32_t par = ((buf ? sb1 : sb0) + static_cast<uint32_t>(db ? (j >> 1) : j)) & 1u;
     const uint32_t s_col = buf * kBlockN;
     const uint32_t bar_p = smem_u32(&bars[kBarPFull0 + buf]);
-    if (!mbar_wait(smem_u32(&bars[kBarSFull0 + buf]), par, abort_flag, a.status)) return;
+    if (!mbar_wait(smem_u32(&bars[kBarSFull0 + buf]), par, abort_flag, a.status)) return false;
     if (!active) {
       mbar_arrive(bar_p);
       continue;
@@ -392,7 +408,7 @@ __device__ __forceinline__ void softmax_tile_role(const AttnArgs &a, int tile, c
     // the previous KV tile is complete here because S of this one was committed after it; with
     // one (db) S runs ahead, so that PV is waited for.
     if (j >= 1 && __any_sync(0xffffffffu, need0 || need1)) {
-      if (db && !mbar_wait(smem_u32(&bars[kBarPVDone]), (j - 1) & 1, abort_flag, a.status)) return;
+      if (db && !mbar_wait(smem_u32(&bars[kBarPVDone]), (pvb + j - 1) & 1, abort_flag, a.status)) return false;
       tc_fence_after();
 #pragma unroll 1
       for (int part = 0; part < D / 32; ++part) {
@@ -435,8 +451,15 @@ __device__ __forceinline__ void softmax_tile_role(const AttnArgs &a, int tile, c
   l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
   l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
   l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-  if (!active) return;  // warp-uniform
-  if (!mbar_wait(bar_o, 0, abort_flag, a.status)) return;
+  // Every warp waits for this item's last PV before it arrives on O-free, also one with no valid
+  // row: an arrival before that could land in the previous item's O-free phase and release O while
+  // that item's epilogue still reads it.
+  const uint32_t bar_free = smem_u32(&bars[kBarOFree0 + tile]);
+  if (!mbar_wait(bar_o, ob & 1, abort_flag, a.status)) return false;
+  if (!active) {  // warp-uniform: no row of this warp is stored, O is not read
+    mbar_arrive(bar_free);
+    return true;
+  }
   tc_fence_after();
   // Epilogue in the softmax layout: O of rows R0, R1 in 32-column parts (16x256b), each thread
   // writing two adjacent bf16 per 8-column chunk; a quad covers 16 contiguous bytes of a row.
@@ -463,83 +486,109 @@ __device__ __forceinline__ void softmax_tile_role(const AttnArgs &a, int tile, c
     if (st0) a.lse[(int64_t)h0 * a.N + t0] = (m0 + log2f(l0)) * kLn2;
     if (st1) a.lse[(int64_t)h1 * a.N + t1] = (m1 + log2f(l1)) * kLn2;
   }
+  // this warp's TMEM loads of O are complete: the next work item's first PV may overwrite it
+  tc_fence_before();
+  mbar_arrive(bar_free);
+  return true;
 }
 
-// One CTA = two 128-row query tiles of one segment that share every K/V tile
-// (one tile when the second would hold no valid row).  With lg = 0 (odd or
-// non-dividing GQA group) the tiles are 128 tokens of the query heads h0 and
-// h0 + 1 of one kv head; with lg = log2(G) each row is a (token, head) pair of
-// the G query heads of kv head g, so a tile covers 128 / G tokens and a
+// One work item = two 128-row query tiles of one segment that share every K/V
+// tile (one tile when the second would hold no valid row).  With lg = 0 (odd
+// or non-dividing GQA group) the tiles are 128 tokens of the query heads h0
+// and h0 + 1 of one kv head; with lg = log2(G) each row is a (token, head) pair
+// of the G query heads of kv head g, so a tile covers 128 / G tokens and a
 // single decode token still fills G rows.
+struct WorkItem {
+  TileRows tr0, tr1;
+  int32_t s, c0, P, g, Tp, T;
+  bool two, valid;
+};
+
+__device__ __forceinline__ WorkItem decode_item(const AttnArgs &a, int32_t unit) {
+  WorkItem w;
+  const int32_t pair_idx = unit / a.heads_per_pair, hsel = unit % a.heads_per_pair;
+  const int2 pr = a.pairs[pair_idx];
+  w.s = pr.x;
+  const int32_t m = pr.y;
+  w.c0 = a.cu[w.s];
+  const int32_t n = a.cu[w.s + 1] - w.c0;
+  w.P = a.pos[w.c0];
+  if (a.lg > 0) {
+    const int32_t subs = a.group >> 1;  // CTAs' worth of items per kv head for one 128-token pair
+    w.g = hsel / subs;
+    const int32_t tpt = kBlockM >> a.lg;
+    w.tr0.tok0 = m * kBlockM + (hsel - w.g * subs) * 2 * tpt;
+    w.tr1.tok0 = w.tr0.tok0 + tpt;
+    w.tr0.head0 = w.tr1.head0 = w.g * a.group;
+    w.tr0.lg = w.tr1.lg = a.lg;
+    w.tr0.rows_valid = min(kBlockM, max(0, n - w.tr0.tok0) << a.lg);
+    w.tr1.rows_valid = min(kBlockM, max(0, n - w.tr1.tok0) << a.lg);
+    w.two = w.tr1.rows_valid > 0;
+  } else {
+    w.two = (a.group & 1) == 0;
+    const int32_t h0 = w.two ? 2 * hsel : hsel;
+    w.g = h0 / a.group;
+    w.tr0.tok0 = w.tr1.tok0 = m * kBlockM;
+    w.tr0.head0 = h0;
+    w.tr1.head0 = h0 + 1;
+    w.tr0.lg = w.tr1.lg = 0;
+    w.tr0.rows_valid = w.tr1.rows_valid = min(kBlockM, n - m * kBlockM);
+  }
+  w.valid = w.tr0.rows_valid > 0;  // else every token of the item lies past the segment
+  const TileRows &trl = w.two ? w.tr1 : w.tr0;  // the tile holding the item's last token
+  const int32_t end_tok = trl.tok0 + (trl.rows_valid >> trl.lg);
+  w.Tp = (w.P + kBlockN - 1) / kBlockN;                 // prefix KV tiles
+  w.T = w.valid ? w.Tp + (end_tok - 1) / kBlockN + 1 : 0;  // + own tiles up to the last token's
+  return w;
+}
+
+// Persistent: the TMA warp claims the next non-empty work item of the
+// planner's longest-first list from a global counter (dynamic longest-first
+// scheduling over the SMs) and publishes it to the other roles through a
+// two-entry queue in shared memory; every role walks the same sequence.  The K/V
+// ring and all barriers run on across items, so the producer streams the next
+// item's Q and K/V while the current one finishes, and the next item's first
+// QK overlaps the current epilogue (its first PV waits until O has been read).
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_constant__ AttnArgs a) {
   using L = SmemLayout<D>;
   constexpr int kHalves = D / 64;
+  constexpr int ns = kStages;  // ring slots, after both Q buffers
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bars[kNumBars];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
+  __shared__ int32_t s_unit[2];
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int32_t pair_idx = blockIdx.x / a.heads_per_pair;
-  if (pair_idx >= *a.num_pairs) return;  // uniform over the CTA
-  const int2 pr = a.pairs[pair_idx];
-  const int32_t s = pr.x, m = pr.y;
-  const int32_t hsel = blockIdx.x % a.heads_per_pair;
-  const int32_t c0 = a.cu[s];
-  const int32_t n = a.cu[s + 1] - c0;
-  const int32_t P = a.pos[c0];
-  TileRows tr0, tr1;
-  int32_t g;
-  bool two;
-  if (a.lg > 0) {
-    const int32_t subs = a.group >> 1;  // CTAs per kv head for one 128-token item
-    g = hsel / subs;
-    const int32_t tpt = kBlockM >> a.lg;
-    tr0.tok0 = m * kBlockM + (hsel - g * subs) * 2 * tpt;
-    tr1.tok0 = tr0.tok0 + tpt;
-    tr0.head0 = tr1.head0 = g * a.group;
-    tr0.lg = tr1.lg = a.lg;
-    tr0.rows_valid = min(kBlockM, max(0, n - tr0.tok0) << a.lg);
-    tr1.rows_valid = min(kBlockM, max(0, n - tr1.tok0) << a.lg);
-    if (tr0.rows_valid == 0) return;  // every token of this CTA lies past the segment (uniform)
-    two = tr1.rows_valid > 0;
-  } else {
-    two = (a.group & 1) == 0;  // two query heads of one kv head per CTA
-    const int32_t h0 = two ? 2 * hsel : hsel;
-    g = h0 / a.group;
-    tr0.tok0 = tr1.tok0 = m * kBlockM;
-    tr0.head0 = h0;
-    tr1.head0 = h0 + 1;
-    tr0.lg = tr1.lg = 0;
-    tr0.rows_valid = tr1.rows_valid = min(kBlockM, n - m * kBlockM);
-  }
-  const TileRows &trl = two ? tr1 : tr0;  // the tile holding the CTA's last token
-  const int32_t end_tok = trl.tok0 + (trl.rows_valid >> trl.lg);
-  const int32_t Tp = (P + kBlockN - 1) / kBlockN;  // prefix KV tiles
-  const int32_t T = Tp + (end_tok - 1) / kBlockN + 1;  // + own tiles up to the last token's
+  const int32_t n_units = *a.num_pairs * a.heads_per_pair;
+  if ((int32_t)blockIdx.x >= n_units) return;  // uniform over the CTA
 
   const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
-  // K/V ring: four slots after both Q buffers, or five from the second Q buffer on when it is unused.
-  const int ns = two ? kStages : kStagesMax;
-  const uint32_t ring = two ? L::kRing : L::kQ1;
-  auto slot_addr = [&](int slot) { return sbase + ring + slot * L::kTileBytes; };
+  auto slot_addr = [&](int slot) { return sbase + L::kRing + slot * L::kTileBytes; };
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
   if (threadIdx.x == 0) {
     mbar_init(bar(kBarQFull), 1);
+    mbar_init(bar(kBarQEmpty), 1);
     for (int i = 0; i < kStagesMax; ++i) {
       mbar_init(bar(kBarSlotFull0 + i), 1);
       mbar_init(bar(kBarSlotEmpty0 + i), 1);
+      mbar_init(bar(kBarSlotGo0 + i), 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(kBarSFull0 + i), 1);
       mbar_init(bar(kBarPFull0 + i), 2 * kBlockM);
       mbar_init(bar(kBarODone0 + i), 1);
+      mbar_init(bar(kBarOFree0 + i), 2 * kBlockM);
     }
     mbar_init(bar(kBarFinal), 1);
     mbar_init(bar(kBarPVDone), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(kBarUnitFull0 + i), 1);
+      mbar_init(bar(kBarUnitEmpty0 + i), kUnitReaders);
+    }
     s_abort = 0;
     fence_mbar_init();
   }
@@ -553,134 +602,240 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   const uint32_t tmem = s_tmem;
   volatile int *abort_flag = &s_abort;
 
+  // Barrier completions before the current item, replayed identically by every role:
+  // S-full / P-full per buffer, PV-done, O-done and O-free uses per tile, items done.
+  uint32_t cs0 = 0, cs1 = 0, cpv = 0, co0 = 0, co1 = 0, items = 0;
+  auto advance = [&](const WorkItem &w) {
+    if (w.two) {
+      cs0 += w.T;
+      cs1 += w.T;
+      ++co0;
+      ++co1;
+    } else {
+      cs0 += (w.T + 1) >> 1;
+      cs1 += w.T >> 1;
+      cpv += w.T;
+      ++co0;
+    }
+    ++items;
+  };
+  // Work item i of this CTA as published by the TMA warp (-1: none left).  Every lane of a reading
+  // warp waits and reads; lane 0 then frees the entry for item i + 2.
+  auto next_unit = [&](uint32_t i, int32_t &u) -> bool {
+    const int k = i & 1;
+    if (!mbar_wait(bar(kBarUnitFull0 + k), (i >> 1) & 1, abort_flag, a.status)) return false;
+    u = *reinterpret_cast<volatile int32_t *>(&s_unit[k]);
+    __syncwarp(__activemask());  // the MMA warp reads with lane 0 alone
+    if (lane == 0) mbar_arrive(bar(kBarUnitEmpty0 + k));
+    return true;
+  };
+
   if (warp < 16) {
     // ------------------------------------------------------------ softmax + epilogue
     const int tile = warp >> 3;
-    if (two)
-      softmax_tile_role<D, false>(a, tile, tile ? tr1 : tr0, T, Tp, P, c0, tmem, bars, abort_flag);
-    else if (tile == 0)
-      softmax_tile_role<D, true>(a, 0, tr0, T, Tp, P, c0, tmem, bars, abort_flag);
+    for (uint32_t i = 0;; ++i) {
+      int32_t u;
+      if (!next_unit(i, u) || u < 0) break;
+      const WorkItem w = decode_item(a, u);
+      bool ok = true;
+      if (w.two)
+        ok = softmax_tile_role<D, false>(a, tile, tile ? w.tr1 : w.tr0, w.T, w.Tp, w.P, w.c0, tmem, bars,
+                                         abort_flag, cs0, cs1, cpv, tile ? co1 : co0);
+      else if (tile == 0)
+        ok = softmax_tile_role<D, true>(a, 0, w.tr0, w.T, w.Tp, w.P, w.c0, tmem, bars, abort_flag, cs0, cs1, cpv,
+                                        co0);
+      else  // tile 1 idles through a one-tile item but may not run ahead of its S-full completions
+        ok = mbar_wait(smem_u32(&bars[kBarODone0 + 0]), co0 & 1, abort_flag, a.status);
+      if (!ok) break;
+      advance(w);
+    }
   } else if (warp == kWarpTma || warp >= kWarpAux0) {
     // ------------------------------------------------------------ TMA producers
     // Warp 16 loads Q and the segment's own K/V tiles and arms every slot; the page copies of a
-    // prefix tile are split over warps 16, 18 and 19 (page pi by warp pi mod 3), since one
-    // warp issues its TMA copies one after another.  All three follow the same load sequence
-    // and slot waits.
+    // prefix tile are split over warps 16, 18 and 19 (page pi by warp pi mod 3), since one warp
+    // issues its TMA copies one after another.  All three follow the same load sequence.
     const int pw = warp == kWarpTma ? 0 : warp - kWarpAux0 + 1;
     if (pw == 0 && lane == 0) {
       tma_prefetch_desc(a.lg > 0 ? &a.tm_qp : &a.tm_q);
       tma_prefetch_desc(&a.tm_k);
       tma_prefetch_desc(&a.tm_v);
-      if (Tp > 0) {
+      if (a.num_pages > 0) {
         tma_prefetch_desc(&a.tm_kc);
         tma_prefetch_desc(&a.tm_vc);
       }
-      mbar_arrive_expect_tx(bar(kBarQFull), (two ? 2 : 1) * L::kTileBytes);
-      // box {64, 1, 128} of tm_q, or {64, G, 128 / G} of tm_qp: 128 rows of 128 bytes either way
-      const void *qmap = a.lg > 0 ? static_cast<const void *>(&a.tm_qp) : static_cast<const void *>(&a.tm_q);
-#pragma unroll
-      for (int hf = 0; hf < kHalves; ++hf) {
-        tma_load_3d(sbase + L::kQ0 + hf * L::kHalfBytes, qmap, bar(kBarQFull), hf * 64, tr0.head0, c0 + tr0.tok0);
-        if (two)
-          tma_load_3d(sbase + L::kQ1 + hf * L::kHalfBytes, qmap, bar(kBarQFull), hf * 64, tr1.head0,
-                      c0 + tr1.tok0);
-      }
     }
-    // Lane pi (< pages per tile) copies page pi of every prefix tile.  Block-table entries come in
-    // batches of 32 (one per lane, covering 32 / pages-per-tile tiles), fetched two batches ahead
-    // and validated only when used, so no copy waits on a block-table read.
     const int32_t ppt = kBlockN / a.page_size;  // 1, 2, 4 or 8
-    const int32_t tpb = 32 / ppt;               // tiles per batch (a power of two)
+    const int32_t tpb = 32 / ppt;               // tiles per block-table batch (a power of two)
     const uint32_t page_bytes = a.page_size * 128u;
-    const int64_t bt_row = (int64_t)s * a.max_pages;
-    auto fetch = [&](int32_t j0) -> int32_t {  // raw entry of logical page j0 * ppt + lane, or -1
-      const int32_t lp = j0 * ppt + lane;
-      return (j0 < Tp && lp * a.page_size < P) ? __ldg(&a.block_table[bt_row + lp]) : -1;
-    };
-    int32_t bt_cur = fetch(0), bt_nxt = fetch(tpb), bt_nx2 = fetch(2 * tpb);
-    int32_t ph0 = a.num_pages, ph1 = a.num_pages;  // this lane's page of the last two K tiles
-    int32_t last_k = -1;
-    // The helper warps stop after the last prefix copy: V_(Tp-1), load 2Tp - 1 with two query
-    // tiles, else 2Tp while K runs ahead (Tp - 1 < T - 2) and Tp - 1 + T after.
-    const int32_t n_loads =
-        pw == 0 ? 2 * T : (Tp == 0 ? 0 : (two ? 2 * Tp : (Tp - 1 < T - 2 ? 2 * Tp + 1 : Tp + T)));
-    int32_t issued = 0;
-    int slot = -1;
-    uint32_t round = 0;  // load ld fills slot ld % ns for the (ld / ns)-th time
-    for (int32_t ld = 0; ld < n_loads; ++ld) {
-      if (++slot == ns) {
-        slot = 0;
-        ++round;
+    // Helpers do not wait on slot-empty (they skip the fills they take no part in, so they could drift
+    // two phases from it): warp 16 arrives on the slot's go barrier for every prefix fill after its
+    // own slot-empty wait, and the helpers wait on those in order, one go per prefix fill of a slot.
+    uint32_t go[kStages] = {0, 0, 0, 0, 0};
+    const bool helpers = ppt > 1;
+    int64_t lbase = 0;  // ring loads issued before the current item (all producer warps count them)
+    int64_t issued = 0;
+    uint32_t q_issued = 0;  // Q loads issued (warp 16)
+    bool ok = true;
+    for (uint32_t i = 0; ok; ++i) {
+      int32_t u = -1;
+      if (pw == 0) {
+        // claim the next work item with at least one valid row and publish it
+        int okq = 1;
+        if (lane == 0) {
+          for (;;) {
+            const int32_t c = atomicAdd(a.work_counter, 1);
+            if (c >= n_units) break;
+            if (decode_item(a, c).valid) {
+              u = c;
+              break;
+            }
+          }
+          const int k = i & 1;
+          if (i >= 2) okq = mbar_wait(bar(kBarUnitEmpty0 + k), ((i >> 1) - 1) & 1, abort_flag, a.status);
+          if (okq) {
+            s_unit[k] = u;
+            mbar_arrive(bar(kBarUnitFull0 + k));
+          }
+        }
+        if (!__shfl_sync(0xffffffffu, okq, 0)) break;
+        u = __shfl_sync(0xffffffffu, u, 0);
+      } else if (!next_unit(i, u)) {
+        break;
       }
-      int ok = 1;
-      if (lane == 0 && round > 0)
-        ok = mbar_wait(bar(kBarSlotEmpty0 + slot), (round - 1) & 1, abort_flag, a.status);
-      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-      // Loads follow the order the MMAs consume them: K_j, V_j alternating with two query tiles;
-      // with one, K runs two tiles ahead of V: K0, K1, V0, K2, V1, ..., K(T-1), V(T-2), V(T-1).
-      int32_t j;
-      bool is_v;
-      if (two) {
-        j = ld >> 1;
-        is_v = ld & 1;
-      } else if (ld < 2) {
-        is_v = ld == 1 && T == 1;
-        j = is_v ? 0 : ld;
-      } else {
-        const int32_t t = ld - 2;
-        if (t < 2 * (T - 2)) {
-          is_v = (t & 1) == 0;
-          j = is_v ? (t >> 1) : (t >> 1) + 2;
+      if (u < 0) break;
+      const WorkItem w = decode_item(a, u);
+      const int32_t T = w.T, Tp = w.Tp, P = w.P, c0 = w.c0, g = w.g;
+      const bool two = w.two;
+      if (pw == 0 && lane == 0) {
+        // Q of this item once the previous item's last QK has read the buffers
+        if (items > 0) ok = mbar_wait(bar(kBarQEmpty), (items - 1) & 1, abort_flag, a.status);
+        if (ok) {
+          mbar_arrive_expect_tx(bar(kBarQFull), (two ? 2 : 1) * L::kTileBytes);
+          // box {64, 1, 128} of tm_q, or {64, G, 128 / G} of tm_qp: 128 rows of 128 bytes either way
+          const void *qmap = a.lg > 0 ? static_cast<const void *>(&a.tm_qp) : static_cast<const void *>(&a.tm_q);
+#pragma unroll
+          for (int hf = 0; hf < kHalves; ++hf) {
+            tma_load_3d(sbase + L::kQ0 + hf * L::kHalfBytes, qmap, bar(kBarQFull), hf * 64, w.tr0.head0,
+                        c0 + w.tr0.tok0);
+            if (two)
+              tma_load_3d(sbase + L::kQ1 + hf * L::kHalfBytes, qmap, bar(kBarQFull), hf * 64, w.tr1.head0,
+                          c0 + w.tr1.tok0);
+          }
+          q_issued = items + 1;
+        }
+      }
+      if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
+      // Page ids in warp-wide batches of 32 entries, fetched two batches ahead, validated at use.
+      const int64_t bt_row = (int64_t)w.s * a.max_pages;
+      auto fetch = [&](int32_t j0) -> int32_t {  // raw entry of logical page j0 * ppt + lane, or -1
+        const int32_t lp = j0 * ppt + lane;
+        return (j0 < Tp && lp * a.page_size < P) ? __ldg(&a.block_table[bt_row + lp]) : -1;
+      };
+      int32_t bt_cur = fetch(0), bt_nxt = fetch(tpb), bt_nx2 = fetch(2 * tpb);
+      int32_t ph0 = a.num_pages, ph1 = a.num_pages;  // this lane's page of the last two K tiles
+      int32_t last_k = -1;
+      // Helper warps stop after the item's last prefix copy: V_(Tp-1), load 2Tp - 1 with two query
+      // tiles, else 2Tp while K runs ahead (Tp - 1 < T - 2) and Tp - 1 + T after.
+      // A helper that owns no page of a tile (page size 64 or 128) waits for nothing at all.
+      const int32_t n_loads =
+          pw == 0 ? 2 * T
+                  : (Tp == 0 || ppt <= pw ? 0 : (two ? 2 * Tp : (Tp - 1 < T - 2 ? 2 * Tp + 1 : Tp + T)));
+      for (int32_t ld = 0; ld < n_loads; ++ld) {
+        const int64_t gl = lbase + ld;
+        const int slot = (int)(gl % ns);
+        const int64_t round = gl / ns;
+        // Loads follow the order the MMAs consume them: K_j, V_j alternating with two query tiles;
+        // with one, K runs two tiles ahead of V: K0, K1, V0, K2, V1, ..., K(T-1), V(T-2), V(T-1).
+        int32_t j;
+        bool is_v;
+        if (two) {
+          j = ld >> 1;
+          is_v = ld & 1;
+        } else if (ld < 2) {
+          is_v = ld == 1 && T == 1;
+          j = is_v ? 0 : ld;
         } else {
-          is_v = true;
-          j = t - T + 2;
+          const int32_t t = ld - 2;
+          if (t < 2 * (T - 2)) {
+            is_v = (t & 1) == 0;
+            j = is_v ? (t >> 1) : (t >> 1) + 2;
+          } else {
+            is_v = true;
+            j = t - T + 2;
+          }
         }
-      }
-      const uint32_t dst = slot_addr(slot);
-      const uint32_t fb = bar(kBarSlotFull0 + slot);
-      if (pw == 0 && lane == 0) mbar_arrive_expect_tx(fb, L::kTileBytes);
-      __syncwarp();
-      int32_t phys = a.num_pages;  // past the prefix end, or a bad entry: zero fill
-      if (!is_v) {
+        const uint32_t dst = slot_addr(slot);
+        const uint32_t fb = bar(kBarSlotFull0 + slot);
+        int okw = 1;
+        if (pw == 0) {
+          if (lane == 0) {
+            if (round > 0)
+              okw = mbar_wait(bar(kBarSlotEmpty0 + slot), (uint32_t)(round - 1) & 1, abort_flag, a.status);
+            if (okw) {
+              mbar_arrive_expect_tx(fb, L::kTileBytes);
+              if (helpers && j < Tp) mbar_arrive(bar(kBarSlotGo0 + slot));
+            }
+          }
+        } else if (j < Tp) {
+          uint32_t k = 0;
+#pragma unroll
+          for (int sl = 0; sl < kStages; ++sl)
+            if (sl == slot) k = go[sl]++;
+          if (lane == 0) okw = mbar_wait(bar(kBarSlotGo0 + slot), k & 1, abort_flag, a.status);
+        }
+        if (!__shfl_sync(0xffffffffu, okw, 0)) {
+          ok = false;
+          break;
+        }
+        int32_t phys = a.num_pages;  // past the prefix end, or a bad entry: zero fill
+        if (!is_v) {
+          if (j < Tp) {
+            if (j > 0 && (j & (tpb - 1)) == 0) {
+              bt_cur = bt_nxt;
+              bt_nxt = bt_nx2;
+              bt_nx2 = fetch(j + 2 * tpb);
+            }
+            const int32_t e = __shfl_sync(0xffffffffu, bt_cur, (j & (tpb - 1)) * ppt + (lane & (ppt - 1)));
+            if (lane < ppt && (j * ppt + lane) * a.page_size < P) {
+              if (e >= 0 && e < a.num_pages) phys = e;
+              else if (lane % kPageIssuers == pw) atomicOr(a.status, UNIP_DEV_BAD_PAGES);
+            }
+          }
+          ph1 = ph0;
+          ph0 = phys;
+          last_k = j;
+        } else {
+          phys = last_k == j ? ph0 : ph1;  // V_j follows K_j or K_(j+1)
+        }
         if (j < Tp) {
-          if (j > 0 && (j & (tpb - 1)) == 0) {
-            bt_cur = bt_nxt;
-            bt_nxt = bt_nx2;
-            bt_nx2 = fetch(j + 2 * tpb);
-          }
-          const int32_t e = __shfl_sync(0xffffffffu, bt_cur, (j & (tpb - 1)) * ppt + (lane & (ppt - 1)));
-          if (lane < ppt && (j * ppt + lane) * a.page_size < P) {
-            if (e >= 0 && e < a.num_pages) phys = e;
-            else if (lane % kPageIssuers == pw) atomicOr(a.status, UNIP_DEV_BAD_PAGES);
-          }
-        }
-        ph1 = ph0;
-        ph0 = phys;
-        last_k = j;
-      } else {
-        phys = last_k == j ? ph0 : ph1;  // V_j follows K_j or K_(j+1)
-      }
-      if (j < Tp) {
-        const void *map = is_v ? static_cast<const void *>(&a.tm_vc) : static_cast<const void *>(&a.tm_kc);
-        if (lane < ppt && lane % kPageIssuers == pw) {
+          const void *map = is_v ? static_cast<const void *>(&a.tm_vc) : static_cast<const void *>(&a.tm_kc);
+          if (lane < ppt && lane % kPageIssuers == pw) {
 #pragma unroll
-          for (int hf = 0; hf < kHalves; ++hf)
-            tma_load_4d(dst + hf * L::kHalfBytes + lane * page_bytes, map, fb, hf * 64, g, 0, phys);
-        }
-      } else if (pw == 0 && lane == 0) {
-        const void *map = is_v ? static_cast<const void *>(&a.tm_v) : static_cast<const void *>(&a.tm_k);
-        const int32_t krow = c0 + (j - Tp) * kBlockN;
+            for (int hf = 0; hf < kHalves; ++hf)
+              tma_load_4d(dst + hf * L::kHalfBytes + lane * page_bytes, map, fb, hf * 64, g, 0, phys);
+          }
+        } else if (pw == 0 && lane == 0) {
+          const void *map = is_v ? static_cast<const void *>(&a.tm_v) : static_cast<const void *>(&a.tm_k);
+          const int32_t krow = c0 + (j - Tp) * kBlockN;
 #pragma unroll
-        for (int hf = 0; hf < kHalves; ++hf) tma_load_3d(dst + hf * L::kHalfBytes, map, fb, hf * 64, g, krow);
+          for (int hf = 0; hf < kHalves; ++hf) tma_load_3d(dst + hf * L::kHalfBytes, map, fb, hf * 64, g, krow);
+        }
+        issued = gl + 1;
       }
-      issued = ld + 1;
+      lbase += 2 * T;
+      advance(w);
     }
     if (lane == 0 && *abort_flag) {
       // Let copies already in flight land before the CTA's shared memory is released.
-      for (int32_t ld = max(0, issued - ns); ld < issued; ++ld) {
+      for (int64_t gl = max((int64_t)0, issued - ns); gl < issued; ++gl) {
         const uint64_t t0 = globaltimer_ns();
-        while (!mbar_try_wait(bar(kBarSlotFull0 + ld % ns), (ld / ns) & 1) &&
+        while (!mbar_try_wait(bar(kBarSlotFull0 + (int)(gl % ns)), (uint32_t)(gl / ns) & 1) &&
                globaltimer_ns() - t0 < kWaitLimitNs) {
+        }
+      }
+      if (pw == 0 && q_issued > 0) {
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(bar(kBarQFull), (q_issued - 1) & 1) && globaltimer_ns() - t0 < kWaitLimitNs) {
         }
       }
     }
@@ -693,11 +848,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       // (in 16-byte units) to the start-address field.
       const uint64_t dq0 = sdesc_sw128(sbase + L::kQ0, 16, 1024);
       const uint64_t dq1 = sdesc_sw128(sbase + L::kQ1, 16, 1024);
-      const uint64_t dk = sdesc_sw128(sbase + ring, 16, 1024);
-      const uint64_t dv = sdesc_sw128(sbase + ring, L::kHalfBytes, 1024);
+      const uint64_t dk = sdesc_sw128(sbase + L::kRing, 16, 1024);
+      const uint64_t dv = sdesc_sw128(sbase + L::kRing, L::kHalfBytes, 1024);
       const uint32_t d_s0 = tmem, d_s1 = tmem + kBlockN;
       const uint32_t d_o0 = tmem + kTmemO, d_o1 = tmem + kTmemO + 128;
-      // K_j is load 2j and V_j load 2j+1 of the ring: slot ld % ns, phase (ld / ns) & 1.
       auto slot_desc = [&](uint64_t d, int slot) { return d + ((uint64_t)(slot * L::kTileBytes) >> 4); };
       auto qk = [&](uint32_t d_s, uint64_t dq, uint64_t dkb) {
 #pragma unroll
@@ -711,94 +865,103 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         for (int kk = 0; kk < kBlockN / 16; ++kk)
           umma_bf16_ts(d_o, p_tmem + kk * 8, dvb + (uint64_t)((kk * 2048) >> 4), idesc_pv, kk > 0 ? 1u : acc_first);
       };
-      bool ok = mbar_wait(bar(kBarQFull), 0, abort_flag, a.status) &&
-                mbar_wait(bar(kBarSlotFull0 + 0), 0, abort_flag, a.status);
-      if (!two) {
-        // One query tile: S is double-buffered over both S regions, so QK(j+2) runs while the
-        // softmax of KV tile j does.  Order: QK(0), QK(1), then PV(j), QK(j+2) for each j.
-        if (ok) {
-          tc_fence_after();
-          qk(d_s0, dq0, slot_desc(dk, 0));
-          umma_commit(bar(kBarSFull0 + 0));
-          umma_commit(bar(kBarSlotEmpty0 + 0));
-          if (T > 1) {
-            if ((ok = mbar_wait(bar(kBarSlotFull0 + 1), 0, abort_flag, a.status))) {  // K_1 = load 1
-              qk(d_s1, dq0, slot_desc(dk, 1));
-              umma_commit(bar(kBarSFull0 + 1));
-              umma_commit(bar(kBarSlotEmpty0 + 1));
-            }
-          }
-        }
-        // Load index of V_j: 2j + 2 while K still runs ahead (j < T - 2), then j + T; of K_m: 2m - 1.
-        for (int32_t j = 0; ok && j < T; ++j) {
-          const int32_t iv = j < T - 2 ? 2 * j + 2 : j + T, ik = 2 * j + 3;
-          const int vslot = iv % ns, kslot = ik % ns;
-          const uint32_t vphase = (iv / ns) & 1, kphase = (ik / ns) & 1;
-          const int buf = j & 1;
-          const uint32_t d_s = tmem + buf * kBlockN;
-          ok = mbar_wait(bar(kBarPFull0 + buf), (j >> 1) & 1, abort_flag, a.status) &&
-               mbar_wait(bar(kBarSlotFull0 + vslot), vphase, abort_flag, a.status);
-          if (!ok) break;
-          tc_fence_after();
-          pv(d_o0, d_s, slot_desc(dv, vslot), j > 0 ? 1u : 0u);
-          umma_commit(bar(kBarPVDone));
-          umma_commit(bar(kBarSlotEmpty0 + vslot));
-          if (j + 1 == T) umma_commit(bar(kBarODone0 + 0));
-          if (j + 2 < T) {
-            if (!(ok = mbar_wait(bar(kBarSlotFull0 + kslot), kphase, abort_flag, a.status))) break;
-            qk(d_s, dq0, slot_desc(dk, kslot));
-            umma_commit(bar(kBarSFull0 + buf));
-            umma_commit(bar(kBarSlotEmpty0 + kslot));
-          }
-        }
-        ok = false;  // the two-tile schedule below is skipped
-      }
-      if (ok) {
-        tc_fence_after();
-        const uint64_t dk0 = slot_desc(dk, 0);
-        qk(d_s0, dq0, dk0);
-        umma_commit(bar(kBarSFull0 + 0));
-        if (two) {
-          qk(d_s1, dq1, dk0);
-          umma_commit(bar(kBarSFull0 + 1));
-        }
-        umma_commit(bar(kBarSlotEmpty0 + 0));
-      }
-      int vslot = 1, kslot = 2;            // V_0 = load 1, K_1 = load 2 (ns >= 4)
-      uint32_t vphase = 0, kphase = 0;
-      for (int32_t j = 0; ok && j < T; ++j) {
-        const bool more = j + 1 < T;
-        const uint64_t dvj = slot_desc(dv, vslot), dkn = slot_desc(dk, kslot);
-        const uint32_t acc = j > 0 ? 1u : 0u;
-        // tile 0: PV(j), then QK(j+1); K_(j+1) is waited for first so that both go out back to back
-        ok = mbar_wait(bar(kBarSlotFull0 + vslot), vphase, abort_flag, a.status) &&
-             (!more || mbar_wait(bar(kBarSlotFull0 + kslot), kphase, abort_flag, a.status)) &&
-             mbar_wait(bar(kBarPFull0 + 0), j & 1, abort_flag, a.status);
+      // ring load gl sits in slot gl % ns and completes phase (gl / ns) & 1
+      auto full = [&](int64_t gl) {
+        return mbar_wait(bar(kBarSlotFull0 + (int)(gl % ns)), (uint32_t)(gl / ns) & 1, abort_flag, a.status);
+      };
+      auto release = [&](int64_t gl) { umma_commit(bar(kBarSlotEmpty0 + (int)(gl % ns))); };
+      // O of tile t may be overwritten once the previous item's epilogue has read it
+      auto o_free = [&](int t, uint32_t uses) {
+        return uses == 0 || mbar_wait(bar(kBarOFree0 + t), (uses - 1) & 1, abort_flag, a.status);
+      };
+      int64_t lbase = 0;
+      bool ok = true;
+      for (uint32_t i = 0; ok; ++i) {
+        int32_t u;
+        if (!next_unit(i, u) || u < 0) break;
+        const WorkItem w = decode_item(a, u);
+        const int32_t T = w.T;
+        ok = mbar_wait(bar(kBarQFull), items & 1, abort_flag, a.status) && full(lbase);
         if (!ok) break;
         tc_fence_after();
-        pv(d_o0, d_s0, dvj, acc);
-        if (!more) umma_commit(bar(kBarODone0 + 0));
-        if (!two) umma_commit(bar(kBarSlotEmpty0 + vslot));
-        if (more) {
-          qk(d_s0, dq0, dkn);
+        if (!w.two) {
+          // One query tile: S is double-buffered over both S regions, so QK(j+2) runs while the
+          // softmax of KV tile j does.  Order: QK(0), QK(1), then PV(j), QK(j+2) for each j.
+          // Load index of K_0, K_1: 0, 1; of K_m (m >= 2): 2m - 1; of V_j: 2j + 2 while K still runs
+          // ahead (j < T - 2), then j + T.
+          qk(d_s0, dq0, slot_desc(dk, (int)(lbase % ns)));
           umma_commit(bar(kBarSFull0 + 0));
-          if (!two) umma_commit(bar(kBarSlotEmpty0 + kslot));
-        }
-        if (two) {
-          // tile 1: PV(j), then QK(j+1)
-          if (!(ok = mbar_wait(bar(kBarPFull0 + 1), j & 1, abort_flag, a.status))) break;
-          tc_fence_after();
-          pv(d_o1, d_s1, dvj, acc);
-          if (!more) umma_commit(bar(kBarODone0 + 1));
-          if (more) {
-            qk(d_s1, dq1, dkn);
-            umma_commit(bar(kBarSFull0 + 1));  // first: the softmax of tile 1 waits on it
-            umma_commit(bar(kBarSlotEmpty0 + kslot));
+          release(lbase);
+          if (T > 1) {
+            if (!(ok = full(lbase + 1))) break;
+            qk(d_s1, dq0, slot_desc(dk, (int)((lbase + 1) % ns)));
+            umma_commit(bar(kBarSFull0 + 1));
+            release(lbase + 1);
           }
-          umma_commit(bar(kBarSlotEmpty0 + vslot));
+          if (T <= 2) umma_commit(bar(kBarQEmpty));
+          for (int32_t j = 0; ok && j < T; ++j) {
+            const int buf = j & 1;
+            const uint32_t d_s = tmem + buf * kBlockN;
+            const int64_t iv = lbase + (j < T - 2 ? 2 * j + 2 : j + T), ik = lbase + 2 * j + 3;
+            ok = mbar_wait(bar(kBarPFull0 + buf), ((buf ? cs1 : cs0) + (j >> 1)) & 1, abort_flag, a.status) &&
+                 full(iv) && (j > 0 || o_free(0, co0));
+            if (!ok) break;
+            tc_fence_after();
+            pv(d_o0, d_s, slot_desc(dv, (int)(iv % ns)), j > 0 ? 1u : 0u);
+            umma_commit(bar(kBarPVDone));
+            release(iv);
+            if (j + 1 == T) umma_commit(bar(kBarODone0 + 0));
+            if (j + 2 < T) {
+              if (!(ok = full(ik))) break;
+              qk(d_s, dq0, slot_desc(dk, (int)(ik % ns)));
+              umma_commit(bar(kBarSFull0 + buf));
+              release(ik);
+              if (j + 3 == T) umma_commit(bar(kBarQEmpty));  // QK(T-1): the last read of Q
+            }
+          }
+        } else {
+          // Two query tiles: K_j is load 2j, V_j load 2j + 1.
+          const uint64_t dk0 = slot_desc(dk, (int)(lbase % ns));
+          qk(d_s0, dq0, dk0);
+          umma_commit(bar(kBarSFull0 + 0));
+          qk(d_s1, dq1, dk0);
+          umma_commit(bar(kBarSFull0 + 1));
+          release(lbase);
+          if (T == 1) umma_commit(bar(kBarQEmpty));
+          for (int32_t j = 0; ok && j < T; ++j) {
+            const bool more = j + 1 < T;
+            const int64_t iv = lbase + 2 * j + 1, ik = lbase + 2 * j + 2;
+            const uint64_t dvj = slot_desc(dv, (int)(iv % ns)), dkn = slot_desc(dk, (int)(ik % ns));
+            const uint32_t acc = j > 0 ? 1u : 0u;
+            // tile 0: PV(j), then QK(j+1); K_(j+1) is waited for first so that both go out back to back
+            ok = full(iv) && (!more || full(ik)) &&
+                 mbar_wait(bar(kBarPFull0 + 0), (cs0 + j) & 1, abort_flag, a.status) && (j > 0 || o_free(0, co0));
+            if (!ok) break;
+            tc_fence_after();
+            pv(d_o0, d_s0, dvj, acc);
+            if (!more) umma_commit(bar(kBarODone0 + 0));
+            if (more) {
+              qk(d_s0, dq0, dkn);
+              umma_commit(bar(kBarSFull0 + 0));
+            }
+            // tile 1: PV(j), then QK(j+1)
+            if (!(ok = mbar_wait(bar(kBarPFull0 + 1), (cs1 + j) & 1, abort_flag, a.status) &&
+                       (j > 0 || o_free(1, co1))))
+              break;
+            tc_fence_after();
+            pv(d_o1, d_s1, dvj, acc);
+            if (!more) umma_commit(bar(kBarODone0 + 1));
+            if (more) {
+              qk(d_s1, dq1, dkn);
+              umma_commit(bar(kBarSFull0 + 1));  // first: the softmax of tile 1 waits on it
+              release(ik);
+              if (j + 2 == T) umma_commit(bar(kBarQEmpty));  // QK(T-1): the last read of Q
+            }
+            release(iv);
+          }
         }
-        if ((vslot += 2) >= ns) { vslot -= ns; vphase ^= 1u; }
-        if ((kslot += 2) >= ns) { kslot -= ns; kphase ^= 1u; }
+        lbase += 2 * T;
+        advance(w);
       }
       // Every tcgen05 op of this CTA has landed before TMEM is released.
       umma_commit(bar(kBarFinal));
@@ -926,6 +1089,7 @@ UNIP_API int32_t unip_prefill_attention(const void *q, const void *k, const void
   args.block_table = has_cache ? paged->block_table : nullptr;
   args.pairs = pairs;
   args.num_pairs = header;
+  args.work_counter = header + 1;
   args.out = static_cast<__nv_bfloat16 *>(out);
   args.lse = lse;
   args.status = status;
@@ -940,8 +1104,11 @@ UNIP_API int32_t unip_prefill_attention(const void *q, const void *k, const void
   args.max_pages = has_cache ? paged->max_pages_per_seq : 0;
   const float scale = prm->scale > 0.f ? prm->scale : 1.0f / sqrtf((float)D);
   args.scale_log2 = scale * kLog2e;
-  const int64_t grid = (int64_t)max_pairs * args.heads_per_pair;
-  if (grid > 0x7FFFFFFF) return UNIP_ERR_UNSUPPORTED;
+  // persistent grid: one CTA per SM (fewer when the plan cannot hold that many work items)
+  const int64_t units_bound = (int64_t)max_pairs * args.heads_per_pair;
+  if (units_bound > 0x7FFFFFFF) return UNIP_ERR_UNSUPPORTED;
+  const int sms = device_sm_count();
+  const int64_t grid = std::min<int64_t>(units_bound, sms > 0 ? sms : 1);
   const cudaError_t e = D == 128 ? launch_attention<128>(args, (int)grid, st) : launch_attention<64>(args, (int)grid, st);
   return e == cudaSuccess ? UNIP_OK : UNIP_ERR_CUDA;
 }
