@@ -13,10 +13,11 @@
 //   * A device planner (one CTA) validates cu_seqlens / positions, cuts every
 //     segment into 128-token items and orders them longest-first by their
 //     number of 128-key KV tiles, with light items (prefix-streaming tiles of
-//     fewer than 128 valid rows) spread evenly among the heavy ones.  The
-//     attention grid is launched with a host-side upper bound; surplus CTAs
-//     exit at once.
-//   * One CTA = two 128-row query tiles that share every K/V tile.  With an
+//     fewer than 128 valid rows) spread evenly among the heavy ones.
+//   * Persistent grid, one CTA per SM: the TMA warp claims work items in that
+//     order from a global counter and publishes them to the other roles; the
+//     K/V ring, the Q buffers and every barrier run on across items.
+//   * One work item = two 128-row query tiles that share every K/V tile.  With an
 //     even GQA group G dividing 128, a tile's rows are (token, head) pairs of
 //     the G query heads of one kv head (128 / G tokens per tile, so a decode
 //     token fills G rows); otherwise 128 tokens of query heads h0 and h0 + 1.
@@ -29,9 +30,8 @@
 //     Warp 16 is the TMA producer, warp 17 the tcgen05 issuer, warps 18-19
 //     share the page copies of prefix tiles with warp 16 (TMA copies issue
 //     one after another within a warp).
-//   * K and V tiles stream through a ring of 128-byte-swizzled TMA tiles: 5
-//     slots with two query tiles, 6 with one (the second Q buffer joins);
-//     a slot is released by a tcgen05.commit after its last MMA.
+//   * K and V tiles stream through a 5-slot ring of 128-byte-swizzled TMA
+//     tiles; a slot is released by a tcgen05.commit after its last MMA.
 //   * TMEM (512 columns): S of each query tile (128 fp32 columns) and O of
 //     each query tile (D columns).  P is written back as bf16 pairs over the
 //     first 64 columns of its S region and read by the PV MMA from TMEM; V is
