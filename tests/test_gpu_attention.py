@@ -111,6 +111,20 @@ def test_decode_batch_with_prefixes(hq, hkv, d):
     _check(_batch_with_prefixes(Ps, ns, hq, hkv, d, 16, seed=hq * 100 + d))
 
 
+@pytest.mark.parametrize("hq,hkv,page,d,seed", [(32, 8, 16, 128, 21), (16, 2, 64, 64, 22), (12, 2, 32, 128, 23)])
+def test_many_segments_with_prefixes(hq, hkv, page, d, seed):
+    """More work items than SMs, mixing one- and two-tile items and paged prefixes of every length,
+    so that each persistent CTA walks many items (the ring, the Q buffers and O run on across them)."""
+    rng = np.random.default_rng(seed)
+    S = 260
+    ns = rng.integers(1, 300, S).tolist()
+    ns[::7] = [1] * len(ns[::7])                       # decode-like segments
+    Ps = rng.integers(0, 1500, S).tolist()
+    Ps[::5] = [0] * len(Ps[::5])                       # some segments without a prefix
+    wl = _batch_with_prefixes(Ps, ns, hq, hkv, d, page, seed)
+    _check(wl, sample_rows(wl, 300))
+
+
 def test_chunked_equals_one_shot():
     one, chunks = W.chunked()
     outs = []
