@@ -235,7 +235,9 @@ UNIP_API int32_t unip_topp_select(const float *imp, const int32_t *blk_cu,
  * and strides multiples of 8).  Same results as unip_topp_select followed by
  * unip_gather_tokens, with the index build folded into the gather so that the
  * call launches two kernels; the gather may start while Top-p finishes
- * (programmatic dependent launch).  Workspace as unip_topp_select.  With
+ * (programmatic dependent launch).  With a single segment (num_segs == 1)
+ * it is one launch: every CTA selects the segment's blocks itself and copies
+ * its share of the kept rows.  Workspace as unip_topp_select.  With
  * hidden == hidden_out == NULL and d_model == 0 no rows are copied (the
  * selection and index outputs only).
  * ------------------------------------------------------------------------- */

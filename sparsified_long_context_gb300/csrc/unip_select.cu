@@ -17,6 +17,10 @@
 //                 the ranked masses need no second read), exclusive scan of
 //                 the ranked integer masses, keep decision per block,
 //                 exclusive scan of kept lengths; writes the segment's count.
+//   select_gather_onepass_kernel  one segment in the call: every CTA selects
+//                 the segment's blocks itself, stages the kept offsets and
+//                 copies its share of the kept rows (one launch, no grid
+//                 waits for another).
 //   index_kernel  one thread per source token: every CTA scans the
 //                 per-segment counts into shared memory (CTA 0 also writes
 //                 cu_seqlens_kept and n_kept), then writes gather_idx and
@@ -88,38 +92,16 @@ __device__ __forceinline__ void bitonic_sort_regs(unsigned long long &key, unsig
   }
 }
 
-__global__ void __launch_bounds__(kToppThreads) topp_kernel(
-    const float *__restrict__ imp, const int32_t *__restrict__ blk_cu, const int32_t *__restrict__ cu, int32_t B,
-    double p, uint32_t flags, uint8_t *__restrict__ keep, int32_t *__restrict__ kept_off,
-    int32_t *__restrict__ seg_kept, int32_t cap, uint32_t *__restrict__ status) {
-  extern __shared__ unsigned long long skeys[];  // cap rank keys, then cap keep flags
-  uint8_t *skeep = reinterpret_cast<uint8_t *>(skeys + cap);
-  __shared__ unsigned long long sh64[32];
-  __shared__ int32_t sh32[32];
-  __shared__ uint32_t s_bad;
+// Keep flags of one scored segment (nb blocks from imp[b0]) into skeep[0, nb), run by all
+// kToppThreads threads of the CTA: fixed-point masses, exact totals, rank keys sorted (register
+// bitonic up to 512 blocks, rank counting up to 1024, shared-memory bitonic beyond; skeys holds
+// the padded sort), ranked exclusive scan, keep while below the integer threshold.  Returns false
+// (status raised) when a score is not in [0, 1].
+__device__ bool select_segment_blocks(const float *__restrict__ imp, int32_t b0, int32_t nb, double p,
+                                      uint32_t flags, unsigned long long *skeys, uint8_t *skeep,
+                                      unsigned long long *sh64, uint32_t *s_bad, uint32_t *status) {
   const int tid = threadIdx.x;
-  // A gather launched as a programmatic dependent may start now; it waits for this grid's results.
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  // This grid may itself run as a programmatic dependent of the importance kernels: no memory is
-  // touched before their results are visible.
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int32_t s = blockIdx.x;
-  const int32_t n = cu[s + 1] - cu[s];
-  const int32_t b0 = blk_cu[s], nb = blk_cu[s + 1] - blk_cu[s];
-
-  if (nb == 0) {  // not scored: every token is kept
-    if (tid == 0) seg_kept[s] = n > 0 ? n : 0;
-    return;
-  }
-  // cap (a power of two) bounds the padded sort of every segment that fits the call's token count
-  if (nb > kMaxBlocks || nb > cap || n <= 0 || nb != (n + B - 1) / B) {
-    if (tid == 0) {
-      atomicOr(status, nb > kMaxBlocks ? UNIP_DEV_TOO_MANY_BLOCKS : UNIP_DEV_BAD_BLOCKS);
-      seg_kept[s] = 0;
-    }
-    return;
-  }
-  if (tid == 0) s_bad = 0;
+  if (tid == 0) *s_bad = 0;
   int npow = 1;
   while (npow < nb) npow <<= 1;
   const bool f_first = (flags & UNIP_KEEP_FIRST) != 0;
@@ -150,16 +132,13 @@ __global__ void __launch_bounds__(kToppThreads) topp_kernel(
     }
     skeys[b] = key;
   }
-  if (bad) atomicOr(&s_bad, 1u);
+  if (bad) atomicOr(s_bad, 1u);
   unsigned long long T, CF;
   block_excl_scan<unsigned long long>(tsum, sh64, &T);
   block_excl_scan<unsigned long long>(fsum, sh64, &CF);
-  if (s_bad) {
-    if (tid == 0) {
-      atomicOr(status, UNIP_DEV_BAD_SCORES);
-      seg_kept[s] = 0;
-    }
-    return;
+  if (*s_bad) {
+    if (tid == 0) atomicOr(status, UNIP_DEV_BAD_SCORES);
+    return false;
   }
   if (T == 0) {
     for (int b = tid; b < nb; b += kToppThreads) skeep[b] = 1;
@@ -276,6 +255,44 @@ __global__ void __launch_bounds__(kToppThreads) topp_kernel(
     }
   }
   __syncthreads();
+  return true;
+}
+
+__global__ void __launch_bounds__(kToppThreads) topp_kernel(
+    const float *__restrict__ imp, const int32_t *__restrict__ blk_cu, const int32_t *__restrict__ cu, int32_t B,
+    double p, uint32_t flags, uint8_t *__restrict__ keep, int32_t *__restrict__ kept_off,
+    int32_t *__restrict__ seg_kept, int32_t cap, uint32_t *__restrict__ status) {
+  extern __shared__ unsigned long long skeys[];  // cap rank keys, then cap keep flags
+  uint8_t *skeep = reinterpret_cast<uint8_t *>(skeys + cap);
+  __shared__ unsigned long long sh64[32];
+  __shared__ int32_t sh32[32];
+  __shared__ uint32_t s_bad;
+  const int tid = threadIdx.x;
+  // A gather launched as a programmatic dependent may start now; it waits for this grid's results.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // This grid may itself run as a programmatic dependent of the importance kernels: no memory is
+  // touched before their results are visible.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int32_t s = blockIdx.x;
+  const int32_t n = cu[s + 1] - cu[s];
+  const int32_t b0 = blk_cu[s], nb = blk_cu[s + 1] - blk_cu[s];
+
+  if (nb == 0) {  // not scored: every token is kept
+    if (tid == 0) seg_kept[s] = n > 0 ? n : 0;
+    return;
+  }
+  // cap (a power of two) bounds the padded sort of every segment that fits the call's token count
+  if (nb > kMaxBlocks || nb > cap || n <= 0 || nb != (n + B - 1) / B) {
+    if (tid == 0) {
+      atomicOr(status, nb > kMaxBlocks ? UNIP_DEV_TOO_MANY_BLOCKS : UNIP_DEV_BAD_BLOCKS);
+      seg_kept[s] = 0;
+    }
+    return;
+  }
+  if (!select_segment_blocks(imp, b0, nb, p, flags, skeys, skeep, sh64, &s_bad, status)) {
+    if (tid == 0) seg_kept[s] = 0;
+    return;
+  }
   // 4. keep flags out, kept-token offsets in block order
   const int ipb = (nb + kToppThreads - 1) / kToppThreads;
   const int bb0 = tid * ipb;
@@ -456,6 +473,85 @@ __global__ void __launch_bounds__(kIndexThreads) select_gather_kernel(
   }
 }
 
+// One segment in the call (a single long prompt): every CTA selects the segment's blocks itself
+// (a few microseconds of shared-memory work on at most UNIP_TOPP_MAX_BLOCKS scores), stages the
+// kept offsets and copies its share of the kept rows, so no grid waits for another; CTA 0 writes
+// the keep mask, cu_seqlens_kept and n_kept.  Same results as topp_kernel + select_gather_kernel.
+__global__ void __launch_bounds__(kToppThreads) select_gather_onepass_kernel(
+    const float *__restrict__ imp, const int32_t *__restrict__ blk_cu, const int32_t *__restrict__ cu,
+    const int32_t *__restrict__ pos, int32_t B, double p, uint32_t flags, int32_t cap, uint8_t *__restrict__ keep,
+    const uint4 *__restrict__ hidden, int32_t num_rows, int64_t stride16, int32_t vec_per_row,
+    uint4 *__restrict__ out, int64_t out_stride16, int32_t *__restrict__ cu_kept, int32_t *__restrict__ n_kept,
+    int32_t *__restrict__ gather_idx, int32_t *__restrict__ pos_kept, uint32_t *__restrict__ status) {
+  extern __shared__ unsigned long long skeys[];  // cap rank keys, cap kept offsets (int32), cap flags
+  int32_t *skoff = reinterpret_cast<int32_t *>(skeys + cap);
+  uint8_t *skeep = reinterpret_cast<uint8_t *>(skoff + cap);
+  __shared__ unsigned long long sh64[32];
+  __shared__ int32_t sh32[32];
+  __shared__ uint32_t s_bad;
+  const int tid = threadIdx.x, lane = tid & 31;
+  // the importance results are visible past here (this grid is a programmatic dependent of them)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int32_t c0 = cu[0], n = cu[1] - cu[0];
+  const int32_t b0 = blk_cu[0], nb = blk_cu[1] - blk_cu[0];
+  int32_t total = 0;
+  if (nb == 0) {  // not scored: every token is kept
+    total = n > 0 ? n : 0;
+  } else if (nb > kMaxBlocks || nb > cap || n <= 0 || nb != (n + B - 1) / B) {
+    if (blockIdx.x == 0 && tid == 0)
+      atomicOr(status, nb > kMaxBlocks ? UNIP_DEV_TOO_MANY_BLOCKS : UNIP_DEV_BAD_BLOCKS);
+  } else if (select_segment_blocks(imp, b0, nb, p, flags, skeys, skeep, sh64, &s_bad, status)) {
+    // kept-token offsets in block order (exclusive), kept in shared memory
+    const int ipb = (nb + kToppThreads - 1) / kToppThreads;
+    const int bb0 = tid * ipb;
+    int32_t lsum = 0;
+    for (int e = 0; e < ipb; ++e) {
+      const int b = bb0 + e;
+      if (b < nb && skeep[b]) lsum += min(B, n - b * B);
+    }
+    int32_t run = block_excl_scan<int32_t>(lsum, sh32, &total);
+    for (int e = 0; e < ipb; ++e) {
+      const int b = bb0 + e;
+      if (b < nb) {
+        skoff[b] = run;
+        if (blockIdx.x == 0) keep[b0 + b] = skeep[b];
+        if (skeep[b]) run += min(B, n - b * B);
+      }
+    }
+  }
+  if (blockIdx.x == 0 && tid == 0) {
+    cu_kept[0] = 0;
+    cu_kept[1] = total;
+    *n_kept = total;
+  }
+  __syncthreads();
+  const int warps_per_block = kToppThreads / 32;
+  for (int32_t r = blockIdx.x * warps_per_block + (tid >> 5); r < total; r += gridDim.x * warps_per_block) {
+    int32_t src;
+    if (nb == 0) {
+      src = c0 + r;
+    } else {
+      // block: last b with skoff[b] <= r (a dropped block shares its offset with the next kept one)
+      int32_t lo = 0, hi = nb - 1;
+      while (lo < hi) {
+        const int32_t mid = (lo + hi + 1) >> 1;
+        if (skoff[mid] <= r) lo = mid; else hi = mid - 1;
+      }
+      if (!skeep[lo]) continue;
+      src = c0 + lo * B + (r - skoff[lo]);
+    }
+    if (src < 0 || src >= num_rows) {
+      if (lane == 0) atomicOr(status, UNIP_DEV_BAD_INDEX);
+      continue;
+    }
+    if (lane == 0) {
+      gather_idx[r] = src;
+      pos_kept[r] = pos[src];
+    }
+    warp_copy_row(hidden + (int64_t)src * stride16, out + (int64_t)r * out_stride16, vec_per_row, lane);
+  }
+}
+
 // Top-p launch: shared memory for the padded sort of the largest segment the call can hold
 // (a power of two of at least total_tokens / B + 2 blocks, at most UNIP_TOPP_MAX_BLOCKS).
 cudaError_t launch_topp(const float *imp, const int32_t *blk_cu, const int32_t *cu_seqlens, int32_t num_segs,
@@ -589,6 +685,41 @@ UNIP_API int32_t unip_select_gather(const float *imp, const int32_t *blk_cu, con
         cudaMemsetAsync(n_kept, 0, sizeof(int32_t), st) != cudaSuccess)
       return UNIP_ERR_CUDA;
     return UNIP_OK;
+  }
+  if (num_segs == 1) {  // one segment: selection and gather in one grid
+    static bool configured1[64] = {false};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && !configured1[dev]) {
+      if (cudaFuncSetAttribute(select_gather_onepass_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               kMaxBlocks * ((int)sizeof(unsigned long long) + 5)) != cudaSuccess)
+        return UNIP_ERR_CUDA;
+      configured1[dev] = true;
+    }
+    int32_t cap = 16;
+    const int64_t need = (int64_t)total_tokens / block_size + 2;
+    while (cap < need && cap < kMaxBlocks) cap <<= 1;
+    const int sms1 = device_sm_count();
+    const int warps = kToppThreads / 32;
+    int64_t blocks1 = ((int64_t)(total_tokens > 0 ? total_tokens : 1) + warps - 1) / warps;
+    const int64_t max_blocks1 = (int64_t)(sms1 > 0 ? sms1 : 1) * kGatherCtasPerSm;
+    if (blocks1 > max_blocks1) blocks1 = max_blocks1;
+    cudaLaunchConfig_t cfg1 = {};
+    cfg1.gridDim = dim3((unsigned)blocks1);
+    cfg1.blockDim = dim3(kToppThreads);
+    cfg1.dynamicSmemBytes = (size_t)cap * (sizeof(unsigned long long) + 5);
+    cfg1.stream = st;
+    cudaLaunchAttribute attr1[1];
+    attr1[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr1[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg1.attrs = attr1;
+    cfg1.numAttrs = 1;
+    const cudaError_t e1 = cudaLaunchKernelEx(
+        &cfg1, select_gather_onepass_kernel, imp, blk_cu, cu_seqlens, positions, block_size, p, flags, cap, keep,
+        static_cast<const uint4 *>(hidden), total_tokens, rows ? (int64_t)(row_stride / 8) : 0,
+        (int32_t)(d_model / 8), static_cast<uint4 *>(hidden_out), rows ? (int64_t)(out_row_stride / 8) : 0,
+        cu_seqlens_kept, n_kept, gather_idx, positions_kept, status);
+    return e1 == cudaSuccess ? UNIP_OK : UNIP_ERR_CUDA;
   }
   uint8_t *ws = static_cast<uint8_t *>(workspace);
   int32_t *seg_kept = reinterpret_cast<int32_t *>(ws + kWsHeaderBytes);
