@@ -239,8 +239,7 @@ __global__ void __launch_bounds__(kPlanThreads) attn_plan_kernel(const int32_t *
 // ---------------------------------------------------------------------------
 // Attention kernel
 // ---------------------------------------------------------------------------
-constexpr int kStages = 5;        // K/V ring slots (each holds one K or one V tile) with two query tiles
-constexpr int kStagesMax = 6;     // with one query tile the second Q buffer becomes a sixth slot
+constexpr int kStages = 5;        // K/V ring slots (each holds one K or one V tile)
 // 4 softmax warpgroups (8 warps per query tile, 16 rows each) + one control
 // warpgroup (TMA warp, MMA warp, 2 idle warps); 96 registers per thread.
 constexpr int kThreads = 640;
@@ -264,18 +263,18 @@ struct SmemLayout {
 enum BarId {
   kBarQFull = 0,
   kBarSlotFull0 = 1,                      // + slot
-  kBarSlotEmpty0 = 1 + kStagesMax,        // + slot
-  kBarSFull0 = 1 + 2 * kStagesMax,        // + tile: S in TMEM
-  kBarPFull0 = 3 + 2 * kStagesMax,        // + tile: P in TMEM and O rescaled (both column halves)
-  kBarODone0 = 5 + 2 * kStagesMax,        // + tile: last PV done
-  kBarFinal = 7 + 2 * kStagesMax,
-  kBarPVDone = 8 + 2 * kStagesMax,        // one query tile: each PV done (O may be rescaled)
-  kBarQEmpty = 9 + 2 * kStagesMax,        // last QK of a work item done: Q buffers may be reloaded
-  kBarOFree0 = 10 + 2 * kStagesMax,       // + tile: epilogue read O (count 256)
-  kBarSlotGo0 = 12 + 2 * kStagesMax,      // + slot: a prefix fill of the slot may be issued (helpers)
-  kBarUnitFull0 = 12 + 3 * kStagesMax,    // + k: work item i (k = i & 1) published in s_unit[k]
-  kBarUnitEmpty0 = 14 + 3 * kStagesMax,   // + k: every consumer warp has read s_unit[k]
-  kNumBars = 16 + 3 * kStagesMax
+  kBarSlotEmpty0 = 1 + kStages,        // + slot
+  kBarSFull0 = 1 + 2 * kStages,        // + tile: S in TMEM
+  kBarPFull0 = 3 + 2 * kStages,        // + tile: P in TMEM and O rescaled (both column halves)
+  kBarODone0 = 5 + 2 * kStages,        // + tile: last PV done
+  kBarFinal = 7 + 2 * kStages,
+  kBarPVDone = 8 + 2 * kStages,        // one query tile: each PV done (O may be rescaled)
+  kBarQEmpty = 9 + 2 * kStages,        // last QK of a work item done: Q buffers may be reloaded
+  kBarOFree0 = 10 + 2 * kStages,       // + tile: epilogue read O (count 256)
+  kBarSlotGo0 = 12 + 2 * kStages,      // + slot: a prefix fill of the slot may be issued (helpers)
+  kBarUnitFull0 = 12 + 3 * kStages,    // + k: work item i (k = i & 1) published in s_unit[k]
+  kBarUnitEmpty0 = 14 + 3 * kStages,   // + k: every consumer warp has read s_unit[k]
+  kNumBars = 16 + 3 * kStages
 };
 
 __device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
@@ -470,16 +469,19 @@ __device__ __forceinline__ bool softmax_tile_role(const AttnArgs &a, int tile, c
   const bool st0 = R0 < tr.rows_valid, st1 = R1 < tr.rows_valid;
   __nv_bfloat16 *o0 = a.out + ((int64_t)t0 * a.Hq + h0) * D + cq;
   __nv_bfloat16 *o1 = a.out + ((int64_t)t1 * a.Hq + h1) * D + cq;
+  // all of O (D / 32 parts of 16 values) in flight before one wait, then the stores
+  float o[D / 2];  // o[16 part + 4k + {0,1}]: row R0, columns 32 part + 8k + cq + {0,1}; + {2,3}: row R1
+#pragma unroll
+  for (int part = 0; part < D / 32; ++part) tmem_ld_16x256b_x4(tw + o_col + part * 32, o + 16 * part);
+  tmem_wait_ld();
 #pragma unroll
   for (int part = 0; part < D / 32; ++part) {
-    float o[16];  // o[4k + {0,1}]: row R0, columns 32 part + 8k + cq + {0,1}; o[4k + {2,3}]: row R1
-    tmem_ld_16x256b_x4(tw + o_col + part * 32, o);
-    tmem_wait_ld();
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const int col = part * 32 + 8 * k;
-      if (st0) *reinterpret_cast<uint32_t *>(o0 + col) = pack_bf16x2(o[4 * k] * inv0, o[4 * k + 1] * inv0);
-      if (st1) *reinterpret_cast<uint32_t *>(o1 + col) = pack_bf16x2(o[4 * k + 2] * inv1, o[4 * k + 3] * inv1);
+      const float *v = o + 16 * part + 4 * k;
+      if (st0) *reinterpret_cast<uint32_t *>(o0 + col) = pack_bf16x2(v[0] * inv0, v[1] * inv0);
+      if (st1) *reinterpret_cast<uint32_t *>(o1 + col) = pack_bf16x2(v[2] * inv1, v[3] * inv1);
     }
   }
   if ((lane & 3) == 0 && a.lse) {
@@ -514,7 +516,7 @@ __device__ __forceinline__ WorkItem decode_item(const AttnArgs &a, int32_t unit)
   const int32_t n = a.cu[w.s + 1] - w.c0;
   w.P = a.pos[w.c0];
   if (a.lg > 0) {
-    const int32_t subs = a.group >> 1;  // CTAs' worth of items per kv head for one 128-token pair
+    const int32_t subs = a.group >> 1;  // work items per kv head for one 128-token pair
     w.g = hsel / subs;
     const int32_t tpt = kBlockM >> a.lg;
     w.tr0.tok0 = m * kBlockM + (hsel - w.g * subs) * 2 * tpt;
@@ -572,7 +574,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   if (threadIdx.x == 0) {
     mbar_init(bar(kBarQFull), 1);
     mbar_init(bar(kBarQEmpty), 1);
-    for (int i = 0; i < kStagesMax; ++i) {
+    for (int i = 0; i < kStages; ++i) {
       mbar_init(bar(kBarSlotFull0 + i), 1);
       mbar_init(bar(kBarSlotEmpty0 + i), 1);
       mbar_init(bar(kBarSlotGo0 + i), 1);
