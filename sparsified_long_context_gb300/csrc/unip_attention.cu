@@ -104,6 +104,8 @@ __global__ void __launch_bounds__(kPlanThreads) attn_plan_kernel(const int32_t *
   __shared__ int32_t s_base[kPlanThreads + 1];
   __shared__ uint32_t s_err;
   const int tid = threadIdx.x;
+  // the attention grid may be scheduled now: it sets itself up, then waits for this plan
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   for (int b = tid; b < 2 * kHistBins; b += kPlanThreads) (&s_hist[0][0])[b] = 0;
   if (tid == 0) s_err = (cu[0] != 0 || cu[S] != N) ? UNIP_DEV_BAD_SEQLENS : 0u;
   __syncthreads();
@@ -564,8 +566,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int32_t n_units = *a.num_pairs * a.heads_per_pair;
-  if ((int32_t)blockIdx.x >= n_units) return;  // uniform over the CTA
 
   const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
   auto slot_addr = [&](int slot) { return sbase + L::kRing + slot * L::kTileBytes; };
@@ -603,6 +603,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   tc_fence_after();
   const uint32_t tmem = s_tmem;
   volatile int *abort_flag = &s_abort;
+  // This grid runs as a programmatic dependent of its planner: the set-up above overlaps the plan,
+  // which is read only past here.  A CTA that finds no work left claims nothing and tears down.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int32_t n_units = *a.num_pairs * a.heads_per_pair;
 
   // Barrier completions before the current item, replayed identically by every role:
   // S-full / P-full per buffer, PV-done, O-done and O-free uses per tile, items done.
@@ -992,8 +996,17 @@ cudaError_t launch_attention(const AttnArgs &args, int grid, cudaStream_t stream
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
-  attn_fwd_kernel<D><<<grid, kThreads, L::kDynamic, stream>>>(args);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = L::kDynamic;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // may start while the planner runs
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, attn_fwd_kernel<D>, args);
 }
 
 int32_t max_pairs_for(int32_t total_tokens, int32_t num_segs) {
