@@ -213,3 +213,72 @@ def test_fused_select_gather_matches_oracle(name):
     torch.cuda.synchronize()
     assert Bd.unip_get_device_status(clear=True) == 0
     _check_selection(wl, bufs)
+
+
+@pytest.mark.parametrize("L,B_,with_hidden", [(1, 16, True), (300 * 16 - 5, 16, True), (1000 * 16, 16, False),
+                                              (1250 * 16 - 3, 16, True), (777, 64, False)])
+def test_single_segment_one_launch_path(L, B_, with_hidden):
+    """unip_select_gather with one segment (the one-launch path): every sort regime of the selection,
+    with and without hidden rows, bit-exact against the oracle fed the same scores."""
+    from sparsified_long_context_gb300 import binding as Bd
+    rng = np.random.default_rng(L + B_)
+    nb = -(-L // B_)
+    x = rng.random(nb) ** 6
+    x[rng.integers(0, nb, max(1, nb // 10))] = 0.0          # zero-mass blocks
+    x[: nb // 3] = np.round(x[: nb // 3] * 8) / 8 + 1e-3     # many exact ties
+    if x.sum() == 0:
+        x[0] = 1.0
+    imp = (x / x.sum()).astype(np.float32)
+    cu = np.array([0, L], np.int32)
+    bc = np.array([0, nb], np.int32)
+    pos = np.arange(7, 7 + L, dtype=np.int32)                # positions past a 7-token prefix
+    d = 64
+    hid = W.f32_to_bf16_bits(rng.standard_normal((L, d), dtype=np.float32))
+    dev = "cuda"
+    cap = Bd.unip_importance_capacity(L, 1, B_)
+    imp_t = torch.zeros(cap, dtype=torch.float32, device=dev)
+    imp_t[:nb] = torch.from_numpy(imp)
+    for p, flags in [(0.0, 3), (0.5, 1), (0.95, 3), (1.0, 0), (0.9, 2)]:
+        keep = torch.full((cap,), 9, dtype=torch.uint8, device=dev)
+        gi = torch.full((L,), -1, dtype=torch.int32, device=dev)
+        pk = torch.full((L,), -1, dtype=torch.int32, device=dev)
+        ck = torch.empty(2, dtype=torch.int32, device=dev)
+        nk = torch.empty(1, dtype=torch.int32, device=dev)
+        h_t = torch.from_numpy(hid).view(torch.bfloat16).to(dev) if with_hidden else None
+        out = torch.zeros((L, d), dtype=torch.bfloat16, device=dev) if with_hidden else None
+        Bd.unip_get_device_status(clear=True)
+        Bd.unip_select_gather(imp_t, torch.from_numpy(bc).to(dev), torch.from_numpy(cu).to(dev),
+                              torch.from_numpy(pos).to(dev), keep, gi, ck, pk, nk, h_t, out, block_size=B_, p=p,
+                              flags=flags)
+        torch.cuda.synchronize()
+        assert Bd.unip_get_device_status(clear=True) == 0
+        ref = oracle.topp_select(imp, bc, p, flags)
+        assert np.array_equal(keep[:nb].cpu().numpy(), ref), (L, p, flags)
+        rgi, rck, rpk, rm = oracle.index_build(ref, bc, cu, pos, B_)
+        m = int(nk.item())
+        assert m == rm and np.array_equal(ck.cpu().numpy(), rck)
+        assert np.array_equal(gi[:m].cpu().numpy(), rgi) and np.array_equal(pk[:m].cpu().numpy(), rpk)
+        if with_hidden:
+            got = out[:m].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+            assert np.array_equal(got, oracle.gather(hid, rgi))
+
+
+def test_single_unscored_segment_keeps_everything():
+    from sparsified_long_context_gb300 import binding as Bd
+    L, B_ = 333, 64
+    dev = "cuda"
+    cap = Bd.unip_importance_capacity(L, 1, B_)
+    imp_t = torch.zeros(cap, dtype=torch.float32, device=dev)
+    keep = torch.zeros(cap, dtype=torch.uint8, device=dev)
+    gi = torch.full((L,), -1, dtype=torch.int32, device=dev)
+    pk = torch.full((L,), -1, dtype=torch.int32, device=dev)
+    ck = torch.empty(2, dtype=torch.int32, device=dev)
+    nk = torch.empty(1, dtype=torch.int32, device=dev)
+    pos = torch.arange(L, dtype=torch.int32, device=dev)
+    Bd.unip_select_gather(imp_t, torch.tensor([0, 0], dtype=torch.int32, device=dev),
+                          torch.tensor([0, L], dtype=torch.int32, device=dev), pos, keep, gi, ck, pk, nk, None, None,
+                          block_size=B_, p=0.5)
+    torch.cuda.synchronize()
+    assert Bd.unip_get_device_status(clear=True) == 0
+    assert int(nk.item()) == L and ck.cpu().tolist() == [0, L]
+    assert np.array_equal(gi.cpu().numpy(), np.arange(L)) and np.array_equal(pk.cpu().numpy(), np.arange(L))
