@@ -172,28 +172,41 @@ __global__ void __launch_bounds__(kScoreThreadsTc, 1) imp_score_tc_kernel(const 
   const uint32_t tmem = s_tmem;
   volatile int *abort_flag = &s_abort;
   struct It {
-    int32_t g, s, c, gi;
+    int32_t g, s, c, gi, c0, n, bk0, nbs;  // bk0, nbs: the segment's first block and block count
   };
+  // Each role decodes iteration i + 1 while it works on i: the work-list and cu_seqlens reads are a
+  // chain of dependent global loads that would otherwise sit in front of every unit.
   auto decode = [&](int64_t i) {
     It r;
+    if (i >= n_iter) {
+      r.g = r.s = r.c = r.gi = -1;
+      r.c0 = r.n = r.bk0 = r.nbs = 0;
+      return r;
+    }
     const int64_t u = u0 + i / ngroups;
     r.gi = (int32_t)(i % ngroups);
     r.g = (int32_t)(u / n_items);
     const int2 item = a.items[u % n_items];
     r.s = item.x;
     r.c = item.y;
+    r.c0 = a.cu[r.s];
+    r.n = a.cu[r.s + 1] - r.c0;
+    r.bk0 = a.blk_cu[r.s];
+    r.nbs = a.blk_cu[r.s + 1] - r.bk0;
     return r;
   };
   auto same_q = [](const It &x, const It &y) { return x.s == y.s && x.g == y.g && x.gi == y.gi; };
 
   if (warp == kScoreWarpTma) {
     if (lane == 0) {
-      It prev = {-1, -1, -1, -1};
+      It prev = {-1, -1, -1, -1, 0, 0, 0, 0};
       uint32_t qn = 0;
       int64_t issued = 0;
+      It nxt = decode(0);
       for (int64_t i = 0; i < n_iter; ++i) {
-        const It it = decode(i);
-        const int32_t c0 = a.cu[it.s], n = a.cu[it.s + 1] - c0;
+        const It it = nxt;
+        nxt = decode(i + 1);
+        const int32_t c0 = it.c0, n = it.n;
         if (!same_q(it, prev)) {
           if (qn > 0 && !mbar_wait(bar(kSbQEmpty), (qn - 1) & 1, abort_flag, a.status)) break;
           const int32_t W = min(B, n), hn = min(hpg, group - it.gi * hpg);
@@ -232,11 +245,13 @@ __global__ void __launch_bounds__(kScoreThreadsTc, 1) imp_score_tc_kernel(const 
     }
   } else if (warp == kScoreWarpMma) {
     if (lane == 0) {
-      It prev = {-1, -1, -1, -1};
+      It prev = {-1, -1, -1, -1, 0, 0, 0, 0};
       uint32_t qn = 0;
       bool ok = true;
+      It nxt = decode(0);
       for (int64_t i = 0; ok && i < n_iter; ++i) {
-        const It it = decode(i);
+        const It it = nxt;
+        nxt = decode(i + 1);
         if (!same_q(it, prev)) {
           ok = mbar_wait(bar(kSbQFull), qn & 1, abort_flag, a.status);
           ++qn;
@@ -258,7 +273,7 @@ __global__ void __launch_bounds__(kScoreThreadsTc, 1) imp_score_tc_kernel(const 
         }
         umma_commit(bar(kSbSFull0 + slot));
         umma_commit(bar(kSbKEmpty0 + slot));
-        if (i + 1 == n_iter || !same_q(decode(i + 1), it)) umma_commit(bar(kSbQEmpty));  // last MMA on this Q
+        if (i + 1 == n_iter || !same_q(nxt, it)) umma_commit(bar(kSbQEmpty));  // last MMA on this Q
       }
       // Every tcgen05 op of this CTA has landed before TMEM is released.
       umma_commit(bar(kSbFinal));
@@ -274,11 +289,13 @@ __global__ void __launch_bounds__(kScoreThreadsTc, 1) imp_score_tc_kernel(const 
     const uint32_t tl = tmem + (static_cast<uint32_t>(32 * qd) << 16);
     const int32_t bpc = 128 / B;
     bool live = true;
-    It prev = {-1, -1, -1, -1};
+    It prev = {-1, -1, -1, -1, 0, 0, 0, 0};
     float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
+    It nxt = decode(0);
     for (int64_t i = 0; i < n_iter; ++i) {
-      const It it = decode(i);
-      const int32_t c0 = a.cu[it.s], n = a.cu[it.s + 1] - c0;
+      const It it = nxt;
+      nxt = decode(i + 1);
+      const int32_t c0 = it.c0, n = it.n;
       const int32_t W = min(B, n), wrow0 = n - W;
       const int32_t hn = min(hpg, group - it.gi * hpg), ncols = hn * B;
       if (!same_q(it, prev)) {
@@ -332,8 +349,8 @@ __global__ void __launch_bounds__(kScoreThreadsTc, 1) imp_score_tc_kernel(const 
       asm volatile("bar.sync 1, 256;" ::: "memory");
       if (ch == 0) {
         v += s_key[key];
-        const int32_t nb_seg = a.blk_cu[it.s + 1] - a.blk_cu[it.s];
-        const int64_t pbase = (int64_t)a.blk_cu[it.s] + it.c * bpc;
+        const int32_t nb_seg = it.nbs;
+        const int64_t pbase = (int64_t)it.bk0 + it.c * bpc;
         if (B <= 32) {
           for (int off = B / 2; off >= 1; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
           if ((key & (B - 1)) == 0) {
