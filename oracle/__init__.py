@@ -61,8 +61,10 @@ def _load():
             lib.oracle_topp_select.argtypes = [P, P, i32, f64, u32, P]
             lib.oracle_index_build.argtypes = [P, P, P, P, i32, i32, P, P, P, P]
             lib.oracle_gather.argtypes = [P, i64, i32, P, i32, i32, P]
+            lib.oracle_attention_compacted.argtypes = [P, P, P, P, i32, P, P, i32, P, P, i32, i32, P, i32,
+                                                       i32, i32, i32, f64, P, i32, P, P, i32]
             for f in (lib.oracle_attention, lib.oracle_block_importance, lib.oracle_topp_select,
-                      lib.oracle_index_build, lib.oracle_gather):
+                      lib.oracle_index_build, lib.oracle_gather, lib.oracle_attention_compacted):
                 f.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -94,12 +96,17 @@ def _check(rc, what):
 
 def attention(q, k, v, cu_seqlens, positions, num_heads_q, num_heads_kv, head_dim,
               k_cache=None, v_cache=None, block_table=None, page_size=16, scale=None,
-              rows=None, nthreads=None):
+              rows=None, nthreads=None, prefix_lens=None):
     """Causal packed / chunked attention in fp64.
 
     q [N,Hq,D], k/v [N,Hkv,D] (uint16 bf16 bits); k_cache/v_cache
     [num_pages,page,Hkv,D]; block_table [S,max_pages].  Returns (out, lse):
     out float64 [R,Hq,D], lse float64 [R,Hq] with R = len(rows) or N.
+
+    prefix_lens (int32 [S]): a compacted stream (kept tokens after selection):
+    positions only increase inside a segment, a token sees its segment's tokens
+    at or before its position, and segment s's cached prefix holds prefix_lens[s]
+    tokens.  Without it positions are contiguous and the prefix is the first one.
     """
     lib = _load()
     q, k, v = _c(q, np.uint16), _c(k, np.uint16), _c(v, np.uint16)
@@ -113,11 +120,19 @@ def attention(q, k, v, cu_seqlens, positions, num_heads_q, num_heads_kv, head_di
     r = n if rows_a is None else len(rows_a)
     out = np.zeros((r, num_heads_q, head_dim), np.float64)
     lse = np.zeros((r, num_heads_q), np.float64)
-    rc = lib.oracle_attention(_ptr(q), _ptr(k), _ptr(v), _ptr(cu), len(cu) - 1, _ptr(pos), n,
-                              _ptr(kc), _ptr(vc), num_pages, page_size, _ptr(bt), max_pages,
-                              num_heads_q, num_heads_kv, head_dim, float(scale or 0.0),
-                              _ptr(rows_a), r, _ptr(out), _ptr(lse),
-                              int(nthreads or default_threads()))
+    if prefix_lens is None:
+        rc = lib.oracle_attention(_ptr(q), _ptr(k), _ptr(v), _ptr(cu), len(cu) - 1, _ptr(pos), n,
+                                  _ptr(kc), _ptr(vc), num_pages, page_size, _ptr(bt), max_pages,
+                                  num_heads_q, num_heads_kv, head_dim, float(scale or 0.0),
+                                  _ptr(rows_a), r, _ptr(out), _ptr(lse),
+                                  int(nthreads or default_threads()))
+    else:
+        pl = _c(prefix_lens, np.int32)
+        rc = lib.oracle_attention_compacted(_ptr(q), _ptr(k), _ptr(v), _ptr(cu), len(cu) - 1, _ptr(pos),
+                                            _ptr(pl), n, _ptr(kc), _ptr(vc), num_pages, page_size, _ptr(bt),
+                                            max_pages, num_heads_q, num_heads_kv, head_dim, float(scale or 0.0),
+                                            _ptr(rows_a), r, _ptr(out), _ptr(lse),
+                                            int(nthreads or default_threads()))
     _check(rc, "attention")
     return out, lse
 

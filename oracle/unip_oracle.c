@@ -82,6 +82,7 @@ static int check_segments(const int32_t *cu, int32_t S, const int32_t *pos, int3
 typedef struct {
   const uint16_t *q, *k, *v, *kc, *vc;
   const int32_t *cu, *pos, *bt, *rows;
+  const int32_t *plen; /* compacted stream: explicit prefix length per segment (else NULL) */
   int32_t S, N, num_pages, page_size, max_pages, Hq, Hkv, D, n_rows;
   double scale;
   double *out, *lse;
@@ -227,6 +228,115 @@ int oracle_attention(const uint16_t *q, const uint16_t *k, const uint16_t *v,
   J.out = out; J.lse = lse; J.next = 0; J.total = (int64_t)n_rows * Hq;
   pthread_mutex_init(&J.lock, NULL);
   int rc = run_threads(attn_worker, &J, nthreads);
+  pthread_mutex_destroy(&J.lock);
+  return rc ? rc : J.err;
+}
+
+/*
+ * Attention over a compacted stream (the UniPrefill review, section 3: the
+ * tokens dropped by the selection leave every later sub-layer).  Segment s
+ * holds its kept tokens cu[s] .. cu[s+1]-1 with their original positions,
+ * increasing but possibly with gaps; its cached prefix (pages of block_table
+ * row s) holds plen[s] tokens, which need not equal the first position (a
+ * later layer's cache holds kept tokens only).  Token t with query head h
+ * attends to the whole prefix and to the segment's own tokens u whose
+ * position is at most t's (pos[u] <= pos[t]); the rest as oracle_attention.
+ */
+static void *attn_compacted_worker(void *arg) {
+  attn_job_t *J = (attn_job_t *)arg;
+  double *sc = NULL, *acc = NULL;
+  int32_t *vis = NULL;
+  int64_t cap = 0;
+  acc = (double *)malloc(sizeof(double) * (size_t)J->D);
+  vis = (int32_t *)malloc(sizeof(int32_t) * (size_t)(J->N > 0 ? J->N : 1));
+  if (!acc || !vis) { J->err = ORC_ENOMEM; free(acc); free(vis); return NULL; }
+  for (;;) {
+    int64_t w = take_work(&J->next, &J->lock, J->total);
+    if (w < 0) break;
+    int32_t r = (int32_t)(w / J->Hq), h = (int32_t)(w % J->Hq);
+    int32_t t = J->rows ? J->rows[r] : r;
+    int32_t s = segment_of(J->cu, J->S, t);
+    int32_t c0 = J->cu[s], n = J->cu[s + 1] - c0;
+    int32_t P = J->plen[s];
+    int32_t g = h / (J->Hq / J->Hkv);
+    int32_t n_own = 0; /* own tokens at or before t's position */
+    for (int32_t u = 0; u < n; u++)
+      if (J->pos[c0 + u] <= J->pos[t]) vis[n_own++] = u;
+    int64_t nk = (int64_t)P + n_own;
+    if (nk > cap) {
+      free(sc);
+      cap = nk;
+      sc = (double *)malloc(sizeof(double) * (size_t)cap);
+      if (!sc) { J->err = ORC_ENOMEM; free(acc); free(vis); return NULL; }
+    }
+    const uint16_t *qr = J->q + ((int64_t)t * J->Hq + h) * J->D;
+    double m = -INFINITY;
+    for (int64_t kk = 0; kk < nk; kk++) {
+      const uint16_t *kr = kv_row(J, 0, s, P, g, kk < P ? kk : (int64_t)P + vis[kk - P]);
+      double dot = 0.0;
+      for (int32_t d = 0; d < J->D; d++) dot += bf16_to_f64(qr[d]) * bf16_to_f64(kr[d]);
+      sc[kk] = dot * J->scale;
+      if (sc[kk] > m) m = sc[kk];
+    }
+    double denom = 0.0;
+    for (int32_t d = 0; d < J->D; d++) acc[d] = 0.0;
+    for (int64_t kk = 0; kk < nk; kk++) {
+      double e = exp(sc[kk] - m);
+      denom += e;
+      const uint16_t *vr = kv_row(J, 1, s, P, g, kk < P ? kk : (int64_t)P + vis[kk - P]);
+      for (int32_t d = 0; d < J->D; d++) acc[d] += e * bf16_to_f64(vr[d]);
+    }
+    double *o = J->out + ((int64_t)r * J->Hq + h) * J->D;
+    for (int32_t d = 0; d < J->D; d++) o[d] = acc[d] / denom;
+    if (J->lse) J->lse[(int64_t)r * J->Hq + h] = m + log(denom);
+  }
+  free(sc);
+  free(acc);
+  free(vis);
+  return NULL;
+}
+
+int oracle_attention_compacted(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                               const int32_t *cu_seqlens, int32_t num_segs,
+                               const int32_t *positions, const int32_t *prefix_lens, int32_t total_tokens,
+                               const uint16_t *k_cache, const uint16_t *v_cache,
+                               int32_t num_pages, int32_t page_size,
+                               const int32_t *block_table, int32_t max_pages,
+                               int32_t Hq, int32_t Hkv, int32_t D, double scale,
+                               const int32_t *rows, int32_t n_rows,
+                               double *out, double *lse, int32_t nthreads) {
+  if (Hq <= 0 || Hkv <= 0 || D <= 0 || Hq % Hkv != 0 || !prefix_lens) return ORC_EINVAL;
+  if (num_segs < 0 || total_tokens < 0 || cu_seqlens[0] != 0 || cu_seqlens[num_segs] != total_tokens)
+    return ORC_EINVAL;
+  if (!rows && n_rows != total_tokens) return ORC_EINVAL;
+  for (int32_t s = 0; s < num_segs; s++) {
+    int32_t a = cu_seqlens[s], b = cu_seqlens[s + 1];
+    if (b < a || prefix_lens[s] < 0) return ORC_EINVAL;
+    for (int32_t t = a; t < b; t++) /* positions increase inside a segment */
+      if (positions[t] < 0 || (t > a && positions[t] <= positions[t - 1])) return ORC_EINVAL;
+    int32_t P = prefix_lens[s];
+    if (P == 0 || a == b) continue;
+    if (!k_cache || !v_cache || !block_table || page_size <= 0) return ORC_EINVAL;
+    int32_t need = (P + page_size - 1) / page_size;
+    if (need > max_pages) return ORC_EINVAL;
+    for (int32_t p = 0; p < need; p++) {
+      int32_t pg = block_table[(int64_t)s * max_pages + p];
+      if (pg < 0 || pg >= num_pages) return ORC_EINVAL;
+    }
+  }
+  if (rows)
+    for (int32_t r = 0; r < n_rows; r++)
+      if (rows[r] < 0 || rows[r] >= total_tokens) return ORC_EINVAL;
+  attn_job_t J;
+  memset(&J, 0, sizeof J);
+  J.q = q; J.k = k; J.v = v; J.kc = k_cache; J.vc = v_cache;
+  J.cu = cu_seqlens; J.pos = positions; J.plen = prefix_lens; J.bt = block_table; J.rows = rows;
+  J.S = num_segs; J.N = total_tokens; J.num_pages = num_pages; J.page_size = page_size;
+  J.max_pages = max_pages; J.Hq = Hq; J.Hkv = Hkv; J.D = D; J.n_rows = n_rows;
+  J.scale = scale > 0.0 ? scale : 1.0 / sqrt((double)D);
+  J.out = out; J.lse = lse; J.next = 0; J.total = (int64_t)n_rows * Hq;
+  pthread_mutex_init(&J.lock, NULL);
+  int rc = run_threads(attn_compacted_worker, &J, nthreads);
   pthread_mutex_destroy(&J.lock);
   return rc ? rc : J.err;
 }

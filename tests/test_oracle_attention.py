@@ -185,3 +185,84 @@ def test_rejects_non_contiguous_positions_and_missing_pages():
     pos[:37] += 16  # first segment now claims a 16-token prefix but no pages are given
     with pytest.raises(oracle.OracleError):
         oracle.attention(wl.q, wl.k, wl.v, wl.cu_seqlens, pos, 4, 2, 64)
+
+
+def test_compacted_reduces_to_packed_when_nothing_was_dropped():
+    """With every token kept, contiguous positions and the first position as prefix length, the
+    compacted-stream oracle is the packed / chunked one, bit for bit."""
+    wl = W.tiny_packed()
+    pl = wl.positions[wl.cu_seqlens[:-1]]
+    a = oracle.attention(wl.q, wl.k, wl.v, wl.cu_seqlens, wl.positions, 4, 2, 64)
+    b = oracle.attention(wl.q, wl.k, wl.v, wl.cu_seqlens, wl.positions, 4, 2, 64, prefix_lens=pl)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+    rng = np.random.default_rng(31)
+    P, n, hq, hkv, d = 70, 45, 4, 2, 32
+    k_all, v_all = _rand_bits(rng, (P + n, hkv, d)), _rand_bits(rng, (P + n, hkv, d))
+    q = _rand_bits(rng, (n, hq, d))
+    kc, vc, perm = _paged(k_all[:P], v_all[:P], 16, rng)
+    kw = dict(k_cache=kc, v_cache=vc, block_table=perm[None], page_size=16)
+    pos = np.arange(P, P + n, dtype=np.int32)
+    a = oracle.attention(q, k_all[P:], v_all[P:], np.array([0, n], np.int32), pos, hq, hkv, d, **kw)
+    b = oracle.attention(q, k_all[P:], v_all[P:], np.array([0, n], np.int32), pos, hq, hkv, d,
+                         prefix_lens=np.array([P], np.int32), **kw)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def test_compacted_matches_sdpa_with_position_mask():
+    """Kept tokens with gaps in their positions behind a cached prefix of a different length: torch SDPA
+    over [prefix keys, own keys] with the mask 'prefix: always; own key u: pos[u] <= pos[t]'."""
+    rng = np.random.default_rng(32)
+    hq, hkv, d, page = 4, 2, 32, 16
+    lengths, prefixes = [23, 1, 40], [37, 5, 0]
+    segs_q, segs_k, segs_v, pos, pages = [], [], [], [], []
+    kc_all, vc_all, bt_rows = [], [], []
+    n_pages_total = 0
+    for L, P in zip(lengths, prefixes):
+        segs_q.append(_rand_bits(rng, (L, hq, d)))
+        segs_k.append(_rand_bits(rng, (L, hkv, d)))
+        segs_v.append(_rand_bits(rng, (L, hkv, d)))
+        gaps = rng.integers(1, 4, L)                         # strictly increasing, with gaps
+        pos.append((P + 3 + np.cumsum(gaps)).astype(np.int32))
+        pk, pv = _rand_bits(rng, (P, hkv, d)), _rand_bits(rng, (P, hkv, d))
+        npg = max(1, -(-P // page))
+        kcs = np.zeros((npg, page, hkv, d), np.uint16)
+        vcs = np.zeros_like(kcs)
+        for p_ in range(npg):
+            a_, b_ = p_ * page, min(P, (p_ + 1) * page)
+            kcs[p_, : b_ - a_], vcs[p_, : b_ - a_] = pk[a_:b_], pv[a_:b_]
+        kc_all.append(kcs)
+        vc_all.append(vcs)
+        bt_rows.append(np.arange(n_pages_total, n_pages_total + npg))
+        pages.append((pk, pv))
+        n_pages_total += npg
+    max_p = max(len(r) for r in bt_rows)
+    bt = np.full((len(lengths), max_p), -1, np.int32)
+    for s_, r in enumerate(bt_rows):
+        bt[s_, : len(r)] = r
+    q, k, v = np.concatenate(segs_q), np.concatenate(segs_k), np.concatenate(segs_v)
+    cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+    positions = np.concatenate(pos)
+    out, lse = oracle.attention(q, k, v, cu, positions, hq, hkv, d, k_cache=np.concatenate(kc_all),
+                                v_cache=np.concatenate(vc_all), block_table=bt, page_size=page,
+                                prefix_lens=np.array(prefixes, np.int32))
+    grp = hq // hkv
+    for s_, (L, P) in enumerate(zip(lengths, prefixes)):
+        pk, pv = pages[s_]
+        K = np.concatenate([pk, segs_k[s_]])                 # [P + L, hkv, d]
+        V = np.concatenate([pv, segs_v[s_]])
+        mask = np.ones((L, P + L), bool)
+        mask[:, P:] = pos[s_][None, :] <= pos[s_][:, None]
+        qt = torch.from_numpy(_f64(segs_q[s_])).permute(1, 0, 2)[None]
+        kt = torch.from_numpy(_f64(K)).permute(1, 0, 2)[None].repeat_interleave(grp, dim=1)
+        vt = torch.from_numpy(_f64(V)).permute(1, 0, 2)[None].repeat_interleave(grp, dim=1)
+        ref = F.scaled_dot_product_attention(qt, kt, vt, attn_mask=torch.from_numpy(mask))[0].permute(1, 0, 2)
+        assert np.max(np.abs(out[cu[s_]:cu[s_ + 1]] - ref.numpy())) < 1e-12
+
+
+def test_compacted_rejects_non_increasing_positions():
+    rng = np.random.default_rng(33)
+    q, k, v = _rand_bits(rng, (6, 2, 16)), _rand_bits(rng, (6, 1, 16)), _rand_bits(rng, (6, 1, 16))
+    cu = np.array([0, 6], np.int32)
+    with pytest.raises(oracle.OracleError):
+        oracle.attention(q, k, v, cu, np.array([0, 2, 2, 5, 6, 9], np.int32), 2, 1, 16,
+                         prefix_lens=np.array([0], np.int32))
