@@ -146,6 +146,29 @@ UNIP_API int32_t unip_prefill_attention(const void *q, const void *k, const void
                                         void *stream);
 
 /* ---------------------------------------------------------------------------
+ * Attention over a compacted stream ([UP] section 3: the tokens a selection
+ * dropped leave every later sub-layer): the kept tokens of each segment
+ * (cu_seqlens_kept of unip_topp_select / unip_select_gather) with their
+ * original positions, which increase inside a segment but may have gaps.
+ * Token t of segment s attends to the prefix_lens[s] cached keys of its
+ * segment (block_table row s; a later layer's cache holds kept tokens only,
+ * so the prefix length is given, not derived from a position) and to its
+ * segment's own tokens u with positions[u] <= positions[t]; nothing of other
+ * segments.  prefix_lens: device int32 [num_segs], >= 0 (a bad value raises
+ * UNIP_DEV_BAD_POSITIONS; non-increasing positions too).  Everything else,
+ * including the workspace, as unip_prefill_attention.
+ * ------------------------------------------------------------------------- */
+UNIP_API int32_t unip_compacted_attention(const void *q, const void *k, const void *v,
+                                          const int32_t *cu_seqlens, int32_t num_segs,
+                                          const int32_t *positions, const int32_t *prefix_lens,
+                                          int32_t total_tokens,
+                                          const unip_paged_kv *paged,
+                                          const unip_attn_params *prm,
+                                          void *out, float *lse,
+                                          void *workspace, size_t workspace_bytes,
+                                          void *stream);
+
+/* ---------------------------------------------------------------------------
  * Attention without caller-provided workspace.  The paper has no counterpart:
  * this is a library convenience.  It computes exactly what
  * unip_prefill_attention computes, but its scratch (the tile plan) lives in a

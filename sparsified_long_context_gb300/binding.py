@@ -74,6 +74,9 @@ def load(build_if_missing: bool = True):
         lib.unip_attention_workspace_size.argtypes = [i32, i32, pp]
         lib.unip_prefill_attention.restype = i32
         lib.unip_prefill_attention.argtypes = [P, P, P, P, i32, P, i32, ctypes.POINTER(_PagedKV), pp, P, P, P, sz, P]
+        lib.unip_compacted_attention.restype = i32
+        lib.unip_compacted_attention.argtypes = [P, P, P, P, i32, P, P, i32, ctypes.POINTER(_PagedKV), pp, P, P, P,
+                                                 sz, P]
         lib.unip_prefill_attention_noalloc.restype = i32
         lib.unip_prefill_attention_noalloc.argtypes = [P, P, P, P, i32, P, i32, ctypes.POINTER(_PagedKV), pp, P, P,
                                                        P]
@@ -168,6 +171,30 @@ def unip_prefill_attention(q, k, v, cu_seqlens, positions, out, lse=None, *, num
                                     ctypes.byref(prm), _ptr(out), _ptr(lse), _ptr(workspace),
                                     workspace.numel(), _stream(stream))
     _check(rc, "unip_prefill_attention")
+    return out, lse
+
+
+def unip_compacted_attention(q, k, v, cu_seqlens, positions, prefix_lens, out, lse=None, *, num_heads_q,
+                             num_heads_kv, head_dim, k_cache=None, v_cache=None, block_table=None, page_size=16,
+                             scale=None, workspace=None, stream=None):
+    """Attention over a compacted stream: kept tokens with their (increasing) original positions and an
+    explicit cached-prefix length per segment (prefix_lens, int32 [S] on the device)."""
+    lib = load()
+    n = int(q.shape[0])
+    S = int(cu_seqlens.shape[0]) - 1
+    prm = _params(num_heads_q, num_heads_kv, head_dim, scale)
+    need = lib.unip_attention_workspace_size(n, S, ctypes.byref(prm))
+    if workspace is None:
+        workspace = _workspace(need, q.device)
+    paged_p = None
+    if k_cache is not None:
+        paged = _PagedKV(_ptr(k_cache), _ptr(v_cache), int(k_cache.shape[0]), int(page_size), _ptr(block_table),
+                         int(block_table.shape[1]))
+        paged_p = ctypes.byref(paged)
+    rc = lib.unip_compacted_attention(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), S, _ptr(positions),
+                                      _ptr(prefix_lens), n, paged_p, ctypes.byref(prm), _ptr(out), _ptr(lse),
+                                      _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(rc, "unip_compacted_attention")
     return out, lse
 
 

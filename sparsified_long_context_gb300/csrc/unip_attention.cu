@@ -70,6 +70,7 @@ struct AttnArgs {
   CUtensorMap tm_q, tm_qp, tm_k, tm_v, tm_kc, tm_vc;
   const int32_t *cu;
   const int32_t *pos;
+  const int32_t *prefix_lens;  // compacted stream: cached prefix length per segment (else the first position)
   const int32_t *block_table;
   const int2 *pairs;
   const int32_t *num_pairs;
@@ -92,7 +93,8 @@ struct TileRows {
 // Planner
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kPlanThreads) attn_plan_kernel(const int32_t *__restrict__ cu,
-                                                                 const int32_t *__restrict__ pos, int32_t S,
+                                                                 const int32_t *__restrict__ pos,
+                                                                 const int32_t *__restrict__ prefix_lens, int32_t S,
                                                                  int32_t N, int32_t has_cache, int32_t page_size,
                                                                  int32_t max_pages, int32_t lg,
                                                                  int32_t *__restrict__ header,
@@ -132,8 +134,8 @@ __global__ void __launch_bounds__(kPlanThreads) attn_plan_kernel(const int32_t *
   for (int s = s0; s < s1; ++s) {
     const int32_t n = cu[s + 1] - cu[s];
     if (n == 0) continue;
-    const int32_t P = pos[cu[s]];
-    if (P < 0) err |= UNIP_DEV_BAD_POSITIONS;
+    const int32_t P = prefix_lens ? prefix_lens[s] : pos[cu[s]];
+    if (P < 0 || pos[cu[s]] < 0) err |= UNIP_DEV_BAD_POSITIONS;
     if (P > 0 && (!has_cache || (P + page_size - 1) / page_size > max_pages)) err |= UNIP_DEV_BAD_PAGES;
     my_pairs += (n + kBlockM - 1) / kBlockM;
   }
@@ -145,7 +147,8 @@ __global__ void __launch_bounds__(kPlanThreads) attn_plan_kernel(const int32_t *
     for (int t = tid; t < N; t += kPlanThreads) {
       if (t == 0) continue;
       const int32_t prev = pos[t - 1], cur = pos[t];
-      if (cur != prev + 1) {
+      // contiguous positions, or (compacted stream) increasing ones
+      if (prefix_lens ? cur <= prev : cur != prev + 1) {
         // allowed only at a segment start (some s with cu[s] == t)
         s_cur = find_segment(cu, S, t);
         if (cu[s_cur] != t) err |= UNIP_DEV_BAD_POSITIONS;
@@ -184,7 +187,7 @@ __global__ void __launch_bounds__(kPlanThreads) attn_plan_kernel(const int32_t *
       if (rem < nt) {
         seg = sg;
         m = rem;
-        const int32_t P = pos[cu[sg]];
+        const int32_t P = prefix_lens ? prefix_lens[sg] : pos[cu[sg]];
         cost = (P + kBlockN - 1) / kBlockN + rem + 1;
         const int32_t tok = len - rem * kBlockM;
         light = (P > 0 && tok < (kBlockM >> lg)) ? 1 : 0;
@@ -516,7 +519,7 @@ __device__ __forceinline__ WorkItem decode_item(const AttnArgs &a, int32_t unit)
   const int32_t m = pr.y;
   w.c0 = a.cu[w.s];
   const int32_t n = a.cu[w.s + 1] - w.c0;
-  w.P = a.pos[w.c0];
+  w.P = a.prefix_lens ? a.prefix_lens[w.s] : a.pos[w.c0];
   if (a.lg > 0) {
     const int32_t subs = a.group >> 1;  // work items per kv head for one 128-token pair
     w.g = hsel / subs;
@@ -1026,10 +1029,12 @@ UNIP_API size_t unip_attention_workspace_size(int32_t total_tokens, int32_t num_
   return kWsHeaderBytes + align_up(sizeof(int2) * (size_t)max_pairs_for(total_tokens, num_segs), 256);
 }
 
-UNIP_API int32_t unip_prefill_attention(const void *q, const void *k, const void *v, const int32_t *cu_seqlens,
-                                        int32_t num_segs, const int32_t *positions, int32_t total_tokens,
-                                        const unip_paged_kv *paged, const unip_attn_params *prm, void *out,
-                                        float *lse, void *workspace, size_t workspace_bytes, void *stream) {
+// Both entry points: prefix_lens == NULL takes each segment's prefix length from its first position
+// (contiguous positions); otherwise the stream is compacted (increasing positions, explicit prefixes).
+static int32_t attention_entry(const void *q, const void *k, const void *v, const int32_t *cu_seqlens,
+                               int32_t num_segs, const int32_t *positions, const int32_t *prefix_lens,
+                               int32_t total_tokens, const unip_paged_kv *paged, const unip_attn_params *prm,
+                               void *out, float *lse, void *workspace, size_t workspace_bytes, void *stream) {
   if (!prm || !cu_seqlens || num_segs < 0 || total_tokens < 0) return UNIP_ERR_INVALID_ARGUMENT;
   const int32_t Hq = prm->num_heads_q, Hkv = prm->num_heads_kv, D = prm->head_dim;
   if (Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0) return UNIP_ERR_INVALID_ARGUMENT;
@@ -1093,7 +1098,8 @@ UNIP_API int32_t unip_prefill_attention(const void *q, const void *k, const void
   int32_t *header = static_cast<int32_t *>(workspace);
   int2 *pairs = reinterpret_cast<int2 *>(static_cast<uint8_t *>(workspace) + kWsHeaderBytes);
   const int32_t max_pairs = max_pairs_for(total_tokens, num_segs);
-  attn_plan_kernel<<<1, kPlanThreads, 0, st>>>(cu_seqlens, positions, num_segs, total_tokens, has_cache ? 1 : 0,
+  attn_plan_kernel<<<1, kPlanThreads, 0, st>>>(cu_seqlens, positions, prefix_lens, num_segs, total_tokens,
+                                               has_cache ? 1 : 0,
                                                has_cache ? paged->page_size : 16,
                                                has_cache ? paged->max_pages_per_seq : 0, lg, header, pairs,
                                                max_pairs, status);
@@ -1101,6 +1107,7 @@ UNIP_API int32_t unip_prefill_attention(const void *q, const void *k, const void
 
   args.cu = cu_seqlens;
   args.pos = positions;
+  args.prefix_lens = prefix_lens;
   args.block_table = has_cache ? paged->block_table : nullptr;
   args.pairs = pairs;
   args.num_pairs = header;
@@ -1126,6 +1133,24 @@ UNIP_API int32_t unip_prefill_attention(const void *q, const void *k, const void
   const int64_t grid = std::min<int64_t>(units_bound, sms > 0 ? sms : 1);
   const cudaError_t e = D == 128 ? launch_attention<128>(args, (int)grid, st) : launch_attention<64>(args, (int)grid, st);
   return e == cudaSuccess ? UNIP_OK : UNIP_ERR_CUDA;
+}
+
+UNIP_API int32_t unip_prefill_attention(const void *q, const void *k, const void *v, const int32_t *cu_seqlens,
+                                        int32_t num_segs, const int32_t *positions, int32_t total_tokens,
+                                        const unip_paged_kv *paged, const unip_attn_params *prm, void *out,
+                                        float *lse, void *workspace, size_t workspace_bytes, void *stream) {
+  return attention_entry(q, k, v, cu_seqlens, num_segs, positions, nullptr, total_tokens, paged, prm, out, lse,
+                         workspace, workspace_bytes, stream);
+}
+
+UNIP_API int32_t unip_compacted_attention(const void *q, const void *k, const void *v, const int32_t *cu_seqlens,
+                                          int32_t num_segs, const int32_t *positions, const int32_t *prefix_lens,
+                                          int32_t total_tokens, const unip_paged_kv *paged,
+                                          const unip_attn_params *prm, void *out, float *lse, void *workspace,
+                                          size_t workspace_bytes, void *stream) {
+  if (num_segs > 0 && !prefix_lens) return UNIP_ERR_INVALID_ARGUMENT;
+  return attention_entry(q, k, v, cu_seqlens, num_segs, positions, prefix_lens, total_tokens, paged, prm, out,
+                         lse, workspace, workspace_bytes, stream);
 }
 
 }  // extern "C"

@@ -158,3 +158,67 @@ def test_mixed_step_sampled():
     dec = rows[rows < 256][:8]
     rows = np.concatenate([dec, rows[rows >= 256]]).astype(np.int32)
     _check(wl, rows)
+
+
+def _compact(wl, B, rng, drop=0.5):
+    """Drop random B-token blocks of every segment (first and last kept), as a selection would; returns
+    the kept stream (q, k, v rows, cu_seqlens_kept, original positions) and each segment's prefix length."""
+    cu = wl.cu_seqlens
+    keep_rows, lens = [], []
+    for s in range(wl.num_segs):
+        a, b = int(cu[s]), int(cu[s + 1])
+        n = b - a
+        nb = -(-n // B) if n else 0
+        kb = rng.random(nb) >= drop
+        if nb:
+            kb[0] = kb[-1] = True
+        rows = [a + i for i in range(n) if kb[i // B]]
+        keep_rows += rows
+        lens.append(len(rows))
+    rows = np.array(keep_rows, np.int64)
+    cu_k = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    return (wl.q[rows], wl.k[rows], wl.v[rows], cu_k, wl.positions[rows].astype(np.int32),
+            wl.prefix_lens.astype(np.int32))
+
+
+def _check_compacted(wl, B, seed, drop=0.5):
+    from sparsified_long_context_gb300 import binding as Bd
+    rng = np.random.default_rng(seed)
+    q, k, v, cu_k, pos_k, plen = _compact(wl, B, rng, drop)
+    hq, hkv, d = wl.num_heads_q, wl.num_heads_kv, wl.head_dim
+    kw_o, kw_g = {}, {}
+    if wl.cache is not None:
+        kc, vc = wl.cache.pages_numpy(np.arange(wl.cache.num_pages))
+        kw_o = dict(k_cache=kc, v_cache=vc, block_table=wl.block_table, page_size=wl.cache.page_size)
+        kct, vct = wl.cache.to_torch("cuda")
+        kw_g = dict(k_cache=kct, v_cache=vct, block_table=torch.from_numpy(wl.block_table).cuda(),
+                    page_size=wl.cache.page_size)
+    n = int(cu_k[-1])
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    out = torch.empty((n, hq, d), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((hq, n), dtype=torch.float32, device="cuda")
+    Bd.unip_get_device_status(clear=True)
+    Bd.unip_compacted_attention(dev(q).view(torch.bfloat16), dev(k).view(torch.bfloat16), dev(v).view(torch.bfloat16),
+                                dev(cu_k), dev(pos_k), dev(plen), out, lse, num_heads_q=hq, num_heads_kv=hkv,
+                                head_dim=d, **kw_g)
+    torch.cuda.synchronize()
+    st = Bd.unip_get_device_status(clear=True)
+    assert st == 0, Bd.describe_status(st)
+    ref_o, ref_l = oracle.attention(q, k, v, cu_k, pos_k, hq, hkv, d, prefix_lens=plen, **kw_o)
+    assert_close(bf16_tensor_to_f64(out), ref_o, what="compacted out")
+    assert_close(lse.cpu().numpy().astype(np.float64).T, ref_l, max_abs=LSE_ABS, mean_abs=LSE_ABS,
+                 what="compacted lse")
+
+
+@pytest.mark.parametrize("lengths,hq,hkv,d,B", [([300, 37, 700, 129], 8, 2, 128, 16), ([1000, 5, 64], 32, 8, 128, 64),
+                                                ([513, 77], 4, 4, 64, 32)])
+def test_compacted_stream_packed(lengths, hq, hkv, d, B):
+    """Attention of a later layer over the kept tokens (original positions with gaps), no cached prefix."""
+    _check_compacted(W.packed(lengths, hq, hkv, d, seed=sum(lengths)), B, seed=len(lengths) + B)
+
+
+@pytest.mark.parametrize("hq,hkv,d,page", [(32, 8, 128, 16), (8, 2, 64, 64)])
+def test_compacted_stream_with_prefixes(hq, hkv, d, page):
+    """Kept tokens of chunks behind cached prefixes (paged), including single decode-like tokens."""
+    wl = _batch_with_prefixes([1000, 17, 300, 2048, 0, 64], [200, 1, 130, 65, 300, 3], hq, hkv, d, page, seed=hq + d)
+    _check_compacted(wl, 16, seed=page)
