@@ -46,6 +46,17 @@ class _PagedKV(ctypes.Structure):
                 ("max_pages_per_seq", ctypes.c_int32)]
 
 
+class _StepBuffers(ctypes.Structure):
+    _fields_ = [("cu_seqlens", ctypes.c_void_p), ("positions", ctypes.c_void_p), ("slot_mapping", ctypes.c_void_p),
+                ("block_table", ctypes.c_void_p), ("request_ids", ctypes.c_void_p), ("seg_mask", ctypes.c_void_p),
+                ("finished_ids", ctypes.c_void_p)]
+
+
+class _StepCounts(ctypes.Structure):
+    _fields_ = [("num_segs", ctypes.c_int32), ("num_tokens", ctypes.c_int32), ("num_decode", ctypes.c_int32),
+                ("num_finished", ctypes.c_int32)]
+
+
 def library_path() -> str:
     return native_build.LIB_PATH
 
@@ -95,6 +106,21 @@ def load(build_if_missing: bool = True):
                                            P, sz, P]
         lib.unip_gather_tokens.restype = i32
         lib.unip_gather_tokens.argtypes = [P, i32, i64, i32, P, P, i32, P, i64, P]
+        lib.unip_ffd_pack.restype = i32
+        lib.unip_ffd_pack.argtypes = [P, i32, i32, P, P, P]
+        lib.unip_pack_metadata.restype = i32
+        lib.unip_pack_metadata.argtypes = [P, i32, P, P, P, P]
+        lib.unip_step_builder_create.restype = i32
+        lib.unip_step_builder_create.argtypes = [i32, i32, i32, i32, i32, i32, ctypes.POINTER(P)]
+        lib.unip_step_builder_destroy.restype = None
+        lib.unip_step_builder_destroy.argtypes = [P]
+        lib.unip_step_builder_add.restype = i32
+        lib.unip_step_builder_add.argtypes = [P, i32, i32, ctypes.POINTER(ctypes.c_int32)]
+        lib.unip_step_builder_next.restype = i32
+        lib.unip_step_builder_next.argtypes = [P, ctypes.POINTER(_StepBuffers), ctypes.POINTER(_StepCounts)]
+        lib.unip_step_builder_state.restype = i32
+        lib.unip_step_builder_state.argtypes = [P, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32),
+                                                ctypes.POINTER(ctypes.c_int32)]
         _lib = lib
         return lib
 
@@ -302,3 +328,108 @@ def unip_gather_tokens(hidden, gather_idx, n_kept, out, *, stream=None):
                                 int(out.shape[0]), _ptr(out), int(out.stride(0)), _stream(stream))
     _check(rc, "unip_gather_tokens")
     return out
+
+
+# ---------------------------------------------------------------------------
+# Host-side batch builders (include/unip_sched.h).  These take and return
+# numpy arrays in host memory; the library does the packing and scheduling.
+
+def _host_i32(a):
+    import numpy as np
+    return np.ascontiguousarray(a, dtype=np.int32)
+
+
+def unip_ffd_pack(lengths, capacity: int):
+    """First-fit-decreasing packing -> (order int32[n], bin_cu int32[num_bins + 1])."""
+    import numpy as np
+    lengths = _host_i32(lengths)
+    n = int(lengths.size)
+    order = np.empty(n, np.int32)
+    bin_cu = np.zeros(n + 1, np.int32)
+    nb = ctypes.c_int32(0)
+    _check(load().unip_ffd_pack(lengths.ctypes.data if n else None, n, int(capacity),
+                                order.ctypes.data if n else None, bin_cu.ctypes.data, ctypes.byref(nb)),
+           "unip_ffd_pack")
+    return order, bin_cu[: nb.value + 1].copy()
+
+
+def unip_pack_metadata(lengths, order):
+    """Packed-stream metadata -> (cu_seqlens, positions, src_index), int32 host arrays."""
+    import numpy as np
+    lengths = _host_i32(lengths)
+    order = _host_i32(order)
+    n = int(lengths.size)
+    if order.size != n:
+        raise UnipError("order must have one entry per prompt")
+    total = int(lengths.astype(np.int64).sum())
+    cu = np.zeros(n + 1, np.int32)
+    pos = np.empty(total, np.int32)
+    src = np.empty(total, np.int32)
+    _check(load().unip_pack_metadata(lengths.ctypes.data if n else None, n, order.ctypes.data if n else None,
+                                     cu.ctypes.data, pos.ctypes.data if total else None,
+                                     src.ctypes.data if total else None), "unip_pack_metadata")
+    return cu, pos, src
+
+
+class StepBuilder:
+    """Token-budget step builder with a paged KV cache (unip_step_builder_*).
+
+    ``next()`` returns a dict of host int32/uint8 arrays trimmed to the step:
+    cu_seqlens, positions, slot_mapping, block_table [S, max_pages_per_seq],
+    request_ids, seg_mask, finished_ids, num_decode.
+    """
+
+    def __init__(self, token_budget: int, page_size: int, num_pages: int, max_pages_per_seq: int,
+                 max_seqs: int, chunk_multiple: int = 1):
+        import numpy as np
+        self._lib = load()
+        h = ctypes.c_void_p(None)
+        _check(self._lib.unip_step_builder_create(int(token_budget), int(page_size), int(num_pages),
+                                                  int(max_pages_per_seq), int(max_seqs), int(chunk_multiple),
+                                                  ctypes.byref(h)), "unip_step_builder_create")
+        self._h = h
+        self.token_budget, self.page_size, self.num_pages = int(token_budget), int(page_size), int(num_pages)
+        self.max_pages_per_seq, self.max_seqs = int(max_pages_per_seq), int(max_seqs)
+        self._cu = np.zeros(self.max_seqs + 1, np.int32)
+        self._pos = np.zeros(self.token_budget, np.int32)
+        self._slot = np.zeros(self.token_budget, np.int32)
+        self._bt = np.zeros((self.max_seqs, self.max_pages_per_seq), np.int32)
+        self._rid = np.zeros(self.max_seqs, np.int32)
+        self._mask = np.zeros(self.max_seqs, np.uint8)
+        self._fin = np.zeros(self.max_seqs, np.int32)
+        self._bufs = _StepBuffers(*(a.ctypes.data for a in (self._cu, self._pos, self._slot, self._bt, self._rid,
+                                                              self._mask, self._fin)))
+
+    def close(self):
+        if getattr(self, "_h", None) is not None and self._h.value is not None:
+            self._lib.unip_step_builder_destroy(self._h)
+            self._h = ctypes.c_void_p(None)
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def add(self, prompt_len: int, max_new_tokens: int) -> int:
+        rid = ctypes.c_int32(-1)
+        _check(self._lib.unip_step_builder_add(self._h, int(prompt_len), int(max_new_tokens), ctypes.byref(rid)),
+               "unip_step_builder_add")
+        return rid.value
+
+    def state(self):
+        """(requests with prompt tokens left, requests decoding, free pages)."""
+        a, b, c = ctypes.c_int32(0), ctypes.c_int32(0), ctypes.c_int32(0)
+        _check(self._lib.unip_step_builder_state(self._h, ctypes.byref(a), ctypes.byref(b), ctypes.byref(c)),
+               "unip_step_builder_state")
+        return a.value, b.value, c.value
+
+    def next(self) -> dict:
+        cnt = _StepCounts()
+        _check(self._lib.unip_step_builder_next(self._h, ctypes.byref(self._bufs), ctypes.byref(cnt)),
+               "unip_step_builder_next")
+        s, n = cnt.num_segs, cnt.num_tokens
+        return {"cu_seqlens": self._cu[: s + 1].copy(), "positions": self._pos[:n].copy(),
+                "slot_mapping": self._slot[:n].copy(), "block_table": self._bt[:s].copy(),
+                "request_ids": self._rid[:s].copy(), "seg_mask": self._mask[:s].copy(),
+                "finished_ids": self._fin[: cnt.num_finished].copy(), "num_decode": cnt.num_decode}

@@ -1,6 +1,6 @@
 """Compiles libunip.so in-tree with nvcc for sm_103a (GB300).
 
-Each .cu file under csrc/ is compiled to an object in parallel, then linked
+Each .cu (device) and .cpp (host-only) file under csrc/ is compiled to an object in parallel, then linked
 into ``_build/libunip.so`` with the CUDA runtime linked statically, so the
 library loads on a machine without a GPU driver (the driver is only looked up
 at the first CUDA call).
@@ -33,12 +33,12 @@ def nvcc_path() -> str:
 
 
 def sources():
-    return sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cu"))
+    return sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cu", ".cpp")))
 
 
 def _deps():
     files = sources() + [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cuh", ".h"))]
-    files.append(os.path.join(INCLUDE, "unip.h"))
+    files += [os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE) if f.endswith(".h")]
     files.append(os.path.abspath(__file__))
     return files
 
@@ -60,7 +60,7 @@ def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
     objs = []
 
     def compile_one(src):
-        obj = os.path.join(OUT_DIR, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(OUT_DIR, os.path.splitext(os.path.basename(src))[0] + ".o")
         cmd = [nvcc] + flags + ["-c", src, "-o", obj]
         if verbose:
             print(" ".join(cmd), file=sys.stderr)

@@ -1,22 +1,27 @@
 """The C-ABI library builds for sm_103a, loads without a GPU and exports every
-entry point declared in include/unip.h (no compute calls here)."""
+entry point declared in include/*.h (no compute calls here)."""
 import ctypes
 import os
 import re
 
 from sparsified_long_context_gb300 import binding, native_build
 
-HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "unip.h")
+INCLUDE = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
 
 
 def declared_symbols():
-    text = open(HEADER).read()
-    return re.findall(r"UNIP_API\s+[\w\s\*]+?\b(unip_\w+)\s*\(", text)
+    names = []
+    for f in sorted(os.listdir(INCLUDE)):
+        if f.endswith(".h"):
+            text = open(os.path.join(INCLUDE, f)).read()
+            names += re.findall(r"UNIP_API\s+[\w\s\*]+?\b(unip_\w+)\s*\(", text)
+    return names
 
 
 def test_header_declares_the_four_calls():
     names = set(declared_symbols())
-    for n in ("unip_prefill_attention", "unip_block_importance", "unip_topp_select", "unip_gather_tokens"):
+    for n in ("unip_prefill_attention", "unip_block_importance", "unip_topp_select", "unip_gather_tokens",
+              "unip_ffd_pack", "unip_step_builder_next"):
         assert n in names
 
 
