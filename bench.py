@@ -431,7 +431,7 @@ def main():
     cpu = None
     if not args.no_cpu_baseline and world == 1:
         cpu = cpu_baseline(wl, args.cpu_seconds)
-    launches = kernels_per_step(di.hidden is not None, fused_select=True) * args.steps
+    launches = kernels_per_step(di.hidden is not None, fused_select=True, num_segs=wl.num_segs) * args.steps
     traffic = recorded_traffic(os.path.join(ROOT, "sparsified_long_context_gb300", "csrc", "unip_attention.cu"),
                                "attn_fwd_long_single.md")
     line = {

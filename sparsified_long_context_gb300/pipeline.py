@@ -135,10 +135,11 @@ def run_step(di: DeviceInputs, bufs: StepBuffers, stream=None):
     run_select(di, bufs, stream=stream)
 
 
-def kernels_per_step(has_hidden: bool = True, fused_select: bool = False) -> int:
+def kernels_per_step(has_hidden: bool = True, fused_select: bool = False, num_segs: int = 2) -> int:
     """libunip kernels one step launches (up to 12000 segments)."""
     # attention: plan + attention; importance: plan + score + norm;
-    # Top-p: select + index, gather: 1  -- or the fused select + gather: 2
+    # Top-p: select + index, gather: 1  -- or the fused select + gather: 2,
+    # one launch when the stream holds a single segment
     if fused_select:
-        return 2 + 3 + 2
+        return 2 + 3 + (1 if num_segs == 1 else 2)
     return 2 + 3 + 2 + (1 if has_hidden else 0)
