@@ -99,6 +99,48 @@ def recorded_traffic(kernel_src: str, summary: str):
         return None
 
 
+def rope_append_part(di, flush, stream, hbm_peak: float, reps: int = 10):
+    """unip_rope_append_kv on copies of the step's q and k (and its v), every token
+    appended to a paged cache whose pages are in shuffled order; timed alone with
+    CUDA events after an L2 flush.  Rotary embedding + append is not part of the
+    step (its q and k are taken as already rotated); it is measured beside it."""
+    import torch
+    from sparsified_long_context_gb300 import binding as B
+    n, hq, d = (int(x) for x in di.q.shape)
+    hkv = int(di.k.shape[1])
+    page = 16
+    num_pages = -(-n // page)
+    dev = di.q.device
+    q = di.q.clone()
+    k = di.k.clone()
+    kc = torch.empty((num_pages, page, hkv, d), dtype=torch.bfloat16, device=dev)
+    vc = torch.empty_like(kc)
+    g = torch.Generator(device="cpu").manual_seed(7)
+    perm = torch.randperm(num_pages, generator=g).to(torch.int32)
+    t = torch.arange(n, dtype=torch.int32)
+    slots = (perm[t // page] * page + t % page).to(dev)
+    ts = []
+    for i in range(reps + 2):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        B.unip_rope_append_kv(q, k, di.v, di.positions, num_heads_q=hq, num_heads_kv=hkv, head_dim=d,
+                              rope_theta=500000.0, slot_mapping=slots, k_cache=kc, v_cache=vc, page_size=page,
+                              stream=stream)
+        e1.record(stream)
+        ts.append((e0, e1))
+    torch.cuda.synchronize()
+    st = B.unip_get_device_status(clear=True)
+    if st:
+        raise SystemExit(f"device status after rotary append: {B.describe_status(st)}")
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ts[2:])
+    nbytes = n * d * 2 * (2 * hq + 5 * hkv) + 8 * n   # q, k read+written; v read; k, v cache rows written
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    del q, k, kc, vc
+    return {"ms": ms, "bytes": nbytes, "gbs": gbs, "frac_hbm": gbs / hbm_peak,
+            "how": "separate launch on the step's q/k/v, theta 500000, every token appended, L2 flushed"}
+
+
 class ClockSampler:
     """nvidia-smi clock / throttle sampling during the timed region."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -394,6 +436,7 @@ def main():
     peaks, peak_src = load_peaks()
     bf16_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    rope = rope_append_part(di, flush, stream, hbm_peak)
 
     # ---- end to end through the C ABI with host buffers (pinned), copies inside the timed region
     host = {}
@@ -449,6 +492,7 @@ def main():
                                     "[L2 flush, importance]",
             "select_gather_bytes": sg_bytes, "select_gather_gbs": sg_gbs,
             "select_gather_frac_hbm": sg_gbs / hbm_peak, "n_kept": n_kept, "n_blocks": n_blocks,
+            "rope_append": rope,
             "peaks": f"{peak_src}: bf16 {bf16_peak} TFLOP/s, HBM {hbm_peak} GB/s",
         },
         "roofline": {"bound": "tensor", "achieved": attn_tflops, "peak": bf16_peak, "unit": "TFLOP/s",

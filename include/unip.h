@@ -274,6 +274,39 @@ UNIP_API int32_t unip_select_gather(const float *imp, const int32_t *blk_cu, con
                                     void *hidden_out, int64_t out_row_stride,
                                     void *workspace, size_t workspace_bytes, void *stream);
 
+/* Rotary position embedding of q and k in place, by each token's own
+ * position, and append of the rotated k and of v into the paged KV cache.
+ * [PP]: a packed stream restarts the positional encoding of every prompt,
+ * so the positions passed here are the restarted ones (segment-local for
+ * prompts without a prefix, absolute for chunks that continue one).  The
+ * encoding is the rotary one (RoFormer): channel pair i of every head turns
+ * by positions[t] * rope_theta^(-2i/D),
+ *     (a, b) -> (a cos w - b sin w, b cos w + a sin w),
+ * with pairs (i, i + D/2) when interleaved = 0 and (2i, 2i+1) when 1.  The
+ * angle is formed in double precision and reduced to [-pi, pi] before the
+ * single-precision sine and cosine; results are rounded to bf16 (RNE).
+ * [CP]: a chunk's K/V join the paged cache that later chunks and decodes
+ * attend to.
+ *   q             bf16 [N][H_q][D], rotated in place; NULL skips q
+ *   k             bf16 [N][H_kv][D], rotated in place
+ *   v             bf16 [N][H_kv][D] (read only when appending)
+ *   positions     int32 [N] (needed when rope_theta > 0)
+ *   prm           H_q, H_kv, D (D a multiple of 16, 16..256); scale unused
+ *   rope_theta    base of the frequencies (e.g. 10000 or 500000); <= 0
+ *                 skips the rotation (append only)
+ *   slot_mapping  int32 [N] or NULL (no append): token t's rotated k row and
+ *                 v row go to slot s = page * page_size + offset of k_cache /
+ *                 v_cache ([num_pages][page_size][H_kv][D] bf16); s < 0
+ *                 skips the token (padding); s >= num_pages * page_size sets
+ *                 UNIP_DEV_BAD_INDEX and skips it
+ * Every pointer is 16-byte aligned device memory; asynchronous on `stream`.
+ * Errors: INVALID_ARGUMENT (NULL where needed, negative sizes, interleaved
+ * not 0/1, NaN theta), UNSUPPORTED (D), ALIGNMENT. */
+UNIP_API int32_t unip_rope_append_kv(void *q, void *k, const void *v, const int32_t *positions, int32_t num_tokens,
+                                     const unip_attn_params *prm, double rope_theta, int32_t interleaved,
+                                     const int32_t *slot_mapping, void *k_cache, void *v_cache, int32_t num_pages,
+                                     int32_t page_size, void *stream);
+
 /* ---------------------------------------------------------------------------
  * Row gather ([UP] section 3: the kept tokens' hidden states form the stream
  * of the later layers):  out[i][:] = hidden[gather_idx[i]][:] for

@@ -106,6 +106,8 @@ def load(build_if_missing: bool = True):
                                            P, sz, P]
         lib.unip_gather_tokens.restype = i32
         lib.unip_gather_tokens.argtypes = [P, i32, i64, i32, P, P, i32, P, i64, P]
+        lib.unip_rope_append_kv.restype = i32
+        lib.unip_rope_append_kv.argtypes = [P, P, P, P, i32, pp, f64, i32, P, P, P, i32, i32, P]
         lib.unip_ffd_pack.restype = i32
         lib.unip_ffd_pack.argtypes = [P, i32, i32, P, P, P]
         lib.unip_pack_metadata.restype = i32
@@ -329,6 +331,21 @@ def unip_gather_tokens(hidden, gather_idx, n_kept, out, *, stream=None):
     _check(rc, "unip_gather_tokens")
     return out
 
+
+def unip_rope_append_kv(q, k, v=None, positions=None, *, num_heads_q, num_heads_kv, head_dim,
+                        rope_theta=10000.0, interleaved=False, slot_mapping=None, k_cache=None, v_cache=None,
+                        page_size=16, stream=None):
+    """Rotary embedding of q and k in place by `positions`; with `slot_mapping`,
+    also writes the rotated k and v rows into the paged caches."""
+    lib = load()
+    n = int(k.shape[0])
+    prm = _params(num_heads_q, num_heads_kv, head_dim, 0.0)
+    num_pages = int(k_cache.shape[0]) if k_cache is not None else 0
+    rc = lib.unip_rope_append_kv(_ptr(q), _ptr(k), _ptr(v), _ptr(positions), n, ctypes.byref(prm),
+                                 float(rope_theta), 1 if interleaved else 0, _ptr(slot_mapping), _ptr(k_cache),
+                                 _ptr(v_cache), num_pages, int(page_size), _stream(stream))
+    _check(rc, "unip_rope_append_kv")
+    return q, k
 
 # ---------------------------------------------------------------------------
 # Host-side batch builders (include/unip_sched.h).  These take and return

@@ -54,3 +54,21 @@ def test_host_rejects_bad_arguments_before_launch():
     rc = lib.unip_topp_select(None, None, None, None, 1, 10, 16, 1.5, 3, None, 0, None, None, None, None, None, 0,
                               None)
     assert rc == -1
+
+
+def test_rope_host_checks_before_launch():
+    lib = binding.load()
+    prm = binding._params(8, 2, 72, 0.0)    # D not a multiple of 16
+    assert lib.unip_rope_append_kv(None, ctypes.c_void_p(16), None, ctypes.c_void_p(16), 10, ctypes.byref(prm),
+                                   10000.0, 0, None, None, None, 0, 16, None) == -2
+    prm = binding._params(8, 2, 128, 0.0)
+    assert lib.unip_rope_append_kv(None, ctypes.c_void_p(16), None, ctypes.c_void_p(16), 10, ctypes.byref(prm),
+                                   10000.0, 2, None, None, None, 0, 16, None) == -1     # layout flag
+    assert lib.unip_rope_append_kv(None, None, None, None, 10, ctypes.byref(prm),
+                                   10000.0, 0, None, None, None, 0, 16, None) == -1     # k missing
+    assert lib.unip_rope_append_kv(None, ctypes.c_void_p(16), None, ctypes.c_void_p(16), 10, ctypes.byref(prm),
+                                   10000.0, 0, ctypes.c_void_p(16), None, None, 4, 16, None) == -1  # caches missing
+    assert lib.unip_rope_append_kv(None, ctypes.c_void_p(24), None, ctypes.c_void_p(16), 10, ctypes.byref(prm),
+                                   10000.0, 0, None, None, None, 0, 16, None) == -5     # misaligned k
+    assert lib.unip_rope_append_kv(None, None, None, None, 0, ctypes.byref(prm),
+                                   10000.0, 0, None, None, None, 0, 16, None) == 0      # nothing to do
