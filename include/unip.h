@@ -283,8 +283,10 @@ UNIP_API int32_t unip_select_gather(const float *imp, const int32_t *blk_cu, con
  * by positions[t] * rope_theta^(-2i/D),
  *     (a, b) -> (a cos w - b sin w, b cos w + a sin w),
  * with pairs (i, i + D/2) when interleaved = 0 and (2i, 2i+1) when 1.  The
- * angle is formed in double precision and reduced to [-pi, pi] before the
- * single-precision sine and cosine; results are rounded to bf16 (RNE).
+ * angle modulo one turn is exact integer arithmetic on a 64-bit fixed-point
+ * turns-per-position value (double-precision frequency), so it stays within
+ * ~1e-6 rad for any int32 position; the rotation is single precision and
+ * the results are rounded to bf16 (RNE).
  * [CP]: a chunk's K/V join the paged cache that later chunks and decodes
  * attend to.
  *   q             bf16 [N][H_q][D], rotated in place; NULL skips q

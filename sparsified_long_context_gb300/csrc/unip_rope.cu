@@ -17,31 +17,32 @@
 //
 // HBM-bound, one pass: every q and k element is read once and written once in
 // place, and the rotated k and the v rows are written once more into the
-// cache.  A CTA takes 8 tokens at a time: first the (cos, sin) table of those
-// tokens goes to shared memory, shared by all heads; then the q rows, the k
-// rows and the v rows of the 8 tokens, each a contiguous range of memory, are
-// streamed with 16-byte accesses, four units per thread in flight.
+// cache.  A CTA takes 16 tokens at a time: first the (cos, sin) table of those
+// tokens goes to shared memory, shared by all heads; then one flat loop runs
+// over the 16-byte units of the q rows, the k rows and the v rows of the 16
+// tokens (each a contiguous range of memory), four units per thread in
+// flight, so the three streams overlap.
 //
-// Angle accuracy: the frequencies theta^(-2i/D) and the product with the
-// position are formed in double precision and reduced to [-pi, pi] with a
-// two-part 2*pi (Cody-Waite reduction), after which sincosf of the reduced
-// single-precision angle is within ~1e-7 rad of the exact rotation even for
-// positions in the millions (frequencies in single precision would be off by
-// up to ~1e-2 rad at position 65536).
+// Angle: each frequency theta^(-2i/D) is turned, once per CTA, into the turns
+// it makes per position, a fraction F_i of a full turn held as a 64-bit
+// fixed-point number.  A token's angle is then position * F_i modulo one
+// turn, which 64-bit integer multiplication gives exactly (the wrap-around is
+// the modulo), so the range reduction costs no floating point; the top 32
+// bits become a single-precision argument of sincospif.  The only errors are
+// F_i's double-precision rounding (below 3e-16 relative, ~6e-7 rad at
+// position 2^31, ~1e-9 rad at 2^22) and the 24-bit argument (2e-7 rad).
 #include "unip_internal.cuh"
 
 namespace unip {
 namespace {
 
 constexpr int kRopeThreads = 256;
-constexpr int kRopeTok = 8;       // tokens per CTA iteration
+constexpr int kRopeTok = 16;      // tokens per CTA iteration
 constexpr int kRopeBatch = 4;     // units per thread in flight
 constexpr int kRopeMaxHalf = 128; // D <= 256
 
-// 2*pi as a double plus the double nearest to its remainder, and 1/(2*pi).
-constexpr double kTwoPiHi = 6.283185307179586;
-constexpr double kTwoPiLo = 2.4492935982947064e-16;
-constexpr double kInvTwoPi = 0.15915494309189535;
+// 2*pi rounded to double.
+constexpr double kTwoPi = 6.283185307179586;
 
 struct RopeArgs {
   uint4 *q;                 // [N][Hq][D] bf16, rotated in place (may be null)
@@ -101,107 +102,93 @@ __device__ __forceinline__ void turn_inter(uint4 &v, const float2 *cs) {
   v.w = turn_pair(v.w, cs[3]);
 }
 
-// Rotates (and/or appends) the rows of H heads of nt tokens starting at
-// `rows`; a unit is one 16-byte vector (interleaved) or a pair of vectors
-// half a row apart (half layout).  slots is offset to the first token.
 template <bool kInter>
-__device__ __forceinline__ void rotate_rows(uint4 *rows, int nt, int H, int vr, int half, const float2 *cs,
-                                            bool rotate, const int32_t *slots, uint4 *cache, int64_t num_slots,
-                                            uint32_t *status) {
-  const int ur = kInter ? vr : vr / 2;  // units per head row
-  const int n_units = nt * H * ur;
-  for (int u0 = threadIdx.x; u0 < n_units; u0 += kRopeThreads * kRopeBatch) {
-    uint4 va[kRopeBatch], vb[kRopeBatch];
-#pragma unroll
-    for (int b = 0; b < kRopeBatch; ++b) {
-      const int u = u0 + b * kRopeThreads;
-      if (u < n_units) {
-        const int row = u / ur, c = u - row * ur;
-        const int off = row * vr + c;
-        va[b] = ld_v4(rows + off);
-        if (!kInter) vb[b] = ld_v4(rows + off + vr / 2);
-      }
-    }
-#pragma unroll
-    for (int b = 0; b < kRopeBatch; ++b) {
-      const int u = u0 + b * kRopeThreads;
-      if (u >= n_units) break;
-      const int row = u / ur, c = u - row * ur;
-      const int tl = row / H, h = row - tl * H;
-      const int off = row * vr + c;
-      if (rotate) {
-        if (kInter) {
-          turn_inter(va[b], cs + tl * half + 4 * c);
-        } else {
-          turn_half(va[b], vb[b], cs + tl * half + 8 * c);
-        }
-        st_v4(rows + off, va[b]);
-        if (!kInter) st_v4(rows + off + vr / 2, vb[b]);
-      }
-      if (slots) {
-        const int32_t slot = slots[tl];
-        if (slot >= 0 && slot < num_slots) {
-          uint4 *dst = cache + ((int64_t)slot * H + h) * vr + c;
-          st_v4(dst, va[b]);
-          if (!kInter) st_v4(dst + vr / 2, vb[b]);
-        } else if (slot >= num_slots && h == 0 && c == 0) {
-          atomicOr(status, UNIP_DEV_BAD_INDEX);
-        }
-      }
-    }
-  }
-}
-
-template <bool kInter>
-__global__ void __launch_bounds__(kRopeThreads) rope_append_kernel(RopeArgs a) {
-  __shared__ double s_inv[kRopeMaxHalf];
-  __shared__ float2 s_cs[kRopeTok * kRopeMaxHalf];
+__global__ void __launch_bounds__(kRopeThreads, 3) rope_append_kernel(RopeArgs a) {
+  __shared__ uint64_t s_turn[kRopeMaxHalf];          // F_i: turns per position, 64-bit fraction
+  __shared__ float2 s_cs[kRopeTok * kRopeMaxHalf];   // (cos, sin) per token and frequency
   const int half = a.D >> 1;
-  const int vr = a.D >> 3;  // 16-byte vectors per head row
+  const int vr = a.D >> 3;                 // 16-byte vectors per head row
+  const int ur = kInter ? vr : vr >> 1;    // rotation units per head row
   if (a.rotate)
-    for (int i = threadIdx.x; i < half; i += kRopeThreads) s_inv[i] = exp2(-(2.0 * i / a.D) * a.log2_theta);
+    for (int i = threadIdx.x; i < half; i += kRopeThreads) {
+      double turns = exp2(-(2.0 * i / a.D) * a.log2_theta) / kTwoPi;   // < 1/(2 pi) when theta >= 1
+      turns -= floor(turns);                                            // whole turns do not matter
+      s_turn[i] = (uint64_t)(turns * 18446744073709551616.0);          // * 2^64
+    }
+  const int per_q = a.Hq * ur, per_k = a.Hkv * ur, per_v = a.Hkv * vr;
   const int64_t groups = ((int64_t)a.N + kRopeTok - 1) / kRopeTok;
   for (int64_t g = blockIdx.x; g < groups; g += gridDim.x) {
     const int64_t t0 = g * kRopeTok;
     const int nt = (a.N - t0) < kRopeTok ? (int)(a.N - t0) : kRopeTok;
-    __syncthreads();  // s_inv written; the previous group's table no longer read
+    __syncthreads();  // s_turn written; the previous group's table no longer read
     if (a.rotate) {
       for (int e = threadIdx.x; e < nt * half; e += kRopeThreads) {
         const int tl = e / half, i = e - tl * half;
-        const double ang = (double)a.pos[t0 + tl] * s_inv[i];
-        const double turns = rint(ang * kInvTwoPi);
-        double r = fma(-turns, kTwoPiHi, ang);
-        r = fma(-turns, kTwoPiLo, r);
-        float s, c;
-        sincosf((float)r, &s, &c);
-        s_cs[tl * half + i] = make_float2(c, s);
+        const uint64_t frac = (uint64_t)(int64_t)a.pos[t0 + tl] * s_turn[i];  // mod 2^64 = mod one turn
+        float sn, cs;
+        sincospif((float)(int32_t)(frac >> 32) * 0x1p-31f, &sn, &cs);         // half-turns in [-1, 1)
+        s_cs[tl * half + i] = make_float2(cs, sn);
       }
     }
     __syncthreads();
+    const int n_q = (a.q && a.rotate) ? nt * per_q : 0;
+    const int n_qk = n_q + nt * per_k;
+    const int total = n_qk + (a.slots ? nt * per_v : 0);
+    uint4 *qg = a.q ? a.q + t0 * a.Hq * vr : nullptr;
+    uint4 *kg = a.k + t0 * a.Hkv * vr;
+    const uint4 *vg = a.slots ? a.v + t0 * per_v : nullptr;
     const int32_t *slots = a.slots ? a.slots + t0 : nullptr;
-    if (a.q && a.rotate)
-      rotate_rows<kInter>(a.q + t0 * a.Hq * vr, nt, a.Hq, vr, half, s_cs, true, nullptr, nullptr, 0, a.status);
-    rotate_rows<kInter>(a.k + t0 * a.Hkv * vr, nt, a.Hkv, vr, half, s_cs, a.rotate != 0, slots, a.kc,
-                        a.num_slots, a.status);
-    if (slots) {
-      // v rows of the group are contiguous; copy them to their slots.
-      const int per_tok = a.Hkv * vr;
-      const int n_units = nt * per_tok;
-      const uint4 *src = a.v + t0 * per_tok;
-      for (int u0 = threadIdx.x; u0 < n_units; u0 += kRopeThreads * kRopeBatch) {
-        uint4 r[kRopeBatch];
+    for (int u0 = threadIdx.x; u0 < total; u0 += kRopeThreads * kRopeBatch) {
+      uint4 va[kRopeBatch], vb[kRopeBatch];
 #pragma unroll
-        for (int b = 0; b < kRopeBatch; ++b) {
-          const int u = u0 + b * kRopeThreads;
-          if (u < n_units) r[b] = ld_v4(src + u);
+      for (int b = 0; b < kRopeBatch; ++b) {
+        const int u = u0 + b * kRopeThreads;
+        if (u < n_qk) {
+          const bool is_q = u < n_q;
+          const int w = is_q ? u : u - n_q;
+          const int row = w / ur, c = w - row * ur;
+          const uint4 *p = (is_q ? qg : kg) + row * vr + c;
+          va[b] = ld_v4(p);
+          if (!kInter) vb[b] = ld_v4(p + (vr >> 1));
+        } else if (u < total) {
+          va[b] = ld_v4(vg + (u - n_qk));
         }
+      }
 #pragma unroll
-        for (int b = 0; b < kRopeBatch; ++b) {
-          const int u = u0 + b * kRopeThreads;
-          if (u >= n_units) break;
-          const int tl = u / per_tok;
+      for (int b = 0; b < kRopeBatch; ++b) {
+        const int u = u0 + b * kRopeThreads;
+        if (u >= total) break;
+        if (u < n_qk) {
+          const bool is_q = u < n_q;
+          const int w = is_q ? u : u - n_q;
+          const int H = is_q ? a.Hq : a.Hkv;
+          const int row = w / ur, c = w - row * ur;
+          const int tl = row / H, h = row - tl * H;
+          uint4 *p = (is_q ? qg : kg) + row * vr + c;
+          if (a.rotate) {
+            if (kInter) {
+              turn_inter(va[b], s_cs + tl * half + 4 * c);
+            } else {
+              turn_half(va[b], vb[b], s_cs + tl * half + 8 * c);
+            }
+            st_v4(p, va[b]);
+            if (!kInter) st_v4(p + (vr >> 1), vb[b]);
+          }
+          if (!is_q && slots) {
+            const int32_t slot = slots[tl];
+            if (slot >= 0 && slot < a.num_slots) {
+              uint4 *dst = a.kc + ((int64_t)slot * a.Hkv + h) * vr + c;
+              st_v4(dst, va[b]);
+              if (!kInter) st_v4(dst + (vr >> 1), vb[b]);
+            } else if (slot >= a.num_slots && h == 0 && c == 0) {
+              atomicOr(a.status, UNIP_DEV_BAD_INDEX);
+            }
+          }
+        } else {
+          const int w = u - n_qk;
+          const int tl = w / per_v;
           const int32_t slot = slots[tl];
-          if (slot >= 0 && slot < a.num_slots) st_v4(a.vc + (int64_t)slot * per_tok + (u - tl * per_tok), r[b]);
+          if (slot >= 0 && slot < a.num_slots) st_v4(a.vc + (int64_t)slot * per_v + (w - tl * per_v), va[b]);
         }
       }
     }
