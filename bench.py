@@ -349,7 +349,7 @@ def main():
                     choices=["long_single", "mixed_step", "prepacked", "tiny_packed"])
     ap.add_argument("--tokens", type=int, default=32768,
                     help="prompt length of the long_single workload (profiling runs use a shorter one)")
-    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-step-seconds", type=float, default=6.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -361,8 +361,8 @@ def main():
 
     import torch
     from sparsified_long_context_gb300 import binding as B
-    from sparsified_long_context_gb300.pipeline import (DeviceInputs, StepBuffers, kernels_per_step, run_attention,
-                                                        run_importance, run_select_gather)
+    from sparsified_long_context_gb300.pipeline import (DeviceInputs, StepBuffers, StreamedSteps, kernels_per_step,
+                                                        run_attention, run_importance, run_select_gather)
     world, rank, local = dist_setup(args)
     torch.cuda.set_device(local)
     dist = None
@@ -438,34 +438,27 @@ def main():
     hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     rope = rope_append_part(di, flush, stream, hbm_peak)
 
-    # ---- end to end through the C ABI with host buffers (pinned), copies inside the timed region
-    host = {}
-    for name in ("q", "k", "v", "hidden", "cu_seqlens", "positions", "seg_mask"):
-        t = getattr(di, name)
-        if t is not None:
-            host[name] = t.cpu().pin_memory()
-    out_host = torch.empty(bufs.out.shape, dtype=bufs.out.dtype).pin_memory()
-    hid_host = None
-    if bufs.hidden_out is not None:
-        hid_host = torch.empty(bufs.hidden_out.shape, dtype=bufs.hidden_out.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in host.values())
-    d2h_list = []
+    # ---- end to end through the public API with host buffers (pinned): every step uploads its
+    #      inputs and downloads its results inside the timed region; StreamedSteps overlaps
+    #      step i+1's upload and step i-1's download with step i's kernels (two device sets).
+    import dataclasses
+    di2 = dataclasses.replace(di, **{f: getattr(di, f).clone() for f in StreamedSteps.FIELDS
+                                     if getattr(di, f) is not None})
+    streamer = StreamedSteps([(di, bufs), (di2, StepBuffers(di2))], stream)
+    batch = streamer.host_batch(di)
+    h2d = streamer.bytes_up(batch)
+    streamer.run([batch], 2)   # warm-up of the copy streams
     torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
     e2e_t0 = time.perf_counter()
-    for _ in range(args.e2e_steps):
-        for name, t in host.items():
-            getattr(di, name).copy_(t, non_blocking=True)
-        step()
-        out_host.copy_(bufs.out, non_blocking=True)
-        m = int(bufs.n_kept.item())  # result size lives on the device
-        if hid_host is not None:
-            hid_host[:m].copy_(bufs.hidden_out[:m], non_blocking=True)
-        torch.cuda.synchronize()
-        d2h_list.append(out_host.numel() * 2 + 4 + m * d_model * 2)
+    kept = streamer.run([batch], args.e2e_steps)
     e2e_dt = max_over_ranks(time.perf_counter() - e2e_t0, dist, f"cuda:{local}")
+    d2h_list = [bufs.out.numel() * 2 + 4 + m * d_model * 2 for m in kept]
     e2e_value = flops_step * world * args.e2e_steps / e2e_dt / 1e12
+    st = B.unip_get_device_status(clear=True)
+    if st:
+        raise SystemExit(f"device status after end-to-end steps: {B.describe_status(st)}")
 
     if rank != 0:
         if dist is not None:
@@ -502,7 +495,9 @@ def main():
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": int(statistics.mean(d2h_list)),
-                "how": "pinned host inputs copied in, 4 C-ABI calls, out + n_kept + compacted hidden copied back"},
+                "how": "pipeline.StreamedSteps: every step uploads its inputs from pinned host memory and downloads "
+                       "out, n_kept and the compacted hidden rows; uploads and downloads run on their own streams, "
+                       "overlapping the neighbouring steps' kernels (two device sets)", "steps": args.e2e_steps},
         "gpu_launches": launches,
         "clocks": clk.summary(),
         "wall_s_timed_region": wall1 - wall0,

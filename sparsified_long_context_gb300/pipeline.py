@@ -143,3 +143,104 @@ def kernels_per_step(has_hidden: bool = True, fused_select: bool = False, num_se
     if fused_select:
         return 2 + 3 + (1 if num_segs == 1 else 2)
     return 2 + 3 + 2 + (1 if has_hidden else 0)
+
+
+class StreamedSteps:
+    """The step over batches that live in pinned host memory, with the copies
+    overlapped with the kernels.
+
+    Two device sets (inputs + step buffers) alternate.  While batch i's kernels
+    run on the compute stream, batch i+1's inputs are uploaded on an upload
+    stream and batch i-1's results (attention output, n_kept and the n_kept
+    compacted hidden rows) are downloaded on a download stream into pinned host
+    buffers.  Events order the three streams; the host waits only for a batch's
+    n_kept (to size its hidden-row copy) after the next batch is already queued,
+    and for a set's last download before uploading into it again.
+    """
+
+    FIELDS = ("q", "k", "v", "hidden", "cu_seqlens", "positions", "seg_mask")
+
+    def __init__(self, sets, compute_stream=None):
+        import torch
+        if len(sets) != 2:
+            raise ValueError("StreamedSteps alternates between two device sets")
+        self.sets = sets
+        dev = sets[0][0].q.device
+        self.cs = compute_stream or torch.cuda.current_stream(dev)
+        self.up = torch.cuda.Stream(device=dev)
+        self.down = torch.cuda.Stream(device=dev)
+        self.out_host = [torch.empty(b.out.shape, dtype=b.out.dtype).pin_memory() for _, b in sets]
+        self.hid_host = [None if b.hidden_out is None else
+                         torch.empty(b.hidden_out.shape, dtype=b.hidden_out.dtype).pin_memory() for _, b in sets]
+        self.nk_host = torch.zeros(2, dtype=torch.int32).pin_memory()
+        self.fields = [f for f in self.FIELDS if getattr(sets[0][0], f) is not None]
+
+    def host_batch(self, di: DeviceInputs):
+        """Pinned host copies of a device set's input fields (a batch to stream)."""
+        return {f: getattr(di, f).cpu().pin_memory() for f in self.fields}
+
+    def bytes_up(self, batch) -> int:
+        return sum(t.numel() * t.element_size() for t in batch.values())
+
+    def run(self, batches, steps: int, on_result=None):
+        """Runs `steps` steps, step i on batches[i % len(batches)].  Returns the
+        n_kept of every step; on_result(i, out_host, hidden_rows_host, n_kept) is
+        called once step i's downloads have landed (before its buffers are reused)."""
+        import torch
+        ev = [[torch.cuda.Event() for _ in range(4)] for _ in range(2)]  # uploaded, computed, nk, downloaded
+        n_kept = [0] * steps
+        used = [None, None]   # step whose results a set holds
+
+        def finish_download(i, s):
+            _, bufs = self.sets[s]
+            ev[s][2].synchronize()
+            m = int(self.nk_host[s])
+            n_kept[i] = m
+            with torch.cuda.stream(self.down):
+                if self.hid_host[s] is not None and m > 0:
+                    self.hid_host[s][:m].copy_(bufs.hidden_out[:m], non_blocking=True)
+                self.down.record_event(ev[s][3])
+
+        def release(s):
+            i = used[s]
+            if i is None:
+                return
+            ev[s][3].synchronize()
+            if on_result is not None:
+                hid = None if self.hid_host[s] is None else self.hid_host[s][:n_kept[i]]
+                on_result(i, self.out_host[s], hid, n_kept[i])
+            used[s] = None
+
+        pending = None
+        for i in range(steps):
+            s = i % 2
+            di, bufs = self.sets[s]
+            batch = batches[i % len(batches)]
+            if used[s] is not None:
+                release(s)
+            with torch.cuda.stream(self.up):
+                for f, t in batch.items():
+                    getattr(di, f).copy_(t, non_blocking=True)
+                self.up.record_event(ev[s][0])
+            self.cs.wait_event(ev[s][0])
+            run_attention(di, bufs, self.cs)
+            run_importance(di, bufs, self.cs)
+            run_select_gather(di, bufs, stream=self.cs)
+            self.cs.record_event(ev[s][1])
+            # The previous step's hidden rows go on the download stream before this
+            # step's downloads, which wait for this step's kernels.
+            if pending is not None:
+                finish_download(*pending)
+            with torch.cuda.stream(self.down):
+                self.down.wait_event(ev[s][1])
+                self.out_host[s].copy_(bufs.out, non_blocking=True)
+                self.nk_host[s:s + 1].copy_(bufs.n_kept, non_blocking=True)
+                self.down.record_event(ev[s][2])
+            used[s] = i
+            pending = (i, s)
+        if pending is not None:
+            finish_download(*pending)
+        for s in sorted((s for s in (0, 1) if used[s] is not None), key=lambda s: used[s]):
+            release(s)
+        torch.cuda.synchronize()
+        return n_kept
