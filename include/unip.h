@@ -119,6 +119,22 @@ UNIP_API const char *unip_status_string(int32_t code);
  * device), and clears it when clear != 0.  Returns UNIP_OK or UNIP_ERR_CUDA. */
 UNIP_API int32_t unip_get_device_status(uint32_t *bits, int32_t clear);
 
+/* Shape of the attention work items, process-wide (all devices, all later
+ * calls of unip_prefill_attention, unip_compacted_attention and the noalloc
+ * variant).  A work item is two 128-row query tiles that share every K/V tile
+ * (one tile's softmax overlaps the other's MMAs), or one tile.  AUTO takes one
+ * tile per item when even twice the most two-tile items the call can hold
+ * (from N, S and the heads) leave SMs idle -- a short chunk behind a long
+ * prefix -- and two otherwise.  PAIRED and SINGLE force one shape (tests,
+ * tuning); odd GQA groups always use one tile.  Results do not depend on the
+ * shape beyond floating-point summation order, which is the same (every row's
+ * keys are visited in the same tile order either way).
+ * Errors: INVALID_ARGUMENT for an unknown mode. */
+#define UNIP_ATTN_SCHEDULE_AUTO 0
+#define UNIP_ATTN_SCHEDULE_PAIRED 1
+#define UNIP_ATTN_SCHEDULE_SINGLE 2
+UNIP_API int32_t unip_set_attention_schedule(int32_t mode);
+
 /* ---------------------------------------------------------------------------
  * Attention ([CP] causal mask over absolute positions with a cached prefix,
  * [PP] block-diagonal mask and restarted positions).

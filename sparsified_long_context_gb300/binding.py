@@ -23,6 +23,7 @@ UNIP_OK = 0
 UNIP_KEEP_FIRST = 0x1
 UNIP_KEEP_LAST = 0x2
 UNIP_TOPP_MAX_BLOCKS = 8192
+UNIP_ATTN_SCHEDULE_AUTO, UNIP_ATTN_SCHEDULE_PAIRED, UNIP_ATTN_SCHEDULE_SINGLE = 0, 1, 2
 
 DEV_STATUS_BITS = {
     0x1: "bad cu_seqlens", 0x2: "bad positions", 0x4: "bad pages", 0x8: "device wait timeout",
@@ -106,6 +107,8 @@ def load(build_if_missing: bool = True):
                                            P, sz, P]
         lib.unip_gather_tokens.restype = i32
         lib.unip_gather_tokens.argtypes = [P, i32, i64, i32, P, P, i32, P, i64, P]
+        lib.unip_set_attention_schedule.restype = i32
+        lib.unip_set_attention_schedule.argtypes = [i32]
         lib.unip_rope_append_kv.restype = i32
         lib.unip_rope_append_kv.argtypes = [P, P, P, P, i32, pp, f64, i32, P, P, P, i32, i32, P]
         lib.unip_ffd_pack.restype = i32
@@ -172,6 +175,11 @@ def unip_get_device_status(clear: bool = True) -> int:
 
 def describe_status(bits: int) -> str:
     return ", ".join(v for k, v in DEV_STATUS_BITS.items() if bits & k) or "ok"
+
+
+def unip_set_attention_schedule(mode: int):
+    """Work-item shape of later attention calls: AUTO, PAIRED (two query tiles) or SINGLE (one)."""
+    _check(load().unip_set_attention_schedule(int(mode)), "unip_set_attention_schedule")
 
 
 def unip_attention_workspace_size(total_tokens, num_segs, hq, hkv, d) -> int:

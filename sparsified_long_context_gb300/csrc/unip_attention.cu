@@ -50,6 +50,8 @@
 #include <cstring>
 #include <mutex>
 
+#include <atomic>
+
 #include "unip_internal.cuh"
 
 namespace unip {
@@ -80,6 +82,7 @@ struct AttnArgs {
   uint32_t *status;
   int32_t S, N, Hq, group, heads_per_pair, num_pages, page_size, max_pages;
   int32_t lg;  // 0: a tile's rows are 128 tokens of one head; log2(group): rows are (token, head of the group)
+  int32_t single;  // 1: every work item is one query tile (calls with too few items to fill the GPU)
   float scale_log2;
 };
 
@@ -504,7 +507,9 @@ __device__ __forceinline__ bool softmax_tile_role(const AttnArgs &a, int tile, c
 // or non-dividing GQA group) the tiles are 128 tokens of the query heads h0
 // and h0 + 1 of one kv head; with lg = log2(G) each row is a (token, head) pair
 // of the G query heads of kv head g, so a tile covers 128 / G tokens and a
-// single decode token still fills G rows.
+// single decode token still fills G rows.  When a call holds too few items to
+// give every SM one (a short chunk), `single` makes every item one tile, twice
+// as many items at the same total work.
 struct WorkItem {
   TileRows tr0, tr1;
   int32_t s, c0, P, g, Tp, T;
@@ -521,18 +526,18 @@ __device__ __forceinline__ WorkItem decode_item(const AttnArgs &a, int32_t unit)
   const int32_t n = a.cu[w.s + 1] - w.c0;
   w.P = a.prefix_lens ? a.prefix_lens[w.s] : a.pos[w.c0];
   if (a.lg > 0) {
-    const int32_t subs = a.group >> 1;  // work items per kv head for one 128-token pair
+    const int32_t subs = a.single ? a.group : (a.group >> 1);  // work items per kv head for one 128-token pair
     w.g = hsel / subs;
     const int32_t tpt = kBlockM >> a.lg;
-    w.tr0.tok0 = m * kBlockM + (hsel - w.g * subs) * 2 * tpt;
+    w.tr0.tok0 = m * kBlockM + (hsel - w.g * subs) * (a.single ? 1 : 2) * tpt;
     w.tr1.tok0 = w.tr0.tok0 + tpt;
     w.tr0.head0 = w.tr1.head0 = w.g * a.group;
     w.tr0.lg = w.tr1.lg = a.lg;
     w.tr0.rows_valid = min(kBlockM, max(0, n - w.tr0.tok0) << a.lg);
     w.tr1.rows_valid = min(kBlockM, max(0, n - w.tr1.tok0) << a.lg);
-    w.two = w.tr1.rows_valid > 0;
+    w.two = !a.single && w.tr1.rows_valid > 0;
   } else {
-    w.two = (a.group & 1) == 0;
+    w.two = !a.single && (a.group & 1) == 0;
     const int32_t h0 = w.two ? 2 * hsel : hsel;
     w.g = h0 / a.group;
     w.tr0.tok0 = w.tr1.tok0 = m * kBlockM;
@@ -1012,6 +1017,9 @@ cudaError_t launch_attention(const AttnArgs &args, int grid, cudaStream_t stream
   return cudaLaunchKernelEx(&cfg, attn_fwd_kernel<D>, args);
 }
 
+// Work-item shape of every attention call of the process (unip_set_attention_schedule).
+std::atomic<int> g_attention_schedule{UNIP_ATTN_SCHEDULE_AUTO};
+
 int32_t max_pairs_for(int32_t total_tokens, int32_t num_segs) {
   return (total_tokens + kBlockM - 1) / kBlockM + num_segs;
 }
@@ -1022,6 +1030,13 @@ int32_t max_pairs_for(int32_t total_tokens, int32_t num_segs) {
 using namespace unip;
 
 extern "C" {
+
+UNIP_API int32_t unip_set_attention_schedule(int32_t mode) {
+  if (mode != UNIP_ATTN_SCHEDULE_AUTO && mode != UNIP_ATTN_SCHEDULE_PAIRED && mode != UNIP_ATTN_SCHEDULE_SINGLE)
+    return UNIP_ERR_INVALID_ARGUMENT;
+  g_attention_schedule.store(mode, std::memory_order_relaxed);
+  return UNIP_OK;
+}
 
 UNIP_API size_t unip_attention_workspace_size(int32_t total_tokens, int32_t num_segs, const unip_attn_params *prm) {
   (void)prm;
@@ -1120,7 +1135,18 @@ static int32_t attention_entry(const void *q, const void *k, const void *v, cons
   args.Hq = Hq;
   args.group = G;
   args.lg = lg;
-  args.heads_per_pair = (args.group % 2 == 0) ? Hq / 2 : Hq;
+  // Two query tiles per work item when the group is even, unless even twice the
+  // most items the call can hold leave SMs idle: then one tile per item.
+  // Query tiles: sum over segments of ceil(n_s / 128) <= ceil(N / 128) + S - 1.
+  const int sms = device_sm_count();
+  const bool even = G % 2 == 0;
+  const int64_t tiles_hi = (int64_t)(total_tokens + kBlockM - 1) / kBlockM + (num_segs > 0 ? num_segs - 1 : 0);
+  const int mode = g_attention_schedule.load(std::memory_order_relaxed);
+  args.single = !even ? 0
+                : mode == UNIP_ATTN_SCHEDULE_SINGLE ? 1
+                : mode == UNIP_ATTN_SCHEDULE_PAIRED ? 0
+                : (2 * tiles_hi * (Hq / 2) <= (int64_t)(sms > 0 ? sms : 1) ? 1 : 0);
+  args.heads_per_pair = (even && !args.single) ? Hq / 2 : Hq;
   args.num_pages = has_cache ? paged->num_pages : 0;
   args.page_size = has_cache ? paged->page_size : 16;
   args.max_pages = has_cache ? paged->max_pages_per_seq : 0;
@@ -1129,7 +1155,6 @@ static int32_t attention_entry(const void *q, const void *k, const void *v, cons
   // persistent grid: one CTA per SM (fewer when the plan cannot hold that many work items)
   const int64_t units_bound = (int64_t)max_pairs * args.heads_per_pair;
   if (units_bound > 0x7FFFFFFF) return UNIP_ERR_UNSUPPORTED;
-  const int sms = device_sm_count();
   const int64_t grid = std::min<int64_t>(units_bound, sms > 0 ? sms : 1);
   const cudaError_t e = D == 128 ? launch_attention<128>(args, (int)grid, st) : launch_attention<64>(args, (int)grid, st);
   return e == cudaSuccess ? UNIP_OK : UNIP_ERR_CUDA;

@@ -72,3 +72,10 @@ def test_rope_host_checks_before_launch():
                                    10000.0, 0, None, None, None, 0, 16, None) == -5     # misaligned k
     assert lib.unip_rope_append_kv(None, None, None, None, 0, ctypes.byref(prm),
                                    10000.0, 0, None, None, None, 0, 16, None) == 0      # nothing to do
+
+
+def test_attention_schedule_modes():
+    lib = binding.load()
+    assert lib.unip_set_attention_schedule(7) == -1
+    for m in (1, 2, 0):
+        assert lib.unip_set_attention_schedule(m) == 0

@@ -125,6 +125,33 @@ def test_many_segments_with_prefixes(hq, hkv, page, d, seed):
     _check(wl, sample_rows(wl, 300))
 
 
+@pytest.mark.parametrize("make", [
+    lambda: W.packed([0, 300, 0, 5], 8, 2, 128, seed=313),                 # (token, head) rows, G 4
+    lambda: W.packed([1000], 8, 1, 64, seed=1073),                          # G 8
+    lambda: W.packed([5, 70, 131], 12, 2, 64, seed=282),                    # even G 6 that does not divide 128
+    lambda: _chunk_with_prefix(513, 512, 4, 2, 128, 16, seed=1025),         # chunk behind a paged prefix
+    lambda: _batch_with_prefixes([1000, 17, 300, 2048, 5, 64, 129, 0], [1, 1, 2, 5, 33, 65, 1, 3],
+                                 32, 8, 128, 16, seed=3328),                # decode tokens and short chunks
+], ids=["g4", "g8", "g6", "chunk", "decode_batch"])
+def test_paired_and_single_items_agree(make):
+    """Two-tile and one-tile work items visit every row's keys in the same order, so the
+    outputs are bit-identical; one of them is also checked against the oracle."""
+    from sparsified_long_context_gb300 import binding as B
+    wl = make()
+    res = {}
+    try:
+        for mode in (B.UNIP_ATTN_SCHEDULE_PAIRED, B.UNIP_ATTN_SCHEDULE_SINGLE):
+            B.unip_set_attention_schedule(mode)
+            res[mode] = _run(wl)
+    finally:
+        B.unip_set_attention_schedule(B.UNIP_ATTN_SCHEDULE_AUTO)
+    (o1, l1), (o2, l2) = res[B.UNIP_ATTN_SCHEDULE_PAIRED], res[B.UNIP_ATTN_SCHEDULE_SINGLE]
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+    ref_o, ref_l = oracle_attention_rows(wl, None)
+    assert_close(o2, ref_o, what=f"{wl.name} out (one-tile items)")
+    assert_close(l2.T, ref_l, max_abs=LSE_ABS, mean_abs=LSE_ABS, what=f"{wl.name} lse (one-tile items)")
+
+
 def test_chunked_equals_one_shot():
     one, chunks = W.chunked()
     outs = []
