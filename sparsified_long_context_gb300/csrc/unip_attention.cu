@@ -295,23 +295,6 @@ __device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, u
       : "memory");
 }
 
-// (d0, d1) = (a0, a1) * (b0, b1) + (c0, c1) in one packed instruction.
-__device__ __forceinline__ void ffma2(float &d0, float &d1, float a0, float a1, float b0, float b1, float c0,
-                                      float c1) {
-  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
-      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
-      "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
-      : "=f"(d0), "=f"(d1)
-      : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
-}
-// (d0, d1) += (a0, a1) in one packed instruction.
-__device__ __forceinline__ void fadd2_acc(float &d0, float &d1, float a0, float a1) {
-  asm("{\n\t.reg .b64 ra, rd;\n\t"
-      "mov.b64 ra, {%2, %3};\n\tmov.b64 rd, {%0, %1};\n\t"
-      "add.f32x2 rd, rd, ra;\n\tmov.b64 {%0, %1}, rd;\n\t}"
-      : "+f"(d0), "+f"(d1)
-      : "f"(a0), "f"(a1));
-}
 
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float r;

@@ -44,6 +44,8 @@ __global__ void __launch_bounds__(kPlanThreads) imp_plan_kernel(const int32_t *_
   __shared__ int32_t s_scan[32];
   __shared__ uint32_t s_err;
   const int tid = threadIdx.x;
+  // the score grid may be scheduled now; it waits for this plan before reading it
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int per = (S + kPlanThreads - 1) / kPlanThreads;
   const int s0 = min(S, tid * per), s1 = min(S, s0 + per);
   if (tid == 0) s_err = (cu[0] != 0 || cu[S] != N) ? UNIP_DEV_BAD_SEQLENS : 0u;
@@ -141,15 +143,20 @@ __global__ void __launch_bounds__(kScoreThreadsTc, 1) imp_score_tc_kernel(const 
   __shared__ __align__(8) uint64_t bars[kSbNum];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
-  __shared__ float s_lse[kMaxCols];
+  __shared__ __align__(16) float s_lse[kMaxCols];
   __shared__ float s_key[128];
   __shared__ float s_red[4];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
+  // launched as a programmatic dependent of the planner: its work list is complete after this
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int32_t n_items = *a.num_items;
   const int64_t U = (int64_t)n_items * a.Hkv;
   const int64_t u0 = U * blockIdx.x / gridDim.x, u1 = U * (blockIdx.x + 1) / gridDim.x;
-  if (u0 >= u1) return;  // uniform over the CTA
+  if (u0 >= u1) {  // uniform over the CTA
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    return;
+  }
   const int32_t B = a.B;
   const int32_t group = a.Hq / a.Hkv;
   const int32_t hpg = a.heads_per_group;     // heads per MMA group
@@ -313,6 +320,9 @@ __global__ void __launch_bounds__(kScoreThreadsTc, 1) imp_score_tc_kernel(const 
       live = live && mbar_wait(bar(kSbSFull0 + slot), (i >> 1) & 1, abort_flag, a.status);
       const int32_t j = it.c * 128 + key;
       const bool kvalid = j < n;
+      // Every key of the chunk lies in the segment and before the window's first row: all columns
+      // are visible (window slots past the segment carry an infinite normaliser and give 0).
+      const bool open_chunk = it.c * 128 + 127 < n && it.c * 128 + 127 <= wrow0;
       if (live) {
         tc_fence_after();
         // this warp's columns: [128 ch, 128 ch + 128) of the group's hn * B (a multiple of 16)
@@ -321,6 +331,19 @@ __global__ void __launch_bounds__(kScoreThreadsTc, 1) imp_score_tc_kernel(const 
           tmem_ld32(tl + slot * kMaxCols + col0, sv);
           tmem_ld32(tl + slot * kMaxCols + col0 + 32, sv + 32);
           tmem_wait_ld();
+          if (open_chunk && col0 + 64 <= ncols) {
+            // no masks: packed (s * c - lse) pairs, four normalisers per shared-memory load
+#pragma unroll
+            for (int x = 0; x < 64; x += 4) {
+              const float4 l4 = *reinterpret_cast<const float4 *>(&s_lse[col0 + x]);
+              float y0, y1, y2, y3;
+              ffma2(y0, y1, sv[x], sv[x + 1], a.scale_log2, a.scale_log2, -l4.x, -l4.y);
+              ffma2(y2, y3, sv[x + 2], sv[x + 3], a.scale_log2, a.scale_log2, -l4.z, -l4.w);
+              fadd2_acc(acc0, acc1, ex2_approx(y0), ex2_approx(y1));
+              fadd2_acc(acc2, acc3, ex2_approx(y2), ex2_approx(y3));
+            }
+            continue;
+          }
 #pragma unroll
           for (int x = 0; x < 64; x += 4) {
             float e[4];
@@ -374,6 +397,8 @@ __global__ void __launch_bounds__(kScoreThreadsTc, 1) imp_score_tc_kernel(const 
   }
   tc_fence_before();
   __syncthreads();
+  // the normaliser may be scheduled now; it waits for every score CTA before reading the masses
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (warp == kScoreWarpMma) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
@@ -386,6 +411,8 @@ __global__ void __launch_bounds__(kNormThreads) imp_norm_kernel(const int32_t *_
   __shared__ float sred[kNormThreads];
   // a Top-p grid launched as a programmatic dependent may be scheduled now; it waits for this one
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // launched as a programmatic dependent of the score grid: its masses are complete after this
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int32_t s = blockIdx.x;
   const int32_t b0 = blk_cu[s], nb = blk_cu[s + 1] - b0;
   if (nb <= 0) return;
@@ -422,8 +449,32 @@ cudaError_t launch_score(const ScoreArgs &args, int grid, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
-  imp_score_tc_kernel<D><<<grid, kScoreThreadsTc, L::kDynamic, stream>>>(args);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kScoreThreadsTc);
+  cfg.dynamicSmemBytes = L::kDynamic;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // may start while the planner runs
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, imp_score_tc_kernel<D>, args);
+}
+
+cudaError_t launch_norm(const int32_t *blk_cu, const float *partial, int32_t Hkv, float *imp, int32_t num_segs,
+                        cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)num_segs);
+  cfg.blockDim = dim3(kNormThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // may start while the score grid drains
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, imp_norm_kernel, blk_cu, partial, Hkv, imp);
 }
 
 int32_t max_items_for(int32_t total_tokens, int32_t num_segs) {
@@ -519,8 +570,7 @@ UNIP_API int32_t unip_block_importance(const void *q, const void *k, const float
   args.scale_log2 = scale * kLog2e;
   cudaError_t e = D == 128 ? launch_score<128>(args, (int)grid, st) : launch_score<64>(args, (int)grid, st);
   if (e != cudaSuccess) return UNIP_ERR_CUDA;
-  imp_norm_kernel<<<num_segs, kNormThreads, 0, st>>>(blk_cu, partial, Hkv, imp);
-  if (cudaGetLastError() != cudaSuccess) return UNIP_ERR_CUDA;
+  if (launch_norm(blk_cu, partial, Hkv, imp, num_segs, st) != cudaSuccess) return UNIP_ERR_CUDA;
   return UNIP_OK;
 }
 
