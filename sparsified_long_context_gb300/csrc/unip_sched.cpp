@@ -174,6 +174,11 @@ struct unip_step_builder {
   std::vector<Request> requests;    // indexed by request id
   std::deque<int32_t> active;       // unfinished request ids in arrival order
   std::vector<int32_t> release;     // ids finished by the last step; pages freed at the next one
+  struct Seg {
+    int32_t id, start, len;
+    bool prefill;
+  };
+  std::vector<Seg> segs;            // the step being built (capacity max_seqs)
 };
 
 extern "C" UNIP_API int32_t unip_step_builder_create(int32_t token_budget, int32_t page_size, int32_t num_pages,
@@ -198,6 +203,11 @@ extern "C" UNIP_API int32_t unip_step_builder_create(int32_t token_budget, int32
     sb->chunk_multiple = chunk_multiple;
     sb->free_pages.resize(num_pages);
     for (int32_t i = 0; i < num_pages; ++i) sb->free_pages[i] = num_pages - 1 - i;  // page 0 on top
+    // A step never holds more than max_seqs segments or finishes more requests than that, and
+    // freed pages never exceed the cache: with this room reserved, building a step allocates
+    // nothing once it has started changing the state.
+    sb->release.reserve(max_seqs);
+    sb->segs.reserve(max_seqs);
   } catch (const std::bad_alloc &) {
     delete sb;
     return UNIP_ERR_TOO_LARGE;
@@ -219,6 +229,7 @@ extern "C" UNIP_API int32_t unip_step_builder_add(unip_step_builder *sb, int32_t
   try {
     const int32_t id = static_cast<int32_t>(sb->requests.size());
     sb->requests.push_back(Request{prompt_len, max_new_tokens, 0, 0, {}});
+    sb->requests.back().pages.reserve(static_cast<size_t>(pages));  // grows without allocating later
     sb->active.push_back(id);
     if (request_id) *request_id = id;
   } catch (const std::bad_alloc &) {
@@ -261,11 +272,9 @@ extern "C" UNIP_API int32_t unip_step_builder_next(unip_step_builder *sb, const 
   }
   sb->release.clear();
 
-  struct Seg {
-    int32_t id, start, len;
-    bool prefill;
-  };
-  std::vector<Seg> segs;
+  using Seg = unip_step_builder::Seg;
+  std::vector<Seg> &segs = sb->segs;
+  segs.clear();
   int32_t budget_left = sb->token_budget;
 
   // Decodes first, one token each, in arrival order.  A decode whose token
@@ -346,12 +355,12 @@ extern "C" UNIP_API int32_t unip_step_builder_next(unip_step_builder *sb, const 
     }
   }
   if (n_fin > 0) {
-    std::deque<int32_t> keep;
-    for (int32_t id : sb->active) {
-      const Request &r = sb->requests[id];
-      if (!(r.computed >= r.prompt_len && r.generated == r.max_new_tokens)) keep.push_back(id);
-    }
-    sb->active.swap(keep);
+    sb->active.erase(std::remove_if(sb->active.begin(), sb->active.end(),
+                                    [&](int32_t id) {
+                                      const Request &r = sb->requests[id];
+                                      return r.computed >= r.prompt_len && r.generated == r.max_new_tokens;
+                                    }),
+                     sb->active.end());
   }
   counts->num_segs = static_cast<int32_t>(segs.size());
   counts->num_tokens = n_tok;
