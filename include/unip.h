@@ -319,7 +319,7 @@ UNIP_API int32_t unip_select_gather(const float *imp, const int32_t *blk_cu, con
  *                 UNIP_DEV_BAD_INDEX and skips it
  * Every pointer is 16-byte aligned device memory; asynchronous on `stream`.
  * Errors: INVALID_ARGUMENT (NULL where needed, negative sizes, interleaved
- * not 0/1, NaN theta), UNSUPPORTED (D), ALIGNMENT. */
+ * not 0/1, NaN or infinite theta), UNSUPPORTED (D), ALIGNMENT. */
 UNIP_API int32_t unip_rope_append_kv(void *q, void *k, const void *v, const int32_t *positions, int32_t num_tokens,
                                      const unip_attn_params *prm, double rope_theta, int32_t interleaved,
                                      const int32_t *slot_mapping, void *k_cache, void *v_cache, int32_t num_pages,

@@ -31,6 +31,8 @@
 // bits become a single-precision argument of sincospif.  The only errors are
 // F_i's double-precision rounding (below 3e-16 relative, ~6e-7 rad at
 // position 2^31, ~1e-9 rad at 2^22) and the 24-bit argument (2e-7 rad).
+#include <cmath>
+
 #include "unip_internal.cuh"
 
 namespace unip {
@@ -112,7 +114,7 @@ __global__ void __launch_bounds__(kRopeThreads, 3) rope_append_kernel(RopeArgs a
   if (a.rotate)
     for (int i = threadIdx.x; i < half; i += kRopeThreads) {
       double turns = exp2(-(2.0 * i / a.D) * a.log2_theta) / kTwoPi;   // < 1/(2 pi) when theta >= 1
-      turns -= floor(turns);                                            // whole turns do not matter
+      turns = fmod(turns, 1.0);                                         // whole turns do not matter
       s_turn[i] = (uint64_t)(turns * 18446744073709551616.0);          // * 2^64
     }
   const int per_q = a.Hq * ur, per_k = a.Hkv * ur, per_v = a.Hkv * vr;
@@ -212,7 +214,7 @@ UNIP_API int32_t unip_rope_append_kv(void *q, void *k, const void *v, const int3
   if (d < 16 || d > 2 * kRopeMaxHalf || d % 16) return UNIP_ERR_UNSUPPORTED;
   const bool rotate = rope_theta > 0.0;
   const bool append = slot_mapping != nullptr;
-  if (!(rope_theta == rope_theta)) return UNIP_ERR_INVALID_ARGUMENT;  // NaN
+  if (!std::isfinite(rope_theta)) return UNIP_ERR_INVALID_ARGUMENT;  // NaN or infinite base
   if (num_tokens == 0 || (!rotate && !append)) return UNIP_OK;
   if (!k || (rotate && !positions)) return UNIP_ERR_INVALID_ARGUMENT;
   if (append && (!v || !k_cache || !v_cache || num_pages < 0 || page_size <= 0)) return UNIP_ERR_INVALID_ARGUMENT;

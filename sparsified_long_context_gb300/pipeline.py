@@ -187,6 +187,8 @@ class StreamedSteps:
         n_kept of every step; on_result(i, out_host, hidden_rows_host, n_kept) is
         called once step i's downloads have landed (before its buffers are reused)."""
         import torch
+        if steps < 0 or (steps > 0 and not batches):
+            raise ValueError("StreamedSteps.run needs at least one batch and steps >= 0")
         ev = [[torch.cuda.Event() for _ in range(4)] for _ in range(2)]  # uploaded, computed, nk, downloaded
         n_kept = [0] * steps
         used = [None, None]   # step whose results a set holds

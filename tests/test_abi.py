@@ -72,6 +72,9 @@ def test_rope_host_checks_before_launch():
                                    10000.0, 0, None, None, None, 0, 16, None) == -5     # misaligned k
     assert lib.unip_rope_append_kv(None, None, None, None, 0, ctypes.byref(prm),
                                    10000.0, 0, None, None, None, 0, 16, None) == 0      # nothing to do
+    for bad in (float("inf"), float("nan")):
+        assert lib.unip_rope_append_kv(None, ctypes.c_void_p(16), None, ctypes.c_void_p(16), 10, ctypes.byref(prm),
+                                       bad, 0, None, None, None, 0, 16, None) == -1
 
 
 def test_attention_schedule_modes():
