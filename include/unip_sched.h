@@ -95,9 +95,10 @@ typedef struct unip_step_counts {
  *   max_pages_per_seq   block-table width (> 0)
  *   max_seqs            most segments in one step (> 0)
  *   chunk_multiple      a chunk that does not finish its prompt ends on a
- *                       multiple of this absolute position (1 = any); with
- *                       the selection block size here, the blocks of every
- *                       chunk line up with the prompt's own blocks
+ *                       multiple of this absolute position (1 = any, at most
+ *                       token_budget); with the selection block size here,
+ *                       the blocks of every chunk line up with the prompt's
+ *                       own blocks
  *   out                 out: the new builder (NULL on error)
  * Errors: INVALID_ARGUMENT for a value out of range, TOO_LARGE when page
  * counts overflow int32 slot numbers or memory runs out. */

@@ -186,8 +186,10 @@ extern "C" UNIP_API int32_t unip_step_builder_create(int32_t token_budget, int32
                                                      int32_t chunk_multiple, unip_step_builder **out) {
   if (!out) return UNIP_ERR_INVALID_ARGUMENT;
   *out = nullptr;
+  // A chunk that stops short of its prompt ends on a multiple of chunk_multiple; with a multiple
+  // above the budget no such chunk fits and a prompt longer than the budget would never start.
   if (token_budget <= 0 || page_size <= 0 || num_pages < 0 || max_pages_per_seq <= 0 || max_seqs <= 0 ||
-      chunk_multiple <= 0)
+      chunk_multiple <= 0 || chunk_multiple > token_budget)
     return UNIP_ERR_INVALID_ARGUMENT;
   if (static_cast<int64_t>(max_pages_per_seq) * page_size > INT32_MAX ||
       static_cast<int64_t>(num_pages) * page_size > INT32_MAX)

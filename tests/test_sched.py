@@ -207,6 +207,8 @@ def test_step_builder_rejects_bad_arguments():
         binding.StepBuilder(0, 16, 10, 4, 4)
     with pytest.raises(binding.UnipError):
         binding.StepBuilder(8, 16, 10, 4, 4, 0)
+    with pytest.raises(binding.UnipError):
+        binding.StepBuilder(8, 16, 10, 4, 4, 16)            # no partial chunk could ever fit the budget
     sb = binding.StepBuilder(8, 16, 10, 4, 4)
     with pytest.raises(binding.UnipError):
         sb.add(0, 1)
