@@ -137,7 +137,7 @@ def test_step_builder_matches_oracle(seed):
     rng = np.random.default_rng(1000 + seed)
     page = int(rng.choice([1, 2, 4, 16]))
     budget = int(rng.integers(1, 48))
-    mult = int(rng.choice([1, 2, 4, 8]))
+    mult = int(rng.choice([m for m in (1, 2, 4, 8) if m <= budget]))
     max_seqs = int(rng.integers(1, 10))
     reqs = [(int(rng.integers(1, 80)), int(rng.integers(1, 7))) for _ in range(int(rng.integers(1, 16)))]
     need = [-(-(L + m - 1) // page) for (L, m) in reqs]
