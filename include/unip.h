@@ -152,6 +152,8 @@ UNIP_API int32_t unip_set_attention_schedule(int32_t mode);
 UNIP_API size_t unip_attention_workspace_size(int32_t total_tokens, int32_t num_segs,
                                               const unip_attn_params *prm);
 
+/* The attention above over a packed / chunked stream.  Returns UNIP_OK, or a
+ * host error code with nothing enqueued. */
 UNIP_API int32_t unip_prefill_attention(const void *q, const void *k, const void *v,
                                         const int32_t *cu_seqlens, int32_t num_segs,
                                         const int32_t *positions, int32_t total_tokens,
@@ -231,9 +233,13 @@ UNIP_API int32_t unip_prefill_attention_noalloc(const void *q, const void *k, co
  * ------------------------------------------------------------------------- */
 UNIP_API int32_t unip_importance_capacity(int32_t total_tokens, int32_t num_segs, int32_t block_size);
 
+/* Bytes of device workspace unip_block_importance needs (work list and
+ * per-kv-head partial masses); 0 for invalid arguments. */
 UNIP_API size_t unip_importance_workspace_size(int32_t total_tokens, int32_t num_segs,
                                                int32_t block_size, const unip_attn_params *prm);
 
+/* The importance above.  Returns UNIP_OK, or a host error code with nothing
+ * enqueued; bad cu_seqlens raise UNIP_DEV_BAD_SEQLENS. */
 UNIP_API int32_t unip_block_importance(const void *q, const void *k, const float *lse,
                                        const int32_t *cu_seqlens, int32_t num_segs,
                                        int32_t total_tokens, const uint8_t *seg_mask,
@@ -257,6 +263,8 @@ UNIP_API int32_t unip_block_importance(const void *q, const void *k, const float
  * ------------------------------------------------------------------------- */
 UNIP_API size_t unip_topp_workspace_size(int32_t total_tokens, int32_t num_segs, int32_t block_size);
 
+/* The selection above.  Returns UNIP_OK, or a host error code with nothing
+ * enqueued; invalid scores raise UNIP_DEV_BAD_SCORES. */
 UNIP_API int32_t unip_topp_select(const float *imp, const int32_t *blk_cu,
                                   const int32_t *cu_seqlens, const int32_t *positions,
                                   int32_t num_segs, int32_t total_tokens, int32_t block_size,
