@@ -27,7 +27,8 @@ def _plain(wl):
     m = int(bufs.n_kept.item())
     st = B.unip_get_device_status(clear=True)
     assert st == 0, B.describe_status(st)
-    return bufs.out.cpu().clone(), m, bufs.hidden_out[:m].cpu().clone()
+    hid = None if bufs.hidden_out is None else bufs.hidden_out[:m].cpu().clone()
+    return bufs.out.cpu().clone(), m, hid
 
 
 @pytest.mark.parametrize("steps", [1, 2, 7])
@@ -59,3 +60,30 @@ def test_streamed_steps_match_plain_steps(steps):
         assert m == r_m == kept[i], (i, m, r_m, kept[i])
         assert torch.equal(out.view(torch.int16), r_out.view(torch.int16)), f"step {i}: attention output differs"
         assert torch.equal(hid.view(torch.int16), r_hid.view(torch.int16)), f"step {i}: hidden rows differ"
+
+
+def test_streamed_chunks_behind_a_paged_prefix():
+    """Chunked-prefill batches (512 tokens behind 1536 and 2560 cached tokens of one paged cache, which
+    both device sets share and which is not re-uploaded) alternate through StreamedSteps; every step's
+    attention output and compaction equal a plain step on the same chunk."""
+    from sparsified_long_context_gb300 import binding as B
+    from sparsified_long_context_gb300.pipeline import DeviceInputs, StepBuffers, StreamedSteps
+    _, chunks = W.chunked()
+    wls = [dataclasses.replace(chunks[c], block_size=64, top_p=0.9, seg_mask=np.ones(1, np.uint8))
+           for c in (3, 5)]
+    ref = [_plain(w) for w in wls]
+    di = DeviceInputs.from_workload(wls[0], "cuda")
+    di2 = dataclasses.replace(di, **{f: getattr(di, f).clone() for f in StreamedSteps.FIELDS
+                                     if getattr(di, f) is not None})
+    streamer = StreamedSteps([(di, StepBuffers(di)), (di2, StepBuffers(di2))])
+    di_b = DeviceInputs.from_workload(wls[1], "cuda")
+    batches = [streamer.host_batch(di), streamer.host_batch(di_b)]
+    seen = {}
+    kept = streamer.run(batches, 5, lambda i, o, h, m: seen.__setitem__(i, (o.clone(), m)))
+    st = B.unip_get_device_status(clear=True)
+    assert st == 0, B.describe_status(st)
+    for i in range(5):
+        out, m = seen[i]
+        r_out, r_m, _ = ref[i % 2]
+        assert m == r_m == kept[i]
+        assert torch.equal(out.view(torch.int16), r_out.view(torch.int16)), f"step {i}"

@@ -70,6 +70,7 @@ CASES = [
     ("chunk_continuation", [513], 16, 16, 128, 10000.0, False, "offset"),
     ("narrow_heads", [9], 2, 1, 16, 10000.0, False, "restart"),
     ("wide_heads", [40], 2, 2, 256, 1000000.0, True, "random"),
+    ("negative_positions_inter", [300], 8, 2, 64, 10000.0, True, "signed"),
 ]
 
 
@@ -82,6 +83,8 @@ def test_rope_and_append_match_oracle(name, lengths, hq, hkv, d, theta, inter, p
         positions = np.concatenate([np.arange(L) for L in lengths]).astype(np.int32)
     elif poskind == "offset":
         positions = (np.arange(n) + (1 << 20) + 12345).astype(np.int32)
+    elif poskind == "signed":
+        positions = rng.integers(-(1 << 21), 1 << 21, n).astype(np.int32)   # the rotation is defined for any integer
     else:
         positions = rng.integers(0, 1 << 22, n).astype(np.int32)
     q = W._normal_bf16(rng, (n, hq, d))

@@ -282,3 +282,54 @@ def test_single_unscored_segment_keeps_everything():
     assert Bd.unip_get_device_status(clear=True) == 0
     assert int(nk.item()) == L and ck.cpu().tolist() == [0, L]
     assert np.array_equal(gi.cpu().numpy(), np.arange(L)) and np.array_equal(pk.cpu().numpy(), np.arange(L))
+
+
+@pytest.mark.parametrize("S", [11999, 12500])
+def test_select_gather_many_segments(S):
+    """unip_select_gather on either side of the segment count where the kept-token offsets stop fitting
+    in shared memory (12000: the call switches to Top-p + index + gather as separate grids): masks,
+    indices, kept offsets, kept positions and gathered rows bit-exact against the oracle."""
+    from sparsified_long_context_gb300 import binding as Bd
+    rng = np.random.default_rng(S)
+    B_, d = 16, 64
+    lengths = rng.integers(0, 120, S)
+    lengths[rng.random(S) < 0.05] = 1
+    scored = rng.random(S) > 0.1                       # some segments are not scored (decode-like)
+    nbs = np.where(scored & (lengths > 0), -(-lengths // B_), 0)
+    cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+    bc = np.concatenate([[0], np.cumsum(nbs)]).astype(np.int32)
+    parts = []
+    for nb in nbs:
+        if nb:
+            x = rng.random(nb) ** 3
+            parts.append((x / x.sum()).astype(np.float32))
+    imp = np.concatenate(parts).astype(np.float32)
+    n = int(cu[-1])
+    pos = np.concatenate([np.arange(L) + (7 if s % 3 == 0 else 0) for s, L in enumerate(lengths)]).astype(np.int32)
+    hid = W.f32_to_bf16_bits(rng.standard_normal((n, d), dtype=np.float32))
+    dev = "cuda"
+    cap = Bd.unip_importance_capacity(n, S, B_)
+    imp_t = torch.zeros(cap, dtype=torch.float32, device=dev)
+    imp_t[: len(imp)] = torch.from_numpy(imp)
+    keep = torch.full((cap,), 7, dtype=torch.uint8, device=dev)
+    gi = torch.full((n,), -1, dtype=torch.int32, device=dev)
+    pk = torch.full((n,), -1, dtype=torch.int32, device=dev)
+    ck = torch.empty(S + 1, dtype=torch.int32, device=dev)
+    nk = torch.empty(1, dtype=torch.int32, device=dev)
+    h_t = torch.from_numpy(hid).view(torch.bfloat16).to(dev)
+    out = torch.zeros_like(h_t)
+    Bd.unip_get_device_status(clear=True)
+    Bd.unip_select_gather(imp_t, torch.from_numpy(bc).to(dev), torch.from_numpy(cu).to(dev),
+                          torch.from_numpy(pos).to(dev), keep, gi, ck, pk, nk, h_t, out, block_size=B_, p=0.9)
+    torch.cuda.synchronize()
+    st = Bd.unip_get_device_status(clear=True)
+    assert st == 0, Bd.describe_status(st)
+    ref = oracle.topp_select(imp, bc, 0.9)
+    assert np.array_equal(keep[: len(imp)].cpu().numpy(), ref)
+    rgi, rck, rpk, rm = oracle.index_build(ref, bc, cu, pos, B_)
+    m = int(nk.item())
+    assert m == rm
+    assert np.array_equal(gi[:m].cpu().numpy(), rgi) and np.array_equal(ck.cpu().numpy(), rck)
+    assert np.array_equal(pk[:m].cpu().numpy(), rpk)
+    got = out[:m].view(torch.int16).cpu().numpy().view(np.uint16)
+    assert np.array_equal(got, oracle.gather(hid, rgi))
