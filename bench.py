@@ -48,6 +48,38 @@ def useful_attention_flops(wl) -> float:
     return 4.0 * wl.head_dim * wl.num_heads_q * pairs
 
 
+def workload_context(wl, attn_ms: float, bf16_peak: float, hbm_peak: float):
+    """Per-workload bounds beside the attention time.
+
+    Continuous-batching step: the prefill chunks are tensor-bound and the decode tokens HBM-bound
+    (their cached K/V), so its roofline time is F_prefill / bf16 peak + decode K/V bytes / HBM peak.
+    Packed batch: the FLOPs that padding every prompt to the longest, or every bin to its capacity
+    (one causal sequence per bin, no block-diagonal mask), would have cost; Prepacking's context."""
+    n = wl.seq_lens.astype(np.float64)
+    P = wl.prefix_lens.astype(np.float64)
+    per = 4.0 * wl.head_dim * wl.num_heads_q * (n * P + n * (n + 1) / 2)
+    if wl.name == "mixed_step":
+        pre = wl.seg_mask.astype(bool)
+        f_pre = float(per[pre].sum())
+        kv_bytes = float(np.sum(P[~pre] + n[~pre]) * wl.num_heads_kv * wl.head_dim * 2 * 2)
+        t_roof = f_pre / (bf16_peak * 1e12) + kv_bytes / (hbm_peak * 1e9)
+        return {"prefill_flops": f_pre, "decode_kv_bytes": kv_bytes, "roofline_ms": t_roof * 1e3,
+                "attention_frac_of_roofline": t_roof * 1e3 / attn_ms,
+                "bound": "F_prefill / bf16 peak + decode K/V bytes / HBM peak"}
+    if wl.name == "prepacked":
+        lmax = float(n.max())
+        bins = wl.meta.get("bins", [])
+        cap = float(wl.meta.get("bin_tokens", 16384))
+        c = 4.0 * wl.head_dim * wl.num_heads_q
+        useful = float(per.sum())
+        pad_max = c * len(n) * lmax * (lmax + 1) / 2
+        pad_bin = c * len(bins) * cap * (cap + 1) / 2
+        return {"useful_flops": useful, "padded_to_max_flops": pad_max, "padded_to_bin_flops": pad_bin,
+                "useful_over_padded_to_max": useful / pad_max, "useful_over_padded_to_bin": useful / pad_bin,
+                "prompts": int(len(n)), "bins": int(len(bins)), "longest_prompt": int(lmax)}
+    return None
+
+
 def rows_flops(wl, rows) -> float:
     cu = wl.cu_seqlens
     P = wl.prefix_lens
@@ -489,6 +521,7 @@ def main():
             "select_gather_bytes": sg_bytes, "select_gather_gbs": sg_gbs,
             "select_gather_frac_hbm": sg_gbs / hbm_peak, "n_kept": n_kept, "n_blocks": n_blocks,
             "rope_append": rope,
+            "workload_context": workload_context(wl, attn_ms, bf16_peak, hbm_peak),
             "peaks": f"{peak_src}: bf16 {bf16_peak} TFLOP/s, HBM {hbm_peak} GB/s",
         },
         "roofline": {"bound": "tensor", "achieved": attn_tflops, "peak": bf16_peak, "unit": "TFLOP/s",
