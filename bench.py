@@ -233,6 +233,8 @@ def build_workload(name: str, rank: int, tokens: int = 32768):
         return W.prepacked(seed=3 + 1000 * rank)
     if name == "tiny_packed":
         return W.tiny_packed(seed=1 + 1000 * rank)
+    if name == "chunked":  # the one-shot prompt: the same useful (query, key) pairs as its eight chunks
+        return W.chunked(seed=2 + 1000 * rank)[0]
     raise SystemExit(f"unknown workload {name}")
 
 
@@ -371,6 +373,113 @@ def incremental_select_ms(di, bufs, flush, stream, reps: int = 10, trials: int =
     return max(d, 1e-6)
 
 
+def bench_chunked(args):
+    """Chunked prefill of one 4096-token prompt (H_q 32, H_kv 8, D 128) in eight 512-token attention
+    calls, chunk c behind the 512c-token prefix of the earlier chunks in a paged cache with shuffled
+    pages.  A step is the eight calls; the L2 is flushed before every call (outside the timed pairs of
+    events).  Reports each chunk and the total, and the one-shot call of the same prompt as context."""
+    import torch
+    from sparsified_long_context_gb300 import binding as B
+    from sparsified_long_context_gb300 import workloads as W
+    from sparsified_long_context_gb300.pipeline import DeviceInputs, StepBuffers, run_attention
+    world, rank, local = dist_setup(args)
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    B.load()
+    B.unip_get_device_status(clear=True)
+    dev = f"cuda:{local}"
+    one, chunks = W.chunked(seed=2 + 1000 * rank)
+    sets = []
+    for c in chunks:
+        di = DeviceInputs.from_workload(c, dev, with_hidden=False)
+        sets.append((di, StepBuffers(di, block_size=64)))
+    di1 = DeviceInputs.from_workload(one, dev, with_hidden=False)
+    b1 = StepBuffers(di1, block_size=64)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    flops = [useful_attention_flops(c) for c in chunks]
+
+    def step(evs=None):
+        for i, (di, bufs) in enumerate(sets):
+            flush.zero_()
+            if evs is not None:
+                evs[i][0].record(stream)
+            run_attention(di, bufs, stream)
+            if evs is not None:
+                evs[i][1].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    st = B.unip_get_device_status(clear=True)
+    if st:
+        raise SystemExit(f"device status after warm-up: {B.describe_status(st)}")
+    evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in sets] for _ in range(args.steps)]
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        wall0 = time.perf_counter()
+        for k in range(args.steps):
+            step(evs[k])
+        torch.cuda.synchronize()
+        wall1 = time.perf_counter()
+    if dist is not None:
+        dist.barrier()
+    st = B.unip_get_device_status(clear=True)
+    if st:
+        raise SystemExit(f"device status after timed steps: {B.describe_status(st)}")
+    per_ms = [statistics.mean(evs[k][i][0].elapsed_time(evs[k][i][1]) for k in range(args.steps))
+              for i in range(len(sets))]
+    total_ms = max_over_ranks(float(sum(per_ms)), dist, dev)
+    value = sum(flops) * world / (total_ms * 1e-3) / 1e12
+    # the one-shot call of the same prompt, as context
+    ts = []
+    for _ in range(args.warmup + args.steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        run_attention(di1, b1, stream)
+        e1.record(stream)
+        ts.append((e0, e1))
+    torch.cuda.synchronize()
+    one_ms = statistics.mean(a.elapsed_time(b) for a, b in ts[args.warmup:])
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return 0
+    peaks, peak_src = load_peaks()
+    bf16_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    per_gpu = value / world
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded, bf16 ~N(0,1))",
+        "config": {"workload": "chunked: one 4096-token prompt in 8 attention calls of 512 tokens behind "
+                               "paged prefixes of 0..3584 tokens (16-token pages, shuffled), H_q 32, H_kv 8, D 128",
+                   "l2": "flushed (256 MB write) before every call",
+                   "parallelism": f"replicas x{world} (independent prompts, no collective)",
+                   "useful_attention_flops_per_step": float(sum(flops))},
+        "parts": {"per_chunk": [{"prefix": int(c.prefix_lens[0]), "ms": m, "tflops": f / (m * 1e-3) / 1e12}
+                                for c, m, f in zip(chunks, per_ms, flops)],
+                  "one_shot_ms": one_ms, "one_shot_tflops": useful_attention_flops(one) / (one_ms * 1e-3) / 1e12},
+        "roofline": {"bound": "tensor", "achieved": per_gpu, "peak": bf16_peak, "unit": "TFLOP/s",
+                     "frac": per_gpu / bf16_peak, "traffic": None,
+                     "kernel": "attn_fwd_kernel<128> (+ its planner), eight calls",
+                     "peak_source": f"{peak_src} bf16_tflops (burst)"},
+        "cpu_baseline": None, "e2e": None,
+        "gpu_launches": 2 * len(sets) * args.steps,
+        "clocks": clk.summary(), "wall_s_timed_region": wall1 - wall0,
+    }
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -378,7 +487,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="unip", choices=["unip", "reference"])
     ap.add_argument("--workload", default="long_single",
-                    choices=["long_single", "mixed_step", "prepacked", "tiny_packed"])
+                    choices=["long_single", "mixed_step", "prepacked", "tiny_packed", "chunked"])
     ap.add_argument("--tokens", type=int, default=32768,
                     help="prompt length of the long_single workload (profiling runs use a shorter one)")
     ap.add_argument("--e2e-steps", type=int, default=20)
@@ -390,6 +499,8 @@ def main():
         args.warmup = 3
     if args.impl == "reference":
         return run_reference(args)
+    if args.workload == "chunked":
+        return bench_chunked(args)
 
     import torch
     from sparsified_long_context_gb300 import binding as B
