@@ -72,7 +72,8 @@ extern "C" {
 #define UNIP_ERR_WORKSPACE (-3)        /* workspace missing, too small or misaligned */
 #define UNIP_ERR_CUDA (-4)             /* CUDA runtime / launch failure */
 #define UNIP_ERR_ALIGNMENT (-5)        /* pointer or row stride not 16-byte aligned */
-#define UNIP_ERR_TOO_LARGE (-6)        /* problem exceeds the built-in scratch of unip_prefill_attention_noalloc */
+#define UNIP_ERR_TOO_LARGE (-6)        /* beyond the noalloc scratch, a step builder's page budget, int32
+                                          sizes or host memory */
 
 /* Device status bits (unip_get_device_status). */
 #define UNIP_DEV_BAD_SEQLENS 0x1u    /* cu_seqlens not monotone / ends wrong */

@@ -83,7 +83,7 @@ UNIP_API const char *unip_status_string(int32_t code) {
     case UNIP_ERR_WORKSPACE: return "workspace missing, too small or misaligned";
     case UNIP_ERR_CUDA: return "CUDA runtime or launch failure";
     case UNIP_ERR_ALIGNMENT: return "pointer or row stride not 16-byte aligned";
-    case UNIP_ERR_TOO_LARGE: return "problem exceeds the built-in scratch of the no-allocation entry point";
+    case UNIP_ERR_TOO_LARGE: return "problem too large (no-allocation scratch, page budget, int32 sizes or host memory)";
     default: return "unknown status";
   }
 }
