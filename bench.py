@@ -490,13 +490,16 @@ def main():
                     choices=["long_single", "mixed_step", "prepacked", "tiny_packed", "chunked"])
     ap.add_argument("--tokens", type=int, default=32768,
                     help="prompt length of the long_single workload (profiling runs use a shorter one)")
-    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--e2e-steps", type=int, default=None,
+                    help="steps of the end-to-end leg (default: --steps)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-step-seconds", type=float, default=6.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.e2e_steps is None:
+        args.e2e_steps = args.steps
     if args.impl == "reference":
         return run_reference(args)
     if args.workload == "chunked":
