@@ -8,6 +8,7 @@ at the first CUDA call).
 from __future__ import annotations
 
 import concurrent.futures as cf
+import fcntl
 import os
 import shutil
 import subprocess
@@ -51,10 +52,21 @@ def up_to_date() -> bool:
 
 
 def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
-    """Build libunip.so if missing or stale; returns its path."""
+    """Build libunip.so if missing or stale; returns its path.
+
+    Processes that build at the same time (the ranks of a multi-GPU run) take a file lock in turn;
+    a process that gets the lock after another one built finds the library up to date."""
     if not force and up_to_date():
         return LIB_PATH
     os.makedirs(OUT_DIR, exist_ok=True)
+    with open(os.path.join(OUT_DIR, ".build.lock"), "w") as lock:
+        fcntl.flock(lock, fcntl.LOCK_EX)
+        if not force and up_to_date():
+            return LIB_PATH
+        return _build_locked(verbose, extra_flags)
+
+
+def _build_locked(verbose: bool, extra_flags) -> str:
     nvcc = nvcc_path()
     flags = NVCC_FLAGS + list(extra_flags or [])
     objs = []
