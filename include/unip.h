@@ -120,6 +120,16 @@ UNIP_API const char *unip_status_string(int32_t code);
  * device), and clears it when clear != 0.  Returns UNIP_OK or UNIP_ERR_CUDA. */
 UNIP_API int32_t unip_get_device_status(uint32_t *bits, int32_t clear);
 
+/* Self-test of the bounded device waits (no page defines it; it checks the
+ * library's error path).  Launches one CTA whose two roles wait on mbarriers
+ * that nothing completes: the first gives up after limit_us microseconds
+ * (1 .. 1000000) and raises UNIP_DEV_TIMEOUT; the second, waiting with the
+ * kernels' own one-second limit, leaves as soon as it sees the first one's
+ * abort.  gave_up: device int32 [3], receives {1, 1, microseconds the second
+ * role waited}.  Nothing faults or hangs; the context stays usable.
+ * Errors: INVALID_ARGUMENT (NULL gave_up, limit out of range). */
+UNIP_API int32_t unip_selftest_bounded_wait(uint32_t limit_us, int32_t *gave_up, void *stream);
+
 /* Shape of the attention work items, process-wide (all devices, all later
  * calls of unip_prefill_attention, unip_compacted_attention and the noalloc
  * variant).  A work item is two 128-row query tiles that share every K/V tile

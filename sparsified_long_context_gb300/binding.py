@@ -107,6 +107,8 @@ def load(build_if_missing: bool = True):
                                            P, sz, P]
         lib.unip_gather_tokens.restype = i32
         lib.unip_gather_tokens.argtypes = [P, i32, i64, i32, P, P, i32, P, i64, P]
+        lib.unip_selftest_bounded_wait.restype = i32
+        lib.unip_selftest_bounded_wait.argtypes = [u32, P, P]
         lib.unip_set_attention_schedule.restype = i32
         lib.unip_set_attention_schedule.argtypes = [i32]
         lib.unip_rope_append_kv.restype = i32
@@ -175,6 +177,12 @@ def unip_get_device_status(clear: bool = True) -> int:
 
 def describe_status(bits: int) -> str:
     return ", ".join(v for k, v in DEV_STATUS_BITS.items() if bits & k) or "ok"
+
+
+def unip_selftest_bounded_wait(limit_us: int, gave_up, stream=None):
+    """Runs the bounded-wait self-test (gave_up: int32 CUDA tensor of 3 elements)."""
+    _check(load().unip_selftest_bounded_wait(int(limit_us), _ptr(gave_up), _stream(stream)),
+           "unip_selftest_bounded_wait")
 
 
 def unip_set_attention_schedule(mode: int):

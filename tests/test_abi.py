@@ -82,3 +82,10 @@ def test_attention_schedule_modes():
     assert lib.unip_set_attention_schedule(7) == -1
     for m in (1, 2, 0):
         assert lib.unip_set_attention_schedule(m) == 0
+
+
+def test_bounded_wait_selftest_checks_its_arguments():
+    lib = binding.load()
+    assert lib.unip_selftest_bounded_wait(0, ctypes.c_void_p(16), None) == -1         # limit 0
+    assert lib.unip_selftest_bounded_wait(2000000, ctypes.c_void_p(16), None) == -1   # above one second
+    assert lib.unip_selftest_bounded_wait(1000, None, None) == -1                      # no result buffer
