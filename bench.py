@@ -223,14 +223,21 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def build_workload(name: str, rank: int, tokens: int = 32768):
+def build_workload(name: str, rank: int, tokens: int = 32768, reference: bool = False):
+    """The workload's seeded inputs.  The prepacked batch is packed by the library's first-fit-decreasing
+    packer (unip_ffd_pack) on this project's arm and by the oracle's packer on the reference arm; the two
+    give the same order (tests/test_sched.py)."""
     from sparsified_long_context_gb300 import workloads as W
     if name == "long_single":
         return W.long_single(seed=4 + 1000 * rank, n=tokens)
     if name == "mixed_step":
         return W.mixed_step(seed=5 + 1000 * rank)
     if name == "prepacked":
-        return W.prepacked(seed=3 + 1000 * rank)
+        if reference:
+            from oracle.scheduling import ffd_order as pack
+        else:
+            from sparsified_long_context_gb300.binding import unip_ffd_pack as pack
+        return W.prepacked(pack, seed=3 + 1000 * rank)
     if name == "tiny_packed":
         return W.tiny_packed(seed=1 + 1000 * rank)
     if name == "chunked":  # the one-shot prompt: the same useful (query, key) pairs as its eight chunks
@@ -273,7 +280,7 @@ def run_reference(args):
     world, rank, _ = dist_setup(args)
     if rank != 0:
         return 0
-    wl = build_workload(args.workload, 0, args.tokens)
+    wl = build_workload(args.workload, 0, args.tokens, reference=True)
     cores = oracle.default_threads()
     rng = np.random.default_rng(123)
     # calibrate a per-step row sample of a few seconds

@@ -205,9 +205,8 @@ UNIP_API int32_t unip_compacted_attention(const void *q, const void *k, const vo
  * needs no workspace pointer.  It is meant for callers that cannot call
  * cudaMalloc or own a device allocator: a host that hands out only the
  * tensors it already owns (a plugin or custom-operator interface without an
- * allocator), code running inside CUDA stream capture, where allocation would
- * break the capture, or a latency-critical path that must not pay for an
- * allocation that may synchronise the device.
+ * allocator), or a latency-critical path that must not pay for an allocation
+ * that may synchronise the device.
  *
  * Limit: ceil(total_tokens / 128) + num_segs <= UNIP_NOALLOC_MAX_TILES;
  * larger problems return UNIP_ERR_TOO_LARGE without enqueuing anything.
@@ -215,6 +214,8 @@ UNIP_API int32_t unip_compacted_attention(const void *q, const void *k, const vo
  * loads the library, until the process exits.
  * The first call on a device looks up the array's device address (with that
  * device current); make that first call before any stream capture begins.
+ * The address is kept for the life of the process: after cudaDeviceReset on
+ * that device it is stale, and the entry point must not be called again.
  * Every call shares the one array per device: calls that may overlap on the
  * GPU (other streams, other host threads) race and must be serialised by the
  * caller.  Arguments, outputs and errors are those of unip_prefill_attention.

@@ -49,6 +49,16 @@ def ffd_pack(lengths, capacity):
     return [b[1] for b in bins]
 
 
+def ffd_order(lengths, capacity):
+    """The packing of ffd_pack as (order, bin_cu): prompts in packed order and bin boundaries."""
+    bins = ffd_pack(lengths, capacity)
+    order = [i for b in bins for i in b]
+    bin_cu = [0]
+    for b in bins:
+        bin_cu.append(bin_cu[-1] + len(b))
+    return order, bin_cu
+
+
 def pack_metadata(lengths, order):
     """cu_seqlens, positions (restarting per prompt) and source token indices."""
     starts = []

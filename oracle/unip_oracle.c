@@ -484,6 +484,7 @@ int oracle_topp_select(const float *imp, const int32_t *blk_cu, int32_t num_segs
     for (int32_t b = 0; b < nb; b++) {
       float f = imp[b0 + b];
       if (!(f >= 0.0f) || f > 1.0f) { free(qv); free(rk); return ORC_EINVAL; }
+      if (f == 0.0f) f = 0.0f; /* -0 is the zero score */
       qv[b] = (uint64_t)floor((double)f * 4294967296.0);
       T += qv[b];
       keep[b0 + b] = 0;
@@ -500,8 +501,10 @@ int oracle_topp_select(const float *imp, const int32_t *blk_cu, int32_t num_segs
     int32_t R = 0;
     for (int32_t b = 0; b < nb; b++) {
       if (keep[b0 + b]) { cum += qv[b]; continue; }
+      float f = imp[b0 + b];
+      if (f == 0.0f) f = 0.0f; /* -0 ranks as the zero score */
       uint32_t bits;
-      memcpy(&bits, &imp[b0 + b], sizeof bits);
+      memcpy(&bits, &f, sizeof bits);
       rk[R].bits = bits;
       rk[R].idx = b;
       R++;

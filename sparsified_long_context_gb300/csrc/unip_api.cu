@@ -1,6 +1,8 @@
 // Host plumbing shared by every entry point: per-device status word,
 // SM count, driver entry point for tensor maps, version and error strings.
 #include <mutex>
+#include <set>
+#include <tuple>
 
 #include "unip_internal.cuh"
 
@@ -47,6 +49,20 @@ int device_sm_count() {
     g_sm_count[dev] = n;
   }
   return g_sm_count[dev];
+}
+
+cudaError_t ensure_dynamic_smem(const void *fn, int bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  static std::mutex mu;
+  static std::set<std::tuple<const void *, int, int>> done;
+  const auto key = std::make_tuple(fn, dev, bytes);
+  std::lock_guard<std::mutex> lk(mu);
+  if (done.count(key)) return cudaSuccess;
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done.insert(key);
+  return e;
 }
 
 CUresult encode_tiled(CUtensorMap *map, CUtensorMapDataType dtype, cuuint32_t rank, void *gaddr,

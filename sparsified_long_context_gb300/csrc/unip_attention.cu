@@ -553,6 +553,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   __shared__ __align__(8) uint64_t bars[kNumBars];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
+  __shared__ int s_tmem_busy;  // 1: tensor-core work could not be confirmed finished, TMEM is kept
   __shared__ int32_t s_unit[2];
 
   const int warp = threadIdx.x >> 5;
@@ -583,6 +584,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       mbar_init(bar(kBarUnitEmpty0 + i), kUnitReaders);
     }
     s_abort = 0;
+    s_tmem_busy = 0;
     fence_mbar_init();
   }
   if (warp == kWarpMma) {
@@ -960,16 +962,25 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         lbase += 2 * T;
         advance(w);
       }
-      // Every tcgen05 op of this CTA has landed before TMEM is released.
+      // Every tcgen05 op of this CTA has landed before TMEM is released.  If that cannot be confirmed
+      // within two wait limits, the columns are not freed under running MMAs: the CTA leaves them
+      // allocated and raises the timeout bit (the context should then be torn down by its owner).
       umma_commit(bar(kBarFinal));
-      const uint64_t t0 = globaltimer_ns();
-      while (!mbar_try_wait(bar(kBarFinal), 0) && globaltimer_ns() - t0 < kWaitLimitNs) {
+      bool drained = false;
+      for (int round = 0; round < 2 && !drained; ++round) {
+        const uint64_t t0 = globaltimer_ns();
+        while (!(drained = mbar_try_wait(bar(kBarFinal), 0)) && globaltimer_ns() - t0 < kWaitLimitNs) {
+        }
+      }
+      if (!drained) {
+        s_tmem_busy = 1;
+        atomicOr(a.status, UNIP_DEV_TIMEOUT);
       }
     }
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == kWarpMma) {
+  if (warp == kWarpMma && !s_tmem_busy) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
@@ -978,15 +989,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
 template <int D>
 cudaError_t launch_attention(const AttnArgs &args, int grid, cudaStream_t stream) {
   using L = SmemLayout<D>;
-  static bool configured[64] = {false};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !configured[dev]) {
-    cudaError_t e =
-        cudaFuncSetAttribute(attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::kDynamic);
-    if (e != cudaSuccess) return e;
-    configured[dev] = true;
-  }
+  const cudaError_t e = ensure_dynamic_smem((const void *)attn_fwd_kernel<D>, (int)L::kDynamic);
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
   cfg.blockDim = dim3(kThreads);

@@ -143,6 +143,7 @@ __global__ void __launch_bounds__(kScoreThreadsTc, 1) imp_score_tc_kernel(const 
   __shared__ __align__(8) uint64_t bars[kSbNum];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
+  __shared__ int s_tmem_busy;  // 1: tensor-core work could not be confirmed finished, TMEM is kept
   __shared__ __align__(16) float s_lse[kMaxCols];
   __shared__ float s_key[128];
   __shared__ float s_red[4];
@@ -167,6 +168,7 @@ __global__ void __launch_bounds__(kScoreThreadsTc, 1) imp_score_tc_kernel(const 
   if (tid == 0) {
     for (int k = 0; k < kSbNum; ++k) mbar_init(bar(k), (k == kSbSEmpty0 || k == kSbSEmpty0 + 1) ? kScoreCompute : 1);
     s_abort = 0;
+    s_tmem_busy = 0;
     fence_mbar_init();
   }
   if (warp == kScoreWarpMma) {
@@ -282,10 +284,19 @@ __global__ void __launch_bounds__(kScoreThreadsTc, 1) imp_score_tc_kernel(const 
         umma_commit(bar(kSbKEmpty0 + slot));
         if (i + 1 == n_iter || !same_q(nxt, it)) umma_commit(bar(kSbQEmpty));  // last MMA on this Q
       }
-      // Every tcgen05 op of this CTA has landed before TMEM is released.
+      // Every tcgen05 op of this CTA has landed before TMEM is released; if that cannot be confirmed
+      // within two wait limits the columns are kept (not freed under running MMAs) and the timeout
+      // bit is raised.
       umma_commit(bar(kSbFinal));
-      const uint64_t t0 = globaltimer_ns();
-      while (!mbar_try_wait(bar(kSbFinal), 0) && globaltimer_ns() - t0 < kWaitLimitNs) {
+      bool drained = false;
+      for (int round = 0; round < 2 && !drained; ++round) {
+        const uint64_t t0 = globaltimer_ns();
+        while (!(drained = mbar_try_wait(bar(kSbFinal), 0)) && globaltimer_ns() - t0 < kWaitLimitNs) {
+        }
+      }
+      if (!drained) {
+        s_tmem_busy = 1;
+        atomicOr(a.status, UNIP_DEV_TIMEOUT);
       }
     }
   } else {
@@ -399,7 +410,7 @@ __global__ void __launch_bounds__(kScoreThreadsTc, 1) imp_score_tc_kernel(const 
   __syncthreads();
   // the normaliser may be scheduled now; it waits for every score CTA before reading the masses
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  if (warp == kScoreWarpMma) {
+  if (warp == kScoreWarpMma && !s_tmem_busy) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
@@ -440,15 +451,8 @@ __global__ void __launch_bounds__(kNormThreads) imp_norm_kernel(const int32_t *_
 template <int D>
 cudaError_t launch_score(const ScoreArgs &args, int grid, cudaStream_t stream) {
   using L = ScoreSmem<D>;
-  static bool configured[64] = {false};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(imp_score_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)L::kDynamic);
-    if (e != cudaSuccess) return e;
-    configured[dev] = true;
-  }
+  const cudaError_t e = ensure_dynamic_smem((const void *)imp_score_tc_kernel<D>, (int)L::kDynamic);
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
   cfg.blockDim = dim3(kScoreThreadsTc);

@@ -17,6 +17,9 @@ namespace unip {
 uint32_t *device_status_ptr();
 // Streaming-multiprocessor count of the current device.
 int device_sm_count();
+// Raises the dynamic shared-memory limit of kernel `fn` to `bytes` on the current device, once per
+// (kernel, device, size); safe to call from several host threads.
+cudaError_t ensure_dynamic_smem(const void *fn, int bytes);
 // cuTensorMapEncodeTiled, fetched from the driver at first use.
 CUresult encode_tiled(CUtensorMap *map, CUtensorMapDataType dtype, cuuint32_t rank, void *gaddr,
                       const cuuint64_t *dims, const cuuint64_t *strides, const cuuint32_t *box,

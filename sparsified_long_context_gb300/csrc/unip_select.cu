@@ -46,7 +46,7 @@ constexpr int kGatherStageBytes = 48 * 1024;  // shared memory of the fused gath
 // f * 2^32 = m * 2^(e - 118).  Zero and subnormal scores are below 2^-126 and give 0.
 __device__ __forceinline__ unsigned long long fixed_mass(float f) {
   const uint32_t u = __float_as_uint(f);
-  const int e = static_cast<int>(u >> 23);  // f >= 0: no sign bit
+  const int e = static_cast<int>(u >> 23);  // f >= 0 with the sign bit clear (-0 is read as +0)
   if (e == 0) return 0ull;
   const unsigned long long m = (u & 0x7FFFFFu) | 0x800000u;
   const int sh = e - 118;
@@ -115,7 +115,9 @@ __device__ bool select_segment_blocks(const float *__restrict__ imp, int32_t b0,
     unsigned long long key = ~0ull;
     uint8_t kf = 0;
     if (b < nb) {
-      const float f = imp[b0 + b];
+      float f = imp[b0 + b];
+      // a zero score is +0 whatever its sign bit: no mass, and ranked as zero
+      if (__float_as_uint(f) == 0x80000000u) f = __uint_as_float(0u);
       if (!(f >= 0.f) || f > 1.f) {
         bad = 1;
       } else {
@@ -557,14 +559,10 @@ __global__ void __launch_bounds__(kToppThreads) select_gather_onepass_kernel(
 cudaError_t launch_topp(const float *imp, const int32_t *blk_cu, const int32_t *cu_seqlens, int32_t num_segs,
                         int32_t total_tokens, int32_t block_size, double p, uint32_t flags, uint8_t *keep,
                         int32_t *kept_off, int32_t *seg_kept, uint32_t *status, cudaStream_t st) {
-  static bool configured[64] = {false};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !configured[dev]) {
-    const cudaError_t e = cudaFuncSetAttribute(topp_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               kMaxBlocks * ((int)sizeof(unsigned long long) + 1));
+  {
+    const cudaError_t e =
+        ensure_dynamic_smem((const void *)topp_kernel, kMaxBlocks * ((int)sizeof(unsigned long long) + 1));
     if (e != cudaSuccess) return e;
-    configured[dev] = true;
   }
   int32_t cap = 16;
   const int64_t need = (int64_t)total_tokens / block_size + 2;
@@ -687,15 +685,9 @@ UNIP_API int32_t unip_select_gather(const float *imp, const int32_t *blk_cu, con
     return UNIP_OK;
   }
   if (num_segs == 1) {  // one segment: selection and gather in one grid
-    static bool configured1[64] = {false};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && !configured1[dev]) {
-      if (cudaFuncSetAttribute(select_gather_onepass_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               kMaxBlocks * ((int)sizeof(unsigned long long) + 5)) != cudaSuccess)
-        return UNIP_ERR_CUDA;
-      configured1[dev] = true;
-    }
+    if (ensure_dynamic_smem((const void *)select_gather_onepass_kernel,
+                            kMaxBlocks * ((int)sizeof(unsigned long long) + 5)) != cudaSuccess)
+      return UNIP_ERR_CUDA;
     int32_t cap = 16;
     const int64_t need = (int64_t)total_tokens / block_size + 2;
     while (cap < need && cap < kMaxBlocks) cap <<= 1;

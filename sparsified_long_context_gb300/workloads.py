@@ -14,7 +14,8 @@ Workloads (one builder per shape):
 * ``chunked``        one 4096-token prompt prefilled in 8 chunks of 512 that
   read earlier chunks through a 16-token paged cache, H_q=32, H_kv=8, D=128.
 * ``prepacked``      64 lognormal prompts (median 512, sigma 1, clipped to
-  32..8192) packed first-fit-decreasing into 16384-token bins.
+  32..8192) packed into 16384-token bins by a packer the caller passes in
+  (the library's first-fit-decreasing packer, or the oracle's).
 * ``long_single``    one 32768-token prompt, heavy keys in 10 spans, block 64,
   p=0.95, hidden d=4096.
 * ``mixed_step``     an 8192-token continuous-batching step: 256 decode tokens
@@ -280,40 +281,43 @@ def tiny_packed(seed: int = 1) -> Workload:
                   d_model=256, name="tiny_packed")
 
 
-def ffd_bins(lengths, capacity: int):
-    """First-fit-decreasing: longest first (ties: lower index), into the first bin with room."""
-    order = sorted(range(len(lengths)), key=lambda i: (-lengths[i], i))
-    bins = []
-    for i in order:
-        for b in bins:
-            if b["free"] >= lengths[i]:
-                b["free"] -= lengths[i]
-                b["items"].append(i)
-                break
-        else:
-            bins.append({"free": capacity - lengths[i], "items": [i]})
-    return [b["items"] for b in bins]
-
-
-def prepacked(seed: int = 3, num_prompts: int = 64, bin_tokens: int = 16384,
+def prepacked(pack, seed: int = 3, num_prompts: int = 64, bin_tokens: int = 16384,
               num_heads_q: int = 32, num_heads_kv: int = 8, head_dim: int = 128) -> Workload:
+    """64 lognormal prompts packed into ``bin_tokens``-token bins.
+
+    The packing itself is method arithmetic, so it is not done here: ``pack``
+    is the packer under use, called as ``pack(lengths, bin_tokens)`` and
+    returning ``(order, bin_cu)`` (the prompts in packed order and the bin
+    boundaries in that order), e.g. the library's ``unip_ffd_pack`` or an
+    adapter over the oracle's.  Prompt contents are drawn per prompt, in
+    prompt order, and then laid out in the packed order, so every packer that
+    returns the same order yields the same stream.
+    """
     rng = np.random.default_rng(seed)
     z = rng.standard_normal(num_prompts)
     lengths = np.clip(np.round(np.exp(math.log(512.0) + 1.0 * z)), 32, 8192).astype(np.int64)
-    bins = ffd_bins([int(x) for x in lengths], bin_tokens)
-    order = [i for b in bins for i in b]
-    packed_lengths = [int(lengths[i]) for i in order]
-    n = sum(packed_lengths)
-    heavy = _heavy_rows(rng, n, 0.05)
+    n = int(lengths.sum())
+    heavy = _heavy_rows(rng, n, 0.05)   # rows of the prompt-order concatenation
     q = _normal_bf16(rng, (n, num_heads_q, head_dim))
     k = _normal_bf16(rng, (n, num_heads_kv, head_dim), heavy)
     v = _normal_bf16(rng, (n, num_heads_kv, head_dim))
+    order, bin_cu = pack([int(x) for x in lengths], bin_tokens)
+    order = [int(i) for i in order]
+    bin_cu = [int(x) for x in bin_cu]
+    if sorted(order) != list(range(num_prompts)):
+        raise ValueError("the packer must place every prompt exactly once")
+    starts = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int64)
+    rows = np.concatenate([np.arange(starts[i], starts[i + 1]) for i in order])
+    packed_lengths = [int(lengths[i]) for i in order]
+    bins = [order[bin_cu[b]:bin_cu[b + 1]] for b in range(len(bin_cu) - 1)]
+    inv = np.empty(n, np.int64)
+    inv[rows] = np.arange(n)
     return Workload("prepacked", num_heads_q, num_heads_kv, head_dim, _cu(packed_lengths),
-                    _positions_for(packed_lengths, [0] * num_prompts), q, k, v,
+                    _positions_for(packed_lengths, [0] * num_prompts), q[rows], k[rows], v[rows],
                     block_size=64, top_p=0.95,  # selection settings of the long-context layer
                     seg_mask=np.ones(num_prompts, np.uint8),
                     meta={"lengths": packed_lengths, "prompt_order": order, "bins": bins,
-                          "bin_tokens": bin_tokens, "heavy_rows": heavy})
+                          "bin_tokens": bin_tokens, "heavy_rows": np.sort(inv[heavy])})
 
 
 def long_single(seed: int = 4, n: int = 32768, num_heads_q: int = 32, num_heads_kv: int = 8,

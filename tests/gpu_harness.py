@@ -13,6 +13,12 @@ MEAN_ABS = 2e-3
 LSE_ABS = 2e-3
 
 
+def library_ffd(lengths, capacity):
+    """The library's first-fit-decreasing packer (host C++ of libunip), as (order, bin_cu)."""
+    from sparsified_long_context_gb300 import binding as B
+    return B.unip_ffd_pack(lengths, capacity)
+
+
 def bf16_tensor_to_f64(t) -> np.ndarray:
     import torch
     return t.detach().float().cpu().numpy().astype(np.float64)

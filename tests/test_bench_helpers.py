@@ -7,6 +7,7 @@ import os
 import numpy as np
 
 import bench
+from oracle.scheduling import ffd_order
 from sparsified_long_context_gb300 import workloads as W
 from sparsified_long_context_gb300.pipeline import kernels_per_step
 
@@ -50,7 +51,7 @@ def test_mixed_step_bound_is_prefill_flops_plus_decode_bytes():
 
 
 def test_prepacked_padding_context():
-    wl = W.prepacked()
+    wl = W.prepacked(ffd_order)
     ctx = bench.workload_context(wl, 1.0, 1000.0, 5000.0)
     lmax = int(wl.seq_lens.max())
     c = 4.0 * 128 * 32

@@ -5,7 +5,8 @@ import pytest
 import oracle
 from sparsified_long_context_gb300 import workloads as W
 
-from gpu_harness import assert_close, bf16_tensor_to_f64, oracle_attention_rows, sample_rows, LSE_ABS
+from gpu_harness import (assert_close, bf16_tensor_to_f64, library_ffd, oracle_attention_rows, sample_rows,
+                         LSE_ABS)
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -169,13 +170,18 @@ def test_chunked_equals_one_shot():
 
 
 def test_prepacked_sampled():
-    wl = W.prepacked()
+    wl = W.prepacked(library_ffd)
     _check(wl, sample_rows(wl, 400))
 
 
 def test_long_single_sampled():
+    """The 32768-token prompt: the last row of every 128-row query tile (it sees the most keys of
+    its tile), the importance window (the last 64 rows) and the stratified sample."""
     wl = W.long_single(d_model=0)
-    _check(wl, sample_rows(wl, 48))
+    n = wl.num_tokens
+    rows = np.union1d(sample_rows(wl, 48), np.arange(127, n, 128))
+    rows = np.union1d(rows, np.arange(n - 64, n)).astype(np.int32)
+    _check(wl, rows)
 
 
 def test_mixed_step_sampled():

@@ -10,7 +10,7 @@ import pytest
 import oracle
 from sparsified_long_context_gb300 import workloads as W
 
-from gpu_harness import assert_close
+from gpu_harness import LSE_ABS, assert_close, library_ffd, oracle_attention_rows
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -61,10 +61,28 @@ def test_tiny_full_chain():
     assert 0 < m <= wl.num_tokens
 
 
-def _importance_vs_oracle_with_gpu_lse(wl, bufs):
-    """Oracle importance fed the GPU's row LSE (rows outside the windows are never read)."""
-    lse_gpu = bufs.lse.cpu().numpy().astype(np.float64).T.copy()
-    ref_imp, ref_bc = oracle.block_importance(wl.q, wl.k, lse_gpu, wl.cu_seqlens, wl.num_heads_q,
+def _window_rows(wl):
+    """Token rows of every scored segment's scoring window: its last min(B, n) rows."""
+    cu, B_ = wl.cu_seqlens, wl.block_size
+    rows = []
+    for s in range(wl.num_segs):
+        a, b = int(cu[s]), int(cu[s + 1])
+        if b > a and (wl.seg_mask is None or wl.seg_mask[s]):
+            rows.extend(range(b - min(B_, b - a), b))
+    return np.array(rows, np.int32)
+
+
+def _importance_vs_oracle(wl, bufs):
+    """Importance against the oracle computed from the oracle's own inputs only: the window rows'
+    LSE comes from the oracle's attention over those rows (prefix pages included), never from the
+    GPU.  The GPU's LSE of the same rows is checked against it on the way."""
+    rows = _window_rows(wl)
+    _, lse_rows = oracle_attention_rows(wl, rows)           # [R, H_q]
+    lse_gpu = bufs.lse.cpu().numpy().astype(np.float64).T    # [N, H_q]
+    assert_close(lse_gpu[rows], lse_rows, max_abs=LSE_ABS, mean_abs=LSE_ABS, what="window-row lse")
+    lse_full = np.zeros((wl.num_tokens, wl.num_heads_q), np.float64)   # only window rows are read
+    lse_full[rows] = lse_rows
+    ref_imp, ref_bc = oracle.block_importance(wl.q, wl.k, lse_full, wl.cu_seqlens, wl.num_heads_q,
                                               wl.num_heads_kv, wl.head_dim, wl.block_size, seg_mask=wl.seg_mask)
     blk_cu = bufs.blk_cu.cpu().numpy()
     assert np.array_equal(blk_cu, ref_bc)
@@ -79,7 +97,7 @@ def _importance_vs_oracle_with_gpu_lse(wl, bufs):
 def test_long_single_chain():
     wl = W.long_single()
     di, bufs = _step(wl)
-    _importance_vs_oracle_with_gpu_lse(wl, bufs)
+    _importance_vs_oracle(wl, bufs)
     _, _, m = _check_selection(wl, bufs)
     assert 0 < m < wl.num_tokens
 
@@ -87,9 +105,19 @@ def test_long_single_chain():
 def test_mixed_step_chain():
     wl = W.mixed_step()
     di, bufs = _step(wl)
-    _importance_vs_oracle_with_gpu_lse(wl, bufs)
+    _importance_vs_oracle(wl, bufs)
     _, _, m = _check_selection(wl, bufs)
     assert m >= 256  # decode tokens are never dropped
+
+
+def test_prepacked_chain():
+    """The prepacked batch (64 prompts, every one scored): importance of all 64 segments against the
+    oracle, then selection and indices bit-exact."""
+    wl = W.prepacked(library_ffd)
+    di, bufs = _step(wl)
+    _importance_vs_oracle(wl, bufs)
+    _, _, m = _check_selection(wl, bufs)
+    assert 0 < m < wl.num_tokens
 
 
 def _topp_direct(imp_np, blk_cu_np, cu_np, B_, p, flags):
@@ -143,6 +171,21 @@ def test_topp_edge_cases_bit_exact(flags):
         assert np.array_equal(keep, ref), (p, flags)
         rgi, rck, rpk, rm = oracle.index_build(ref, bc, cu, pos, B_)
         assert np.array_equal(gi, rgi) and np.array_equal(ck, rck) and np.array_equal(pk, rpk)
+
+
+def test_topp_negative_zero_scores():
+    """-0 scores through the public Top-p call: read as zero (mass and rank), like the oracle."""
+    rng = np.random.default_rng(77)
+    nb = 40
+    x = rng.random(nb).astype(np.float32)
+    x[::5] = 0.0
+    x = (x / x.sum()).astype(np.float32)
+    x[::5] = np.float32(-0.0)
+    bc = np.array([0, nb], np.int32)
+    cu = np.array([0, nb * 16], np.int32)
+    for p, flags in [(0.5, 0), (0.9, 3), (1.0, 0), (1.0, 3)]:
+        keep, gi, ck, pk, pos = _topp_direct(x, bc, cu, 16, p, flags)
+        assert np.array_equal(keep, oracle.topp_select(x, bc, p, flags)), (p, flags)
 
 
 def test_topp_zero_mass_keeps_all():
@@ -201,7 +244,7 @@ def test_fused_select_gather_matches_oracle(name):
     from sparsified_long_context_gb300 import binding as Bd
     from sparsified_long_context_gb300.pipeline import (DeviceInputs, StepBuffers, run_attention, run_importance,
                                                         run_select_gather)
-    wl = W.workload_by_name(name)
+    wl = W.prepacked(library_ffd) if name == "prepacked" else W.workload_by_name(name)
     Bd.unip_get_device_status(clear=True)
     di = DeviceInputs.from_workload(wl, "cuda")
     bufs = StepBuffers(di)

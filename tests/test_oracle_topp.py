@@ -136,6 +136,30 @@ def test_index_build_and_gather():
         assert np.all((seg >= cu[s]) & (seg < cu[s + 1]))
         if nbs[s] == 0:
             assert len(seg) == lengths[s]
+    # brute force, token by token: exactly the tokens of kept blocks (every token of an unscored
+    # segment), in stream order, and the kept offsets are the running counts per segment
+    expect, counts = [], [0]
+    for s, L in enumerate(lengths):
+        for i in range(L):
+            if nbs[s] == 0 or keep[bc[s] + i // B]:
+                expect.append(int(cu[s]) + i)
+        counts.append(len(expect))
+    assert gi.tolist() == expect
+    assert ck.tolist() == counts
     hidden = W.f32_to_bf16_bits(rng.standard_normal((n, 24), dtype=np.float32))
     out = oracle.gather(hidden, gi)
     assert np.array_equal(out, hidden[gi])
+
+
+def test_negative_zero_is_the_zero_score():
+    """A score of -0 is the zero score: no mass, and ranked with (not above) the +0 scores."""
+    imp = np.array([0.25, 0.0, 0.3, 0.0, 0.0, 0.2, 0.25], np.float32)
+    neg = imp.copy()
+    neg[[1, 4]] = np.float32(-0.0)
+    assert np.signbit(neg[1]) and np.signbit(neg[4])
+    bc = np.array([0, 7], np.int32)
+    for p in (0.0, 0.5, 0.8, 0.95, 1.0):
+        for flags in (0, 1, 2, 3):
+            assert np.array_equal(oracle.topp_select(neg, bc, p, flags), oracle.topp_select(imp, bc, p, flags))
+    # with no forced blocks and p = 1 the zero scores are never needed
+    assert oracle.topp_select(neg, bc, 1.0, 0).tolist() == [1, 0, 1, 0, 0, 1, 1]

@@ -2,6 +2,7 @@
 import numpy as np
 import torch
 
+from oracle.scheduling import ffd_order
 from sparsified_long_context_gb300 import workloads as W
 
 
@@ -27,7 +28,7 @@ def test_tiny_packed_shape():
 
 
 def test_prepacked_ffd_structure():
-    wl = W.prepacked()
+    wl = W.prepacked(ffd_order)
     L = wl.meta["lengths"]
     assert len(L) == 64 and min(L) >= 32 and max(L) <= 8192
     for b in wl.meta["bins"]:
@@ -76,3 +77,15 @@ def test_hash_generator_numpy_matches_torch():
     assert np.array_equal(a, b)
     x = W.bf16_bits_to_f32(a[:5000]).astype(np.float64)
     assert abs(x.mean()) < 0.05 and abs(x.std() - 1.0) < 0.05
+
+
+def test_prepacked_stream_is_the_same_under_the_library_and_oracle_packers():
+    """The bench packs the prepacked batch with the library's packer, the reference arm and the CPU tests
+    with the oracle's; both must yield the same stream."""
+    from sparsified_long_context_gb300 import binding as B
+    a, b = W.prepacked(B.unip_ffd_pack), W.prepacked(ffd_order)
+    assert a.meta["prompt_order"] == b.meta["prompt_order"] and a.meta["bins"] == b.meta["bins"]
+    for f in ("cu_seqlens", "positions", "q", "k", "v"):
+        assert np.array_equal(getattr(a, f), getattr(b, f))
+    # rows are laid out prompt by prompt in the packed order: heavy keys follow their rows
+    assert np.array_equal(a.meta["heavy_rows"], b.meta["heavy_rows"])
