@@ -112,22 +112,22 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def recorded_traffic(kernel_src: str, summary: str):
-    """DRAM bytes per launch from a committed ncu summary, if the kernel source is unchanged since."""
-    path = os.path.join(ROOT, "profiles", summary)
+def recorded_traffic(entry: str, table: str = "dram_traffic.json"):
+    """DRAM bytes per launch of a kernel from the committed ncu record (profiles/dram_traffic.json),
+    or None when there is no record or the kernel source has changed since the capture."""
+    path = os.path.join(ROOT, "profiles", table)
     if not os.path.exists(path):
         return None
-    sha = hashlib.sha1(open(kernel_src, "rb").read()).hexdigest()
-    rec = {}
-    for line in open(path):
-        if ":" in line and line.strip().startswith("- "):
-            k, v = line.strip()[2:].split(":", 1)
-            rec[k.strip()] = v.strip().strip("`")
-    if rec.get("kernel_source_sha1") != sha:
+    with open(path) as f:
+        rec = json.load(f).get(entry)
+    if not rec:
+        return None
+    src = os.path.join(ROOT, rec["kernel_source"])
+    if not os.path.exists(src) or hashlib.sha1(open(src, "rb").read()).hexdigest() != rec.get("kernel_source_sha1"):
         return None
     try:
-        return float(rec["dram_bytes_per_launch_full_workload"])
-    except (KeyError, ValueError):
+        return float(rec["dram_bytes_per_launch"])
+    except (KeyError, TypeError, ValueError):
         return None
 
 
@@ -334,19 +334,39 @@ def cpu_baseline(wl, seconds: float):
     dt = time.perf_counter() - t0
     return {"value": rows_flops(wl, rows) / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
             "sample": f"fp64 oracle attention on {n_rows} uniformly sampled query rows x {wl.num_heads_q} heads "
-                      f"of the same workload ({dt:.1f} s); useful FLOPs of those rows / wall time"}
+                      f"of the same workload ({dt:.1f} s); useful FLOPs of those rows / wall time",
+            "tiny_packed_full": tiny_oracle_timing(cores)}
 
 
-def incremental_select_ms(di, bufs, flush, stream, reps: int = 10, trials: int = 5) -> float:
-    """Incremental device time of select+gather in the step: CUDA-graph replays of
-    [L2 flush, importance, select+gather] minus [L2 flush, importance], per step.
+def tiny_oracle_timing(cores: int, reps: int = 5):
+    """The oracle's whole attention of the tiny packed batch (456 tokens), on one thread and on all cores."""
+    import oracle
+    from sparsified_long_context_gb300 import workloads as W
+    wl = W.tiny_packed()
+    flops = useful_attention_flops(wl)
+    out = {}
+    for nt in (1, cores):
+        best = None
+        for _ in range(reps):
+            t0 = time.perf_counter()
+            oracle.attention(wl.q, wl.k, wl.v, wl.cu_seqlens, wl.positions, wl.num_heads_q, wl.num_heads_kv,
+                             wl.head_dim, nthreads=nt)
+            dt = time.perf_counter() - t0
+            best = dt if best is None else min(best, dt)
+        out[f"threads_{nt}"] = {"seconds": best, "tflops": flops / best / 1e12}
+    return out
 
-    CUDA events recorded between the importance and the Top-p launches would break the
-    programmatic-dependent launch between them and add their own latency, so the in-step
-    event pair overstates this part; both are reported.
+
+def incremental_select_ms(di, bufs, flush, stream, reps: int = 10, trials: int = 5):
+    """Device time of importance alone and the incremental time of Top-p + compaction in the step:
+    CUDA-graph replays of [L2 flush, importance + selection + compaction (the fused call)] minus
+    [L2 flush, importance], per step.  Returns (importance_ms, select_gather_ms).
+
+    The selection shares a grid with importance's normaliser and the copy is its programmatic
+    dependent, so no event can be recorded between them without changing the launch chain.
     """
     import torch
-    from sparsified_long_context_gb300.pipeline import run_importance, run_select_gather
+    from sparsified_long_context_gb300.pipeline import run_importance, run_importance_select_gather
 
     cs = torch.cuda.Stream()  # graphs are captured on a side stream
 
@@ -355,9 +375,10 @@ def incremental_select_ms(di, bufs, flush, stream, reps: int = 10, trials: int =
         with torch.cuda.graph(g, stream=cs):
             for _ in range(reps):
                 flush.zero_()
-                run_importance(di, bufs, cs)
                 if with_select:
-                    run_select_gather(di, bufs, stream=cs)
+                    run_importance_select_gather(di, bufs, stream=cs)
+                else:
+                    run_importance(di, bufs, cs)
         return g
 
     def replay_ms(g):
@@ -372,12 +393,145 @@ def incremental_select_ms(di, bufs, flush, stream, reps: int = 10, trials: int =
             ts.append(e0.elapsed_time(e1) / reps)
         return statistics.median(ts)
 
+    def flush_only():
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cs):
+            for _ in range(reps):
+                flush.zero_()
+        return g
+
     torch.cuda.synchronize()
-    g_imp, g_all = capture(False), capture(True)
+    g_fl, g_imp, g_all = flush_only(), capture(False), capture(True)
     torch.cuda.synchronize()
-    d = replay_ms(g_all) - replay_ms(g_imp)
-    del g_imp, g_all
-    return max(d, 1e-6)
+    t_fl, t_imp, t_all = replay_ms(g_fl), replay_ms(g_imp), replay_ms(g_all)
+    del g_fl, g_imp, g_all
+    return max(t_imp - t_fl, 1e-6), max(t_all - t_imp, 1e-6)
+
+
+def _timed_steps(step, flush, stream, seconds: float, max_steps: int, gpu_index: int):
+    """Runs `step(events)` after an L2 flush until about `seconds` of device time is timed; returns the
+    per-step event lists and the clock summary of the timed region.  One untimed step sizes the loop."""
+    import torch
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    flush.zero_()
+    ev[0].record(stream)
+    step(None)
+    ev[1].record(stream)
+    torch.cuda.synchronize()
+    one = max(ev[0].elapsed_time(ev[1]), 1e-3)
+    n = int(max(10, min(max_steps, seconds * 1e3 / (one + 0.05))))
+    evs = []
+    with ClockSampler(gpu_index) as clk:
+        for _ in range(n):
+            flush.zero_()
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+            step(e)
+            evs.append(e)
+        torch.cuda.synchronize()
+    return evs, clk.summary()
+
+
+def part_chunked(rank: int, gpu_index: int, flush, stream, peaks, seconds: float = 0.3):
+    """Config 2 inside the default run: the eight 512-token calls of a 4096-token prompt behind paged
+    prefixes, each through its host-built plan (built once, outside the timed region, as a serving
+    step reuses its plan for every layer); the L2 is flushed before every call."""
+    import torch
+    from sparsified_long_context_gb300 import binding as B
+    from sparsified_long_context_gb300 import workloads as W
+    from sparsified_long_context_gb300.pipeline import (DeviceInputs, StepBuffers, attention_plan, plan_workspace,
+                                                        run_attention_planned)
+    one, chunks = W.chunked(seed=2 + 1000 * rank)
+    sets = []
+    for c in chunks:
+        di = DeviceInputs.from_workload(c, stream.device if hasattr(stream, "device") else "cuda",
+                                        with_hidden=False)
+        plan = attention_plan(c)
+        sets.append((di, StepBuffers(di, block_size=64), plan, plan_workspace(plan, di.q.device)))
+    flops = [useful_attention_flops(c) for c in chunks]
+    import statistics as stt
+    per_call = []
+    clocks = []
+    for i, (di, bufs, plan, ws) in enumerate(sets):
+        def step(e, di=di, bufs=bufs, plan=plan, ws=ws):
+            if e is not None:
+                e[0].record(stream)
+            run_attention_planned(di, bufs, plan, ws, stream)
+            if e is not None:
+                e[1].record(stream)
+        evs, clk = _timed_steps(step, flush, stream, seconds / len(sets), 4000, gpu_index)
+        per_call.append(stt.median(e[0].elapsed_time(e[1]) for e in evs))
+        clocks.append(clk)
+    st = B.unip_get_device_status(clear=True)
+    if st:
+        raise SystemExit(f"device status after the chunked calls: {B.describe_status(st)}")
+    total_ms = float(sum(per_call))
+    tflops = sum(flops) / (total_ms * 1e-3) / 1e12
+    bf16 = float(peaks["bf16_tflops"])
+    sm = [c["sm_mhz"] for c in clocks if c["sm_mhz"]]
+    out = {"workload": "chunked: one 4096-token prompt in 8 calls of 512 tokens behind paged prefixes of "
+                       "0..3584 tokens (16-token pages, shuffled), H_q 32, H_kv 8, D 128",
+           "attention_ms": total_ms, "attention_tflops": tflops, "attention_frac_bf16": tflops / bf16,
+           "per_call": [{"prefix": int(c.prefix_lens[0]), "ms": m, "tflops": f / (m * 1e-3) / 1e12,
+                         "plan": s[2].info}
+                        for c, m, f, s in zip(chunks, per_call, flops, sets)],
+           "timing": "median per call over repeated calls, L2 flushed (256 MB write) before each call",
+           "clocks": {"sm_mhz": stt.median(sm) if sm else None,
+                      "sm_max_mhz": clocks[0]["sm_max_mhz"],
+                      "reasons": sorted({r for c in clocks for r in c["reasons"]}),
+                      "samples": sum(c["samples"] for c in clocks)}}
+    for s in sets:
+        s[2].close()
+    return out
+
+
+def part_step_workload(name: str, rank: int, gpu_index: int, flush, stream, peaks, seconds: float = 0.4):
+    """Configs 3 and 5 inside the default run: attention, importance and the fused select+gather of one
+    step, each with its own device time, fractions of the measured peaks and clock record."""
+    import statistics as stt
+    from sparsified_long_context_gb300 import binding as B
+    from sparsified_long_context_gb300.pipeline import (DeviceInputs, StepBuffers, run_attention,
+                                                        run_importance_select_gather)
+    wl = build_workload(name, rank)
+    di = DeviceInputs.from_workload(wl, f"cuda:{gpu_index}")
+    bufs = StepBuffers(di)
+
+    def step(e):
+        if e is not None:
+            e[0].record(stream)
+        run_attention(di, bufs, stream)
+        if e is not None:
+            e[1].record(stream)
+        run_importance_select_gather(di, bufs, stream=stream)
+        if e is not None:
+            e[2].record(stream)
+
+    for _ in range(3):
+        flush.zero_()
+        step(None)
+    evs, clk = _timed_steps(step, flush, stream, seconds, 2000, gpu_index)
+    st = B.unip_get_device_status(clear=True)
+    if st:
+        raise SystemExit(f"device status after {name}: {B.describe_status(st)}")
+    attn_ms = stt.median(e[0].elapsed_time(e[1]) for e in evs)
+    isg_ms = stt.median(e[1].elapsed_time(e[2]) for e in evs)
+    step_ms = stt.median(e[0].elapsed_time(e[2]) for e in evs)
+    imp_ms, sel_ms = incremental_select_ms(di, bufs, flush, stream)
+    n_kept = int(bufs.n_kept.item())
+    n_blocks = int(bufs.blk_cu[-1].item())
+    d_model = di.hidden.shape[1] if di.hidden is not None else 0
+    sg_bytes = select_gather_bytes(wl, n_blocks, n_kept, d_model)
+    bf16, hbm = float(peaks["bf16_tflops"]), float(peaks["hbm_gbs"])
+    flops = useful_attention_flops(wl)
+    tfl = flops / (attn_ms * 1e-3) / 1e12
+    gbs = sg_bytes / (sel_ms * 1e-3) / 1e9
+    return {"workload": describe(wl), "steps_timed": len(evs),
+            "attention_ms": attn_ms, "attention_tflops": tfl, "attention_frac_bf16": tfl / bf16,
+            "importance_ms": imp_ms, "importance_select_gather_ms_in_step": isg_ms, "step_ms": step_ms,
+            "select_gather_ms": sel_ms, "select_gather_bytes": sg_bytes, "select_gather_gbs": gbs,
+            "select_gather_frac_hbm": gbs / hbm, "n_kept": n_kept, "n_blocks": n_blocks,
+            "workload_context": workload_context(wl, attn_ms, bf16, hbm),
+            "timing": "median per step, L2 flushed (256 MB write) before each step; importance and the "
+                      "select+gather increment from graph replays", "clocks": clk}
 
 
 def bench_chunked(args):
@@ -502,6 +656,9 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-step-seconds", type=float, default=6.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the chunked, prepacked and continuous-batching workloads measured beside the "
+                         "long-context step")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -515,7 +672,7 @@ def main():
     import torch
     from sparsified_long_context_gb300 import binding as B
     from sparsified_long_context_gb300.pipeline import (DeviceInputs, StepBuffers, StreamedSteps, kernels_per_step,
-                                                        run_attention, run_importance, run_select_gather)
+                                                        run_attention, run_importance_select_gather)
     world, rank, local = dist_setup(args)
     torch.cuda.set_device(local)
     dist = None
@@ -537,12 +694,9 @@ def main():
         run_attention(di, bufs, stream)
         if ev is not None:
             ev[1].record(stream)
-        run_importance(di, bufs, stream)
+        run_importance_select_gather(di, bufs, stream=stream)
         if ev is not None:
             ev[2].record(stream)
-        run_select_gather(di, bufs, stream=stream)
-        if ev is not None:
-            ev[3].record(stream)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -552,7 +706,7 @@ def main():
     if st:
         raise SystemExit(f"device status after warm-up: {B.describe_status(st)}")
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
@@ -569,9 +723,8 @@ def main():
     if st:
         raise SystemExit(f"device status after timed steps: {B.describe_status(st)}")
     t_attn = [e[0].elapsed_time(e[1]) for e in evs]
-    t_imp = [e[1].elapsed_time(e[2]) for e in evs]
-    t_sel = [e[2].elapsed_time(e[3]) for e in evs]
-    t_step = [e[0].elapsed_time(e[3]) for e in evs]
+    t_isg = [e[1].elapsed_time(e[2]) for e in evs]
+    t_step = [e[0].elapsed_time(e[2]) for e in evs]
     step_ms = max_over_ranks(float(np.sum(t_step)), dist, f"cuda:{local}")
     ms_per_step = step_ms / args.steps
     value = flops_step * world / (ms_per_step * 1e-3) / 1e12
@@ -581,9 +734,8 @@ def main():
     d_model = di.hidden.shape[1] if di.hidden is not None else 0
     sg_bytes = select_gather_bytes(wl, n_blocks, n_kept, d_model)
     attn_ms = statistics.mean(t_attn)
-    sel_ms_events = statistics.mean(t_sel)
-    sel_ms = incremental_select_ms(di, bufs, flush, stream)
-    imp_ms = statistics.mean(t_imp)
+    isg_ms = statistics.mean(t_isg)
+    imp_ms, sel_ms = incremental_select_ms(di, bufs, flush, stream)
     attn_tflops = flops_step / (attn_ms * 1e-3) / 1e12
     sg_gbs = sg_bytes / (sel_ms * 1e-3) / 1e9
     peaks, peak_src = load_peaks()
@@ -617,15 +769,24 @@ def main():
         if dist is not None:
             dist.destroy_process_group()
         return 0
+    # the other workloads of the benchmark spec, each measured in this process with its own clock record
+    parts_wl = None
+    if not args.no_workloads and args.workload == "long_single":
+        del streamer, di2
+        peaks_now, _ = load_peaks()
+        pk = {"bf16_tflops": float(peaks_now.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])),
+              "hbm_gbs": float(peaks_now.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))}
+        parts_wl = {"chunked": part_chunked(rank, local, flush, stream, pk)}
+        for name in ("prepacked", "mixed_step"):
+            parts_wl[name] = part_step_workload(name, rank, local, flush, stream, pk)
     cpu = None
     if not args.no_cpu_baseline and world == 1:
         cpu = cpu_baseline(wl, args.cpu_seconds)
-    launches = kernels_per_step(di.hidden is not None, fused_select=True, num_segs=wl.num_segs) * args.steps
+    launches = kernels_per_step(fused_importance=True) * args.steps
     # the committed ncu record is of the 32768-token long-context launch: it applies to that workload only
     traffic = None
     if args.workload == "long_single" and wl.num_tokens == 32768:
-        traffic = recorded_traffic(os.path.join(ROOT, "sparsified_long_context_gb300", "csrc", "unip_attention.cu"),
-                                   "attn_fwd_long_single.md")
+        traffic = recorded_traffic("attn_fwd_kernel<128> long_single 32768")
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
@@ -635,15 +796,18 @@ def main():
                    "useful_attention_flops_per_step": flops_step},
         "parts": {
             "attention_ms": attn_ms, "attention_tflops": attn_tflops, "attention_frac_bf16": attn_tflops / bf16_peak,
-            "importance_ms": imp_ms,
-            "select_gather_ms": sel_ms, "select_gather_ms_in_step_events": sel_ms_events,
-            "select_gather_timing": "incremental: graph replays of [L2 flush, importance, select+gather] minus "
-                                    "[L2 flush, importance]",
+            "importance_ms": imp_ms, "importance_select_gather_ms_in_step": isg_ms,
+            "select_gather_ms": sel_ms,
+            "select_gather_timing": "incremental: graph replays of [L2 flush, importance + selection + compaction "
+                                    "(unip_importance_select_gather)] minus [L2 flush, importance "
+                                    "(unip_block_importance)]; importance_ms: [L2 flush, importance] minus "
+                                    "[L2 flush]",
             "select_gather_bytes": sg_bytes, "select_gather_gbs": sg_gbs,
             "select_gather_frac_hbm": sg_gbs / hbm_peak, "n_kept": n_kept, "n_blocks": n_blocks,
             "rope_append": rope,
             "workload_context": workload_context(wl, attn_ms, bf16_peak, hbm_peak),
             "peaks": f"{peak_src}: bf16 {bf16_peak} TFLOP/s, HBM {hbm_peak} GB/s",
+            "workloads": parts_wl,
         },
         "roofline": {"bound": "tensor", "achieved": attn_tflops, "peak": bf16_peak, "unit": "TFLOP/s",
                      "frac": attn_tflops / bf16_peak, "traffic": traffic,

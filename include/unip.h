@@ -198,6 +198,75 @@ UNIP_API int32_t unip_compacted_attention(const void *q, const void *k, const vo
                                           void *stream);
 
 /* ---------------------------------------------------------------------------
+ * Host-planned attention: the same operation as unip_prefill_attention /
+ * unip_compacted_attention, with the work partition computed on the host.
+ *
+ * A serving step knows its batch layout on the host before anything runs
+ * ([CP] "Como funciona o pre-preenchimento segmentado": the scheduler builds
+ * each step from a token budget; unip_step_builder_next returns it).  From
+ * host copies of cu_seqlens and of every segment's cached-prefix length the
+ * plan cuts the call into work items, balances them over the SMs and passes
+ * them to the kernel by value, so no planning kernel runs and no per-item
+ * metadata is read from device memory.  One plan serves every attention call
+ * of the step with that layout (every layer).
+ *
+ * A call with too few work items to fill the GPU (a short chunk behind a long
+ * cached prefix, a few decode tokens with long contexts: [CP] "Ajustar o
+ * orcamento de tokens", later chunks re-read the growing cache) also splits
+ * the key range of its query tiles over several items; each item keeps fp32
+ * partial results (unnormalised output, running maximum and sum) in the
+ * workspace, and the last item of a tile to finish merges them in key order.
+ * The merge order is fixed, so results do not depend on timing, but they
+ * differ from the unsplit computation by floating-point rounding.
+ *
+ * unip_attention_plan_create
+ *   cu_seqlens   host int32 [num_segs + 1] (cu[0] = 0, non-decreasing, cu[S] = total_tokens)
+ *   prefix_lens  host int32 [num_segs]: cached keys before each segment's first token
+ *                (the first position for a contiguous stream; the kept-prefix length for a
+ *                compacted one); NULL: no segment has a prefix
+ *   page_size, max_pages_per_seq: of the paged cache the calls will pass (ignored without prefixes)
+ *   flags        UNIP_PLAN_NO_SPLIT: never split key ranges; UNIP_PLAN_SPLITS(n), 2 <= n <= 255:
+ *                split every query unit's key range into min(n, its key tiles) items instead of
+ *                letting the cost model decide (tuning, tests); UNIP_PLAN_DEVICE: use the device
+ *                planner of unip_prefill_attention (as does any call the plan cannot hold:
+ *                more than 128 segments or 1024 work items)
+ *   num_sms      SMs of the device the calls will run on; 0: the current device's
+ *   *plan        receives a host object; release it with unip_attention_plan_destroy.
+ *   Errors: INVALID_ARGUMENT (bad sizes or metadata, a prefix longer than its pages, num_sms
+ *   negative), UNSUPPORTED (head_dim, page size), TOO_LARGE (host memory).  Nothing touches
+ *   the GPU except, with num_sms 0, a query of the current device's SM count.
+ * unip_attention_plan_workspace_size: bytes of device workspace the runs need (256-aligned).
+ * unip_attention_plan_info: info[0] 1 if host-planned, info[1] work items, info[2] CTAs,
+ *   info[3] split query units, info[4] key splits in total, info[5] 1 if one query tile per item.
+ * unip_prefill_attention_planned
+ *   q, k, v, out, lse, paged: as unip_prefill_attention; q, k, v, out must hold the
+ *   plan's total_tokens rows.  cu_seqlens, positions (and prefix_lens, NULL for a
+ *   contiguous stream) are the device copies of the layout; only a device-planned
+ *   plan reads them.  paged must match the plan's page size and max_pages_per_seq.
+ *   workspace: >= unip_attention_plan_workspace_size bytes, 256-byte aligned, not
+ *   shared with a call that may run at the same time.  The first run of a plan on a
+ *   workspace clears the workspace's ticket area (one small memset on the stream).
+ *   A plan may be used by one host thread at a time.
+ * ------------------------------------------------------------------------- */
+typedef struct unip_attn_plan unip_attn_plan;
+#define UNIP_PLAN_NO_SPLIT 0x1
+#define UNIP_PLAN_DEVICE 0x2
+#define UNIP_PLAN_SPLITS(n) (((n) & 0xFF) << 8)
+UNIP_API int32_t unip_attention_plan_create(const int32_t *cu_seqlens, int32_t num_segs,
+                                            const int32_t *prefix_lens, int32_t total_tokens,
+                                            const unip_attn_params *prm, int32_t page_size,
+                                            int32_t max_pages_per_seq, int32_t flags, int32_t num_sms,
+                                            unip_attn_plan **plan);
+UNIP_API size_t unip_attention_plan_workspace_size(const unip_attn_plan *plan);
+UNIP_API int32_t unip_attention_plan_info(const unip_attn_plan *plan, int32_t *info);
+UNIP_API void unip_attention_plan_destroy(unip_attn_plan *plan);
+UNIP_API int32_t unip_prefill_attention_planned(const unip_attn_plan *plan, const void *q, const void *k,
+                                                const void *v, const int32_t *cu_seqlens,
+                                                const int32_t *positions, const int32_t *prefix_lens,
+                                                const unip_paged_kv *paged, void *out, float *lse,
+                                                void *workspace, size_t workspace_bytes, void *stream);
+
+/* ---------------------------------------------------------------------------
  * Attention without caller-provided workspace.  The paper has no counterpart:
  * this is a library convenience.  It computes exactly what
  * unip_prefill_attention computes, but its scratch (the tile plan) lives in a
@@ -309,6 +378,29 @@ UNIP_API int32_t unip_select_gather(const float *imp, const int32_t *blk_cu, con
                                     const void *hidden, int64_t row_stride, int32_t d_model,
                                     void *hidden_out, int64_t out_row_stride,
                                     void *workspace, size_t workspace_bytes, void *stream);
+
+/* ---------------------------------------------------------------------------
+ * Importance, selection and compaction in one call ([UP] section 3: block
+ * importance at a full-attention layer, then the Top-p block set of section
+ * 1, then the dropped tokens leave the later sub-layers).  The outputs of
+ * unip_block_importance (imp, blk_cu) and of unip_select_gather (keep,
+ * gather_idx, cu_seqlens_kept, positions_kept, n_kept, hidden_out), with the
+ * same bits: the normalisation and the selection of a segment run in one CTA
+ * (the scores never make a round trip through memory before they are ranked),
+ * and the row copy is a programmatic dependent of that grid.  Arguments as in
+ * the two calls; workspace: unip_importance_select_gather_workspace_size()
+ * bytes, 256-byte aligned.  Returns UNIP_OK or a host error code with nothing
+ * enqueued; device errors as in the two calls.
+ * ------------------------------------------------------------------------- */
+UNIP_API size_t unip_importance_select_gather_workspace_size(int32_t total_tokens, int32_t num_segs,
+                                                             int32_t block_size, const unip_attn_params *prm);
+UNIP_API int32_t unip_importance_select_gather(
+    const void *q, const void *k, const float *lse, const int32_t *cu_seqlens, const int32_t *positions,
+    int32_t num_segs, int32_t total_tokens, const uint8_t *seg_mask, int32_t block_size,
+    const unip_attn_params *prm, double p, uint32_t flags, float *imp, int32_t imp_capacity, int32_t *blk_cu,
+    uint8_t *keep, int32_t *gather_idx, int32_t *cu_seqlens_kept, int32_t *positions_kept, int32_t *n_kept,
+    const void *hidden, int64_t row_stride, int32_t d_model, void *hidden_out, int64_t out_row_stride,
+    void *workspace, size_t workspace_bytes, void *stream);
 
 /* Rotary position embedding of q and k in place, by each token's own
  * position, and append of the rotated k and of v into the paged KV cache.

@@ -92,6 +92,17 @@ def load(build_if_missing: bool = True):
         lib.unip_prefill_attention_noalloc.restype = i32
         lib.unip_prefill_attention_noalloc.argtypes = [P, P, P, P, i32, P, i32, ctypes.POINTER(_PagedKV), pp, P, P,
                                                        P]
+        lib.unip_attention_plan_create.restype = i32
+        lib.unip_attention_plan_create.argtypes = [P, i32, P, i32, pp, i32, i32, i32, i32, ctypes.POINTER(P)]
+        lib.unip_attention_plan_workspace_size.restype = sz
+        lib.unip_attention_plan_workspace_size.argtypes = [P]
+        lib.unip_attention_plan_info.restype = i32
+        lib.unip_attention_plan_info.argtypes = [P, P]
+        lib.unip_attention_plan_destroy.restype = None
+        lib.unip_attention_plan_destroy.argtypes = [P]
+        lib.unip_prefill_attention_planned.restype = i32
+        lib.unip_prefill_attention_planned.argtypes = [P, P, P, P, P, P, P, ctypes.POINTER(_PagedKV), P, P, P, sz,
+                                                       P]
         lib.unip_importance_capacity.restype = i32
         lib.unip_importance_capacity.argtypes = [i32, i32, i32]
         lib.unip_importance_workspace_size.restype = sz
@@ -105,6 +116,11 @@ def load(build_if_missing: bool = True):
         lib.unip_select_gather.restype = i32
         lib.unip_select_gather.argtypes = [P, P, P, P, i32, i32, i32, f64, u32, P, i32, P, P, P, P, P, i64, i32, P, i64,
                                            P, sz, P]
+        lib.unip_importance_select_gather_workspace_size.restype = sz
+        lib.unip_importance_select_gather_workspace_size.argtypes = [i32, i32, i32, pp]
+        lib.unip_importance_select_gather.restype = i32
+        lib.unip_importance_select_gather.argtypes = [P, P, P, P, P, i32, i32, P, i32, pp, f64, u32, P, i32, P, P,
+                                                      P, P, P, P, P, i64, i32, P, i64, P, sz, P]
         lib.unip_gather_tokens.restype = i32
         lib.unip_gather_tokens.argtypes = [P, i32, i64, i32, P, P, i32, P, i64, P]
         lib.unip_selftest_bounded_wait.restype = i32
@@ -242,6 +258,80 @@ def unip_compacted_attention(q, k, v, cu_seqlens, positions, prefix_lens, out, l
     return out, lse
 
 
+UNIP_PLAN_NO_SPLIT = 0x1
+UNIP_PLAN_DEVICE = 0x2
+
+
+def UNIP_PLAN_SPLITS(n: int) -> int:
+    return (int(n) & 0xFF) << 8
+
+
+class AttentionPlan:
+    """Host-built work plan of attention calls over one batch layout (unip_attention_plan_*).
+
+    cu_seqlens and prefix_lens are host arrays (numpy or lists); the plan is reused by every call
+    with that layout.  ``workspace_bytes`` is the device workspace a run needs; ``info`` reports
+    whether the plan is host-built, its items, CTAs, split units, key splits and tile shape."""
+
+    def __init__(self, cu_seqlens, prefix_lens, *, num_heads_q, num_heads_kv, head_dim, page_size=16,
+                 max_pages_per_seq=0, scale=None, flags=0, num_sms=0):
+        import numpy as np
+        lib = load()
+        self._lib = lib
+        self._h = None
+        cu = np.ascontiguousarray(cu_seqlens, dtype=np.int32)
+        S = int(cu.shape[0]) - 1
+        pre = None if prefix_lens is None else np.ascontiguousarray(prefix_lens, dtype=np.int32)
+        if pre is not None and pre.shape[0] != S:
+            raise UnipError("prefix_lens must have one entry per segment")
+        self.num_tokens = int(cu[-1])
+        self.num_segs = S
+        self.head_dim = int(head_dim)
+        self.num_heads_q = int(num_heads_q)
+        prm = _params(num_heads_q, num_heads_kv, head_dim, scale)
+        h = ctypes.c_void_p()
+        _check(lib.unip_attention_plan_create(cu.ctypes.data, S, None if pre is None else pre.ctypes.data,
+                                              self.num_tokens, ctypes.byref(prm), int(page_size),
+                                              int(max_pages_per_seq), int(flags), int(num_sms), ctypes.byref(h)),
+               "unip_attention_plan_create")
+        self._h = h
+        self.workspace_bytes = int(lib.unip_attention_plan_workspace_size(h))
+        info = (ctypes.c_int32 * 6)()
+        _check(lib.unip_attention_plan_info(h, info), "unip_attention_plan_info")
+        self.info = {"host": bool(info[0]), "items": info[1], "ctas": info[2], "split_units": info[3],
+                     "splits": info[4], "single": bool(info[5])}
+
+    def close(self):
+        if self._h is not None:
+            self._lib.unip_attention_plan_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def run(self, q, k, v, out, lse=None, *, cu_seqlens=None, positions=None, prefix_lens=None, k_cache=None,
+            v_cache=None, block_table=None, page_size=16, workspace=None, stream=None):
+        """unip_prefill_attention_planned: out [N,Hq,D] bf16 and lse [Hq,N] fp32 (device tensors).
+        cu_seqlens / positions / prefix_lens: the device copies of the layout (read only when the plan
+        fell back to the device planner)."""
+        if workspace is None:
+            workspace = _workspace(self.workspace_bytes, q.device)
+        paged_p = None
+        if k_cache is not None:
+            paged = _PagedKV(_ptr(k_cache), _ptr(v_cache), int(k_cache.shape[0]), int(page_size), _ptr(block_table),
+                             int(block_table.shape[1]))
+            paged_p = ctypes.byref(paged)
+        rc = self._lib.unip_prefill_attention_planned(self._h, _ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens),
+                                                      _ptr(positions), _ptr(prefix_lens), paged_p, _ptr(out),
+                                                      _ptr(lse), _ptr(workspace), workspace.numel(),
+                                                      _stream(stream))
+        _check(rc, "unip_prefill_attention_planned")
+        return out, lse
+
+
 def unip_prefill_attention_noalloc(q, k, v, cu_seqlens, positions, out, lse=None, *, num_heads_q, num_heads_kv,
                                    head_dim, k_cache=None, v_cache=None, block_table=None, page_size=16,
                                    scale=None, stream=None):
@@ -336,6 +426,45 @@ def unip_select_gather(imp, blk_cu, cu_seqlens, positions, keep, gather_idx, cu_
                                 _ptr(cu_seqlens_kept), _ptr(positions_kept), _ptr(n_kept), h_ptr, h_stride,
                                 d_model, o_ptr, o_stride, _ptr(workspace), workspace.numel(), _stream(stream))
     _check(rc, "unip_select_gather")
+
+
+def unip_importance_select_gather_workspace_size(total_tokens, num_segs, block_size, hq, hkv, d) -> int:
+    p = _params(hq, hkv, d, 0.0)
+    return int(load().unip_importance_select_gather_workspace_size(int(total_tokens), int(num_segs), int(block_size),
+                                                                   ctypes.byref(p)))
+
+
+def unip_importance_select_gather(q, k, lse, cu_seqlens, positions, imp, blk_cu, keep, gather_idx, cu_seqlens_kept,
+                                  positions_kept, n_kept, hidden, hidden_out, *, block_size, p, num_heads_q,
+                                  num_heads_kv, head_dim, seg_mask=None, scale=None,
+                                  flags=UNIP_KEEP_FIRST | UNIP_KEEP_LAST, workspace=None, stream=None):
+    """Block importance, Top-p selection and compaction in one call (the outputs of
+    unip_block_importance and unip_select_gather)."""
+    lib = load()
+    n = int(positions.shape[0])
+    S = int(cu_seqlens.shape[0]) - 1
+    prm = _params(num_heads_q, num_heads_kv, head_dim, scale)
+    need = lib.unip_importance_select_gather_workspace_size(n, S, int(block_size), ctypes.byref(prm))
+    if workspace is None:
+        workspace = _workspace(need, q.device)
+    if (hidden is None) != (hidden_out is None):
+        raise UnipError("hidden and hidden_out are given together or not at all")
+    if hidden is None:
+        h_ptr = o_ptr = None
+        h_stride = o_stride = d_model = 0
+    else:
+        for t in (hidden, hidden_out):
+            if not t.is_cuda:
+                raise UnipError("libunip takes CUDA tensors only (no CPU fallback)")
+        h_ptr, o_ptr = hidden.data_ptr(), hidden_out.data_ptr()
+        h_stride, o_stride, d_model = int(hidden.stride(0)), int(hidden_out.stride(0)), int(hidden.shape[1])
+    rc = lib.unip_importance_select_gather(_ptr(q), _ptr(k), _ptr(lse), _ptr(cu_seqlens), _ptr(positions), S, n,
+                                           _ptr(seg_mask), int(block_size), ctypes.byref(prm), float(p), int(flags),
+                                           _ptr(imp), int(imp.numel()), _ptr(blk_cu), _ptr(keep), _ptr(gather_idx),
+                                           _ptr(cu_seqlens_kept), _ptr(positions_kept), _ptr(n_kept), h_ptr, h_stride,
+                                           d_model, o_ptr, o_stride, _ptr(workspace), workspace.numel(),
+                                           _stream(stream))
+    _check(rc, "unip_importance_select_gather")
 
 
 def unip_gather_tokens(hidden, gather_idx, n_kept, out, *, stream=None):

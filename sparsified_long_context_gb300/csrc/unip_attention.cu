@@ -47,18 +47,21 @@
 #include <cuda_bf16.h>
 
 #include <algorithm>
+#include <atomic>
+#include <climits>
+#include <cmath>
 #include <cstring>
 #include <mutex>
+#include <new>
+#include <queue>
+#include <vector>
 
-#include <atomic>
-
+#include "unip_attention_common.cuh"
 #include "unip_internal.cuh"
 
 namespace unip {
 namespace {
 
-constexpr int kBlockM = 128;
-constexpr int kBlockN = 128;
 constexpr int kHistBins = 4096;
 constexpr int kPlanThreads = 1024;
 constexpr int kWsHeaderBytes = 256;
@@ -84,12 +87,6 @@ struct AttnArgs {
   int32_t lg;  // 0: a tile's rows are 128 tokens of one head; log2(group): rows are (token, head of the group)
   int32_t single;  // 1: every work item is one query tile (calls with too few items to fill the GPU)
   float scale_log2;
-};
-
-// Rows of one query tile: row R is token tok0 + (R >> lg) (segment-local) and
-// query head head0 + (R & (2^lg - 1)); rows at or past rows_valid are not stored.
-struct TileRows {
-  int32_t tok0, head0, lg, rows_valid;
 };
 
 // ---------------------------------------------------------------------------
@@ -282,7 +279,9 @@ enum BarId {
   kBarSlotGo0 = 12 + 2 * kStages,      // + slot: a prefix fill of the slot may be issued (helpers)
   kBarUnitFull0 = 12 + 3 * kStages,    // + k: work item i (k = i & 1) published in s_unit[k]
   kBarUnitEmpty0 = 14 + 3 * kStages,   // + k: every consumer warp has read s_unit[k]
-  kNumBars = 16 + 3 * kStages
+  kBarSplitStored0 = 16 + 3 * kStages,  // + tile: split epilogue, every thread stored its partial (count 256)
+  kBarSplitDecided0 = 18 + 3 * kStages, // + tile: split epilogue, the ticket was taken (count 1)
+  kNumBars = 20 + 3 * kStages
 };
 
 __device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
@@ -314,11 +313,160 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
 
 // sb0 / sb1, pvb and ob: completions of S-full 0 / 1, PV-done and this tile's O-done before this
 // work item (the barriers run on across the items of a persistent CTA).  Returns false on a timeout.
-template <int D, bool db>
-__device__ __forceinline__ bool softmax_tile_role(const AttnArgs &a, int tile, const TileRows tr, int32_t T,
-                                                  int32_t Tp, int32_t P, int32_t c0, uint32_t tmem,
+// Split of a host-planned item whose unit's key range is divided over several items.
+struct SplitCtx {
+  float *partial;
+  unsigned long long *tickets;
+  int32_t *last;  // shared memory, one flag per tile
+  uint32_t gen;
+  int32_t split, nsplit, g0;
+};
+
+// Counts this split into the ticket of its (unit, tile); true for the split that completes the
+// count.  The ticket carries the launch generation in its upper half, so a count left by an
+// earlier launch (or an aborted one) reads as zero.
+__device__ __forceinline__ bool split_ticket(unsigned long long *tk, uint32_t gen, int32_t nsplit, uint32_t *status) {
+  const unsigned long long tag = static_cast<unsigned long long>(gen) << 32;
+  unsigned long long cur = atomicAdd(tk, 0ull);
+  for (int it = 0; it < (1 << 20); ++it) {
+    const unsigned long long want = ((cur >> 32) == gen) ? cur + 1 : (tag | 1ull);
+    const unsigned long long prev = atomicCAS(tk, cur, want);
+    if (prev == cur) return static_cast<uint32_t>(want) == static_cast<uint32_t>(nsplit);
+    cur = prev;
+  }
+  atomicOr(status, UNIP_DEV_TIMEOUT);
+  return false;
+}
+
+// Epilogue of a split item.  Every thread of the tile stores the accumulator values it holds and its
+// rows' (m, l) into the split's partial slot; the split that finishes a (unit, tile) last merges the
+// slots of all splits in split order (so the result does not depend on which split finished last):
+//   M = max_k m_k,  w_k = 2^(m_k - M),  out = sum_k w_k O_k / sum_k w_k l_k,  lse = ln 2 (M + log2 sum_k w_k l_k).
+// Warps past the tile's valid rows keep only the barrier protocol.  sep: split epilogues this tile
+// ran before (phase of its two split barriers).  Returns false when a bounded wait gave up.
+template <int D>
+__device__ __noinline__ bool split_epilogue(const AttnArgs &a, const SplitCtx &sp, int tile, const TileRows tr,
+                                            bool active, uint32_t tw, uint32_t o_col, uint32_t bar_free,
+                                            float m0, float l0, float m1, float l1, int32_t c0, uint64_t *bars,
+                                            volatile int *abort_flag, uint32_t sep) {
+  using SL = SplitLayout<D>;
+  constexpr int kC = SL::kChunks;
+  const int lane = threadIdx.x & 31;
+  const int t = threadIdx.x & 255;  // thread of the tile's 256 softmax threads
+  const int wt = (threadIdx.x >> 5) & 7;
+  const int R0 = 32 * (wt & 3) + 16 * (wt >> 2) + (lane >> 2), R1 = R0 + 8;
+  const int cq = 2 * (lane & 3);
+  auto slot_chunk = [&](int32_t k, int c) {
+    const size_t slot = (size_t)(sp.g0 + k) * 2 + tile;
+    return reinterpret_cast<float4 *>(sp.partial) + (slot * kC + c) * 256 + t;
+  };
+  if (active) {
+    float o[D / 2];
+#pragma unroll
+    for (int part = 0; part < D / 32; ++part) tmem_ld_16x256b_x4(tw + o_col + part * 32, o + 16 * part);
+    tmem_wait_ld();
+    tc_fence_before();
+    mbar_arrive(bar_free);  // O is in registers: the next item's first PV may overwrite it
+#pragma unroll
+    for (int c = 0; c < D / 8; ++c) __stcg(slot_chunk(sp.split, c), make_float4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]));
+    __stcg(slot_chunk(sp.split, D / 8), make_float4(m0, l0, m1, l1));
+  } else {
+    mbar_arrive(bar_free);
+  }
+  // Every thread's partial is stored before thread 0 counts the split in: the mbarrier orders the
+  // tile's stores before thread 0's fence, which makes them visible to the whole GPU before its
+  // ticket update (the pattern of a grid-wide barrier).
+  const uint32_t bar_stored = smem_u32(&bars[kBarSplitStored0 + tile]);
+  const uint32_t bar_decided = smem_u32(&bars[kBarSplitDecided0 + tile]);
+  mbar_arrive(bar_stored);
+  if (t == 0) {
+    const bool ok = mbar_wait(bar_stored, sep & 1, abort_flag, a.status);
+    __threadfence();
+    sp.last[tile] =
+        ok && split_ticket(sp.tickets + (size_t)sp.g0 * 2 + tile, sp.gen, sp.nsplit, a.status) ? 1 : 0;
+    __threadfence();
+    mbar_arrive(bar_decided);  // also after a timeout, so that no thread of the tile waits for it
+  }
+  if (!mbar_wait(bar_decided, sep & 1, abort_flag, a.status)) return false;
+  if (!sp.last[tile] || !active) return true;
+  // Merge.  Loads are batched across splits (independent loads in flight) so that the merge costs a
+  // few L2 round trips rather than one per split.
+  const int32_t n = sp.nsplit;
+  float M0 = -INFINITY, M1 = -INFINITY;
+  for (int32_t k0 = 0; k0 < n; k0 += 8) {
+    float4 st[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) st[u] = k0 + u < n ? __ldcg(slot_chunk(k0 + u, D / 8)) : make_float4(-INFINITY, 0.f, -INFINITY, 0.f);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      M0 = fmaxf(M0, st[u].x);
+      M1 = fmaxf(M1, st[u].z);
+    }
+  }
+  const int32_t tok_r0 = tr.tok0 + (R0 >> tr.lg), tok_r1 = tr.tok0 + (R1 >> tr.lg);
+  const int32_t t0 = c0 + tok_r0, t1 = c0 + tok_r1;
+  const int32_t hm = (1 << tr.lg) - 1;
+  const int32_t h0 = tr.head0 + (R0 & hm), h1 = tr.head0 + (R1 & hm);
+  const bool st0 = R0 < tr.rows_valid, st1 = R1 < tr.rows_valid;
+  __nv_bfloat16 *o0 = a.out + ((int64_t)t0 * a.Hq + h0) * D + cq;
+  __nv_bfloat16 *o1 = a.out + ((int64_t)t1 * a.Hq + h1) * D + cq;
+  // chunk c holds columns 8c + cq + {0, 1} of rows R0 (x, y) and R1 (z, w); four chunks at a time,
+  // three splits per batch of loads
+  constexpr int kG = 4, kB = 3;
+  float L0 = 0.f, L1 = 0.f;
+#pragma unroll 1
+  for (int grp = 0; grp < D / 8 / kG; ++grp) {
+    float4 acc[kG];
+#pragma unroll
+    for (int c = 0; c < kG; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int32_t k0 = 0; k0 < n; k0 += kB) {
+      float4 st[kB], v[kB][kG];
+#pragma unroll
+      for (int u = 0; u < kB; ++u) {
+        const bool in = k0 + u < n;
+        st[u] = in ? __ldcg(slot_chunk(k0 + u, D / 8)) : make_float4(-INFINITY, 0.f, -INFINITY, 0.f);
+#pragma unroll
+        for (int c = 0; c < kG; ++c)
+          v[u][c] = in ? __ldcg(slot_chunk(k0 + u, grp * kG + c)) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < kB; ++u) {
+        const float w0 = ex2_approx(st[u].x - M0), w1 = ex2_approx(st[u].z - M1);
+        if (grp == 0) {
+          L0 += w0 * st[u].y;
+          L1 += w1 * st[u].w;
+        }
+#pragma unroll
+        for (int c = 0; c < kG; ++c) {
+          acc[c].x += w0 * v[u][c].x;
+          acc[c].y += w0 * v[u][c].y;
+          acc[c].z += w1 * v[u][c].z;
+          acc[c].w += w1 * v[u][c].w;
+        }
+      }
+    }
+    const float inv0 = 1.f / L0, inv1 = 1.f / L1;
+#pragma unroll
+    for (int c = 0; c < kG; ++c) {
+      const int col = 8 * (grp * kG + c);
+      if (st0) *reinterpret_cast<uint32_t *>(o0 + col) = pack_bf16x2(acc[c].x * inv0, acc[c].y * inv0);
+      if (st1) *reinterpret_cast<uint32_t *>(o1 + col) = pack_bf16x2(acc[c].z * inv1, acc[c].w * inv1);
+    }
+  }
+  if ((lane & 3) == 0 && a.lse) {
+    if (st0) a.lse[(int64_t)h0 * a.N + t0] = (M0 + log2f(L0)) * kLn2;
+    if (st1) a.lse[(int64_t)h1 * a.N + t1] = (M1 + log2f(L1)) * kLn2;
+  }
+  return true;
+}
+
+// j0: first key tile of this item within its unit's key range (0 unless the range is split).
+template <int D, bool db, bool kHost>
+__device__ __forceinline__ bool softmax_tile_role(const AttnArgs &a, int tile, const TileRows tr, int32_t j0,
+                                                  int32_t T, int32_t Tp, int32_t P, int32_t c0, uint32_t tmem,
                                                   uint64_t *bars, volatile int *abort_flag, uint32_t sb0,
-                                                  uint32_t sb1, uint32_t pvb, uint32_t ob) {
+                                                  uint32_t sb1, uint32_t pvb, uint32_t ob, const SplitCtx &sp,
+                                                  uint32_t &sep) {
   const int wt = (threadIdx.x >> 5) & 7;
   const int lane = threadIdx.x & 31;
   const int q = wt & 3, g = wt >> 2;
@@ -349,9 +497,10 @@ __device__ __forceinline__ bool softmax_tile_role(const AttnArgs &a, int tile, c
     tmem_ld_16x256b_x8(tw + s_col, sv);
     tmem_ld_16x256b_x8(tw + s_col + 64, sv + 32);
     tmem_wait_ld();
-    if (j < Tp) {
-      if (j == Tp - 1) {
-        const int lim = P - j * kBlockN;  // keys at or past the prefix end are not cached tokens
+    const int32_t jg = j0 + j;  // key tile within the unit's range
+    if (jg < Tp) {
+      if (jg == Tp - 1) {
+        const int lim = P - jg * kBlockN;  // keys at or past the prefix end are not cached tokens
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
           const int col = 8 * k + cq;
@@ -360,8 +509,8 @@ __device__ __forceinline__ bool softmax_tile_role(const AttnArgs &a, int tile, c
         }
       }
     } else {
-      // own keys: key (j - Tp) * 128 + col is visible to a row whose token index is at least that
-      const int32_t lim0 = tok_r0 - (j - Tp) * kBlockN, lim1 = tok_r1 - (j - Tp) * kBlockN;
+      // own keys: key (jg - Tp) * 128 + col is visible to a row whose token index is at least that
+      const int32_t lim0 = tok_r0 - (jg - Tp) * kBlockN, lim1 = tok_r1 - (jg - Tp) * kBlockN;
       if (min(lim0, lim1) < kBlockN - 1) {
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
@@ -446,6 +595,13 @@ __device__ __forceinline__ bool softmax_tile_role(const AttnArgs &a, int tile, c
   // that item's epilogue still reads it.
   const uint32_t bar_free = smem_u32(&bars[kBarOFree0 + tile]);
   if (!mbar_wait(bar_o, ob & 1, abort_flag, a.status)) return false;
+  if constexpr (kHost) {
+    if (sp.nsplit > 1) {
+      tc_fence_after();
+      return split_epilogue<D>(a, sp, tile, tr, active, tw, o_col, bar_free, m0, l0, m1, l1, c0, bars, abort_flag,
+                               sep++);
+    }
+  }
   if (!active) {  // warp-uniform: no row of this warp is stored, O is not read
     mbar_arrive(bar_free);
     return true;
@@ -486,56 +642,41 @@ __device__ __forceinline__ bool softmax_tile_role(const AttnArgs &a, int tile, c
 }
 
 // One work item = two 128-row query tiles of one segment that share every K/V
-// tile (one tile when the second would hold no valid row).  With lg = 0 (odd
-// or non-dividing GQA group) the tiles are 128 tokens of the query heads h0
-// and h0 + 1 of one kv head; with lg = log2(G) each row is a (token, head) pair
-// of the G query heads of kv head g, so a tile covers 128 / G tokens and a
-// single decode token still fills G rows.  When a call holds too few items to
-// give every SM one (a short chunk), `single` makes every item one tile, twice
-// as many items at the same total work.
-struct WorkItem {
-  TileRows tr0, tr1;
-  int32_t s, c0, P, g, Tp, T;
-  bool two, valid;
-};
-
+// tile (one tile when the second would hold no valid row); see unit_geometry.
+// When a call holds too few items to give every SM one (a short chunk),
+// `single` makes every item one tile, twice as many items at the same total
+// work.  A host-planned call may also split a unit's key range over several
+// items (WorkItem::j0, T, split, nsplit), merged by the last one to finish.
 __device__ __forceinline__ WorkItem decode_item(const AttnArgs &a, int32_t unit) {
-  WorkItem w;
   const int32_t pair_idx = unit / a.heads_per_pair, hsel = unit % a.heads_per_pair;
   const int2 pr = a.pairs[pair_idx];
-  w.s = pr.x;
-  const int32_t m = pr.y;
-  w.c0 = a.cu[w.s];
-  const int32_t n = a.cu[w.s + 1] - w.c0;
-  w.P = a.prefix_lens ? a.prefix_lens[w.s] : a.pos[w.c0];
-  if (a.lg > 0) {
-    const int32_t subs = a.single ? a.group : (a.group >> 1);  // work items per kv head for one 128-token pair
-    w.g = hsel / subs;
-    const int32_t tpt = kBlockM >> a.lg;
-    w.tr0.tok0 = m * kBlockM + (hsel - w.g * subs) * (a.single ? 1 : 2) * tpt;
-    w.tr1.tok0 = w.tr0.tok0 + tpt;
-    w.tr0.head0 = w.tr1.head0 = w.g * a.group;
-    w.tr0.lg = w.tr1.lg = a.lg;
-    w.tr0.rows_valid = min(kBlockM, max(0, n - w.tr0.tok0) << a.lg);
-    w.tr1.rows_valid = min(kBlockM, max(0, n - w.tr1.tok0) << a.lg);
-    w.two = !a.single && w.tr1.rows_valid > 0;
-  } else {
-    w.two = !a.single && (a.group & 1) == 0;
-    const int32_t h0 = w.two ? 2 * hsel : hsel;
-    w.g = h0 / a.group;
-    w.tr0.tok0 = w.tr1.tok0 = m * kBlockM;
-    w.tr0.head0 = h0;
-    w.tr1.head0 = h0 + 1;
-    w.tr0.lg = w.tr1.lg = 0;
-    w.tr0.rows_valid = w.tr1.rows_valid = min(kBlockM, n - m * kBlockM);
-  }
-  w.valid = w.tr0.rows_valid > 0;  // else every token of the item lies past the segment
-  const TileRows &trl = w.two ? w.tr1 : w.tr0;  // the tile holding the item's last token
-  const int32_t end_tok = trl.tok0 + (trl.rows_valid >> trl.lg);
-  w.Tp = (w.P + kBlockN - 1) / kBlockN;                 // prefix KV tiles
-  w.T = w.valid ? w.Tp + (end_tok - 1) / kBlockN + 1 : 0;  // + own tiles up to the last token's
+  const int32_t c0 = a.cu[pr.x];
+  const int32_t n = a.cu[pr.x + 1] - c0;
+  const int32_t P = a.prefix_lens ? a.prefix_lens[pr.x] : a.pos[c0];
+  return unit_geometry(pr.x, pr.y, hsel, c0, n, P, a.lg, a.group, a.single);
+}
+
+// Item u of a host-built plan.
+__device__ __forceinline__ WorkItem decode_plan_item(const AttnArgs &a, const HostPlanArgs &hp, int32_t u) {
+  const PlanItem it = hp.items[u];
+  const int32_t s = it.w0 & 0xFFFF, hsel = (int32_t)((uint32_t)it.w0 >> 16);
+  const int32_t m = it.w1 & 0xFFFFFF, nsplit = (int32_t)((uint32_t)it.w1 >> 24);
+  WorkItem w = unit_geometry(s, m, hsel, hp.seg[s][0], hp.seg[s][1], hp.seg[s][2], a.lg, a.group, a.single);
+  w.j0 = it.w2 & 0xFFFF;
+  w.T = (int32_t)((uint32_t)it.w2 >> 16);
+  w.nsplit = nsplit;
+  w.g0 = it.w3 & 0xFFFFFF;
+  w.split = (int32_t)((uint32_t)it.w3 >> 24);
   return w;
 }
+
+// Kernel parameter of the host-planned variant; the device-planned one gets a placeholder.
+template <bool kHost>
+struct PlanParam {
+  int32_t unused;
+};
+template <>
+struct PlanParam<true> : HostPlanArgs {};
 
 // Persistent: the TMA warp claims the next non-empty work item of the
 // planner's longest-first list from a global counter (dynamic longest-first
@@ -544,8 +685,13 @@ __device__ __forceinline__ WorkItem decode_item(const AttnArgs &a, int32_t unit)
 // ring and all barriers run on across items, so the producer streams the next
 // item's Q and K/V while the current one finishes, and the next item's first
 // QK overlaps the current epilogue (its first PV waits until O has been read).
-template <int D>
-__global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_constant__ AttnArgs a) {
+// kHost: the work items come from a plan built on the host (kernel parameter hp): CTA b runs items
+// hp.cta_first[b] .. hp.cta_first[b + 1] - 1 in order, and an item may cover part of its unit's key
+// range (split items, merged in the epilogue).  Otherwise a device planner wrote the item list and
+// the CTAs claim items dynamically.
+template <int D, bool kHost>
+__global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_constant__ AttnArgs a,
+                                                               const __grid_constant__ PlanParam<kHost> hp) {
   using L = SmemLayout<D>;
   constexpr int kHalves = D / 64;
   constexpr int ns = kStages;  // ring slots, after both Q buffers
@@ -555,6 +701,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   __shared__ int s_abort;
   __shared__ int s_tmem_busy;  // 1: tensor-core work could not be confirmed finished, TMEM is kept
   __shared__ int32_t s_unit[2];
+  __shared__ int32_t s_last[2];  // split epilogue: this CTA's split finished its (unit, tile) last
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -582,6 +729,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(kBarUnitFull0 + i), 1);
       mbar_init(bar(kBarUnitEmpty0 + i), kUnitReaders);
+      mbar_init(bar(kBarSplitStored0 + i), 2 * kBlockM);
+      mbar_init(bar(kBarSplitDecided0 + i), 1);
     }
     s_abort = 0;
     s_tmem_busy = 0;
@@ -599,7 +748,28 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   // This grid runs as a programmatic dependent of its planner: the set-up above overlaps the plan,
   // which is read only past here.  A CTA that finds no work left claims nothing and tears down.
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int32_t n_units = *a.num_pairs * a.heads_per_pair;
+  int32_t n_units = 0, first_item = 0;
+  if constexpr (kHost) {
+    first_item = hp.cta_first[blockIdx.x];
+    n_units = hp.cta_first[blockIdx.x + 1] - first_item;
+  } else {
+    n_units = *a.num_pairs * a.heads_per_pair;
+  }
+  auto decode = [&](int32_t u) -> WorkItem {
+    if constexpr (kHost) return decode_plan_item(a, hp, u);
+    else return decode_item(a, u);
+  };
+  SplitCtx sp;
+  if constexpr (kHost) {
+    sp.partial = hp.partial;
+    sp.tickets = hp.tickets;
+    sp.gen = hp.gen;
+  } else {
+    sp.partial = nullptr;
+    sp.tickets = nullptr;
+    sp.gen = 0;
+  }
+  sp.last = s_last;
 
   // Barrier completions before the current item, replayed identically by every role:
   // S-full / P-full per buffer, PV-done, O-done and O-free uses per tile, items done.
@@ -632,17 +802,21 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   if (warp < 16) {
     // ------------------------------------------------------------ softmax + epilogue
     const int tile = warp >> 3;
+    uint32_t sep = 0;  // split epilogues of this warp's tile so far
     for (uint32_t i = 0;; ++i) {
       int32_t u;
       if (!next_unit(i, u) || u < 0) break;
-      const WorkItem w = decode_item(a, u);
+      const WorkItem w = decode(u);
+      sp.split = w.split;
+      sp.nsplit = w.nsplit;
+      sp.g0 = w.g0;
       bool ok = true;
       if (w.two)
-        ok = softmax_tile_role<D, false>(a, tile, tile ? w.tr1 : w.tr0, w.T, w.Tp, w.P, w.c0, tmem, bars,
-                                         abort_flag, cs0, cs1, cpv, tile ? co1 : co0);
+        ok = softmax_tile_role<D, false, kHost>(a, tile, tile ? w.tr1 : w.tr0, w.j0, w.T, w.Tp, w.P, w.c0, tmem,
+                                                bars, abort_flag, cs0, cs1, cpv, tile ? co1 : co0, sp, sep);
       else if (tile == 0)
-        ok = softmax_tile_role<D, true>(a, 0, w.tr0, w.T, w.Tp, w.P, w.c0, tmem, bars, abort_flag, cs0, cs1, cpv,
-                                        co0);
+        ok = softmax_tile_role<D, true, kHost>(a, 0, w.tr0, w.j0, w.T, w.Tp, w.P, w.c0, tmem, bars, abort_flag,
+                                               cs0, cs1, cpv, co0, sp, sep);
       else  // tile 1 idles through a one-tile item but may not run ahead of its S-full completions
         ok = mbar_wait(smem_u32(&bars[kBarODone0 + 0]), co0 & 1, abort_flag, a.status);
       if (!ok) break;
@@ -681,12 +855,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         // claim the next work item with at least one valid row and publish it
         int okq = 1;
         if (lane == 0) {
-          for (;;) {
-            const int32_t c = atomicAdd(a.work_counter, 1);
-            if (c >= n_units) break;
-            if (decode_item(a, c).valid) {
-              u = c;
-              break;
+          if constexpr (kHost) {
+            u = static_cast<int32_t>(i) < n_units ? first_item + static_cast<int32_t>(i) : -1;
+          } else {
+            for (;;) {
+              const int32_t c = atomicAdd(a.work_counter, 1);
+              if (c >= n_units) break;
+              if (decode_item(a, c).valid) {
+                u = c;
+                break;
+              }
             }
           }
           const int k = i & 1;
@@ -702,8 +880,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         break;
       }
       if (u < 0) break;
-      const WorkItem w = decode_item(a, u);
-      const int32_t T = w.T, Tp = w.Tp, P = w.P, c0 = w.c0, g = w.g;
+      const WorkItem w = decode(u);
+      const int32_t T = w.T, Tp = w.Tp, P = w.P, c0 = w.c0, g = w.g, j0 = w.j0;
+      const int32_t Tpl = max(0, min(T, Tp - j0));  // prefix tiles among this item's key tiles
       const bool two = w.two;
       if (pw == 0 && lane == 0) {
         // Q of this item once the previous item's last QK has read the buffers
@@ -726,11 +905,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
       // Page ids in warp-wide batches of 32 entries, fetched two batches ahead, validated at use.
       const int64_t bt_row = (int64_t)w.s * a.max_pages;
-      auto fetch = [&](int32_t j0) -> int32_t {  // raw entry of logical page j0 * ppt + lane, or -1
-        const int32_t lp = j0 * ppt + lane;
-        return (j0 < Tp && lp * a.page_size < P) ? __ldg(&a.block_table[bt_row + lp]) : -1;
+      auto fetch = [&](int32_t jb) -> int32_t {  // raw entry of logical page jb * ppt + lane, or -1
+        const int32_t lp = jb * ppt + lane;
+        return (jb < Tp && lp * a.page_size < P) ? __ldg(&a.block_table[bt_row + lp]) : -1;
       };
-      int32_t bt_cur = fetch(0), bt_nxt = fetch(tpb), bt_nx2 = fetch(2 * tpb);
+      const int32_t jb0 = j0 & ~(tpb - 1);  // block-table batch holding the item's first key tile
+      int32_t bt_cur = fetch(jb0), bt_nxt = fetch(jb0 + tpb), bt_nx2 = fetch(jb0 + 2 * tpb);
       int32_t ph0 = a.num_pages, ph1 = a.num_pages;  // this lane's page of the last two K tiles
       int32_t last_k = -1;
       // Helper warps stop after the item's last prefix copy: V_(Tp-1), load 2Tp - 1 with two query
@@ -738,7 +918,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       // A helper that owns no page of a tile (page size 64 or 128) waits for nothing at all.
       const int32_t n_loads =
           pw == 0 ? 2 * T
-                  : (Tp == 0 || ppt <= pw ? 0 : (two ? 2 * Tp : (Tp - 1 < T - 2 ? 2 * Tp + 1 : Tp + T)));
+                  : (Tpl == 0 || ppt <= pw ? 0 : (two ? 2 * Tpl : (Tpl - 1 < T - 2 ? 2 * Tpl + 1 : Tpl + T)));
       for (int32_t ld = 0; ld < n_loads; ++ld) {
         const int64_t gl = lbase + ld;
         const int slot = (int)(gl % ns);
@@ -763,6 +943,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             j = t - T + 2;
           }
         }
+        const int32_t jg = j0 + j;  // key tile within the unit's range
         const uint32_t dst = slot_addr(slot);
         const uint32_t fb = bar(kBarSlotFull0 + slot);
         int okw = 1;
@@ -772,10 +953,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
               okw = mbar_wait(bar(kBarSlotEmpty0 + slot), (uint32_t)(round - 1) & 1, abort_flag, a.status);
             if (okw) {
               mbar_arrive_expect_tx(fb, L::kTileBytes);
-              if (helpers && j < Tp) mbar_arrive(bar(kBarSlotGo0 + slot));
+              if (helpers && jg < Tp) mbar_arrive(bar(kBarSlotGo0 + slot));
             }
           }
-        } else if (j < Tp) {
+        } else if (jg < Tp) {
           uint32_t k = 0;
 #pragma unroll
           for (int sl = 0; sl < kStages; ++sl)
@@ -788,14 +969,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         }
         int32_t phys = a.num_pages;  // past the prefix end, or a bad entry: zero fill
         if (!is_v) {
-          if (j < Tp) {
-            if (j > 0 && (j & (tpb - 1)) == 0) {
+          if (jg < Tp) {
+            if (jg > j0 && (jg & (tpb - 1)) == 0) {
               bt_cur = bt_nxt;
               bt_nxt = bt_nx2;
-              bt_nx2 = fetch(j + 2 * tpb);
+              bt_nx2 = fetch(jg + 2 * tpb);
             }
-            const int32_t e = __shfl_sync(0xffffffffu, bt_cur, (j & (tpb - 1)) * ppt + (lane & (ppt - 1)));
-            if (lane < ppt && (j * ppt + lane) * a.page_size < P) {
+            const int32_t e = __shfl_sync(0xffffffffu, bt_cur, (jg & (tpb - 1)) * ppt + (lane & (ppt - 1)));
+            if (lane < ppt && (jg * ppt + lane) * a.page_size < P) {
               if (e >= 0 && e < a.num_pages) phys = e;
               else if (lane % kPageIssuers == pw) atomicOr(a.status, UNIP_DEV_BAD_PAGES);
             }
@@ -806,7 +987,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         } else {
           phys = last_k == j ? ph0 : ph1;  // V_j follows K_j or K_(j+1)
         }
-        if (j < Tp) {
+        if (jg < Tp) {
           const void *map = is_v ? static_cast<const void *>(&a.tm_vc) : static_cast<const void *>(&a.tm_kc);
           if (lane < ppt && lane % kPageIssuers == pw) {
 #pragma unroll
@@ -815,7 +996,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           }
         } else if (pw == 0 && lane == 0) {
           const void *map = is_v ? static_cast<const void *>(&a.tm_v) : static_cast<const void *>(&a.tm_k);
-          const int32_t krow = c0 + (j - Tp) * kBlockN;
+          const int32_t krow = c0 + (jg - Tp) * kBlockN;
 #pragma unroll
           for (int hf = 0; hf < kHalves; ++hf) tma_load_3d(dst + hf * L::kHalfBytes, map, fb, hf * 64, g, krow);
         }
@@ -878,7 +1059,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       for (uint32_t i = 0; ok; ++i) {
         int32_t u;
         if (!next_unit(i, u) || u < 0) break;
-        const WorkItem w = decode_item(a, u);
+        const WorkItem w = decode(u);
         const int32_t T = w.T;
         ok = mbar_wait(bar(kBarQFull), items & 1, abort_flag, a.status) && full(lbase);
         if (!ok) break;
@@ -986,10 +1167,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   }
 }
 
-template <int D>
-cudaError_t launch_attention(const AttnArgs &args, int grid, cudaStream_t stream) {
+template <int D, bool kHost>
+cudaError_t launch_attention(const AttnArgs &args, const PlanParam<kHost> &plan, int grid, cudaStream_t stream) {
   using L = SmemLayout<D>;
-  const cudaError_t e = ensure_dynamic_smem((const void *)attn_fwd_kernel<D>, (int)L::kDynamic);
+  const cudaError_t e = ensure_dynamic_smem((const void *)attn_fwd_kernel<D, kHost>, (int)L::kDynamic);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
@@ -1000,8 +1181,10 @@ cudaError_t launch_attention(const AttnArgs &args, int grid, cudaStream_t stream
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // may start while the planner runs
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
+  // A host-planned call has no planner: its set-up overlaps the tail of whatever ran before it on the
+  // stream (the kernel reads nothing before griddepcontrol.wait).
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, attn_fwd_kernel<D>, args);
+  return cudaLaunchKernelEx(&cfg, attn_fwd_kernel<D, kHost>, args, plan);
 }
 
 // Work-item shape of every attention call of the process (unip_set_attention_schedule).
@@ -1031,33 +1214,11 @@ UNIP_API size_t unip_attention_workspace_size(int32_t total_tokens, int32_t num_
   return kWsHeaderBytes + align_up(sizeof(int2) * (size_t)max_pairs_for(total_tokens, num_segs), 256);
 }
 
-// Both entry points: prefix_lens == NULL takes each segment's prefix length from its first position
-// (contiguous positions); otherwise the stream is compacted (increasing positions, explicit prefixes).
-static int32_t attention_entry(const void *q, const void *k, const void *v, const int32_t *cu_seqlens,
-                               int32_t num_segs, const int32_t *positions, const int32_t *prefix_lens,
-                               int32_t total_tokens, const unip_paged_kv *paged, const unip_attn_params *prm,
-                               void *out, float *lse, void *workspace, size_t workspace_bytes, void *stream) {
-  if (!prm || !cu_seqlens || num_segs < 0 || total_tokens < 0) return UNIP_ERR_INVALID_ARGUMENT;
+// Tensor maps and shape fields shared by every attention launch (q, k, v token-major; the cache,
+// when given, [page][slot][H_kv][D]).  Returns UNIP_OK or UNIP_ERR_CUDA.
+static int32_t prepare_args(AttnArgs &args, const void *q, const void *k, const void *v, int32_t total_tokens,
+                            const unip_paged_kv *cache, const unip_attn_params *prm, void *out, float *lse) {
   const int32_t Hq = prm->num_heads_q, Hkv = prm->num_heads_kv, D = prm->head_dim;
-  if (Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0) return UNIP_ERR_INVALID_ARGUMENT;
-  if (D != 64 && D != 128) return UNIP_ERR_UNSUPPORTED;
-  if (total_tokens == 0) return UNIP_OK;
-  if (num_segs == 0 || !q || !k || !v || !positions || !out) return UNIP_ERR_INVALID_ARGUMENT;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return UNIP_ERR_ALIGNMENT;
-  const size_t need_ws = unip_attention_workspace_size(total_tokens, num_segs, prm);
-  if (!workspace || workspace_bytes < need_ws || (reinterpret_cast<uintptr_t>(workspace) & 255u))
-    return UNIP_ERR_WORKSPACE;
-  const bool has_cache = paged && paged->k_cache && paged->v_cache && paged->block_table && paged->num_pages > 0;
-  if (has_cache) {
-    const int32_t ps = paged->page_size;
-    if (ps != 16 && ps != 32 && ps != 64 && ps != 128) return UNIP_ERR_UNSUPPORTED;
-    if (paged->max_pages_per_seq <= 0) return UNIP_ERR_INVALID_ARGUMENT;
-    if (!aligned16(paged->k_cache) || !aligned16(paged->v_cache)) return UNIP_ERR_ALIGNMENT;
-  }
-  uint32_t *status = device_status_ptr();
-  if (!status) return UNIP_ERR_CUDA;
-
-  AttnArgs args;
   memset(&args, 0, sizeof(args));
   const cuuint32_t box3[3] = {64, 1, kBlockM};
   // Even groups that divide 128 put (token, head) pairs on a tile's rows.
@@ -1085,17 +1246,64 @@ static int32_t attention_entry(const void *q, const void *k, const void *v, cons
                      CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
       return UNIP_ERR_CUDA;
   }
-  if (has_cache) {
-    const int32_t ps = paged->page_size;
-    const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)Hkv, (cuuint64_t)ps, (cuuint64_t)paged->num_pages};
+  if (cache) {
+    const int32_t ps = cache->page_size;
+    const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)Hkv, (cuuint64_t)ps, (cuuint64_t)cache->num_pages};
     const cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)Hkv * D * 2, (cuuint64_t)ps * Hkv * D * 2};
     const cuuint32_t box4[4] = {64, 1, (cuuint32_t)ps, 1};
-    if (encode_tiled(&args.tm_kc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(paged->k_cache), dims,
+    if (encode_tiled(&args.tm_kc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(cache->k_cache), dims,
                      strides, box4, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS ||
-        encode_tiled(&args.tm_vc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(paged->v_cache), dims,
+        encode_tiled(&args.tm_vc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(cache->v_cache), dims,
                      strides, box4, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
       return UNIP_ERR_CUDA;
+    args.block_table = cache->block_table;
+    args.num_pages = cache->num_pages;
+    args.page_size = cache->page_size;
+    args.max_pages = cache->max_pages_per_seq;
+  } else {
+    args.page_size = 16;
   }
+  args.out = static_cast<__nv_bfloat16 *>(out);
+  args.lse = lse;
+  args.N = total_tokens;
+  args.Hq = Hq;
+  args.group = G;
+  args.lg = lg;
+  const float scale = prm->scale > 0.f ? prm->scale : 1.0f / sqrtf((float)D);
+  args.scale_log2 = scale * kLog2e;
+  return UNIP_OK;
+}
+
+// Both entry points: prefix_lens == NULL takes each segment's prefix length from its first position
+// (contiguous positions); otherwise the stream is compacted (increasing positions, explicit prefixes).
+static int32_t attention_entry(const void *q, const void *k, const void *v, const int32_t *cu_seqlens,
+                               int32_t num_segs, const int32_t *positions, const int32_t *prefix_lens,
+                               int32_t total_tokens, const unip_paged_kv *paged, const unip_attn_params *prm,
+                               void *out, float *lse, void *workspace, size_t workspace_bytes, void *stream) {
+  if (!prm || !cu_seqlens || num_segs < 0 || total_tokens < 0) return UNIP_ERR_INVALID_ARGUMENT;
+  const int32_t Hq = prm->num_heads_q, Hkv = prm->num_heads_kv, D = prm->head_dim;
+  if (Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0) return UNIP_ERR_INVALID_ARGUMENT;
+  if (D != 64 && D != 128) return UNIP_ERR_UNSUPPORTED;
+  if (total_tokens == 0) return UNIP_OK;
+  if (num_segs == 0 || !q || !k || !v || !positions || !out) return UNIP_ERR_INVALID_ARGUMENT;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return UNIP_ERR_ALIGNMENT;
+  const size_t need_ws = unip_attention_workspace_size(total_tokens, num_segs, prm);
+  if (!workspace || workspace_bytes < need_ws || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return UNIP_ERR_WORKSPACE;
+  const bool has_cache = paged && paged->k_cache && paged->v_cache && paged->block_table && paged->num_pages > 0;
+  if (has_cache) {
+    const int32_t ps = paged->page_size;
+    if (ps != 16 && ps != 32 && ps != 64 && ps != 128) return UNIP_ERR_UNSUPPORTED;
+    if (paged->max_pages_per_seq <= 0) return UNIP_ERR_INVALID_ARGUMENT;
+    if (!aligned16(paged->k_cache) || !aligned16(paged->v_cache)) return UNIP_ERR_ALIGNMENT;
+  }
+  uint32_t *status = device_status_ptr();
+  if (!status) return UNIP_ERR_CUDA;
+
+  AttnArgs args;
+  const int32_t prc = prepare_args(args, q, k, v, total_tokens, has_cache ? paged : nullptr, prm, out, lse);
+  if (prc != UNIP_OK) return prc;
+  const int32_t G = args.group, lg = args.lg;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   int32_t *header = static_cast<int32_t *>(workspace);
   int2 *pairs = reinterpret_cast<int2 *>(static_cast<uint8_t *>(workspace) + kWsHeaderBytes);
@@ -1110,18 +1318,11 @@ static int32_t attention_entry(const void *q, const void *k, const void *v, cons
   args.cu = cu_seqlens;
   args.pos = positions;
   args.prefix_lens = prefix_lens;
-  args.block_table = has_cache ? paged->block_table : nullptr;
   args.pairs = pairs;
   args.num_pairs = header;
   args.work_counter = header + 1;
-  args.out = static_cast<__nv_bfloat16 *>(out);
-  args.lse = lse;
   args.status = status;
   args.S = num_segs;
-  args.N = total_tokens;
-  args.Hq = Hq;
-  args.group = G;
-  args.lg = lg;
   // Two query tiles per work item when the group is even, unless even twice the
   // most items the call can hold leave SMs idle: then one tile per item.
   // Query tiles: sum over segments of ceil(n_s / 128) <= ceil(N / 128) + S - 1.
@@ -1134,16 +1335,13 @@ static int32_t attention_entry(const void *q, const void *k, const void *v, cons
                 : mode == UNIP_ATTN_SCHEDULE_PAIRED ? 0
                 : (2 * tiles_hi * (Hq / 2) <= (int64_t)(sms > 0 ? sms : 1) ? 1 : 0);
   args.heads_per_pair = (even && !args.single) ? Hq / 2 : Hq;
-  args.num_pages = has_cache ? paged->num_pages : 0;
-  args.page_size = has_cache ? paged->page_size : 16;
-  args.max_pages = has_cache ? paged->max_pages_per_seq : 0;
-  const float scale = prm->scale > 0.f ? prm->scale : 1.0f / sqrtf((float)D);
-  args.scale_log2 = scale * kLog2e;
   // persistent grid: one CTA per SM (fewer when the plan cannot hold that many work items)
   const int64_t units_bound = (int64_t)max_pairs * args.heads_per_pair;
   if (units_bound > 0x7FFFFFFF) return UNIP_ERR_UNSUPPORTED;
   const int64_t grid = std::min<int64_t>(units_bound, sms > 0 ? sms : 1);
-  const cudaError_t e = D == 128 ? launch_attention<128>(args, (int)grid, st) : launch_attention<64>(args, (int)grid, st);
+  const PlanParam<false> none{0};
+  const cudaError_t e = D == 128 ? launch_attention<128, false>(args, none, (int)grid, st)
+                                 : launch_attention<64, false>(args, none, (int)grid, st);
   return e == cudaSuccess ? UNIP_OK : UNIP_ERR_CUDA;
 }
 
@@ -1163,6 +1361,342 @@ UNIP_API int32_t unip_compacted_attention(const void *q, const void *k, const vo
   if (num_segs > 0 && !prefix_lens) return UNIP_ERR_INVALID_ARGUMENT;
   return attention_entry(q, k, v, cu_seqlens, num_segs, positions, prefix_lens, total_tokens, paged, prm, out,
                          lse, workspace, workspace_bytes, stream);
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Host-built plans
+// ---------------------------------------------------------------------------
+struct unip_attn_plan {
+  int32_t N = 0, S = 0, Hq = 0, Hkv = 0, D = 0, page_size = 16, max_pages = 0;
+  float scale = 0.f;
+  bool any_prefix = false;
+  bool device = false;  // run the device planner instead
+  int32_t single = 0, n_items = 0, n_ctas = 0, n_split_units = 0, n_splits = 0;
+  size_t ticket_bytes = 0, partial_bytes = 0, ws_bytes = 0;
+  unip::HostPlanArgs args;  // seg, cta_first, items (pointers and generation are set per run)
+  std::atomic<void *> ready_ws{nullptr};  // workspace whose ticket area this plan has cleared
+};
+
+namespace unip {
+namespace {
+
+// Cost model of the host planner, in SM cycles (measured periods of the kernel on GB300): a key tile
+// of a two-tile item costs ~3.4k cycles (32 MMAs, one tile's softmax overlapping the other's MMAs);
+// of a one-tile item ~1.6k, ~2.9k when it streams cached pages (its K and V tiles serve one query
+// tile, so page copies bound it); every item adds its Q load, pipeline fill and epilogue.  A split
+// item also stores its fp32 partial (~70 KB per full tile) and takes a ticket, and the split that
+// merges reads every split's partial back through L2: a few round trips of ~3k cycles when many
+// tiles merge at once.  Both scale with the tile's valid rows (warps past them store nothing), so
+// splitting pays for decode-like tiles far more readily than for full prefill tiles.
+constexpr double kCostTile2 = 3400.0, kCostTile1 = 1600.0, kCostTile1Prefix = 2900.0;
+constexpr double kCostItem = 3000.0, kCostSplitFixed = 2000.0, kCostSplitStore = 3000.0;
+constexpr double kCostMergeRound = 3000.0;
+constexpr int32_t kMinSplitTiles = 2;
+constexpr int32_t kMaxSplits = 8;        // the merge reads every split: more would lengthen the tail
+constexpr int32_t kMaxSplitsFull = 2;    // tiles whose rows are mostly valid
+
+double merge_rounds(int32_t n) { return 1.0 + 4.0 * ((n + 2) / 3); }
+
+struct PlanUnit {
+  int32_t s, m, hsel, T, Tp;
+  bool two;
+  double active;  // fraction of the item's softmax warps that hold valid rows (partial-store volume)
+};
+
+double range_cost(const PlanUnit &u, int32_t j0, int32_t T) {
+  if (u.two) return kCostTile2 * T;
+  const int32_t pre = std::max(0, std::min(T, u.Tp - j0));
+  return kCostTile1Prefix * pre + kCostTile1 * (T - pre);
+}
+
+struct Candidate {
+  int32_t single = 0;
+  int32_t L = 0;  // largest key range of one item (INT32_MAX: no split)
+  double makespan = 0.0;
+  int32_t n_items = 0;
+  std::vector<PlanItem> items;       // in CTA order
+  std::vector<uint16_t> cta_first;
+  int32_t n_ctas = 0, n_split_units = 0, n_splits = 0;
+};
+
+// Items of one shape and split length, balanced over `sms` CTAs longest-processing-time first.
+// forced > 0: every unit is split into min(forced, T) ranges instead (L unused).
+bool build_candidate(const std::vector<PlanUnit> &units, int32_t single, int32_t L, int sms, Candidate &c,
+                     int32_t forced = 0) {
+  struct It {
+    PlanItem pi;
+    double cost;
+  };
+  std::vector<It> its;
+  int32_t g = 0, nsu = 0;
+  for (const PlanUnit &u : units) {
+    int32_t n = (u.T > L) ? (u.T + L - 1) / L : 1;
+    n = std::min(n, std::min(u.T, u.active > 0.5 ? kMaxSplitsFull : kMaxSplits));
+    if (forced > 0) n = std::min(forced, u.T);
+    const int32_t base = u.T / n, rem = u.T % n;
+    int32_t j0 = 0;
+    for (int32_t k = 0; k < n; ++k) {
+      const int32_t T = base + (k < rem ? 1 : 0);
+      It it;
+      it.pi.w0 = (int32_t)((uint32_t)u.s | ((uint32_t)u.hsel << 16));
+      it.pi.w1 = (int32_t)((uint32_t)u.m | ((uint32_t)n << 24));
+      it.pi.w2 = (int32_t)((uint32_t)j0 | ((uint32_t)T << 16));
+      it.pi.w3 = (int32_t)((uint32_t)(n > 1 ? g : 0) | ((uint32_t)k << 24));
+      // the last split holds the unit's own (diagonal) tiles and is charged the merge
+      const double vol = 0.25 + 0.75 * u.active;
+      it.cost = kCostItem + range_cost(u, j0, T);
+      if (n > 1) it.cost += kCostSplitFixed + kCostSplitStore * vol;
+      if (n > 1 && k == n - 1) it.cost += kCostMergeRound * merge_rounds(n) * vol;
+      its.push_back(it);
+      j0 += T;
+    }
+    if (n > 1) {
+      g += n;
+      ++nsu;
+    }
+    if ((int64_t)its.size() > kPlanMaxItems || g >= (1 << 24)) return false;
+  }
+  const int32_t n_items = (int32_t)its.size();
+  const int ctas = std::max(1, std::min(sms, n_items));
+  if (ctas > kPlanMaxCtas) return false;
+  std::vector<int32_t> order(n_items);
+  for (int32_t i = 0; i < n_items; ++i) order[i] = i;
+  std::stable_sort(order.begin(), order.end(), [&](int32_t x, int32_t y) { return its[x].cost > its[y].cost; });
+  // least-loaded CTA first (ties: lower index)
+  using Slot = std::pair<double, int>;
+  std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> heap;
+  for (int b = 0; b < ctas; ++b) heap.push({0.0, b});
+  std::vector<std::vector<int32_t>> per(ctas);
+  double mk = 0.0;
+  for (int32_t i : order) {
+    Slot sl = heap.top();
+    heap.pop();
+    per[sl.second].push_back(i);
+    sl.first += its[i].cost;
+    mk = std::max(mk, sl.first);
+    heap.push(sl);
+  }
+  c.single = single;
+  c.L = L;
+  c.makespan = mk;
+  c.n_items = n_items;
+  c.n_ctas = ctas;
+  c.n_split_units = nsu;
+  c.n_splits = g;
+  c.items.clear();
+  c.cta_first.assign(ctas + 1, 0);
+  for (int b = 0; b < ctas; ++b) {
+    c.cta_first[b] = (uint16_t)c.items.size();
+    for (int32_t i : per[b]) c.items.push_back(its[i].pi);
+  }
+  c.cta_first[ctas] = (uint16_t)c.items.size();
+  return true;
+}
+
+void plan_units(const unip_attn_plan &p, const std::vector<int32_t> &cu, const std::vector<int32_t> &pre,
+                int32_t lg, int32_t single, std::vector<PlanUnit> &units) {
+  const int32_t G = p.Hq / p.Hkv;
+  const bool even = G % 2 == 0;
+  const int32_t hpp = (even && !single) ? p.Hq / 2 : p.Hq;
+  units.clear();
+  for (int32_t s = 0; s < p.S; ++s) {
+    const int32_t n = cu[s + 1] - cu[s];
+    for (int32_t m = 0; m * kBlockM < n; ++m)
+      for (int32_t h = 0; h < hpp; ++h) {
+        const WorkItem w = unit_geometry(s, m, h, cu[s], n, pre[s], lg, G, single);
+        if (!w.valid) continue;
+        const int32_t rows = w.tr0.rows_valid + (w.two ? w.tr1.rows_valid : 0);
+        const double active = (double)((rows + 15) / 16) / (w.two ? 16.0 : 8.0);
+        units.push_back({s, m, h, w.T, w.Tp, w.two, active});
+      }
+  }
+}
+
+}  // namespace
+}  // namespace unip
+
+extern "C" {
+
+UNIP_API int32_t unip_attention_plan_create(const int32_t *cu_seqlens, int32_t num_segs, const int32_t *prefix_lens,
+                                            int32_t total_tokens, const unip_attn_params *prm, int32_t page_size,
+                                            int32_t max_pages_per_seq, int32_t flags, int32_t num_sms,
+                                            unip_attn_plan **plan) {
+  if (!plan) return UNIP_ERR_INVALID_ARGUMENT;
+  *plan = nullptr;
+  if (!prm || !cu_seqlens || num_segs < 0 || total_tokens < 0 || (flags & ~0xFF03) || num_sms < 0)
+    return UNIP_ERR_INVALID_ARGUMENT;
+  const int32_t forced = (flags >> 8) & 0xFF;  // UNIP_PLAN_SPLITS(n)
+  if (forced && (flags & UNIP_PLAN_NO_SPLIT)) return UNIP_ERR_INVALID_ARGUMENT;
+  const int32_t Hq = prm->num_heads_q, Hkv = prm->num_heads_kv, D = prm->head_dim;
+  if (Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0) return UNIP_ERR_INVALID_ARGUMENT;
+  if (D != 64 && D != 128) return UNIP_ERR_UNSUPPORTED;
+  std::vector<int32_t> cu(cu_seqlens, cu_seqlens + num_segs + 1);
+  std::vector<int32_t> pre(num_segs, 0);
+  if (cu[0] != 0 || cu[num_segs] != total_tokens) return UNIP_ERR_INVALID_ARGUMENT;
+  bool any_prefix = false;
+  for (int32_t s = 0; s < num_segs; ++s) {
+    if (cu[s + 1] < cu[s]) return UNIP_ERR_INVALID_ARGUMENT;
+    pre[s] = prefix_lens ? prefix_lens[s] : 0;
+    if (pre[s] < 0) return UNIP_ERR_INVALID_ARGUMENT;
+    if (pre[s] > 0 && cu[s + 1] > cu[s]) any_prefix = true;
+  }
+  if (any_prefix) {
+    if (page_size != 16 && page_size != 32 && page_size != 64 && page_size != 128) return UNIP_ERR_UNSUPPORTED;
+    if (max_pages_per_seq <= 0) return UNIP_ERR_INVALID_ARGUMENT;
+    for (int32_t s = 0; s < num_segs; ++s)
+      if (cu[s + 1] > cu[s] && ((int64_t)pre[s] + page_size - 1) / page_size > max_pages_per_seq)
+        return UNIP_ERR_INVALID_ARGUMENT;
+  }
+  unip_attn_plan *p = new (std::nothrow) unip_attn_plan();
+  if (!p) return UNIP_ERR_TOO_LARGE;
+  p->N = total_tokens;
+  p->S = num_segs;
+  p->Hq = Hq;
+  p->Hkv = Hkv;
+  p->D = D;
+  p->scale = prm->scale;
+  p->page_size = any_prefix ? page_size : 16;
+  p->max_pages = any_prefix ? max_pages_per_seq : 0;
+  p->any_prefix = any_prefix;
+  const int32_t G = Hq / Hkv;
+  int32_t lg = 0;
+  if (G % 2 == 0 && kBlockM % G == 0)
+    while ((1 << lg) < G) ++lg;
+  bool host = !(flags & UNIP_PLAN_DEVICE) && num_segs <= kPlanMaxSegs && total_tokens > 0 &&
+              Hq < (1 << 16) && (int64_t)total_tokens / kBlockM < (1 << 24);
+  if (host) {
+    // the key range of a unit must fit the item's 16-bit fields
+    for (int32_t s = 0; s < num_segs && host; ++s)
+      if ((int64_t)(pre[s] + kBlockN - 1) / kBlockN + (int64_t)(cu[s + 1] - cu[s] + kBlockN - 1) / kBlockN >= 65535)
+        host = false;
+  }
+  int sms = num_sms > 0 ? num_sms : device_sm_count();
+  if (sms <= 0) sms = 1;
+  sms = std::min(sms, kPlanMaxCtas);
+  Candidate best;
+  bool found = false;
+  if (host) {
+    const int mode = g_attention_schedule.load(std::memory_order_relaxed);
+    std::vector<int32_t> shapes;
+    if (G % 2 != 0) shapes = {0};
+    else if (mode == UNIP_ATTN_SCHEDULE_PAIRED) shapes = {0};
+    else if (mode == UNIP_ATTN_SCHEDULE_SINGLE) shapes = {1};
+    else shapes = {0, 1};
+    std::vector<PlanUnit> units;
+    Candidate c;
+    for (int32_t single : shapes) {
+      plan_units(*p, cu, pre, lg, single, units);
+      if (units.empty()) continue;
+      int64_t wt = 0;
+      for (const PlanUnit &u : units) wt += u.T;
+      std::vector<int32_t> Ls = {INT32_MAX};
+      if (!(flags & UNIP_PLAN_NO_SPLIT))
+        for (double f : {1.0, 1.5, 2.0, 3.0, 4.0, 6.0, 8.0}) {
+          const int64_t L = std::max<int64_t>(kMinSplitTiles, (int64_t)std::ceil((double)wt / (f * sms)));
+          if (std::find(Ls.begin(), Ls.end(), (int32_t)L) == Ls.end()) Ls.push_back((int32_t)L);
+        }
+      if (forced) Ls = {INT32_MAX};
+      for (int32_t L : Ls) {
+        if (!build_candidate(units, single, L, sms, c, forced)) continue;
+        // a clearly shorter makespan wins; within 2 %, fewer items (less fixed and split overhead)
+        if (!found || c.makespan < best.makespan * 0.98 ||
+            (c.makespan <= best.makespan * 1.02 && c.n_items < best.n_items)) {
+          best = c;
+          found = true;
+        }
+      }
+    }
+  }
+  if (!found) {
+    p->device = true;
+    p->ws_bytes = unip_attention_workspace_size(total_tokens, num_segs, prm);
+    *plan = p;
+    return UNIP_OK;
+  }
+  p->single = best.single;
+  p->n_items = best.n_items;
+  p->n_ctas = best.n_ctas;
+  p->n_split_units = best.n_split_units;
+  p->n_splits = best.n_splits;
+  memset(&p->args, 0, sizeof(p->args));
+  for (int32_t s = 0; s < num_segs; ++s) {
+    p->args.seg[s][0] = cu[s];
+    p->args.seg[s][1] = cu[s + 1] - cu[s];
+    p->args.seg[s][2] = pre[s];
+  }
+  std::copy(best.cta_first.begin(), best.cta_first.end(), p->args.cta_first);
+  std::copy(best.items.begin(), best.items.end(), p->args.items);
+  p->ticket_bytes = align_up(sizeof(unsigned long long) * 2 * (size_t)best.n_splits, 256);
+  p->partial_bytes = split_slot_bytes(D) * 2 * (size_t)best.n_splits;
+  p->ws_bytes = std::max<size_t>(256, p->ticket_bytes + p->partial_bytes);
+  *plan = p;
+  return UNIP_OK;
+}
+
+UNIP_API size_t unip_attention_plan_workspace_size(const unip_attn_plan *plan) { return plan ? plan->ws_bytes : 0; }
+
+UNIP_API int32_t unip_attention_plan_info(const unip_attn_plan *plan, int32_t *info) {
+  if (!plan || !info) return UNIP_ERR_INVALID_ARGUMENT;
+  info[0] = plan->device ? 0 : 1;
+  info[1] = plan->n_items;
+  info[2] = plan->n_ctas;
+  info[3] = plan->n_split_units;
+  info[4] = plan->n_splits;
+  info[5] = plan->single;
+  return UNIP_OK;
+}
+
+UNIP_API void unip_attention_plan_destroy(unip_attn_plan *plan) { delete plan; }
+
+UNIP_API int32_t unip_prefill_attention_planned(const unip_attn_plan *plan, const void *q, const void *k,
+                                                const void *v, const int32_t *cu_seqlens, const int32_t *positions,
+                                                const int32_t *prefix_lens, const unip_paged_kv *paged, void *out,
+                                                float *lse, void *workspace, size_t workspace_bytes, void *stream) {
+  if (!plan) return UNIP_ERR_INVALID_ARGUMENT;
+  unip_attn_params prm;
+  prm.num_heads_q = plan->Hq;
+  prm.num_heads_kv = plan->Hkv;
+  prm.head_dim = plan->D;
+  prm.scale = plan->scale;
+  if (plan->device)
+    return attention_entry(q, k, v, cu_seqlens, plan->S, positions, prefix_lens, plan->N, paged, &prm, out, lse,
+                           workspace, workspace_bytes, stream);
+  if (!q || !k || !v || !out) return UNIP_ERR_INVALID_ARGUMENT;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return UNIP_ERR_ALIGNMENT;
+  if (!workspace || workspace_bytes < plan->ws_bytes || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return UNIP_ERR_WORKSPACE;
+  const bool has_cache = paged && paged->k_cache && paged->v_cache && paged->block_table && paged->num_pages > 0;
+  if (plan->any_prefix) {
+    if (!has_cache) return UNIP_ERR_INVALID_ARGUMENT;
+    if (paged->page_size != plan->page_size || paged->max_pages_per_seq != plan->max_pages)
+      return UNIP_ERR_INVALID_ARGUMENT;
+    if (!aligned16(paged->k_cache) || !aligned16(paged->v_cache)) return UNIP_ERR_ALIGNMENT;
+  }
+  uint32_t *status = device_status_ptr();
+  if (!status) return UNIP_ERR_CUDA;
+  AttnArgs args;
+  const int32_t prc = prepare_args(args, q, k, v, plan->N, plan->any_prefix ? paged : nullptr, &prm, out, lse);
+  if (prc != UNIP_OK) return prc;
+  args.status = status;
+  args.S = plan->S;
+  args.single = plan->single;
+  args.heads_per_pair = 0;  // unused: items name their head selection
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  PlanParam<true> hp;
+  static_cast<HostPlanArgs &>(hp) = plan->args;
+  hp.tickets = reinterpret_cast<unsigned long long *>(workspace);
+  hp.partial = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + plan->ticket_bytes);
+  static std::atomic<uint32_t> g_gen{0};
+  hp.gen = g_gen.fetch_add(1, std::memory_order_relaxed) % 0xFFFFFFFEu + 1u;  // never 0 (cleared tickets)
+  if (plan->n_splits > 0 && plan->ready_ws.load(std::memory_order_relaxed) != workspace) {
+    if (cudaMemsetAsync(workspace, 0, plan->ticket_bytes, st) != cudaSuccess) return UNIP_ERR_CUDA;
+    const_cast<unip_attn_plan *>(plan)->ready_ws.store(workspace, std::memory_order_relaxed);
+  }
+  const cudaError_t e = plan->D == 128 ? launch_attention<128, true>(args, hp, plan->n_ctas, st)
+                                       : launch_attention<64, true>(args, hp, plan->n_ctas, st);
+  return e == cudaSuccess ? UNIP_OK : UNIP_ERR_CUDA;
 }
 
 }  // extern "C"

@@ -31,7 +31,7 @@ namespace {
 
 constexpr int kChunk = 128;        // keys per score CTA
 constexpr int kPlanThreads = 1024;
-constexpr int kNormThreads = 256;
+constexpr int kNormThreads = kImpNormThreads;
 constexpr int kWsHeaderBytes = 256;
 constexpr float kLog2e = 1.44269504088896340736f;
 
@@ -419,7 +419,7 @@ __global__ void __launch_bounds__(kScoreThreadsTc, 1) imp_score_tc_kernel(const 
 __global__ void __launch_bounds__(kNormThreads) imp_norm_kernel(const int32_t *__restrict__ blk_cu,
                                                                  const float *__restrict__ partial, int32_t Hkv,
                                                                  float *__restrict__ imp) {
-  __shared__ float sred[kNormThreads];
+  __shared__ float sred[kImpNormThreads];
   // a Top-p grid launched as a programmatic dependent may be scheduled now; it waits for this one
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // launched as a programmatic dependent of the score grid: its masses are complete after this
@@ -427,25 +427,7 @@ __global__ void __launch_bounds__(kNormThreads) imp_norm_kernel(const int32_t *_
   const int32_t s = blockIdx.x;
   const int32_t b0 = blk_cu[s], nb = blk_cu[s + 1] - b0;
   if (nb <= 0) return;
-  const int tid = threadIdx.x;
-  float t = 0.f;
-  for (int32_t b = tid; b < nb; b += kNormThreads) {
-    float m = 0.f;
-    for (int32_t g = 0; g < Hkv; ++g) m += partial[(int64_t)(b0 + b) * Hkv + g];
-    t += m;
-  }
-  sred[tid] = t;
-  __syncthreads();
-  for (int off = kNormThreads / 2; off >= 1; off >>= 1) {
-    if (tid < off) sred[tid] += sred[tid + off];
-    __syncthreads();
-  }
-  const float inv = 1.f / sred[0];
-  for (int32_t b = tid; b < nb; b += kNormThreads) {
-    float m = 0.f;
-    for (int32_t g = 0; g < Hkv; ++g) m += partial[(int64_t)(b0 + b) * Hkv + g];
-    imp[b0 + b] = m * inv;
-  }
+  normalise_segment(partial, b0, nb, Hkv, imp, sred);
 }
 
 template <int D>
@@ -507,11 +489,13 @@ UNIP_API size_t unip_importance_workspace_size(int32_t total_tokens, int32_t num
   return kWsHeaderBytes + items + part;
 }
 
-UNIP_API int32_t unip_block_importance(const void *q, const void *k, const float *lse, const int32_t *cu_seqlens,
-                                       int32_t num_segs, int32_t total_tokens, const uint8_t *seg_mask,
-                                       int32_t block_size, const unip_attn_params *prm, float *imp,
-                                       int32_t imp_capacity, int32_t *blk_cu, void *workspace,
-                                       size_t workspace_bytes, void *stream) {
+}  // extern "C"
+
+int32_t unip::importance_scores(const void *q, const void *k, const float *lse, const int32_t *cu_seqlens,
+                                int32_t num_segs, int32_t total_tokens, const uint8_t *seg_mask, int32_t block_size,
+                                const unip_attn_params *prm, float *imp, int32_t imp_capacity, int32_t *blk_cu,
+                                void *workspace, size_t workspace_bytes, cudaStream_t st, float **partial_out) {
+  *partial_out = nullptr;
   if (!prm || !cu_seqlens || !blk_cu || num_segs < 0 || total_tokens < 0) return UNIP_ERR_INVALID_ARGUMENT;
   const int32_t Hq = prm->num_heads_q, Hkv = prm->num_heads_kv, D = prm->head_dim;
   if (Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0) return UNIP_ERR_INVALID_ARGUMENT;
@@ -526,7 +510,6 @@ UNIP_API int32_t unip_block_importance(const void *q, const void *k, const float
     return UNIP_ERR_WORKSPACE;
   uint32_t *status = device_status_ptr();
   if (!status) return UNIP_ERR_CUDA;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint8_t *ws = static_cast<uint8_t *>(workspace);
   int32_t *header = reinterpret_cast<int32_t *>(ws);
   const int32_t max_items = max_items_for(total_tokens, num_segs);
@@ -574,7 +557,23 @@ UNIP_API int32_t unip_block_importance(const void *q, const void *k, const float
   args.scale_log2 = scale * kLog2e;
   cudaError_t e = D == 128 ? launch_score<128>(args, (int)grid, st) : launch_score<64>(args, (int)grid, st);
   if (e != cudaSuccess) return UNIP_ERR_CUDA;
-  if (launch_norm(blk_cu, partial, Hkv, imp, num_segs, st) != cudaSuccess) return UNIP_ERR_CUDA;
+  *partial_out = partial;
+  return UNIP_OK;
+}
+
+extern "C" {
+
+UNIP_API int32_t unip_block_importance(const void *q, const void *k, const float *lse, const int32_t *cu_seqlens,
+                                       int32_t num_segs, int32_t total_tokens, const uint8_t *seg_mask,
+                                       int32_t block_size, const unip_attn_params *prm, float *imp,
+                                       int32_t imp_capacity, int32_t *blk_cu, void *workspace,
+                                       size_t workspace_bytes, void *stream) {
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  float *partial = nullptr;
+  const int32_t rc = importance_scores(q, k, lse, cu_seqlens, num_segs, total_tokens, seg_mask, block_size, prm, imp,
+                                       imp_capacity, blk_cu, workspace, workspace_bytes, st, &partial);
+  if (rc != UNIP_OK || !partial) return rc;
+  if (launch_norm(blk_cu, partial, prm->num_heads_kv, imp, num_segs, st) != cudaSuccess) return UNIP_ERR_CUDA;
   return UNIP_OK;
 }
 

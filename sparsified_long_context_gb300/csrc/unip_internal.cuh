@@ -20,6 +20,13 @@ int device_sm_count();
 // Raises the dynamic shared-memory limit of kernel `fn` to `bytes` on the current device, once per
 // (kernel, device, size); safe to call from several host threads.
 cudaError_t ensure_dynamic_smem(const void *fn, int bytes);
+// Importance without its normalisation (plan + persistent score grid of unip_block_importance, same
+// checks and return codes): block masses per kv head land in the workspace; *partial receives their
+// address.  The normalisation follows as a programmatic dependent of the score grid.
+int32_t importance_scores(const void *q, const void *k, const float *lse, const int32_t *cu_seqlens,
+                          int32_t num_segs, int32_t total_tokens, const uint8_t *seg_mask, int32_t block_size,
+                          const unip_attn_params *prm, float *imp, int32_t imp_capacity, int32_t *blk_cu,
+                          void *workspace, size_t workspace_bytes, cudaStream_t st, float **partial);
 // cuTensorMapEncodeTiled, fetched from the driver at first use.
 CUresult encode_tiled(CUtensorMap *map, CUtensorMapDataType dtype, cuuint32_t rank, void *gaddr,
                       const cuuint64_t *dims, const cuuint64_t *strides, const cuuint32_t *box,
@@ -362,6 +369,38 @@ __device__ __forceinline__ void warp_copy_row(const uint4 *__restrict__ src, uin
     for (int u = 0; u < kUnroll; ++u) st_stream(dst + v + 32 * u, r[u]);
   }
   for (; v < vec_per_row; v += 32) st_stream(dst + v, ld_stream(src + v));
+}
+
+// Block masses of one scored segment normalised to importance: imp[b] = M_b / sum_b' M_b', with
+// M_b = sum over kv heads g of partial[b][g].  Run by the first kImpNormThreads threads of a CTA in a
+// fixed order (strided per-thread sums, then a tree), so every caller produces the same fp32 bits.
+// sred: kImpNormThreads floats of shared memory.  Threads past kImpNormThreads take no part but must
+// reach the same __syncthreads.
+constexpr int kImpNormThreads = 256;
+__device__ __forceinline__ void normalise_segment(const float *__restrict__ partial, int32_t b0, int32_t nb,
+                                                  int32_t Hkv, float *__restrict__ imp, float *sred) {
+  const int tid = threadIdx.x;
+  const bool part = tid < kImpNormThreads;
+  float t = 0.f;
+  if (part)
+    for (int32_t b = tid; b < nb; b += kImpNormThreads) {
+      float m = 0.f;
+      for (int32_t g = 0; g < Hkv; ++g) m += partial[(int64_t)(b0 + b) * Hkv + g];
+      t += m;
+    }
+  if (part) sred[tid] = t;
+  __syncthreads();
+  for (int off = kImpNormThreads / 2; off >= 1; off >>= 1) {
+    if (tid < off) sred[tid] += sred[tid + off];
+    __syncthreads();
+  }
+  const float inv = 1.f / sred[0];
+  if (part)
+    for (int32_t b = tid; b < nb; b += kImpNormThreads) {
+      float m = 0.f;
+      for (int32_t g = 0; g < Hkv; ++g) m += partial[(int64_t)(b0 + b) * Hkv + g];
+      imp[b0 + b] = m * inv;
+    }
 }
 
 // Segment holding token t: largest s with cu[s] <= t (cu non-decreasing, t < cu[S]).

@@ -260,6 +260,33 @@ __device__ bool select_segment_blocks(const float *__restrict__ imp, int32_t b0,
   return true;
 }
 
+// Keep flags of a selected segment out to global memory, with the kept-token offset of every block
+// (exclusive, in block order) and the segment's kept-token count.
+__device__ __forceinline__ void write_segment_selection(int32_t s, int32_t b0, int32_t nb, int32_t n, int32_t B,
+                                                        const uint8_t *skeep, uint8_t *__restrict__ keep,
+                                                        int32_t *__restrict__ kept_off,
+                                                        int32_t *__restrict__ seg_kept, int32_t *sh32) {
+  const int tid = threadIdx.x;
+  const int ipb = (nb + kToppThreads - 1) / kToppThreads;
+  const int bb0 = tid * ipb;
+  int32_t lsum = 0;
+  for (int e = 0; e < ipb; ++e) {
+    const int b = bb0 + e;
+    if (b < nb && skeep[b]) lsum += min(B, n - b * B);
+  }
+  int32_t tot;
+  int32_t run = block_excl_scan<int32_t>(lsum, sh32, &tot);
+  for (int e = 0; e < ipb; ++e) {
+    const int b = bb0 + e;
+    if (b < nb) {
+      keep[b0 + b] = skeep[b];
+      kept_off[b0 + b] = run;
+      if (skeep[b]) run += min(B, n - b * B);
+    }
+  }
+  if (tid == 0) seg_kept[s] = tot;
+}
+
 __global__ void __launch_bounds__(kToppThreads) topp_kernel(
     const float *__restrict__ imp, const int32_t *__restrict__ blk_cu, const int32_t *__restrict__ cu, int32_t B,
     double p, uint32_t flags, uint8_t *__restrict__ keep, int32_t *__restrict__ kept_off,
@@ -295,25 +322,49 @@ __global__ void __launch_bounds__(kToppThreads) topp_kernel(
     if (tid == 0) seg_kept[s] = 0;
     return;
   }
-  // 4. keep flags out, kept-token offsets in block order
-  const int ipb = (nb + kToppThreads - 1) / kToppThreads;
-  const int bb0 = tid * ipb;
-  int32_t lsum = 0;
-  for (int e = 0; e < ipb; ++e) {
-    const int b = bb0 + e;
-    if (b < nb && skeep[b]) lsum += min(B, n - b * B);
+  write_segment_selection(s, b0, nb, n, B, skeep, keep, kept_off, seg_kept, sh32);
+}
+
+// Normalisation and Top-p of one segment per CTA: the normaliser of unip_block_importance (the same
+// fp32 arithmetic, so imp has the same bits) followed, in the same CTA, by the selection of
+// topp_kernel on the scores it just wrote; launched as a programmatic dependent of the score grid.
+__global__ void __launch_bounds__(kToppThreads) norm_select_kernel(
+    const int32_t *__restrict__ blk_cu, const int32_t *__restrict__ cu, const float *__restrict__ partial,
+    int32_t Hkv, int32_t B, double p, uint32_t flags, int32_t cap, float *__restrict__ imp,
+    uint8_t *__restrict__ keep, int32_t *__restrict__ kept_off, int32_t *__restrict__ seg_kept,
+    uint32_t *__restrict__ status) {
+  extern __shared__ unsigned long long skeys[];  // cap rank keys, then cap keep flags
+  uint8_t *skeep = reinterpret_cast<uint8_t *>(skeys + cap);
+  __shared__ unsigned long long sh64[32];
+  __shared__ int32_t sh32[32];
+  __shared__ uint32_t s_bad;
+  __shared__ float sred[kImpNormThreads];
+  const int tid = threadIdx.x;
+  // the row-copy grid may be scheduled now; it waits for this grid's results
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // the score grid's masses are complete past here
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int32_t s = blockIdx.x;
+  const int32_t n = cu[s + 1] - cu[s];
+  const int32_t b0 = blk_cu[s], nb = blk_cu[s + 1] - blk_cu[s];
+  if (nb == 0) {  // not scored: every token is kept
+    if (tid == 0) seg_kept[s] = n > 0 ? n : 0;
+    return;
   }
-  int32_t tot;
-  int32_t run = block_excl_scan<int32_t>(lsum, sh32, &tot);
-  for (int e = 0; e < ipb; ++e) {
-    const int b = bb0 + e;
-    if (b < nb) {
-      keep[b0 + b] = skeep[b];
-      kept_off[b0 + b] = run;
-      if (skeep[b]) run += min(B, n - b * B);
+  if (nb > kMaxBlocks || nb > cap || n <= 0 || nb != (n + B - 1) / B) {
+    if (tid == 0) {
+      atomicOr(status, nb > kMaxBlocks ? UNIP_DEV_TOO_MANY_BLOCKS : UNIP_DEV_BAD_BLOCKS);
+      seg_kept[s] = 0;
     }
+    return;
   }
-  if (tid == 0) seg_kept[s] = tot;
+  normalise_segment(partial, b0, nb, Hkv, imp, sred);
+  __syncthreads();  // this CTA's scores are written before it reads them back
+  if (!select_segment_blocks(imp, b0, nb, p, flags, skeys, skeep, sh64, &s_bad, status)) {
+    if (tid == 0) seg_kept[s] = 0;
+    return;
+  }
+  write_segment_selection(s, b0, nb, n, B, skeep, keep, kept_off, seg_kept, sh32);
 }
 
 // Kept-token offsets of every segment from the per-segment counts, into
@@ -581,6 +632,41 @@ cudaError_t launch_topp(const float *imp, const int32_t *blk_cu, const int32_t *
                             seg_kept, cap, status);
 }
 
+// Row copy after a selection grid (programmatic dependent of it): kept-token offsets per segment,
+// then one warp per kept row writes gather_idx / positions_kept and copies the hidden row.
+cudaError_t launch_gather_rows(const void *hidden, int64_t row_stride, int32_t d_model, bool rows,
+                               const int32_t *cu_seqlens, const int32_t *positions, const int32_t *blk_cu,
+                               const uint8_t *keep, const int32_t *kept_off, const int32_t *seg_kept,
+                               int32_t num_segs, int32_t total_tokens, int32_t block_size, void *hidden_out,
+                               int64_t out_row_stride, int32_t *cu_seqlens_kept, int32_t *n_kept,
+                               int32_t *gather_idx, int32_t *positions_kept, uint32_t *status, cudaStream_t st) {
+  const int sms = device_sm_count();
+  const int warps_per_block = kIndexThreads / 32;
+  int64_t blocks = ((int64_t)(total_tokens > 0 ? total_tokens : 1) + warps_per_block - 1) / warps_per_block;
+  const int64_t max_blocks = (int64_t)(sms > 0 ? sms : 1) * kGatherCtasPerSm;
+  if (blocks > max_blocks) blocks = max_blocks;
+  // per-block kept offsets are staged in shared memory when the upper bound on blocks fits
+  const int32_t blk_bound = unip_importance_capacity(total_tokens, num_segs, block_size);
+  const int32_t stage_blocks =
+      (int64_t)(num_segs + 1 + blk_bound) * 4 <= kGatherStageBytes ? blk_bound : 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)blocks);
+  cfg.blockDim = dim3(kIndexThreads);
+  cfg.dynamicSmemBytes = (size_t)(num_segs + 1 + stage_blocks) * sizeof(int32_t);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(
+      &cfg, select_gather_kernel, static_cast<const uint4 *>(hidden), total_tokens,
+      rows ? (int64_t)(row_stride / 8) : 0, (int32_t)(d_model / 8), cu_seqlens, positions, blk_cu, keep, kept_off,
+      seg_kept, num_segs, block_size, total_tokens, static_cast<uint4 *>(hidden_out),
+      rows ? (int64_t)(out_row_stride / 8) : 0, cu_seqlens_kept, n_kept, gather_idx, positions_kept, stage_blocks,
+      status);
+}
+
 }  // namespace
 }  // namespace unip
 
@@ -719,30 +805,94 @@ UNIP_API int32_t unip_select_gather(const float *imp, const int32_t *blk_cu, con
   if (launch_topp(imp, blk_cu, cu_seqlens, num_segs, total_tokens, block_size, p, flags, keep, kept_off, seg_kept,
                   status, st) != cudaSuccess)
     return UNIP_ERR_CUDA;
-  const int sms = device_sm_count();
-  const int warps_per_block = kIndexThreads / 32;
-  int64_t blocks = ((int64_t)(total_tokens > 0 ? total_tokens : 1) + warps_per_block - 1) / warps_per_block;
-  const int64_t max_blocks = (int64_t)(sms > 0 ? sms : 1) * kGatherCtasPerSm;
-  if (blocks > max_blocks) blocks = max_blocks;
-  // per-block kept offsets are staged in shared memory when the upper bound on blocks fits
-  const int32_t blk_bound = unip_importance_capacity(total_tokens, num_segs, block_size);
-  const int32_t stage_blocks =
-      (int64_t)(num_segs + 1 + blk_bound) * 4 <= kGatherStageBytes ? blk_bound : 0;
+  const cudaError_t e = launch_gather_rows(hidden, row_stride, d_model, rows, cu_seqlens, positions, blk_cu, keep,
+                                           kept_off, seg_kept, num_segs, total_tokens, block_size, hidden_out,
+                                           out_row_stride, cu_seqlens_kept, n_kept, gather_idx, positions_kept,
+                                           status, st);
+  return e == cudaSuccess ? UNIP_OK : UNIP_ERR_CUDA;
+}
+
+UNIP_API size_t unip_importance_select_gather_workspace_size(int32_t total_tokens, int32_t num_segs,
+                                                             int32_t block_size, const unip_attn_params *prm) {
+  const size_t a = unip_importance_workspace_size(total_tokens, num_segs, block_size, prm);
+  const size_t b = unip_topp_workspace_size(total_tokens, num_segs, block_size);
+  if (!a || !b) return 0;
+  return align_up(a, 256) + b;
+}
+
+UNIP_API int32_t unip_importance_select_gather(
+    const void *q, const void *k, const float *lse, const int32_t *cu_seqlens, const int32_t *positions,
+    int32_t num_segs, int32_t total_tokens, const uint8_t *seg_mask, int32_t block_size,
+    const unip_attn_params *prm, double p, uint32_t flags, float *imp, int32_t imp_capacity, int32_t *blk_cu,
+    uint8_t *keep, int32_t *gather_idx, int32_t *cu_seqlens_kept, int32_t *positions_kept, int32_t *n_kept,
+    const void *hidden, int64_t row_stride, int32_t d_model, void *hidden_out, int64_t out_row_stride,
+    void *workspace, size_t workspace_bytes, void *stream) {
+  const bool rows = d_model != 0 || hidden || hidden_out;
+  if (rows) {
+    if (!hidden || !hidden_out || d_model <= 0 || row_stride < d_model || out_row_stride < d_model)
+      return UNIP_ERR_INVALID_ARGUMENT;
+    if (!aligned16(hidden) || !aligned16(hidden_out) || (d_model % 8) || (row_stride % 8) || (out_row_stride % 8))
+      return UNIP_ERR_ALIGNMENT;
+  }
+  if (!prm || !cu_seqlens || !blk_cu || !cu_seqlens_kept || !n_kept || num_segs < 0 || total_tokens < 0)
+    return UNIP_ERR_INVALID_ARGUMENT;
+  if (!(p >= 0.0 && p <= 1.0) || (flags & ~(UNIP_KEEP_FIRST | UNIP_KEEP_LAST))) return UNIP_ERR_INVALID_ARGUMENT;
+  if (total_tokens > 0 && (!positions || !gather_idx || !positions_kept)) return UNIP_ERR_INVALID_ARGUMENT;
+  if (!keep || !imp || imp_capacity < unip_importance_capacity(total_tokens, num_segs, block_size))
+    return UNIP_ERR_INVALID_ARGUMENT;
+  const size_t need = unip_importance_select_gather_workspace_size(total_tokens, num_segs, block_size, prm);
+  if (!need || !workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return UNIP_ERR_WORKSPACE;
+  const size_t ws_imp = align_up(unip_importance_workspace_size(total_tokens, num_segs, block_size, prm), 256);
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  void *ws_sel = ws + ws_imp;
+  const size_t ws_sel_bytes = workspace_bytes - ws_imp;
+  if (num_segs >= kIndexSmemSegs) {  // very many segments: the separate calls
+    const int32_t rc = unip_block_importance(q, k, lse, cu_seqlens, num_segs, total_tokens, seg_mask, block_size, prm,
+                                             imp, imp_capacity, blk_cu, workspace, ws_imp, stream);
+    if (rc != UNIP_OK) return rc;
+    return unip_select_gather(imp, blk_cu, cu_seqlens, positions, num_segs, total_tokens, block_size, p, flags, keep,
+                              imp_capacity, gather_idx, cu_seqlens_kept, positions_kept, n_kept, hidden, row_stride,
+                              d_model, hidden_out, out_row_stride, ws_sel, ws_sel_bytes, stream);
+  }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  float *partial = nullptr;
+  int32_t rc = importance_scores(q, k, lse, cu_seqlens, num_segs, total_tokens, seg_mask, block_size, prm, imp,
+                                 imp_capacity, blk_cu, workspace, ws_imp, st, &partial);
+  if (rc != UNIP_OK) return rc;
+  if (!partial)  // nothing was scored (no segment, or no token): every segment keeps all its tokens
+    return unip_select_gather(imp, blk_cu, cu_seqlens, positions, num_segs, total_tokens, block_size, p, flags, keep,
+                              imp_capacity, gather_idx, cu_seqlens_kept, positions_kept, n_kept, hidden, row_stride,
+                              d_model, hidden_out, out_row_stride, ws_sel, ws_sel_bytes, stream);
+  uint32_t *status = device_status_ptr();
+  if (!status) return UNIP_ERR_CUDA;
+  if (ensure_dynamic_smem((const void *)norm_select_kernel, kMaxBlocks * ((int)sizeof(unsigned long long) + 1)) !=
+      cudaSuccess)
+    return UNIP_ERR_CUDA;
+  int32_t cap = 16;
+  const int64_t cap_need = (int64_t)total_tokens / block_size + 2;
+  while (cap < cap_need && cap < kMaxBlocks) cap <<= 1;
+  int32_t *seg_kept = reinterpret_cast<int32_t *>(static_cast<uint8_t *>(ws_sel) + kWsHeaderBytes);
+  int32_t *kept_off = reinterpret_cast<int32_t *>(static_cast<uint8_t *>(ws_sel) + kWsHeaderBytes +
+                                                  align_up(sizeof(int32_t) * num_segs, 256));
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)blocks);
-  cfg.blockDim = dim3(kIndexThreads);
-  cfg.dynamicSmemBytes = (size_t)(num_segs + 1 + stage_blocks) * sizeof(int32_t);
+  cfg.gridDim = dim3((unsigned)num_segs);
+  cfg.blockDim = dim3(kToppThreads);
+  cfg.dynamicSmemBytes = (size_t)cap * (sizeof(unsigned long long) + 1);
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // may start while the score grid drains
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const cudaError_t e = cudaLaunchKernelEx(
-      &cfg, select_gather_kernel, static_cast<const uint4 *>(hidden), total_tokens, rows ? (int64_t)(row_stride / 8) : 0,
-      (int32_t)(d_model / 8), cu_seqlens, positions, blk_cu, (const uint8_t *)keep, (const int32_t *)kept_off,
-      (const int32_t *)seg_kept, num_segs, block_size, total_tokens, static_cast<uint4 *>(hidden_out),
-      rows ? (int64_t)(out_row_stride / 8) : 0, cu_seqlens_kept, n_kept, gather_idx, positions_kept, stage_blocks, status);
+  if (cudaLaunchKernelEx(&cfg, norm_select_kernel, (const int32_t *)blk_cu, cu_seqlens, (const float *)partial,
+                         prm->num_heads_kv, block_size, p, flags, cap, imp, keep, kept_off, seg_kept,
+                         status) != cudaSuccess)
+    return UNIP_ERR_CUDA;
+  const cudaError_t e = launch_gather_rows(hidden, row_stride, d_model, rows, cu_seqlens, positions, blk_cu, keep,
+                                           kept_off, seg_kept, num_segs, total_tokens, block_size, hidden_out,
+                                           out_row_stride, cu_seqlens_kept, n_kept, gather_idx, positions_kept,
+                                           status, st);
   return e == cudaSuccess ? UNIP_OK : UNIP_ERR_CUDA;
 }
 

@@ -84,6 +84,8 @@ class StepBuffers:
         self.ws_imp = torch.empty(max(int(lib.unip_importance_workspace_size(n, S, bs, ctypes.byref(prm))), 256),
                                   dtype=torch.uint8, device=dev)
         self.ws_topp = torch.empty(max(B.unip_topp_workspace_size(n, S, bs), 256), dtype=torch.uint8, device=dev)
+        self.ws_fused = torch.empty(max(B.unip_importance_select_gather_workspace_size(n, S, bs, hq, hkv, d), 256),
+                                    dtype=torch.uint8, device=dev)
 
 
 def run_attention(di: DeviceInputs, bufs: StepBuffers, stream=None):
@@ -93,6 +95,28 @@ def run_attention(di: DeviceInputs, bufs: StepBuffers, stream=None):
                              k_cache=di.k_cache, v_cache=di.v_cache, block_table=di.block_table,
                              page_size=wl.cache.page_size if wl.cache is not None else 16,
                              workspace=bufs.ws_attn, stream=stream)
+
+
+def attention_plan(wl: Workload, flags: int = 0) -> "B.AttentionPlan":
+    """Host-built plan of the workload's attention calls, from its host-side layout."""
+    return B.AttentionPlan(wl.cu_seqlens, wl.prefix_lens, num_heads_q=wl.num_heads_q,
+                           num_heads_kv=wl.num_heads_kv, head_dim=wl.head_dim,
+                           page_size=wl.cache.page_size if wl.cache is not None else 16,
+                           max_pages_per_seq=wl.block_table.shape[1] if wl.block_table is not None else 0,
+                           flags=flags)
+
+
+def plan_workspace(plan, device):
+    import torch
+    return torch.empty(max(plan.workspace_bytes, 256), dtype=torch.uint8, device=device)
+
+
+def run_attention_planned(di: DeviceInputs, bufs: StepBuffers, plan, workspace, stream=None):
+    """unip_prefill_attention_planned with a plan from attention_plan() and its workspace."""
+    wl = di.wl
+    plan.run(di.q, di.k, di.v, bufs.out, bufs.lse, cu_seqlens=di.cu_seqlens, positions=di.positions,
+             k_cache=di.k_cache, v_cache=di.v_cache, block_table=di.block_table,
+             page_size=wl.cache.page_size if wl.cache is not None else 16, workspace=workspace, stream=stream)
 
 
 def run_importance(di: DeviceInputs, bufs: StepBuffers, stream=None):
@@ -123,6 +147,19 @@ def run_select_gather(di: DeviceInputs, bufs: StepBuffers, p: Optional[float] = 
                          workspace=bufs.ws_topp, stream=stream)
 
 
+def run_importance_select_gather(di: DeviceInputs, bufs: StepBuffers, p: Optional[float] = None, stream=None,
+                                 flags: int = B.UNIP_KEEP_FIRST | B.UNIP_KEEP_LAST):
+    """Importance, Top-p and compaction through the fused entry point (importance's normaliser and the
+    selection share one grid; the row copy follows as a programmatic dependent)."""
+    wl = di.wl
+    B.unip_importance_select_gather(di.q, di.k, bufs.lse, di.cu_seqlens, di.positions, bufs.imp, bufs.blk_cu,
+                                    bufs.keep, bufs.gather_idx, bufs.cu_seqlens_kept, bufs.positions_kept,
+                                    bufs.n_kept, di.hidden, bufs.hidden_out, block_size=bufs.block_size,
+                                    p=wl.top_p if p is None else p, num_heads_q=wl.num_heads_q,
+                                    num_heads_kv=wl.num_heads_kv, head_dim=wl.head_dim, seg_mask=di.seg_mask,
+                                    flags=flags, workspace=bufs.ws_fused, stream=stream)
+
+
 def run_select(di: DeviceInputs, bufs: StepBuffers, p: Optional[float] = None, stream=None,
                flags: int = B.UNIP_KEEP_FIRST | B.UNIP_KEEP_LAST):
     run_importance(di, bufs, stream)
@@ -135,11 +172,15 @@ def run_step(di: DeviceInputs, bufs: StepBuffers, stream=None):
     run_select(di, bufs, stream=stream)
 
 
-def kernels_per_step(has_hidden: bool = True, fused_select: bool = False, num_segs: int = 2) -> int:
-    """libunip kernels one step launches (up to 12000 segments)."""
+def kernels_per_step(has_hidden: bool = True, fused_select: bool = False, num_segs: int = 2,
+                     fused_importance: bool = False) -> int:
+    """libunip kernels one step launches (device-planned attention, up to 12000 segments)."""
     # attention: plan + attention; importance: plan + score + norm;
     # Top-p: select + index, gather: 1  -- or the fused select + gather: 2,
-    # one launch when the stream holds a single segment
+    # one launch when the stream holds a single segment -- or importance, selection and
+    # compaction in one call: plan + score + normalise-and-select + row copy
+    if fused_importance:
+        return 2 + 4
     if fused_select:
         return 2 + 3 + (1 if num_segs == 1 else 2)
     return 2 + 3 + 2 + (1 if has_hidden else 0)
@@ -226,8 +267,7 @@ class StreamedSteps:
                 self.up.record_event(ev[s][0])
             self.cs.wait_event(ev[s][0])
             run_attention(di, bufs, self.cs)
-            run_importance(di, bufs, self.cs)
-            run_select_gather(di, bufs, stream=self.cs)
+            run_importance_select_gather(di, bufs, stream=self.cs)
             self.cs.record_event(ev[s][1])
             # The previous step's hidden rows go on the download stream before this
             # step's downloads, which wait for this step's kernels.

@@ -2,6 +2,7 @@
 computed pair counts, the per-workload bounds, the recorded-traffic lookup and
 the per-step launch count (no GPU)."""
 import hashlib
+import json
 import os
 
 import numpy as np
@@ -66,13 +67,13 @@ def test_recorded_traffic_follows_the_kernel_source(tmp_path, monkeypatch):
     src.write_text("// kernel v1\n")
     sha = hashlib.sha1(src.read_bytes()).hexdigest()
     (tmp_path / "profiles").mkdir()
-    (tmp_path / "profiles" / "rec.md").write_text(
-        f"# rec\n\n- kernel_source_sha1: `{sha}`\n- dram_bytes_per_launch_full_workload: `12345`\n")
+    (tmp_path / "profiles" / "dram_traffic.json").write_text(json.dumps(
+        {"k": {"kernel_source": "kernel.cu", "kernel_source_sha1": sha, "dram_bytes_per_launch": 12345}}))
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
-    assert bench.recorded_traffic(str(src), "rec.md") == 12345.0
+    assert bench.recorded_traffic("k") == 12345.0
     src.write_text("// kernel v2\n")                           # changed since the capture: no traffic
-    assert bench.recorded_traffic(str(src), "rec.md") is None
-    assert bench.recorded_traffic(str(src), "missing.md") is None
+    assert bench.recorded_traffic("k") is None
+    assert bench.recorded_traffic("missing") is None
 
 
 def test_launches_per_step():
@@ -80,14 +81,16 @@ def test_launches_per_step():
     assert kernels_per_step(True, fused_select=True, num_segs=260) == 7
     assert kernels_per_step(True, fused_select=False) == 8
     assert kernels_per_step(False, fused_select=False) == 7
+    assert kernels_per_step(fused_importance=True) == 6
 
 
-def test_committed_attention_record_matches_the_source():
-    """The committed ncu record names the sha of the attention source it was captured on; bench.py
-    attaches its DRAM bytes only while the source is unchanged."""
+def test_committed_traffic_records_follow_their_sources():
+    """bench.py attaches a recorded DRAM figure only while the kernel source still hashes as at capture."""
     root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-    src = os.path.join(root, "sparsified_long_context_gb300", "csrc", "unip_attention.cu")
-    got = bench.recorded_traffic(src, "attn_fwd_long_single.md")
-    sha = hashlib.sha1(open(src, "rb").read()).hexdigest()
-    text = open(os.path.join(root, "profiles", "attn_fwd_long_single.md")).read()
-    assert (got is not None) == (sha in text)
+    table = json.load(open(os.path.join(root, "profiles", "dram_traffic.json")))
+    for name, rec in table.items():
+        if name.startswith("_"):
+            continue
+        src = os.path.join(root, rec["kernel_source"])
+        sha = hashlib.sha1(open(src, "rb").read()).hexdigest()
+        assert (bench.recorded_traffic(name) is not None) == (sha == rec["kernel_source_sha1"])

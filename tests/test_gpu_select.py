@@ -376,3 +376,54 @@ def test_select_gather_many_segments(S):
     assert np.array_equal(pk[:m].cpu().numpy(), rpk)
     got = out[:m].view(torch.int16).cpu().numpy().view(np.uint16)
     assert np.array_equal(got, oracle.gather(hid, rgi))
+
+
+def _fused_vs_separate(wl):
+    from sparsified_long_context_gb300 import binding as Bd
+    from sparsified_long_context_gb300.pipeline import (DeviceInputs, StepBuffers, run_attention, run_importance,
+                                                        run_importance_select_gather, run_select_gather)
+    Bd.unip_get_device_status(clear=True)
+    di = DeviceInputs.from_workload(wl, "cuda")
+    bufs = StepBuffers(di)
+    run_attention(di, bufs)
+    run_importance(di, bufs)
+    run_select_gather(di, bufs)
+    torch.cuda.synchronize()
+    assert Bd.unip_get_device_status(clear=True) == 0
+    names = ["imp", "blk_cu", "keep", "gather_idx", "cu_seqlens_kept", "positions_kept", "n_kept"]
+    if bufs.hidden_out is not None:
+        names.append("hidden_out")
+    ref = {n: getattr(bufs, n).clone() for n in names}
+    for n in names:   # poison every output, so the fused call must write each one
+        t = getattr(bufs, n)
+        t.view(torch.uint8).fill_(0xA5)
+    run_importance_select_gather(di, bufs)
+    torch.cuda.synchronize()
+    st = Bd.unip_get_device_status(clear=True)
+    assert st == 0, Bd.describe_status(st)
+    n_blk = int(ref["blk_cu"][-1].item())
+    m = int(ref["n_kept"].item())
+    lim = {"imp": n_blk, "keep": n_blk, "gather_idx": m, "positions_kept": m, "hidden_out": m}
+    for n in names:
+        a, b = getattr(bufs, n), ref[n]
+        if n in lim:
+            a, b = a[: lim[n]], b[: lim[n]]
+        assert torch.equal(a.contiguous().view(torch.uint8), b.contiguous().view(torch.uint8)), n
+    return bufs
+
+
+@pytest.mark.parametrize("name", ["tiny_packed", "long_single", "mixed_step", "prepacked"])
+def test_fused_importance_select_gather_matches_the_separate_calls(name):
+    """unip_importance_select_gather: the bits of unip_block_importance + unip_select_gather (scores, keep
+    mask, indices, kept offsets and positions, compacted rows), and bit-exact against the oracle fed its
+    scores."""
+    wl = W.prepacked(library_ffd) if name == "prepacked" else W.workload_by_name(name)
+    bufs = _fused_vs_separate(wl)
+    _check_selection(wl, bufs)
+
+
+def test_fused_path_with_unscored_and_empty_segments():
+    wl = W.packed([0, 300, 1, 0, 700, 64, 17], 8, 2, 128, seed=61, block_size=32, top_p=0.8, d_model=512)
+    wl.seg_mask = np.array([1, 1, 0, 1, 0, 1, 1], np.uint8)
+    bufs = _fused_vs_separate(wl)
+    _check_selection(wl, bufs)
