@@ -116,6 +116,10 @@ UNIP_API const char *unip_version(void);
 /* Text for a host return code (static storage). */
 UNIP_API const char *unip_status_string(int32_t code);
 
+/* Name of the last CUDA runtime error of the calling host thread (and clears
+ * it): the detail behind a UNIP_ERR_CUDA return.  Static storage. */
+UNIP_API const char *unip_last_cuda_error(void);
+
 /* Reads the current device's status word into *bits (synchronises that
  * device), and clears it when clear != 0.  Returns UNIP_OK or UNIP_ERR_CUDA. */
 UNIP_API int32_t unip_get_device_status(uint32_t *bits, int32_t clear);

@@ -80,6 +80,8 @@ def load(build_if_missing: bool = True):
         lib.unip_version.restype = ctypes.c_char_p
         lib.unip_status_string.restype = ctypes.c_char_p
         lib.unip_status_string.argtypes = [i32]
+        lib.unip_last_cuda_error.restype = ctypes.c_char_p
+        lib.unip_last_cuda_error.argtypes = []
         lib.unip_get_device_status.restype = i32
         lib.unip_get_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32]
         lib.unip_attention_workspace_size.restype = sz
@@ -148,9 +150,15 @@ def load(build_if_missing: bool = True):
         return lib
 
 
+UNIP_ERR_CUDA = -4
+
+
 def _check(rc: int, what: str):
     if rc != UNIP_OK:
-        msg = load().unip_status_string(rc).decode()
+        lib = load()
+        msg = lib.unip_status_string(rc).decode()
+        if rc == UNIP_ERR_CUDA:
+            msg += f": {lib.unip_last_cuda_error().decode()}"
         raise UnipError(f"{what} failed: {msg} (code {rc})")
 
 

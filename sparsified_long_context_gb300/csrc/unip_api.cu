@@ -1,8 +1,8 @@
 // Host plumbing shared by every entry point: per-device status word,
 // SM count, driver entry point for tensor maps, version and error strings.
+#include <map>
 #include <mutex>
-#include <set>
-#include <tuple>
+#include <utility>
 
 #include "unip_internal.cuh"
 
@@ -55,13 +55,16 @@ cudaError_t ensure_dynamic_smem(const void *fn, int bytes) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  // The attribute is one value per kernel and device: it is only ever raised, so that a launch that
+  // needs less shared memory never lowers the limit a larger launch relies on.
   static std::mutex mu;
-  static std::set<std::tuple<const void *, int, int>> done;
-  const auto key = std::make_tuple(fn, dev, bytes);
+  static std::map<std::pair<const void *, int>, int> limit;
+  const auto key = std::make_pair(fn, dev);
   std::lock_guard<std::mutex> lk(mu);
-  if (done.count(key)) return cudaSuccess;
+  const auto it = limit.find(key);
+  if (it != limit.end() && it->second >= bytes) return cudaSuccess;
   e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  if (e == cudaSuccess) done.insert(key);
+  if (e == cudaSuccess) limit[key] = bytes;
   return e;
 }
 
@@ -103,6 +106,8 @@ UNIP_API const char *unip_status_string(int32_t code) {
     default: return "unknown status";
   }
 }
+
+UNIP_API const char *unip_last_cuda_error(void) { return cudaGetErrorString(cudaGetLastError()); }
 
 UNIP_API int32_t unip_get_device_status(uint32_t *bits, int32_t clear) {
   if (!bits) return UNIP_ERR_INVALID_ARGUMENT;

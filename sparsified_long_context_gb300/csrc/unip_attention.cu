@@ -281,7 +281,8 @@ enum BarId {
   kBarUnitEmpty0 = 14 + 3 * kStages,   // + k: every consumer warp has read s_unit[k]
   kBarSplitStored0 = 16 + 3 * kStages,  // + tile: split epilogue, every thread stored its partial (count 256)
   kBarSplitDecided0 = 18 + 3 * kStages, // + tile: split epilogue, the ticket was taken (count 1)
-  kNumBars = 20 + 3 * kStages
+  kBarTile1Start = 20 + 3 * kStages,    // every warp of tile 1 has started work item i (count 8)
+  kNumBars = 21 + 3 * kStages
 };
 
 __device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
@@ -732,6 +733,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       mbar_init(bar(kBarSplitStored0 + i), 2 * kBlockM);
       mbar_init(bar(kBarSplitDecided0 + i), 1);
     }
+    mbar_init(bar(kBarTile1Start), 8);
     s_abort = 0;
     s_tmem_busy = 0;
     fence_mbar_init();
@@ -806,6 +808,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     for (uint32_t i = 0;; ++i) {
       int32_t u;
       if (!next_unit(i, u) || u < 0) break;
+      // Tile 1 idles through one-tile items on tile 0's O-done barrier, so it must never fall two of
+      // that barrier's phases behind (a warp of tile 1 may be late, merging the partials of a split
+      // item): the MMA warp completes an item's O-done only after all of tile 1 has started the item.
+      if (tile == 1 && lane == 0) mbar_arrive(smem_u32(&bars[kBarTile1Start]));
       const WorkItem w = decode(u);
       sp.split = w.split;
       sp.nsplit = w.nsplit;
@@ -1054,6 +1060,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       auto o_free = [&](int t, uint32_t uses) {
         return uses == 0 || mbar_wait(bar(kBarOFree0 + t), (uses - 1) & 1, abort_flag, a.status);
       };
+      // before the PV that completes this item's O-done of tile 0: every warp of tile 1 started the item
+      auto tile1_started = [&]() { return mbar_wait(bar(kBarTile1Start), items & 1, abort_flag, a.status); };
       int64_t lbase = 0;
       bool ok = true;
       for (uint32_t i = 0; ok; ++i) {
@@ -1084,7 +1092,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             const uint32_t d_s = tmem + buf * kBlockN;
             const int64_t iv = lbase + (j < T - 2 ? 2 * j + 2 : j + T), ik = lbase + 2 * j + 3;
             ok = mbar_wait(bar(kBarPFull0 + buf), ((buf ? cs1 : cs0) + (j >> 1)) & 1, abort_flag, a.status) &&
-                 full(iv) && (j > 0 || o_free(0, co0));
+                 full(iv) && (j > 0 || o_free(0, co0)) && (j + 1 < T || tile1_started());
             if (!ok) break;
             tc_fence_after();
             pv(d_o0, d_s, slot_desc(dv, (int)(iv % ns)), j > 0 ? 1u : 0u);
@@ -1115,7 +1123,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             const uint32_t acc = j > 0 ? 1u : 0u;
             // tile 0: PV(j), then QK(j+1); K_(j+1) is waited for first so that both go out back to back
             ok = full(iv) && (!more || full(ik)) &&
-                 mbar_wait(bar(kBarPFull0 + 0), (cs0 + j) & 1, abort_flag, a.status) && (j > 0 || o_free(0, co0));
+                 mbar_wait(bar(kBarPFull0 + 0), (cs0 + j) & 1, abort_flag, a.status) && (j > 0 || o_free(0, co0)) &&
+                 (more || tile1_started());
             if (!ok) break;
             tc_fence_after();
             pv(d_o0, d_s0, dvj, acc);

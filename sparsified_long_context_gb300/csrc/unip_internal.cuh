@@ -17,8 +17,8 @@ namespace unip {
 uint32_t *device_status_ptr();
 // Streaming-multiprocessor count of the current device.
 int device_sm_count();
-// Raises the dynamic shared-memory limit of kernel `fn` to `bytes` on the current device, once per
-// (kernel, device, size); safe to call from several host threads.
+// Raises the dynamic shared-memory limit of kernel `fn` on the current device to at least `bytes`
+// (never lowers it); safe to call from several host threads.
 cudaError_t ensure_dynamic_smem(const void *fn, int bytes);
 // Importance without its normalisation (plan + persistent score grid of unip_block_importance, same
 // checks and return codes): block masses per kv head land in the workspace; *partial receives their

@@ -197,3 +197,40 @@ def test_plan_reused_across_workspaces_and_calls():
     for r in res[1:]:
         assert torch.equal(r.view(torch.int16), res[0].view(torch.int16))
     plan.close()
+
+
+def test_split_items_repeated_without_timeouts():
+    """Split items whose merge keeps some warps of a tile busy while one-tile items follow: 200 runs of a
+    compacted stream with forced splits (2 to 5) must never trip a bounded device wait, and every run
+    gives the bits of the first run with the same split count."""
+    from sparsified_long_context_gb300 import binding as B
+    from test_gpu_attention import _compact
+    wl = _batch_with_prefixes([3000, 17, 300, 2048, 0, 64], [900, 1, 130, 65, 300, 3], 32, 8, 128, 16, seed=77)
+    q, k, v, cu_k, pos_k, plen = _compact(wl, 16, np.random.default_rng(5), 0.5)
+    n = int(cu_k[-1])
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    qd, kd, vd = dev(q).view(torch.bfloat16), dev(k).view(torch.bfloat16), dev(v).view(torch.bfloat16)
+    kct, vct = wl.cache.to_torch("cuda")
+    bt = dev(wl.block_table)
+    plans = {s: B.AttentionPlan(cu_k, plen, num_heads_q=32, num_heads_kv=8, head_dim=128, page_size=16,
+                                max_pages_per_seq=wl.block_table.shape[1], flags=B.UNIP_PLAN_SPLITS(s))
+             for s in (2, 3, 4, 5)}
+    ws = {s: torch.empty(max(p.workspace_bytes, 256), dtype=torch.uint8, device="cuda") for s, p in plans.items()}
+    out = torch.empty((n, 32, 128), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((32, n), dtype=torch.float32, device="cuda")
+    first = {}
+    B.unip_get_device_status(clear=True)
+    for it in range(200):
+        s = 2 + it % 4
+        plans[s].run(qd, kd, vd, out, lse, k_cache=kct, v_cache=vct, block_table=bt, page_size=16,
+                     workspace=ws[s])
+        if it % 20 == 19 or it < 4:
+            torch.cuda.synchronize()
+            st = B.unip_get_device_status(clear=True)
+            assert st == 0, (it, B.describe_status(st))
+            if s not in first:
+                first[s] = out.clone()
+            else:
+                assert torch.equal(out.view(torch.int16), first[s].view(torch.int16)), it
+    for p in plans.values():
+        p.close()

@@ -427,3 +427,20 @@ def test_fused_path_with_unscored_and_empty_segments():
     wl.seg_mask = np.array([1, 1, 0, 1, 0, 1, 1], np.uint8)
     bufs = _fused_vs_separate(wl)
     _check_selection(wl, bufs)
+
+
+def test_launches_with_growing_and_shrinking_shared_memory():
+    """The compaction's shared memory grows with the number of segments and blocks: a large call after a
+    smaller one must still launch (a kernel's shared-memory limit is only ever raised)."""
+    from sparsified_long_context_gb300.pipeline import (DeviceInputs, StepBuffers, run_attention, run_importance,
+                                                        run_select_gather)
+    big = W.packed([20] * 300, 4, 2, 64, seed=71, block_size=16, top_p=0.9, d_model=256)
+    small = W.packed([500, 300], 4, 2, 64, seed=72, block_size=16, top_p=0.9, d_model=256)
+    for wl in (big, small, big):
+        di = DeviceInputs.from_workload(wl, "cuda")
+        bufs = StepBuffers(di)
+        run_attention(di, bufs)
+        run_importance(di, bufs)
+        run_select_gather(di, bufs)
+        torch.cuda.synchronize()
+        _check_selection(wl, bufs)
