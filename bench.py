@@ -10,7 +10,8 @@ attention shape), heavy keys in 10 spans, block 64, p 0.95, hidden d 4096.
 
 Prints one JSON line.  ``value`` = useful attention TFLOP/s over the whole
 step (4*D*H_q*sum_s[n*P + n(n+1)/2] per step / step time), inputs resident
-in HBM, L2 flushed before every step.  ``e2e`` = the same metric with the
+in HBM, L2 flushed before every step (a 256 MB write, then a 256 MB read, so
+no dirty line of the flush is written back inside the timed region).  ``e2e`` = the same metric with the
 inputs copied from pinned host memory and the results read back inside the
 timed region.  ``--impl reference`` times the fp64 CPU oracle instead.
 
@@ -38,6 +39,25 @@ import numpy as np  # noqa: E402
 METRIC = "prefill attn useful TFLOP/s (% BF16 peak); select+gather GB/s (% HBM)"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_FLUSH_BYTES = 256 << 20
+L2_FLUSH_HOW = "256 MB written, then another 256 MB read"
+
+
+class L2Flush:
+    """Empties L2 of the step's data before a timed step: writes one buffer larger than L2, then reads
+    another, so the timed work starts with a cold L2 that also holds no dirty lines of the flush (their
+    write-back would otherwise land inside the next timed region, charged to whatever kernel evicts
+    them).  Capturable in a CUDA graph (no allocation after construction)."""
+
+    def __init__(self, device):
+        import torch
+        self.w = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+        self.r = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+        self.out = torch.empty((), dtype=torch.float32, device=device)
+
+    def __call__(self):
+        import torch
+        self.w.zero_()
+        torch.sum(self.r, dim=0, out=self.out)
 
 
 def useful_attention_flops(wl) -> float:
@@ -153,7 +173,7 @@ def rope_append_part(di, flush, stream, hbm_peak: float, reps: int = 10):
     slots = (perm[t // page] * page + t % page).to(dev)
     ts = []
     for i in range(reps + 2):
-        flush.zero_()
+        flush()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         B.unip_rope_append_kv(q, k, di.v, di.positions, num_heads_q=hq, num_heads_kv=hkv, head_dim=d,
@@ -374,7 +394,7 @@ def incremental_select_ms(di, bufs, flush, stream, reps: int = 10, trials: int =
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=cs):
             for _ in range(reps):
-                flush.zero_()
+                flush()
                 if with_select:
                     run_importance_select_gather(di, bufs, stream=cs)
                 else:
@@ -397,7 +417,7 @@ def incremental_select_ms(di, bufs, flush, stream, reps: int = 10, trials: int =
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=cs):
             for _ in range(reps):
-                flush.zero_()
+                flush()
         return g
 
     torch.cuda.synchronize()
@@ -413,7 +433,7 @@ def _timed_steps(step, flush, stream, seconds: float, max_steps: int, gpu_index:
     per-step event lists and the clock summary of the timed region.  One untimed step sizes the loop."""
     import torch
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
-    flush.zero_()
+    flush()
     ev[0].record(stream)
     step(None)
     ev[1].record(stream)
@@ -423,7 +443,7 @@ def _timed_steps(step, flush, stream, seconds: float, max_steps: int, gpu_index:
     evs = []
     with ClockSampler(gpu_index) as clk:
         for _ in range(n):
-            flush.zero_()
+            flush()
             e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
             step(e)
             evs.append(e)
@@ -474,7 +494,7 @@ def part_chunked(rank: int, gpu_index: int, flush, stream, peaks, seconds: float
            "per_call": [{"prefix": int(c.prefix_lens[0]), "ms": m, "tflops": f / (m * 1e-3) / 1e12,
                          "plan": s[2].info}
                         for c, m, f, s in zip(chunks, per_call, flops, sets)],
-           "timing": "median per call over repeated calls, L2 flushed (256 MB write) before each call",
+           "timing": f"median per call over repeated calls, L2 flushed ({L2_FLUSH_HOW}) before each call",
            "clocks": {"sm_mhz": stt.median(sm) if sm else None,
                       "sm_max_mhz": clocks[0]["sm_max_mhz"],
                       "reasons": sorted({r for c in clocks for r in c["reasons"]}),
@@ -506,7 +526,7 @@ def part_step_workload(name: str, rank: int, gpu_index: int, flush, stream, peak
             e[2].record(stream)
 
     for _ in range(3):
-        flush.zero_()
+        flush()
         step(None)
     evs, clk = _timed_steps(step, flush, stream, seconds, 2000, gpu_index)
     st = B.unip_get_device_status(clear=True)
@@ -530,7 +550,7 @@ def part_step_workload(name: str, rank: int, gpu_index: int, flush, stream, peak
             "select_gather_ms": sel_ms, "select_gather_bytes": sg_bytes, "select_gather_gbs": gbs,
             "select_gather_frac_hbm": gbs / hbm, "n_kept": n_kept, "n_blocks": n_blocks,
             "workload_context": workload_context(wl, attn_ms, bf16, hbm),
-            "timing": "median per step, L2 flushed (256 MB write) before each step; importance and the "
+            "timing": f"median per step, L2 flushed ({L2_FLUSH_HOW}) before each step; importance and the "
                       "select+gather increment from graph replays", "clocks": clk}
 
 
@@ -559,13 +579,13 @@ def bench_chunked(args):
         sets.append((di, StepBuffers(di, block_size=64)))
     di1 = DeviceInputs.from_workload(one, dev, with_hidden=False)
     b1 = StepBuffers(di1, block_size=64)
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush = L2Flush(dev)
     stream = torch.cuda.current_stream()
     flops = [useful_attention_flops(c) for c in chunks]
 
     def step(evs=None):
         for i, (di, bufs) in enumerate(sets):
-            flush.zero_()
+            flush()
             if evs is not None:
                 evs[i][0].record(stream)
             run_attention(di, bufs, stream)
@@ -600,7 +620,7 @@ def bench_chunked(args):
     # the one-shot call of the same prompt, as context
     ts = []
     for _ in range(args.warmup + args.steps):
-        flush.zero_()
+        flush()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         run_attention(di1, b1, stream)
@@ -621,7 +641,7 @@ def bench_chunked(args):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded, bf16 ~N(0,1))",
         "config": {"workload": "chunked: one 4096-token prompt in 8 attention calls of 512 tokens behind "
                                "paged prefixes of 0..3584 tokens (16-token pages, shuffled), H_q 32, H_kv 8, D 128",
-                   "l2": "flushed (256 MB write) before every call",
+                   "l2": f"flushed ({L2_FLUSH_HOW}) before every call",
                    "parallelism": f"replicas x{world} (independent prompts, no collective)",
                    "useful_attention_flops_per_step": float(sum(flops))},
         "parts": {"per_chunk": [{"prefix": int(c.prefix_lens[0]), "ms": m, "tflops": f / (m * 1e-3) / 1e12}
@@ -684,7 +704,7 @@ def main():
     wl = rank_seed_workload(args.workload, rank, args.tokens)
     di = DeviceInputs.from_workload(wl, f"cuda:{local}")
     bufs = StepBuffers(di)
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=f"cuda:{local}")
+    flush = L2Flush(f"cuda:{local}")
     stream = torch.cuda.current_stream()
     flops_step = useful_attention_flops(wl)
 
@@ -699,7 +719,7 @@ def main():
             ev[2].record(stream)
 
     for _ in range(args.warmup):
-        flush.zero_()
+        flush()
         step()
     torch.cuda.synchronize()
     st = B.unip_get_device_status(clear=True)
@@ -713,7 +733,7 @@ def main():
     with ClockSampler(local) as clk:
         wall0 = time.perf_counter()
         for i in range(args.steps):
-            flush.zero_()
+            flush()
             step(evs[i])
         torch.cuda.synchronize()
         wall1 = time.perf_counter()
@@ -791,7 +811,7 @@ def main():
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded, bf16 ~N(0,1), heavy keys x4)",
-        "config": {"workload": describe(wl), "l2": "flushed (256 MB write) before every step",
+        "config": {"workload": describe(wl), "l2": f"flushed ({L2_FLUSH_HOW}) before every step",
                    "parallelism": f"replicas x{world} (independent batches, no collective)",
                    "useful_attention_flops_per_step": flops_step},
         "parts": {

@@ -287,6 +287,57 @@ __device__ __forceinline__ void write_segment_selection(int32_t s, int32_t b0, i
   if (tid == 0) seg_kept[s] = tot;
 }
 
+// Selection of a segment of at most 32 blocks by one warp, block b on lane b (f: its score, read by
+// lanes below nb), in registers: the same fixed-point masses, exact totals and integer threshold as
+// select_segment_blocks, with the exclusive mass of the blocks ranked before a block summed over
+// the lanes holding a smaller key (keys are unique, so that set is exactly the blocks ranked
+// before it).  Writes keep, the kept-token offsets and the segment's count, or only a zero count
+// (status raised) when a score is not in [0, 1].
+__device__ void select_small_segment(float f, int32_t s, int32_t b0, int32_t nb, int32_t n, int32_t B, double p,
+                                     uint32_t flags, uint8_t *__restrict__ keep, int32_t *__restrict__ kept_off,
+                                     int32_t *__restrict__ seg_kept, uint32_t *__restrict__ status) {
+  const int lane = threadIdx.x & 31;
+  const bool live = lane < nb;
+  if (__float_as_uint(f) == 0x80000000u) f = __uint_as_float(0u);  // a zero score is +0
+  const bool bad = live && (!(f >= 0.f) || f > 1.f);
+  if (__any_sync(0xffffffffu, bad)) {
+    if (lane == 0) {
+      atomicOr(status, UNIP_DEV_BAD_SCORES);
+      seg_kept[s] = 0;
+    }
+    return;
+  }
+  const bool forced = live && (((flags & UNIP_KEEP_FIRST) && lane == 0) || ((flags & UNIP_KEEP_LAST) && lane == nb - 1));
+  const unsigned long long qb = live ? fixed_mass(f) : 0ull;
+  unsigned long long T = qb, CF = forced ? qb : 0ull;
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) {
+    T += __shfl_xor_sync(0xffffffffu, T, off);
+    CF += __shfl_xor_sync(0xffffffffu, CF, off);
+  }
+  bool kf = live;  // a zero total keeps every block
+  if (T != 0) {
+    const unsigned long long kthr = mass_threshold(p, T);
+    const unsigned long long key = live && !forced ? rank_key(f, lane) : ~0ull;
+    unsigned long long pre = 0;
+    for (int j = 0; j < nb; ++j) {
+      const unsigned long long kj = __shfl_sync(0xffffffffu, key, j);
+      const unsigned long long qj = __shfl_sync(0xffffffffu, qb, j);
+      if (kj < key) pre += qj;
+    }
+    kf = forced || (live && CF + pre < kthr);
+  }
+  // kept-token offsets in block order (exclusive) and the segment's count
+  const int32_t len = kf ? min(B, n - lane * B) : 0;
+  const int32_t incl = warp_incl_scan(len);
+  const int32_t tot = __shfl_sync(0xffffffffu, incl, 31);
+  if (live) {
+    keep[b0 + lane] = kf ? 1 : 0;
+    kept_off[b0 + lane] = incl - len;
+  }
+  if (lane == 0) seg_kept[s] = tot;
+}
+
 __global__ void __launch_bounds__(kToppThreads) topp_kernel(
     const float *__restrict__ imp, const int32_t *__restrict__ blk_cu, const int32_t *__restrict__ cu, int32_t B,
     double p, uint32_t flags, uint8_t *__restrict__ keep, int32_t *__restrict__ kept_off,
@@ -316,6 +367,12 @@ __global__ void __launch_bounds__(kToppThreads) topp_kernel(
       atomicOr(status, nb > kMaxBlocks ? UNIP_DEV_TOO_MANY_BLOCKS : UNIP_DEV_BAD_BLOCKS);
       seg_kept[s] = 0;
     }
+    return;
+  }
+  if (nb <= 32) {  // one warp, no barriers
+    if (tid < 32)
+      select_small_segment(tid < nb ? imp[b0 + tid] : 0.f, s, b0, nb, n, B, p, flags, keep, kept_off, seg_kept,
+                           status);
     return;
   }
   if (!select_segment_blocks(imp, b0, nb, p, flags, skeys, skeep, sh64, &s_bad, status)) {
@@ -358,6 +415,23 @@ __global__ void __launch_bounds__(kToppThreads) norm_select_kernel(
     }
     return;
   }
+  if (nb <= 32) {
+    // One warp, block b on lane b.  The normaliser's tree over at most 32 nonzero masses (the
+    // other slots add exact zeros) pairs the same partial sums as the lanes' xor butterfly, so the
+    // scores have the bits normalise_segment gives them.
+    if (tid < 32) {
+      float m = 0.f;
+      if (tid < nb)
+        for (int32_t g = 0; g < Hkv; ++g) m += partial[(int64_t)(b0 + tid) * Hkv + g];
+      float t = m;
+#pragma unroll
+      for (int off = 16; off >= 1; off >>= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
+      const float f = m * (1.f / t);
+      if (tid < nb) imp[b0 + tid] = f;
+      select_small_segment(f, s, b0, nb, n, B, p, flags, keep, kept_off, seg_kept, status);
+    }
+    return;
+  }
   normalise_segment(partial, b0, nb, Hkv, imp, sred);
   __syncthreads();  // this CTA's scores are written before it reads them back
   if (!select_segment_blocks(imp, b0, nb, p, flags, skeys, skeep, sh64, &s_bad, status)) {
@@ -367,22 +441,54 @@ __global__ void __launch_bounds__(kToppThreads) norm_select_kernel(
   write_segment_selection(s, b0, nb, n, B, skeep, keep, kept_off, seg_kept, sh32);
 }
 
-// Kept-token offsets of every segment from the per-segment counts, into
-// shared memory (every CTA of the index kernel recomputes them: S is small
-// next to N, and this saves a launch and any cross-CTA handshake).
+// Copies n0 ints of src0 to dst0 and n1 ints of src1 to dst1 (shared memory), each thread issuing
+// all of its loads of a round before any store, so the copy costs about one memory round trip.
+__device__ __forceinline__ void stage_two(int32_t *__restrict__ dst0, const int32_t *__restrict__ src0, int32_t n0,
+                                          int32_t *__restrict__ dst1, const int32_t *__restrict__ src1, int32_t n1) {
+  constexpr int kPer = 8;
+  const int32_t n = n0 + n1;
+  for (int32_t base = 0; base < n; base += kIndexThreads * kPer) {
+    int32_t v[kPer];
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int32_t i = base + u * kIndexThreads + threadIdx.x;
+      v[u] = i < n0 ? src0[i] : (i < n ? src1[i - n0] : 0);
+    }
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int32_t i = base + u * kIndexThreads + threadIdx.x;
+      if (i < n0) dst0[i] = v[u];
+      else if (i < n) dst1[i - n0] = v[u];
+    }
+  }
+}
+
+// Kept-token offsets of every segment, exclusive, in place: soff[0, S) holds the per-segment kept
+// counts on entry (written by this CTA's threads), the offsets on exit, and soff[S] the total.
+// Every CTA of a gather grid recomputes them: S is small next to N, and this saves a launch and
+// any cross-CTA handshake.
+__device__ void segment_offsets_inplace(int32_t S, int32_t *__restrict__ soff, int32_t *sh32) {
+  __syncthreads();
+  const int32_t per = (S + kIndexThreads - 1) / kIndexThreads;
+  const int32_t i0 = threadIdx.x * per;
+  int32_t run = 0;
+  for (int32_t e = 0; e < per && i0 + e < S; ++e) run += soff[i0 + e];
+  int32_t tot;
+  run = block_excl_scan<int32_t>(run, sh32, &tot);  // every count has been read past its barriers
+  for (int32_t e = 0; e < per && i0 + e < S; ++e) {
+    const int32_t c = soff[i0 + e];
+    soff[i0 + e] = run;
+    run += c;
+  }
+  if (threadIdx.x == 0) soff[S] = tot;
+  __syncthreads();
+}
+
+// The same from the counts in global memory.
 __device__ void segment_offsets(const int32_t *__restrict__ seg_kept, int32_t S, int32_t *__restrict__ soff,
                                 int32_t *sh32) {
-  int32_t carry = 0;
-  for (int base = 0; base < S; base += kIndexThreads) {
-    const int sidx = base + threadIdx.x;
-    const int32_t v = sidx < S ? seg_kept[sidx] : 0;
-    int32_t tot;
-    const int32_t ex = block_excl_scan<int32_t>(v, sh32, &tot);
-    if (sidx < S) soff[sidx] = carry + ex;
-    carry += tot;
-  }
-  if (threadIdx.x == 0) soff[S] = carry;
-  __syncthreads();
+  stage_two(soff, seg_kept, S, nullptr, nullptr, 0);
+  segment_offsets_inplace(S, soff, sh32);
 }
 
 __global__ void __launch_bounds__(kIndexThreads) index_kernel(
@@ -473,12 +579,14 @@ __global__ void __launch_bounds__(kIndexThreads) select_gather_kernel(
   extern __shared__ int32_t soff[];  // S + 1 kept-token offsets, then (optionally) per-block kept offsets
   __shared__ int32_t sh32[32];
   asm volatile("griddepcontrol.wait;" ::: "memory");  // the Top-p grid's results are visible past here
+  // The block count, the staged block offsets and the segment counts are loaded in one round trip:
+  // stage_blocks bounds the call's blocks and the workspace holds that many offsets, so the entries
+  // past the real count are read (never used) instead of waiting for the count first.
   const int32_t nblk = blk_cu[S];
   int32_t *skoff = soff + S + 1;
+  stage_two(soff, seg_kept, S, skoff, kept_off, stage_blocks);
   const bool staged = nblk <= stage_blocks;
-  if (staged)
-    for (int32_t b = threadIdx.x; b < nblk; b += kIndexThreads) skoff[b] = kept_off[b];
-  segment_offsets(seg_kept, S, soff, sh32);
+  segment_offsets_inplace(S, soff, sh32);  // its barriers publish skoff
   if (blockIdx.x == 0) {
     for (int i = threadIdx.x; i <= S; i += kIndexThreads) cu_kept[i] = soff[i];
     if (threadIdx.x == 0) *n_kept = soff[S];

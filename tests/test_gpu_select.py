@@ -173,10 +173,10 @@ def test_topp_edge_cases_bit_exact(flags):
         assert np.array_equal(gi, rgi) and np.array_equal(ck, rck) and np.array_equal(pk, rpk)
 
 
-def test_topp_negative_zero_scores():
+@pytest.mark.parametrize("nb", [13, 32, 40])   # one-warp path (up to 32 blocks) and the CTA path
+def test_topp_negative_zero_scores(nb):
     """-0 scores through the public Top-p call: read as zero (mass and rank), like the oracle."""
-    rng = np.random.default_rng(77)
-    nb = 40
+    rng = np.random.default_rng(77 + nb)
     x = rng.random(nb).astype(np.float32)
     x[::5] = 0.0
     x = (x / x.sum()).astype(np.float32)
@@ -186,6 +186,34 @@ def test_topp_negative_zero_scores():
     for p, flags in [(0.5, 0), (0.9, 3), (1.0, 0), (1.0, 3)]:
         keep, gi, ck, pk, pos = _topp_direct(x, bc, cu, 16, p, flags)
         assert np.array_equal(keep, oracle.topp_select(x, bc, p, flags)), (p, flags)
+
+
+@pytest.mark.parametrize("bad", [np.nan, -0.25, 1.5])
+def test_topp_invalid_scores_raise_status(bad):
+    """A score outside [0, 1] (or NaN) in a segment of either selection path raises the bad-scores bit
+    and that segment keeps nothing; a valid segment in the same call is still selected exactly."""
+    rng = np.random.default_rng(11)
+    B_ = 16
+    nbs = [5, 40, 8]                       # one-warp path, CTA path, one-warp path
+    parts = []
+    for nb in nbs:
+        x = rng.random(nb)
+        parts.append((x / x.sum()).astype(np.float32))
+    from sparsified_long_context_gb300 import binding as B
+    parts[0][2] = bad
+    parts[1][7] = bad
+    imp = np.concatenate(parts).astype(np.float32)
+    bc = np.concatenate([[0], np.cumsum(nbs)]).astype(np.int32)
+    cu = (bc * B_).astype(np.int32)
+    B.unip_get_device_status(clear=True)
+    keep, gi, ck, pk, pos = _topp_direct(imp, bc, cu, B_, 0.9, 0)
+    st = B.unip_get_device_status(clear=True)
+    assert st & 0x10, B.describe_status(st)                  # UNIP_DEV_BAD_SCORES
+    assert ck[1] - ck[0] == 0 and ck[2] - ck[1] == 0         # the two invalid segments keep nothing
+    good = parts[2]
+    ref = oracle.topp_select(good, np.array([0, len(good)], np.int32), 0.9, 0)
+    assert np.array_equal(keep[bc[2]:bc[3]], ref)
+    assert ck[3] - ck[2] == int(ref.sum()) * B_
 
 
 def test_topp_zero_mass_keeps_all():
