@@ -1399,9 +1399,9 @@ namespace {
 // merges reads every split's partial back through L2: a few round trips of ~3k cycles when many
 // tiles merge at once.  Both scale with the tile's valid rows (warps past them store nothing), so
 // splitting pays for decode-like tiles far more readily than for full prefill tiles.
-constexpr double kCostTile2 = 3400.0, kCostTile1 = 1600.0, kCostTile1Prefix = 2900.0;
+constexpr double kCostTile2 = 3400.0, kCostTile2Prefix = 3900.0, kCostTile1 = 1600.0, kCostTile1Prefix = 2900.0;
 constexpr double kCostItem = 3000.0, kCostSplitFixed = 2000.0, kCostSplitStore = 3000.0;
-constexpr double kCostMergeRound = 3000.0;
+constexpr double kCostMergeRound = 5000.0;  // a round of the merge's loads reads partials another SM wrote
 constexpr int32_t kMinSplitTiles = 2;
 constexpr int32_t kMaxSplits = 8;        // the merge reads every split: more would lengthen the tail
 constexpr int32_t kMaxSplitsFull = 2;    // tiles whose rows are mostly valid
@@ -1415,8 +1415,8 @@ struct PlanUnit {
 };
 
 double range_cost(const PlanUnit &u, int32_t j0, int32_t T) {
-  if (u.two) return kCostTile2 * T;
-  const int32_t pre = std::max(0, std::min(T, u.Tp - j0));
+  const int32_t pre = std::max(0, std::min(T, u.Tp - j0));  // key tiles read through the block table
+  if (u.two) return kCostTile2Prefix * pre + kCostTile2 * (T - pre);
   return kCostTile1Prefix * pre + kCostTile1 * (T - pre);
 }
 
