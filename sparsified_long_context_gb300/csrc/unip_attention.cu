@@ -252,6 +252,7 @@ constexpr int kWarpTma = 16;
 constexpr int kWarpMma = 17;
 constexpr int kWarpAux0 = 18;     // warps 18, 19: extra issuers of paged K/V copies
 constexpr int kPageIssuers = 3;   // TMA copies issue one at a time per warp: pages go to 3 warps
+constexpr int kUnitSlots = 4;     // published work items in flight (a power of two)
 constexpr int kUnitReaders = 19;  // warps that read a published work item: 16 softmax, MMA, 2 helpers
 
 template <int D>
@@ -277,12 +278,12 @@ enum BarId {
   kBarQEmpty = 9 + 2 * kStages,        // last QK of a work item done: Q buffers may be reloaded
   kBarOFree0 = 10 + 2 * kStages,       // + tile: epilogue read O (count 256)
   kBarSlotGo0 = 12 + 2 * kStages,      // + slot: a prefix fill of the slot may be issued (helpers)
-  kBarUnitFull0 = 12 + 3 * kStages,    // + k: work item i (k = i & 1) published in s_unit[k]
-  kBarUnitEmpty0 = 14 + 3 * kStages,   // + k: every consumer warp has read s_unit[k]
-  kBarSplitStored0 = 16 + 3 * kStages,  // + tile: split epilogue, every thread stored its partial (count 256)
-  kBarSplitDecided0 = 18 + 3 * kStages, // + tile: split epilogue, the ticket was taken (count 1)
-  kBarTile1Start = 20 + 3 * kStages,    // every warp of tile 1 has started work item i (count 8)
-  kNumBars = 21 + 3 * kStages
+  kBarUnitFull0 = 12 + 3 * kStages,    // + k: work item i (k = i % kUnitSlots) published in s_unit[k]
+  kBarUnitEmpty0 = 16 + 3 * kStages,   // + k: every consumer warp has read s_unit[k]
+  kBarSplitStored0 = 20 + 3 * kStages,  // + tile: split epilogue, every thread stored its partial (count 256)
+  kBarSplitDecided0 = 22 + 3 * kStages, // + tile: split epilogue, the ticket was taken (count 1)
+  kBarTile1Start = 24 + 3 * kStages,    // every warp of tile 1 has started work item i (count 8)
+  kNumBars = 25 + 3 * kStages
 };
 
 __device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
@@ -648,13 +649,22 @@ __device__ __forceinline__ bool softmax_tile_role(const AttnArgs &a, int tile, c
 // `single` makes every item one tile, twice as many items at the same total
 // work.  A host-planned call may also split a unit's key range over several
 // items (WorkItem::j0, T, split, nsplit), merged by the last one to finish.
-__device__ __forceinline__ WorkItem decode_item(const AttnArgs &a, int32_t unit) {
+// What unit_geometry needs of a device-planned unit: three dependent reads of global memory
+// (the planner's pair, the segment's bounds, its cached prefix), done once by the warp that claims
+// the unit and published with it in shared memory.
+struct ItemInputs {
+  int32_t s, m, hsel, c0, n, P;
+};
+__device__ __forceinline__ ItemInputs item_inputs(const AttnArgs &a, int32_t unit) {
   const int32_t pair_idx = unit / a.heads_per_pair, hsel = unit % a.heads_per_pair;
   const int2 pr = a.pairs[pair_idx];
   const int32_t c0 = a.cu[pr.x];
   const int32_t n = a.cu[pr.x + 1] - c0;
   const int32_t P = a.prefix_lens ? a.prefix_lens[pr.x] : a.pos[c0];
-  return unit_geometry(pr.x, pr.y, hsel, c0, n, P, a.lg, a.group, a.single);
+  return ItemInputs{pr.x, pr.y, hsel, c0, n, P};
+}
+__device__ __forceinline__ WorkItem item_geometry(const AttnArgs &a, const ItemInputs &in) {
+  return unit_geometry(in.s, in.m, in.hsel, in.c0, in.n, in.P, a.lg, a.group, a.single);
 }
 
 // Item u of a host-built plan.
@@ -701,7 +711,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
   __shared__ int s_tmem_busy;  // 1: tensor-core work could not be confirmed finished, TMEM is kept
-  __shared__ int32_t s_unit[2];
+  __shared__ int32_t s_unit[kUnitSlots][8];  // published items: id, then its ItemInputs (device planner)
   __shared__ int32_t s_last[2];  // split epilogue: this CTA's split finished its (unit, tile) last
 
   const int warp = threadIdx.x >> 5;
@@ -727,9 +737,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     }
     mbar_init(bar(kBarFinal), 1);
     mbar_init(bar(kBarPVDone), 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kUnitSlots; ++i) {
       mbar_init(bar(kBarUnitFull0 + i), 1);
       mbar_init(bar(kBarUnitEmpty0 + i), kUnitReaders);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(bar(kBarSplitStored0 + i), 2 * kBlockM);
       mbar_init(bar(kBarSplitDecided0 + i), 1);
     }
@@ -757,9 +769,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   } else {
     n_units = *a.num_pairs * a.heads_per_pair;
   }
-  auto decode = [&](int32_t u) -> WorkItem {
+  auto decode = [&](int32_t u, const ItemInputs &in) -> WorkItem {
     if constexpr (kHost) return decode_plan_item(a, hp, u);
-    else return decode_item(a, u);
+    else return item_geometry(a, in);
   };
   SplitCtx sp;
   if constexpr (kHost) {
@@ -791,11 +803,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     ++items;
   };
   // Work item i of this CTA as published by the TMA warp (-1: none left).  Every lane of a reading
-  // warp waits and reads; lane 0 then frees the entry for item i + 2.
-  auto next_unit = [&](uint32_t i, int32_t &u) -> bool {
-    const int k = i & 1;
-    if (!mbar_wait(bar(kBarUnitFull0 + k), (i >> 1) & 1, abort_flag, a.status)) return false;
-    u = *reinterpret_cast<volatile int32_t *>(&s_unit[k]);
+  // warp waits and reads; lane 0 then frees the entry for item i + kUnitSlots.
+  auto next_unit = [&](uint32_t i, int32_t &u, ItemInputs &in) -> bool {
+    const int k = i & (kUnitSlots - 1);
+    if (!mbar_wait(bar(kBarUnitFull0 + k), (i / kUnitSlots) & 1, abort_flag, a.status)) return false;
+    const volatile int32_t *e = s_unit[k];
+    u = e[0];
+    in = ItemInputs{e[1], e[2], e[3], e[4], e[5], e[6]};
     __syncwarp(__activemask());  // the MMA warp reads with lane 0 alone
     if (lane == 0) mbar_arrive(bar(kBarUnitEmpty0 + k));
     return true;
@@ -807,12 +821,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     uint32_t sep = 0;  // split epilogues of this warp's tile so far
     for (uint32_t i = 0;; ++i) {
       int32_t u;
-      if (!next_unit(i, u) || u < 0) break;
+      ItemInputs in;
+      if (!next_unit(i, u, in) || u < 0) break;
       // Tile 1 idles through one-tile items on tile 0's O-done barrier, so it must never fall two of
       // that barrier's phases behind (a warp of tile 1 may be late, merging the partials of a split
       // item): the MMA warp completes an item's O-done only after all of tile 1 has started the item.
       if (tile == 1 && lane == 0) mbar_arrive(smem_u32(&bars[kBarTile1Start]));
-      const WorkItem w = decode(u);
+      const WorkItem w = decode(u, in);
       sp.split = w.split;
       sp.nsplit = w.nsplit;
       sp.g0 = w.g0;
@@ -855,38 +870,74 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     int64_t issued = 0;
     uint32_t q_issued = 0;  // Q loads issued (warp 16)
     bool ok = true;
+    // Work items are claimed and published ahead: when item i starts, items i + 1 and i + 2 are
+    // already out, so the claim (an atomic on the work counter and three dependent reads of the
+    // item's metadata) is off the path from one item's last PV to the next item's first QK even when
+    // items are short.  Publishing item j waits only for every reader to have taken item
+    // j - kUnitSlots, at most item i - 2.
+    static_assert(kUnitSlots >= 4, "items i .. i + 2 published while readers may still hold item i - 1");
+    // lane 0 of warp 16: item i of this CTA (-1 for none) and, device-planned, its inputs
+    auto claim = [&](uint32_t i, ItemInputs &in) -> int32_t {
+      in = ItemInputs{0, 0, 0, 0, 0, 0};
+      if constexpr (kHost) {
+        return static_cast<int32_t>(i) < n_units ? first_item + static_cast<int32_t>(i) : -1;
+      } else {
+        for (;;) {
+          const int32_t c = atomicAdd(a.work_counter, 1);
+          if (c >= n_units) return -1;
+          in = item_inputs(a, c);
+          if (item_geometry(a, in).valid) return c;
+        }
+      }
+    };
+    uint32_t n_published = 0;  // lane 0 of warp 16: items published so far
+    bool end_published = false;  // lane 0 of warp 16: the -1 that ends the list is out
+    auto publish_to = [&](uint32_t upto) -> int {  // lane 0 of warp 16; 0 when a wait gave up
+      for (; !end_published && n_published < upto; ++n_published) {
+        const uint32_t i = n_published;
+        const int k = i & (kUnitSlots - 1);
+        if (i >= kUnitSlots &&
+            !mbar_wait(bar(kBarUnitEmpty0 + k), (i / kUnitSlots - 1) & 1, abort_flag, a.status))
+          return 0;
+        ItemInputs in;
+        const int32_t u = claim(i, in);
+        s_unit[k][0] = u;
+        s_unit[k][1] = in.s;
+        s_unit[k][2] = in.m;
+        s_unit[k][3] = in.hsel;
+        s_unit[k][4] = in.c0;
+        s_unit[k][5] = in.n;
+        s_unit[k][6] = in.P;
+        mbar_arrive(bar(kBarUnitFull0 + k));
+        if (u < 0) end_published = true;
+      }
+      return 1;
+    };
     for (uint32_t i = 0; ok; ++i) {
       int32_t u = -1;
+      ItemInputs in{0, 0, 0, 0, 0, 0};
       if (pw == 0) {
-        // claim the next work item with at least one valid row and publish it
         int okq = 1;
         if (lane == 0) {
-          if constexpr (kHost) {
-            u = static_cast<int32_t>(i) < n_units ? first_item + static_cast<int32_t>(i) : -1;
-          } else {
-            for (;;) {
-              const int32_t c = atomicAdd(a.work_counter, 1);
-              if (c >= n_units) break;
-              if (decode_item(a, c).valid) {
-                u = c;
-                break;
-              }
-            }
-          }
-          const int k = i & 1;
-          if (i >= 2) okq = mbar_wait(bar(kBarUnitEmpty0 + k), ((i >> 1) - 1) & 1, abort_flag, a.status);
-          if (okq) {
-            s_unit[k] = u;
-            mbar_arrive(bar(kBarUnitFull0 + k));
-          }
+          okq = publish_to(i + 3);
+          // item i as this lane published it (its own earlier shared-memory stores)
+          const int k = i & (kUnitSlots - 1);
+          u = s_unit[k][0];
+          in = ItemInputs{s_unit[k][1], s_unit[k][2], s_unit[k][3], s_unit[k][4], s_unit[k][5], s_unit[k][6]};
         }
         if (!__shfl_sync(0xffffffffu, okq, 0)) break;
         u = __shfl_sync(0xffffffffu, u, 0);
-      } else if (!next_unit(i, u)) {
+        in.s = __shfl_sync(0xffffffffu, in.s, 0);
+        in.m = __shfl_sync(0xffffffffu, in.m, 0);
+        in.hsel = __shfl_sync(0xffffffffu, in.hsel, 0);
+        in.c0 = __shfl_sync(0xffffffffu, in.c0, 0);
+        in.n = __shfl_sync(0xffffffffu, in.n, 0);
+        in.P = __shfl_sync(0xffffffffu, in.P, 0);
+      } else if (!next_unit(i, u, in)) {
         break;
       }
       if (u < 0) break;
-      const WorkItem w = decode(u);
+      const WorkItem w = decode(u, in);
       const int32_t T = w.T, Tp = w.Tp, P = w.P, c0 = w.c0, g = w.g, j0 = w.j0;
       const int32_t Tpl = max(0, min(T, Tp - j0));  // prefix tiles among this item's key tiles
       const bool two = w.two;
@@ -1066,8 +1117,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       bool ok = true;
       for (uint32_t i = 0; ok; ++i) {
         int32_t u;
-        if (!next_unit(i, u) || u < 0) break;
-        const WorkItem w = decode(u);
+        ItemInputs in;
+        if (!next_unit(i, u, in) || u < 0) break;
+        const WorkItem w = decode(u, in);
         const int32_t T = w.T;
         ok = mbar_wait(bar(kBarQFull), items & 1, abort_flag, a.status) && full(lbase);
         if (!ok) break;
