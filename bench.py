@@ -377,26 +377,46 @@ def tiny_oracle_timing(cores: int, reps: int = 5):
     return out
 
 
+def select_copy_split(sel_ms, split, n_kept: int, d_model: int, hbm: float):
+    """The select+gather increment's two parts timed apart: the selection with its compaction indices
+    (the fused call with no hidden row copied, as an increment over importance) and the row copy alone
+    (unip_gather_tokens on the indices that call left), with the copy's rate against HBM.  In the fused
+    call the copy starts while the selection ends, so the parts add up to more than select_gather_ms."""
+    if split is None or not d_model:
+        return None
+    idx_ms, copy_ms = split
+    row_bytes = 2.0 * 2 * d_model * n_kept
+    gbs = row_bytes / (copy_ms * 1e-3) / 1e9
+    return {"select_index_ms": idx_ms, "row_copy_ms": copy_ms, "row_copy_bytes": row_bytes,
+            "row_copy_gbs": gbs, "row_copy_frac_hbm": gbs / hbm,
+            "overlap_ms": idx_ms + copy_ms - sel_ms,
+            "how": "graph replays, L2 flushed before each: [importance + fused call without rows] minus "
+                   "[importance]; [unip_gather_tokens] minus [flush]"}
+
+
 def incremental_select_ms(di, bufs, flush, stream, reps: int = 10, trials: int = 5):
     """Device time of importance alone and the incremental time of Top-p + compaction in the step:
     CUDA-graph replays of [L2 flush, importance + selection + compaction (the fused call)] minus
-    [L2 flush, importance], per step.  Returns (importance_ms, select_gather_ms).
+    [L2 flush, importance], per step.  Returns (importance_ms, select_gather_ms, split): split is None
+    when the workload has no hidden rows, else (select_index_ms, row_copy_ms) -- the same increment with
+    no hidden row copied, and the row copy alone (unip_gather_tokens on the compaction indices).
 
     The selection shares a grid with importance's normaliser and the copy is its programmatic
     dependent, so no event can be recorded between them without changing the launch chain.
     """
     import torch
+    from sparsified_long_context_gb300 import binding as B
     from sparsified_long_context_gb300.pipeline import run_importance, run_importance_select_gather
 
     cs = torch.cuda.Stream()  # graphs are captured on a side stream
 
-    def capture(with_select):
+    def capture(with_select, rows=True):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=cs):
             for _ in range(reps):
                 flush()
                 if with_select:
-                    run_importance_select_gather(di, bufs, stream=cs)
+                    run_importance_select_gather(di, bufs, stream=cs, rows=rows)
                 else:
                     run_importance(di, bufs, cs)
         return g
@@ -413,19 +433,27 @@ def incremental_select_ms(di, bufs, flush, stream, reps: int = 10, trials: int =
             ts.append(e0.elapsed_time(e1) / reps)
         return statistics.median(ts)
 
-    def flush_only():
+    def flush_only(copy=False):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=cs):
             for _ in range(reps):
                 flush()
+                if copy:
+                    B.unip_gather_tokens(di.hidden, bufs.gather_idx, bufs.n_kept, bufs.hidden_out, stream=cs)
         return g
 
+    has_rows = di.hidden is not None
     torch.cuda.synchronize()
     g_fl, g_imp, g_all = flush_only(), capture(False), capture(True)
+    g_idx, g_cp = (capture(True, rows=False), flush_only(copy=True)) if has_rows else (None, None)
     torch.cuda.synchronize()
     t_fl, t_imp, t_all = replay_ms(g_fl), replay_ms(g_imp), replay_ms(g_all)
-    del g_fl, g_imp, g_all
-    return max(t_imp - t_fl, 1e-6), max(t_all - t_imp, 1e-6)
+    split = None
+    if has_rows:
+        # g_all left this input's compaction indices in bufs, so the copy graph moves exactly the kept rows
+        split = (max(replay_ms(g_idx) - t_imp, 1e-6), max(replay_ms(g_cp) - t_fl, 1e-6))
+    del g_fl, g_imp, g_all, g_idx, g_cp
+    return max(t_imp - t_fl, 1e-6), max(t_all - t_imp, 1e-6), split
 
 
 def _timed_steps(step, flush, stream, seconds: float, max_steps: int, gpu_index: int):
@@ -535,12 +563,13 @@ def part_step_workload(name: str, rank: int, gpu_index: int, flush, stream, peak
     attn_ms = stt.median(e[0].elapsed_time(e[1]) for e in evs)
     isg_ms = stt.median(e[1].elapsed_time(e[2]) for e in evs)
     step_ms = stt.median(e[0].elapsed_time(e[2]) for e in evs)
-    imp_ms, sel_ms = incremental_select_ms(di, bufs, flush, stream)
+    imp_ms, sel_ms, split = incremental_select_ms(di, bufs, flush, stream)
     n_kept = int(bufs.n_kept.item())
     n_blocks = int(bufs.blk_cu[-1].item())
     d_model = di.hidden.shape[1] if di.hidden is not None else 0
     sg_bytes = select_gather_bytes(wl, n_blocks, n_kept, d_model)
     bf16, hbm = float(peaks["bf16_tflops"]), float(peaks["hbm_gbs"])
+    split = select_copy_split(sel_ms, split, n_kept, d_model, hbm)
     flops = useful_attention_flops(wl)
     tfl = flops / (attn_ms * 1e-3) / 1e12
     gbs = sg_bytes / (sel_ms * 1e-3) / 1e9
@@ -548,8 +577,8 @@ def part_step_workload(name: str, rank: int, gpu_index: int, flush, stream, peak
             "attention_ms": attn_ms, "attention_tflops": tfl, "attention_frac_bf16": tfl / bf16,
             "importance_ms": imp_ms, "importance_select_gather_ms_in_step": isg_ms, "step_ms": step_ms,
             "select_gather_ms": sel_ms, "select_gather_bytes": sg_bytes, "select_gather_gbs": gbs,
-            "select_gather_frac_hbm": gbs / hbm, "n_kept": n_kept, "n_blocks": n_blocks,
-            "workload_context": workload_context(wl, attn_ms, bf16, hbm),
+            "select_gather_frac_hbm": gbs / hbm, "select_gather_split": split, "n_kept": n_kept,
+            "n_blocks": n_blocks, "workload_context": workload_context(wl, attn_ms, bf16, hbm),
             "timing": f"median per step, L2 flushed ({L2_FLUSH_HOW}) before each step; importance and the "
                       "select+gather increment from graph replays", "clocks": clk}
 
@@ -755,7 +784,7 @@ def main():
     sg_bytes = select_gather_bytes(wl, n_blocks, n_kept, d_model)
     attn_ms = statistics.mean(t_attn)
     isg_ms = statistics.mean(t_isg)
-    imp_ms, sel_ms = incremental_select_ms(di, bufs, flush, stream)
+    imp_ms, sel_ms, split = incremental_select_ms(di, bufs, flush, stream)
     attn_tflops = flops_step / (attn_ms * 1e-3) / 1e12
     sg_gbs = sg_bytes / (sel_ms * 1e-3) / 1e9
     peaks, peak_src = load_peaks()
@@ -823,7 +852,9 @@ def main():
                                     "(unip_block_importance)]; importance_ms: [L2 flush, importance] minus "
                                     "[L2 flush]",
             "select_gather_bytes": sg_bytes, "select_gather_gbs": sg_gbs,
-            "select_gather_frac_hbm": sg_gbs / hbm_peak, "n_kept": n_kept, "n_blocks": n_blocks,
+            "select_gather_frac_hbm": sg_gbs / hbm_peak,
+            "select_gather_split": select_copy_split(sel_ms, split, n_kept, d_model, hbm_peak),
+            "n_kept": n_kept, "n_blocks": n_blocks,
             "rope_append": rope,
             "workload_context": workload_context(wl, attn_ms, bf16_peak, hbm_peak),
             "peaks": f"{peak_src}: bf16 {bf16_peak} TFLOP/s, HBM {hbm_peak} GB/s",

@@ -148,13 +148,15 @@ def run_select_gather(di: DeviceInputs, bufs: StepBuffers, p: Optional[float] = 
 
 
 def run_importance_select_gather(di: DeviceInputs, bufs: StepBuffers, p: Optional[float] = None, stream=None,
-                                 flags: int = B.UNIP_KEEP_FIRST | B.UNIP_KEEP_LAST):
+                                 flags: int = B.UNIP_KEEP_FIRST | B.UNIP_KEEP_LAST, rows: bool = True):
     """Importance, Top-p and compaction through the fused entry point (importance's normaliser and the
-    selection share one grid; the row copy follows as a programmatic dependent)."""
+    selection share one grid; the row copy follows as a programmatic dependent).  rows=False: the
+    selection and the compaction indices only, no hidden row copied."""
     wl = di.wl
+    hidden, hidden_out = (di.hidden, bufs.hidden_out) if rows else (None, None)
     B.unip_importance_select_gather(di.q, di.k, bufs.lse, di.cu_seqlens, di.positions, bufs.imp, bufs.blk_cu,
                                     bufs.keep, bufs.gather_idx, bufs.cu_seqlens_kept, bufs.positions_kept,
-                                    bufs.n_kept, di.hidden, bufs.hidden_out, block_size=bufs.block_size,
+                                    bufs.n_kept, hidden, hidden_out, block_size=bufs.block_size,
                                     p=wl.top_p if p is None else p, num_heads_q=wl.num_heads_q,
                                     num_heads_kv=wl.num_heads_kv, head_dim=wl.head_dim, seg_mask=di.seg_mask,
                                     flags=flags, workspace=bufs.ws_fused, stream=stream)
