@@ -371,36 +371,77 @@ __device__ __forceinline__ void warp_copy_row(const uint4 *__restrict__ src, uin
   for (; v < vec_per_row; v += 32) st_stream(dst + v, ld_stream(src + v));
 }
 
+// M_b = sum over kv heads g = 0, 1, ... of row[g], in that order, with the loads of a group of heads
+// issued before its adds (one memory round trip per 8 heads instead of one per head).
+__device__ __forceinline__ float block_mass(const float *__restrict__ row, int32_t Hkv) {
+  constexpr int kG = 8;
+  float m = 0.f;
+  for (int32_t g0 = 0; g0 < Hkv; g0 += kG) {
+    float v[kG];
+#pragma unroll
+    for (int u = 0; u < kG; ++u) v[u] = g0 + u < Hkv ? row[g0 + u] : 0.f;
+#pragma unroll
+    for (int u = 0; u < kG; ++u)
+      if (g0 + u < Hkv) m += v[u];
+  }
+  return m;
+}
+
 // Block masses of one scored segment normalised to importance: imp[b] = M_b / sum_b' M_b', with
 // M_b = sum over kv heads g of partial[b][g].  Run by the first kImpNormThreads threads of a CTA in a
-// fixed order (strided per-thread sums, then a tree), so every caller produces the same fp32 bits.
-// sred: kImpNormThreads floats of shared memory.  Threads past kImpNormThreads take no part but must
-// reach the same __syncthreads.
+// fixed order (strided per-thread sums, then a pairwise tree: element i takes element i + off for
+// off = 128, 64, ..., 1), so every caller produces the same fp32 bits.  The tree's levels from 128
+// down to 32 are summed by warp 0 from registers and the last five by an xor butterfly: both pair
+// exactly the elements the in-place tree pairs.  sred: kImpNormThreads floats of shared memory.
+// Threads past kImpNormThreads take no part but must reach the same __syncthreads.
 constexpr int kImpNormThreads = 256;
 __device__ __forceinline__ void normalise_segment(const float *__restrict__ partial, int32_t b0, int32_t nb,
                                                   int32_t Hkv, float *__restrict__ imp, float *sred) {
+  static_assert(kImpNormThreads == 256, "the register tree below covers 8 warps");
+  constexpr int kHeld = 4;  // masses of a thread's first kHeld blocks stay in registers
   const int tid = threadIdx.x;
   const bool part = tid < kImpNormThreads;
+  float held[kHeld];
   float t = 0.f;
-  if (part)
-    for (int32_t b = tid; b < nb; b += kImpNormThreads) {
-      float m = 0.f;
-      for (int32_t g = 0; g < Hkv; ++g) m += partial[(int64_t)(b0 + b) * Hkv + g];
-      t += m;
+  if (part) {
+#pragma unroll
+    for (int k = 0; k < kHeld; ++k) {
+      const int32_t b = tid + k * kImpNormThreads;
+      held[k] = b < nb ? block_mass(partial + (int64_t)(b0 + b) * Hkv, Hkv) : 0.f;
     }
-  if (part) sred[tid] = t;
-  __syncthreads();
-  for (int off = kImpNormThreads / 2; off >= 1; off >>= 1) {
-    if (tid < off) sred[tid] += sred[tid + off];
-    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < kHeld; ++k)
+      if (tid + k * kImpNormThreads < nb) t += held[k];
+    for (int32_t b = tid + kHeld * kImpNormThreads; b < nb; b += kImpNormThreads)
+      t += block_mass(partial + (int64_t)(b0 + b) * Hkv, Hkv);
+    sred[tid] = t;
   }
+  __syncthreads();
+  if (tid < 32) {
+    float e[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) e[k] = sred[tid + 32 * k];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) e[k] += e[k + 4];  // off = 128
+#pragma unroll
+    for (int k = 0; k < 2; ++k) e[k] += e[k + 2];  // off = 64
+    float v = e[0] + e[1];                          // off = 32
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    __syncwarp();
+    if (tid == 0) sred[0] = v;
+  }
+  __syncthreads();
   const float inv = 1.f / sred[0];
-  if (part)
-    for (int32_t b = tid; b < nb; b += kImpNormThreads) {
-      float m = 0.f;
-      for (int32_t g = 0; g < Hkv; ++g) m += partial[(int64_t)(b0 + b) * Hkv + g];
-      imp[b0 + b] = m * inv;
+  if (part) {
+#pragma unroll
+    for (int k = 0; k < kHeld; ++k) {
+      const int32_t b = tid + k * kImpNormThreads;
+      if (b < nb) imp[b0 + b] = held[k] * inv;
     }
+    for (int32_t b = tid + kHeld * kImpNormThreads; b < nb; b += kImpNormThreads)
+      imp[b0 + b] = block_mass(partial + (int64_t)(b0 + b) * Hkv, Hkv) * inv;
+  }
 }
 
 // Segment holding token t: largest s with cu[s] <= t (cu non-decreasing, t < cu[S]).

@@ -33,6 +33,7 @@ namespace unip {
 namespace {
 
 constexpr int kToppThreads = 512;
+static_assert(kToppThreads <= 512, "block_sum2 holds one slot per warp for at most 16 warps");
 constexpr int kIndexThreads = 256;
 constexpr int kMaxBlocks = UNIP_TOPP_MAX_BLOCKS;
 constexpr int kRankCountMax = 1024;  // segments up to this many blocks rank by counting instead of sorting
@@ -68,28 +69,56 @@ __device__ __forceinline__ float key_score(unsigned long long key) {
   return __uint_as_float(~static_cast<uint32_t>(key >> 32));
 }
 
-// Bitonic sort of NPOW keys, one per thread (threads past NPOW hold padding): strides below 32
-// exchange through warp shuffles, larger ones through shared memory.  Every loop is unrolled, so
-// each stage is a shuffle (or a shared-memory swap) and a compare with constant lane masks.
-template <int NPOW>
-__device__ __forceinline__ void bitonic_sort_regs(unsigned long long &key, unsigned long long *skeys, int tid) {
-#pragma unroll
-  for (int size = 2; size <= NPOW; size <<= 1) {
-#pragma unroll
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      unsigned long long other;
-      if (stride >= 32) {
-        __syncthreads();
-        if (tid < NPOW) skeys[tid] = key;
-        __syncthreads();
-        other = tid < NPOW ? skeys[tid ^ stride] : key;
-      } else {
-        other = __shfl_xor_sync(0xffffffffu, key, stride);
-      }
+// Bitonic sort of npow keys (a power of two, at most the CTA's threads), one per thread (threads
+// past npow hold padding): strides below 32 exchange through warp shuffles, larger ones through
+// shared memory.  The loop over sizes is not unrolled: a selection runs once per call, usually
+// after other work has pushed its code out of L2, and a fully unrolled 45-stage network for 512 keys
+// spent longer fetching its instructions than executing them.
+__device__ __forceinline__ void bitonic_sort_regs(unsigned long long &key, unsigned long long *skeys, int tid,
+                                                  int npow) {
+#pragma unroll 1
+  for (int size = 2; size <= npow; size <<= 1) {
+#pragma unroll 1
+    for (int stride = size >> 1; stride >= 32; stride >>= 1) {
+      __syncthreads();
+      if (tid < npow) skeys[tid] = key;
+      __syncthreads();
+      const unsigned long long other = tid < npow ? skeys[tid ^ stride] : key;
       const bool take_min = ((tid & stride) == 0) == ((tid & size) == 0);
       key = take_min ? (other < key ? other : key) : (other > key ? other : key);
     }
+#pragma unroll
+    for (int stride = 16; stride > 0; stride >>= 1) {
+      if (stride < size) {  // uniform over the CTA
+        const unsigned long long other = __shfl_xor_sync(0xffffffffu, key, stride);
+        const bool take_min = ((tid & stride) == 0) == ((tid & size) == 0);
+        key = take_min ? (other < key ? other : key) : (other > key ? other : key);
+      }
+    }
   }
+}
+
+// Sums of a and b over the CTA (at most 16 warps), returned to every thread.  Integer sums are exact,
+// so their order does not matter.  sh: 32 elements of shared memory, free again on return.
+__device__ __forceinline__ void block_sum2(unsigned long long &a, unsigned long long &b, unsigned long long *sh) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) {
+    a += __shfl_xor_sync(0xffffffffu, a, off);
+    b += __shfl_xor_sync(0xffffffffu, b, off);
+  }
+  if (lane == 0) {
+    sh[wid] = a;
+    sh[16 + wid] = b;
+  }
+  __syncthreads();
+  a = 0;
+  b = 0;
+  for (int w = 0; w < nw; ++w) {
+    a += sh[w];
+    b += sh[16 + w];
+  }
+  __syncthreads();
 }
 
 // Keep flags of one scored segment (nb blocks from imp[b0]) into skeep[0, nb), run by all
@@ -135,9 +164,8 @@ __device__ bool select_segment_blocks(const float *__restrict__ imp, int32_t b0,
     skeys[b] = key;
   }
   if (bad) atomicOr(s_bad, 1u);
-  unsigned long long T, CF;
-  block_excl_scan<unsigned long long>(tsum, sh64, &T);
-  block_excl_scan<unsigned long long>(fsum, sh64, &CF);
+  unsigned long long T = tsum, CF = fsum;
+  block_sum2(T, CF, sh64);  // its barrier also publishes s_bad
   if (*s_bad) {
     if (tid == 0) atomicOr(status, UNIP_DEV_BAD_SCORES);
     return false;
@@ -145,22 +173,10 @@ __device__ bool select_segment_blocks(const float *__restrict__ imp, int32_t b0,
   if (T == 0) {
     for (int b = tid; b < nb; b += kToppThreads) skeep[b] = 1;
   } else if (npow <= kToppThreads) {
-    // Up to 512 blocks: bitonic sort with one key per thread, in registers; strides below 32
-    // exchange through warp shuffles, larger ones through shared memory.
+    // Up to 512 blocks: bitonic sort with one key per thread, in registers.
     const unsigned long long kthr = mass_threshold(p, T);
     unsigned long long key = tid < npow ? skeys[tid] : ~0ull;
-    switch (npow) {  // fully unrolled network for the padded size
-      case 1: break;
-      case 2: bitonic_sort_regs<2>(key, skeys, tid); break;
-      case 4: bitonic_sort_regs<4>(key, skeys, tid); break;
-      case 8: bitonic_sort_regs<8>(key, skeys, tid); break;
-      case 16: bitonic_sort_regs<16>(key, skeys, tid); break;
-      case 32: bitonic_sort_regs<32>(key, skeys, tid); break;
-      case 64: bitonic_sort_regs<64>(key, skeys, tid); break;
-      case 128: bitonic_sort_regs<128>(key, skeys, tid); break;
-      case 256: bitonic_sort_regs<256>(key, skeys, tid); break;
-      default: bitonic_sort_regs<512>(key, skeys, tid); break;
-    }
+    bitonic_sort_regs(key, skeys, tid, npow);
     // thread tid now holds the key of rank tid; forced blocks and padding sort last
     const unsigned long long m = key != ~0ull ? fixed_mass(key_score(key)) : 0ull;
     unsigned long long tot;
