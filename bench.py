@@ -831,7 +831,7 @@ def main():
     cpu = None
     if not args.no_cpu_baseline and world == 1:
         cpu = cpu_baseline(wl, args.cpu_seconds)
-    launches = kernels_per_step(fused_importance=True) * args.steps
+    launches = kernels_per_step(fused_importance=True, num_segs=wl.num_segs) * args.steps
     # the committed ncu record is of the 32768-token long-context launch: it applies to that workload only
     traffic = None
     if args.workload == "long_single" and wl.num_tokens == 32768:

@@ -393,10 +393,12 @@ __device__ __forceinline__ float block_mass(const float *__restrict__ row, int32
 // off = 128, 64, ..., 1), so every caller produces the same fp32 bits.  The tree's levels from 128
 // down to 32 are summed by warp 0 from registers and the last five by an xor butterfly: both pair
 // exactly the elements the in-place tree pairs.  sred: kImpNormThreads floats of shared memory.
-// Threads past kImpNormThreads take no part but must reach the same __syncthreads.
+// The scores go to imp[b0 + b] and, when sdst is given, also to sdst[b] (shared memory); imp may be
+// null.  Threads past kImpNormThreads take no part but must reach the same __syncthreads.
 constexpr int kImpNormThreads = 256;
 __device__ __forceinline__ void normalise_segment(const float *__restrict__ partial, int32_t b0, int32_t nb,
-                                                  int32_t Hkv, float *__restrict__ imp, float *sred) {
+                                                  int32_t Hkv, float *__restrict__ imp, float *sred,
+                                                  float *sdst = nullptr) {
   static_assert(kImpNormThreads == 256, "the register tree below covers 8 warps");
   constexpr int kHeld = 4;  // masses of a thread's first kHeld blocks stay in registers
   const int tid = threadIdx.x;
@@ -437,10 +439,17 @@ __device__ __forceinline__ void normalise_segment(const float *__restrict__ part
 #pragma unroll
     for (int k = 0; k < kHeld; ++k) {
       const int32_t b = tid + k * kImpNormThreads;
-      if (b < nb) imp[b0 + b] = held[k] * inv;
+      if (b < nb) {
+        const float f = held[k] * inv;
+        if (imp) imp[b0 + b] = f;
+        if (sdst) sdst[b] = f;
+      }
     }
-    for (int32_t b = tid + kHeld * kImpNormThreads; b < nb; b += kImpNormThreads)
-      imp[b0 + b] = block_mass(partial + (int64_t)(b0 + b) * Hkv, Hkv) * inv;
+    for (int32_t b = tid + kHeld * kImpNormThreads; b < nb; b += kImpNormThreads) {
+      const float f = block_mass(partial + (int64_t)(b0 + b) * Hkv, Hkv) * inv;
+      if (imp) imp[b0 + b] = f;
+      if (sdst) sdst[b] = f;
+    }
   }
 }
 

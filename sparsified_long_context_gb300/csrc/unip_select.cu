@@ -650,52 +650,43 @@ __global__ void __launch_bounds__(kIndexThreads) select_gather_kernel(
   }
 }
 
-// One segment in the call (a single long prompt): every CTA selects the segment's blocks itself
-// (a few microseconds of shared-memory work on at most UNIP_TOPP_MAX_BLOCKS scores), stages the
-// kept offsets and copies its share of the kept rows, so no grid waits for another; CTA 0 writes
-// the keep mask, cu_seqlens_kept and n_kept.  Same results as topp_kernel + select_gather_kernel.
-__global__ void __launch_bounds__(kToppThreads) select_gather_onepass_kernel(
-    const float *__restrict__ imp, const int32_t *__restrict__ blk_cu, const int32_t *__restrict__ cu,
-    const int32_t *__restrict__ pos, int32_t B, double p, uint32_t flags, int32_t cap, uint8_t *__restrict__ keep,
-    const uint4 *__restrict__ hidden, int32_t num_rows, int64_t stride16, int32_t vec_per_row,
-    uint4 *__restrict__ out, int64_t out_stride16, int32_t *__restrict__ cu_kept, int32_t *__restrict__ n_kept,
-    int32_t *__restrict__ gather_idx, int32_t *__restrict__ pos_kept, uint32_t *__restrict__ status) {
-  extern __shared__ unsigned long long skeys[];  // cap rank keys, cap kept offsets (int32), cap flags
-  int32_t *skoff = reinterpret_cast<int32_t *>(skeys + cap);
-  uint8_t *skeep = reinterpret_cast<uint8_t *>(skoff + cap);
-  __shared__ unsigned long long sh64[32];
-  __shared__ int32_t sh32[32];
-  __shared__ uint32_t s_bad;
-  const int tid = threadIdx.x, lane = tid & 31;
-  // the importance results are visible past here (this grid is a programmatic dependent of them)
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int32_t c0 = cu[0], n = cu[1] - cu[0];
-  const int32_t b0 = blk_cu[0], nb = blk_cu[1] - blk_cu[0];
-  int32_t total = 0;
-  if (nb == 0) {  // not scored: every token is kept
-    total = n > 0 ? n : 0;
-  } else if (nb > kMaxBlocks || nb > cap || n <= 0 || nb != (n + B - 1) / B) {
-    if (blockIdx.x == 0 && tid == 0)
-      atomicOr(status, nb > kMaxBlocks ? UNIP_DEV_TOO_MANY_BLOCKS : UNIP_DEV_BAD_BLOCKS);
-  } else if (select_segment_blocks(imp, b0, nb, p, flags, skeys, skeep, sh64, &s_bad, status)) {
-    // kept-token offsets in block order (exclusive), kept in shared memory
-    const int ipb = (nb + kToppThreads - 1) / kToppThreads;
-    const int bb0 = tid * ipb;
-    int32_t lsum = 0;
-    for (int e = 0; e < ipb; ++e) {
-      const int b = bb0 + e;
-      if (b < nb && skeep[b]) lsum += min(B, n - b * B);
-    }
-    int32_t run = block_excl_scan<int32_t>(lsum, sh32, &total);
-    for (int e = 0; e < ipb; ++e) {
-      const int b = bb0 + e;
-      if (b < nb) {
-        skoff[b] = run;
-        if (blockIdx.x == 0) keep[b0 + b] = skeep[b];
-        if (skeep[b]) run += min(B, n - b * B);
-      }
+// Kept-token offsets of a one-segment call's blocks (exclusive, in block order) into skoff from the
+// keep flags the CTA selected itself; CTA 0 also writes the keep mask.  Returns the kept-token count.
+__device__ __forceinline__ int32_t onepass_offsets(int32_t n, int32_t b0, int32_t nb, int32_t B, const uint8_t *skeep,
+                                                   int32_t *skoff, uint8_t *__restrict__ keep, int32_t *sh32) {
+  const int tid = threadIdx.x;
+  const int ipb = (nb + kToppThreads - 1) / kToppThreads;
+  const int bb0 = tid * ipb;
+  int32_t lsum = 0;
+  for (int e = 0; e < ipb; ++e) {
+    const int b = bb0 + e;
+    if (b < nb && skeep[b]) lsum += min(B, n - b * B);
+  }
+  int32_t total;
+  int32_t run = block_excl_scan<int32_t>(lsum, sh32, &total);
+  for (int e = 0; e < ipb; ++e) {
+    const int b = bb0 + e;
+    if (b < nb) {
+      skoff[b] = run;
+      if (blockIdx.x == 0) keep[b0 + b] = skeep[b];
+      if (skeep[b]) run += min(B, n - b * B);
     }
   }
+  return total;
+}
+
+// The rest of a one-segment call once every CTA knows the kept blocks (skeep, skoff) and their token
+// count: CTA 0 writes cu_seqlens_kept and n_kept, and each warp of the grid takes kept rows r in turn,
+// writing gather_idx / positions_kept and copying the hidden row.  Consecutive rows go to consecutive
+// CTAs, so a short list of rows still spreads over every SM.  nb == 0: every token is kept.
+__device__ __forceinline__ void onepass_copy(int32_t total, int32_t c0, int32_t nb, int32_t B, const uint8_t *skeep,
+                                             const int32_t *skoff, const int32_t *__restrict__ pos,
+                                             const uint4 *__restrict__ hidden, int32_t num_rows, int64_t stride16,
+                                             int32_t vec_per_row, uint4 *__restrict__ out, int64_t out_stride16,
+                                             int32_t *__restrict__ cu_kept, int32_t *__restrict__ n_kept,
+                                             int32_t *__restrict__ gather_idx, int32_t *__restrict__ pos_kept,
+                                             uint32_t *__restrict__ status) {
+  const int tid = threadIdx.x, lane = tid & 31;
   if (blockIdx.x == 0 && tid == 0) {
     cu_kept[0] = 0;
     cu_kept[1] = total;
@@ -703,7 +694,7 @@ __global__ void __launch_bounds__(kToppThreads) select_gather_onepass_kernel(
   }
   __syncthreads();
   const int warps_per_block = kToppThreads / 32;
-  for (int32_t r = blockIdx.x * warps_per_block + (tid >> 5); r < total; r += gridDim.x * warps_per_block) {
+  for (int32_t r = (tid >> 5) * gridDim.x + blockIdx.x; r < total; r += gridDim.x * warps_per_block) {
     int32_t src;
     if (nb == 0) {
       src = c0 + r;
@@ -727,6 +718,80 @@ __global__ void __launch_bounds__(kToppThreads) select_gather_onepass_kernel(
     }
     warp_copy_row(hidden + (int64_t)src * stride16, out + (int64_t)r * out_stride16, vec_per_row, lane);
   }
+}
+
+// One segment in the call (a single long prompt): every CTA selects the segment's blocks itself
+// (a few microseconds of shared-memory work on at most UNIP_TOPP_MAX_BLOCKS scores), stages the
+// kept offsets and copies its share of the kept rows, so no grid waits for another; CTA 0 writes
+// the keep mask, cu_seqlens_kept and n_kept.  Same results as topp_kernel + select_gather_kernel.
+__global__ void __launch_bounds__(kToppThreads) select_gather_onepass_kernel(
+    const float *__restrict__ imp, const int32_t *__restrict__ blk_cu, const int32_t *__restrict__ cu,
+    const int32_t *__restrict__ pos, int32_t B, double p, uint32_t flags, int32_t cap, uint8_t *__restrict__ keep,
+    const uint4 *__restrict__ hidden, int32_t num_rows, int64_t stride16, int32_t vec_per_row,
+    uint4 *__restrict__ out, int64_t out_stride16, int32_t *__restrict__ cu_kept, int32_t *__restrict__ n_kept,
+    int32_t *__restrict__ gather_idx, int32_t *__restrict__ pos_kept, uint32_t *__restrict__ status) {
+  extern __shared__ unsigned long long skeys[];  // cap rank keys, cap kept offsets (int32), cap flags
+  int32_t *skoff = reinterpret_cast<int32_t *>(skeys + cap);
+  uint8_t *skeep = reinterpret_cast<uint8_t *>(skoff + cap);
+  __shared__ unsigned long long sh64[32];
+  __shared__ int32_t sh32[32];
+  __shared__ uint32_t s_bad;
+  // the importance results are visible past here (this grid is a programmatic dependent of them)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int32_t c0 = cu[0], n = cu[1] - cu[0];
+  const int32_t b0 = blk_cu[0], nb = blk_cu[1] - blk_cu[0];
+  int32_t total = 0;
+  if (nb == 0) {  // not scored: every token is kept
+    total = n > 0 ? n : 0;
+  } else if (nb > kMaxBlocks || nb > cap || n <= 0 || nb != (n + B - 1) / B) {
+    if (blockIdx.x == 0 && threadIdx.x == 0)
+      atomicOr(status, nb > kMaxBlocks ? UNIP_DEV_TOO_MANY_BLOCKS : UNIP_DEV_BAD_BLOCKS);
+  } else if (select_segment_blocks(imp, b0, nb, p, flags, skeys, skeep, sh64, &s_bad, status)) {
+    total = onepass_offsets(n, b0, nb, B, skeep, skoff, keep, sh32);
+  }
+  onepass_copy(total, c0, nb, B, skeep, skoff, pos, hidden, num_rows, stride16, vec_per_row, out, out_stride16,
+               cu_kept, n_kept, gather_idx, pos_kept, status);
+}
+
+// The fused importance call with one segment: every CTA normalises the segment's block masses itself
+// (the normaliser of unip_block_importance, so the scores have the same bits; CTA 0 writes them out),
+// selects from its own copy of the scores in shared memory and copies its share of the kept rows, as
+// select_gather_onepass_kernel does.  One grid after the score grid, none waiting for another.
+__global__ void __launch_bounds__(kToppThreads) norm_select_gather_onepass_kernel(
+    const int32_t *__restrict__ blk_cu, const int32_t *__restrict__ cu, const float *__restrict__ partial,
+    int32_t Hkv, const int32_t *__restrict__ pos, int32_t B, double p, uint32_t flags, int32_t cap,
+    float *__restrict__ imp, uint8_t *__restrict__ keep, const uint4 *__restrict__ hidden, int32_t num_rows,
+    int64_t stride16, int32_t vec_per_row, uint4 *__restrict__ out, int64_t out_stride16,
+    int32_t *__restrict__ cu_kept, int32_t *__restrict__ n_kept, int32_t *__restrict__ gather_idx,
+    int32_t *__restrict__ pos_kept, uint32_t *__restrict__ status) {
+  // cap rank keys, cap int32 that hold the scores during the selection and the kept offsets after
+  // it (the selection reads each score once, before it writes anything else), cap flags
+  extern __shared__ unsigned long long skeys[];
+  int32_t *skoff = reinterpret_cast<int32_t *>(skeys + cap);
+  float *sscore = reinterpret_cast<float *>(skoff);
+  uint8_t *skeep = reinterpret_cast<uint8_t *>(skoff + cap);
+  __shared__ unsigned long long sh64[32];
+  __shared__ int32_t sh32[32];
+  __shared__ uint32_t s_bad;
+  __shared__ float sred[kImpNormThreads];
+  // the score grid's masses are complete past here
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int32_t c0 = cu[0], n = cu[1] - cu[0];
+  const int32_t b0 = blk_cu[0], nb = blk_cu[1] - blk_cu[0];
+  int32_t total = 0;
+  if (nb == 0) {  // not scored: every token is kept
+    total = n > 0 ? n : 0;
+  } else if (nb > kMaxBlocks || nb > cap || n <= 0 || nb != (n + B - 1) / B) {
+    if (blockIdx.x == 0 && threadIdx.x == 0)
+      atomicOr(status, nb > kMaxBlocks ? UNIP_DEV_TOO_MANY_BLOCKS : UNIP_DEV_BAD_BLOCKS);
+  } else {
+    normalise_segment(partial, b0, nb, Hkv, blockIdx.x == 0 ? imp : nullptr, sred, sscore);
+    __syncthreads();  // the scores in shared memory are complete
+    if (select_segment_blocks(sscore, 0, nb, p, flags, skeys, skeep, sh64, &s_bad, status))
+      total = onepass_offsets(n, b0, nb, B, skeep, skoff, keep, sh32);
+  }
+  onepass_copy(total, c0, nb, B, skeep, skoff, pos, hidden, num_rows, stride16, vec_per_row, out, out_stride16,
+               cu_kept, n_kept, gather_idx, pos_kept, status);
 }
 
 // Top-p launch: shared memory for the padded sort of the largest segment the call can hold
@@ -894,7 +959,9 @@ UNIP_API int32_t unip_select_gather(const float *imp, const int32_t *blk_cu, con
       return UNIP_ERR_CUDA;
     return UNIP_OK;
   }
-  if (num_segs == 1) {  // one segment: selection and gather in one grid
+  // One segment: selection and gather in one grid.  One CTA per SM, since every CTA runs the same
+  // selection and two CTAs on an SM would share its issue slots.
+  if (num_segs == 1) {
     if (ensure_dynamic_smem((const void *)select_gather_onepass_kernel,
                             kMaxBlocks * ((int)sizeof(unsigned long long) + 5)) != cudaSuccess)
       return UNIP_ERR_CUDA;
@@ -904,7 +971,7 @@ UNIP_API int32_t unip_select_gather(const float *imp, const int32_t *blk_cu, con
     const int sms1 = device_sm_count();
     const int warps = kToppThreads / 32;
     int64_t blocks1 = ((int64_t)(total_tokens > 0 ? total_tokens : 1) + warps - 1) / warps;
-    const int64_t max_blocks1 = (int64_t)(sms1 > 0 ? sms1 : 1) * kGatherCtasPerSm;
+    const int64_t max_blocks1 = sms1 > 0 ? sms1 : 1;
     if (blocks1 > max_blocks1) blocks1 = max_blocks1;
     cudaLaunchConfig_t cfg1 = {};
     cfg1.gridDim = dim3((unsigned)blocks1);
@@ -990,12 +1057,42 @@ UNIP_API int32_t unip_importance_select_gather(
                               d_model, hidden_out, out_row_stride, ws_sel, ws_sel_bytes, stream);
   uint32_t *status = device_status_ptr();
   if (!status) return UNIP_ERR_CUDA;
-  if (ensure_dynamic_smem((const void *)norm_select_kernel, kMaxBlocks * ((int)sizeof(unsigned long long) + 1)) !=
-      cudaSuccess)
-    return UNIP_ERR_CUDA;
   int32_t cap = 16;
   const int64_t cap_need = (int64_t)total_tokens / block_size + 2;
   while (cap < cap_need && cap < kMaxBlocks) cap <<= 1;
+  if (num_segs == 1) {  // one segment: normalisation, selection and row copy in one grid
+    if (ensure_dynamic_smem((const void *)norm_select_gather_onepass_kernel,
+                            kMaxBlocks * ((int)sizeof(unsigned long long) + 5)) != cudaSuccess)
+      return UNIP_ERR_CUDA;
+    // One CTA per SM: every CTA runs the same selection, and two on an SM share its issue slots
+    // (the 45-stage network of 512 blocks took ~6 us instead of ~4.3 us); 16 copying warps per SM
+    // still keep 128 KB of row loads in flight there.
+    const int sms1 = device_sm_count();
+    const int warps = kToppThreads / 32;
+    int64_t blocks1 = ((int64_t)(total_tokens > 0 ? total_tokens : 1) + warps - 1) / warps;
+    const int64_t max_blocks1 = sms1 > 0 ? sms1 : 1;
+    if (blocks1 > max_blocks1) blocks1 = max_blocks1;
+    cudaLaunchConfig_t cfg1 = {};
+    cfg1.gridDim = dim3((unsigned)blocks1);
+    cfg1.blockDim = dim3(kToppThreads);
+    cfg1.dynamicSmemBytes = (size_t)cap * (sizeof(unsigned long long) + 5);
+    cfg1.stream = st;
+    cudaLaunchAttribute attr1[1];
+    attr1[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // may start while the score grid drains
+    attr1[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg1.attrs = attr1;
+    cfg1.numAttrs = 1;
+    const cudaError_t e1 = cudaLaunchKernelEx(
+        &cfg1, norm_select_gather_onepass_kernel, (const int32_t *)blk_cu, cu_seqlens, (const float *)partial,
+        prm->num_heads_kv, positions, block_size, p, flags, cap, imp, keep, static_cast<const uint4 *>(hidden),
+        total_tokens, rows ? (int64_t)(row_stride / 8) : 0, (int32_t)(d_model / 8),
+        static_cast<uint4 *>(hidden_out), rows ? (int64_t)(out_row_stride / 8) : 0, cu_seqlens_kept, n_kept,
+        gather_idx, positions_kept, status);
+    return e1 == cudaSuccess ? UNIP_OK : UNIP_ERR_CUDA;
+  }
+  if (ensure_dynamic_smem((const void *)norm_select_kernel, kMaxBlocks * ((int)sizeof(unsigned long long) + 1)) !=
+      cudaSuccess)
+    return UNIP_ERR_CUDA;
   int32_t *seg_kept = reinterpret_cast<int32_t *>(static_cast<uint8_t *>(ws_sel) + kWsHeaderBytes);
   int32_t *kept_off = reinterpret_cast<int32_t *>(static_cast<uint8_t *>(ws_sel) + kWsHeaderBytes +
                                                   align_up(sizeof(int32_t) * num_segs, 256));

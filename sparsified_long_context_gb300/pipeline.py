@@ -180,9 +180,10 @@ def kernels_per_step(has_hidden: bool = True, fused_select: bool = False, num_se
     # attention: plan + attention; importance: plan + score + norm;
     # Top-p: select + index, gather: 1  -- or the fused select + gather: 2,
     # one launch when the stream holds a single segment -- or importance, selection and
-    # compaction in one call: plan + score + normalise-and-select + row copy
+    # compaction in one call: plan + score + normalise-and-select + row copy, the last two one
+    # grid when the stream holds a single segment
     if fused_importance:
-        return 2 + 4
+        return 2 + (3 if num_segs == 1 else 4)
     if fused_select:
         return 2 + 3 + (1 if num_segs == 1 else 2)
     return 2 + 3 + 2 + (1 if has_hidden else 0)

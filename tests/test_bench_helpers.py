@@ -82,6 +82,7 @@ def test_launches_per_step():
     assert kernels_per_step(True, fused_select=False) == 8
     assert kernels_per_step(False, fused_select=False) == 7
     assert kernels_per_step(fused_importance=True) == 6
+    assert kernels_per_step(fused_importance=True, num_segs=1) == 5
 
 
 def test_committed_traffic_records_follow_their_sources():

@@ -29,12 +29,12 @@ def _step(wl):
     return di, bufs
 
 
-def _check_selection(wl, bufs):
+def _check_selection(wl, bufs, flags=oracle.KEEP_FIRST | oracle.KEEP_LAST):
     blk_cu = bufs.blk_cu.cpu().numpy()
     nblk = int(blk_cu[-1])
     imp = bufs.imp[:nblk].cpu().numpy()
     keep = bufs.keep[:nblk].cpu().numpy()
-    ref_keep = oracle.topp_select(imp, blk_cu, wl.top_p)
+    ref_keep = oracle.topp_select(imp, blk_cu, wl.top_p, flags)
     assert np.array_equal(keep, ref_keep)
     gi, ck, pk, m = oracle.index_build(ref_keep, blk_cu, wl.cu_seqlens, wl.positions, wl.block_size)
     n_kept = int(bufs.n_kept.cpu().item())
@@ -406,7 +406,7 @@ def test_select_gather_many_segments(S):
     assert np.array_equal(got, oracle.gather(hid, rgi))
 
 
-def _fused_vs_separate(wl):
+def _fused_vs_separate(wl, flags=oracle.KEEP_FIRST | oracle.KEEP_LAST):
     from sparsified_long_context_gb300 import binding as Bd
     from sparsified_long_context_gb300.pipeline import (DeviceInputs, StepBuffers, run_attention, run_importance,
                                                         run_importance_select_gather, run_select_gather)
@@ -415,7 +415,7 @@ def _fused_vs_separate(wl):
     bufs = StepBuffers(di)
     run_attention(di, bufs)
     run_importance(di, bufs)
-    run_select_gather(di, bufs)
+    run_select_gather(di, bufs, flags=flags)
     torch.cuda.synchronize()
     assert Bd.unip_get_device_status(clear=True) == 0
     names = ["imp", "blk_cu", "keep", "gather_idx", "cu_seqlens_kept", "positions_kept", "n_kept"]
@@ -425,7 +425,7 @@ def _fused_vs_separate(wl):
     for n in names:   # poison every output, so the fused call must write each one
         t = getattr(bufs, n)
         t.view(torch.uint8).fill_(0xA5)
-    run_importance_select_gather(di, bufs)
+    run_importance_select_gather(di, bufs, flags=flags)
     torch.cuda.synchronize()
     st = Bd.unip_get_device_status(clear=True)
     assert st == 0, Bd.describe_status(st)
@@ -448,6 +448,22 @@ def test_fused_importance_select_gather_matches_the_separate_calls(name):
     wl = W.prepacked(library_ffd) if name == "prepacked" else W.workload_by_name(name)
     bufs = _fused_vs_separate(wl)
     _check_selection(wl, bufs)
+
+
+@pytest.mark.parametrize("L,B_,p,d_model,flags", [
+    (1500, 64, 0.9, 256, 3),     # 24 blocks
+    (5000, 16, 0.8, 0, 0),       # 313 blocks, register network; selection and indices only
+    (8192 - 37, 16, 0.95, 128, 1),  # 510 blocks
+    (12000, 16, 0.95, 128, 2),   # 750 blocks: ranks by counting
+    (40000 + 5, 16, 0.9, 64, 3),  # 2501 blocks: shared-memory network, ragged last block
+])
+def test_fused_single_segment_matches_the_separate_calls(L, B_, p, d_model, flags):
+    """One segment in the fused call: every CTA of one grid normalises the block masses, selects and
+    copies its share of the rows.  Scores, keep mask, indices and rows must have the bits of the separate
+    calls and match the oracle's selection on those scores, for every flag combination."""
+    wl = W.packed([L], 4, 2, 64, seed=90 + L % 97, block_size=B_, top_p=p, d_model=d_model)
+    bufs = _fused_vs_separate(wl, flags)
+    _check_selection(wl, bufs, flags)
 
 
 def test_fused_path_with_unscored_and_empty_segments():
