@@ -451,6 +451,9 @@ def test_fused_importance_select_gather_matches_the_separate_calls(name):
 
 
 @pytest.mark.parametrize("L,B_,p,d_model,flags", [
+    (1, 16, 0.9, 64, 3),         # one token, one block
+    (63, 64, 0.5, 64, 0),        # one partial block, no forced blocks
+    (65, 64, 0.99, 64, 1),       # a full block and a one-token block
     (1500, 64, 0.9, 256, 3),     # 24 blocks
     (5000, 16, 0.8, 0, 0),       # 313 blocks, register network; selection and indices only
     (8192 - 37, 16, 0.95, 128, 1),  # 510 blocks
