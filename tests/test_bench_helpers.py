@@ -95,3 +95,15 @@ def test_committed_traffic_records_follow_their_sources():
         src = os.path.join(root, rec["kernel_source"])
         sha = hashlib.sha1(open(src, "rb").read()).hexdigest()
         assert (bench.recorded_traffic(name) is not None) == (sha == rec["kernel_source_sha1"])
+
+
+def test_select_copy_split_reports_the_copy_rate_of_the_kept_rows():
+    # 2176 kept rows of 4096 bf16: 17.8 MB read and as much written
+    sp = bench.select_copy_split(0.012, (0.006, 0.0055), 2176, 4096, 6744.6)
+    assert sp["row_copy_bytes"] == 2 * 2 * 4096 * 2176
+    assert abs(sp["row_copy_gbs"] - sp["row_copy_bytes"] / 0.0055e-3 / 1e9) < 1e-6
+    assert abs(sp["row_copy_frac_hbm"] - sp["row_copy_gbs"] / 6744.6) < 1e-12
+    assert abs(sp["overlap_ms"] - (0.006 + 0.0055 - 0.012)) < 1e-12
+    # no hidden rows in the workload: nothing to split
+    assert bench.select_copy_split(0.03, None, 100, 0, 6744.6) is None
+    assert bench.select_copy_split(0.03, (0.01, 0.01), 100, 0, 6744.6) is None
