@@ -25,6 +25,10 @@ UNIP_KEEP_LAST = 0x2
 UNIP_TOPP_MAX_BLOCKS = 8192
 UNIP_ATTN_SCHEDULE_AUTO, UNIP_ATTN_SCHEDULE_PAIRED, UNIP_ATTN_SCHEDULE_SINGLE = 0, 1, 2
 
+# device status bits (include/unip.h)
+UNIP_DEV_BAD_SEQLENS, UNIP_DEV_BAD_POSITIONS, UNIP_DEV_BAD_PAGES, UNIP_DEV_TIMEOUT = 0x1, 0x2, 0x4, 0x8
+UNIP_DEV_BAD_SCORES, UNIP_DEV_TOO_MANY_BLOCKS, UNIP_DEV_BAD_INDEX, UNIP_DEV_BAD_BLOCKS = 0x10, 0x20, 0x40, 0x80
+
 DEV_STATUS_BITS = {
     0x1: "bad cu_seqlens", 0x2: "bad positions", 0x4: "bad pages", 0x8: "device wait timeout",
     0x10: "bad importance scores", 0x20: "too many blocks in a segment", 0x40: "bad gather index",

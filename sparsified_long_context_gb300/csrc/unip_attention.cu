@@ -140,18 +140,29 @@ __global__ void __launch_bounds__(kPlanThreads) attn_plan_kernel(const int32_t *
     my_pairs += (n + kBlockM - 1) / kBlockM;
   }
   // Positions contiguous inside each segment: pos[t] - pos[t-1] == 1 unless t starts a segment.
-  // Independent loads, four tokens per thread in flight.
+  // Each thread issues the loads of kPosBatch tokens before it compares any: after an L2 flush the
+  // positions come from HBM, and four tokens in flight left a 32k-token call with ~16 dependent
+  // rounds of HBM latency in its planner.
   {
-    int32_t s_cur = 0;
-#pragma unroll 4
-    for (int t = tid; t < N; t += kPlanThreads) {
-      if (t == 0) continue;
-      const int32_t prev = pos[t - 1], cur = pos[t];
-      // contiguous positions, or (compacted stream) increasing ones
-      if (prefix_lens ? cur <= prev : cur != prev + 1) {
-        // allowed only at a segment start (some s with cu[s] == t)
-        s_cur = find_segment(cu, S, t);
-        if (cu[s_cur] != t) err |= UNIP_DEV_BAD_POSITIONS;
+    constexpr int kPosBatch = 16;
+    for (int t0 = tid; t0 < N; t0 += kPlanThreads * kPosBatch) {
+      int32_t prv[kPosBatch], cur[kPosBatch];
+#pragma unroll
+      for (int u = 0; u < kPosBatch; ++u) {
+        const int t = t0 + u * kPlanThreads;
+        const bool in = t > 0 && t < N;
+        cur[u] = in ? pos[t] : 0;
+        prv[u] = in ? pos[t - 1] : 0;
+      }
+#pragma unroll
+      for (int u = 0; u < kPosBatch; ++u) {
+        const int t = t0 + u * kPlanThreads;
+        // contiguous positions, or (compacted stream) increasing ones
+        if (t > 0 && t < N && (prefix_lens ? cur[u] <= prv[u] : cur[u] != prv[u] + 1)) {
+          // allowed only at a segment start (some s with cu[s] == t)
+          const int32_t s_cur = find_segment(cu, S, t);
+          if (cu[s_cur] != t) err |= UNIP_DEV_BAD_POSITIONS;
+        }
       }
     }
   }

@@ -89,3 +89,12 @@ def test_bounded_wait_selftest_checks_its_arguments():
     assert lib.unip_selftest_bounded_wait(0, ctypes.c_void_p(16), None) == -1         # limit 0
     assert lib.unip_selftest_bounded_wait(2000000, ctypes.c_void_p(16), None) == -1   # above one second
     assert lib.unip_selftest_bounded_wait(1000, None, None) == -1                      # no result buffer
+
+
+def test_binding_status_bits_match_the_header():
+    text = open(os.path.join(INCLUDE, "unip.h")).read()
+    bits = {name: int(val, 16) for name, val in re.findall(r"#define (UNIP_DEV_\w+) (0x[0-9a-fA-F]+)u", text)}
+    assert len(bits) == 8
+    for name, val in bits.items():
+        assert getattr(binding, name) == val, name
+        assert val in binding.DEV_STATUS_BITS, name
