@@ -12,15 +12,22 @@
 // top-ranked blocks.
 //
 // Kernels
-//   topp_kernel   one CTA per segment: bitonic sort of 64-bit rank keys in
-//                 shared memory (each key also carries its block's score, so
-//                 the ranked masses need no second read), exclusive scan of
-//                 the ranked integer masses, keep decision per block,
-//                 exclusive scan of kept lengths; writes the segment's count.
-//   select_gather_onepass_kernel  one segment in the call: every CTA selects
-//                 the segment's blocks itself, stages the kept offsets and
-//                 copies its share of the kept rows (one launch, no grid
-//                 waits for another).
+//   topp_kernel   one CTA per segment: bitonic sort of 64-bit rank keys
+//                 (each key also carries its block's score, so the ranked
+//                 masses need no second read), exclusive scan of the ranked
+//                 integer masses, keep decision per block, exclusive scan of
+//                 kept lengths; writes the segment's count.  Segments of at
+//                 most 32 blocks are selected by one warp.
+//   norm_select_kernel  the same per segment after importance's normaliser,
+//                 in the CTA that normalised the scores.
+//   select_gather_kernel  the row copy after either of them (a programmatic
+//                 dependent): kept offsets staged in shared memory, one warp
+//                 per kept row.
+//   select_gather_onepass_kernel, norm_select_gather_onepass_kernel  one
+//                 segment in the call: every CTA (one per SM) selects the
+//                 segment's blocks itself (the second also normalises the
+//                 masses first), stages the kept offsets and copies its share
+//                 of the kept rows (one launch, no grid waits for another).
 //   index_kernel  one thread per source token: every CTA scans the
 //                 per-segment counts into shared memory (CTA 0 also writes
 //                 cu_seqlens_kept and n_kept), then writes gather_idx and
