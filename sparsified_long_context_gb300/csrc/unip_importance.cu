@@ -100,10 +100,15 @@ struct ScoreArgs {
   float scale_log2;
 };
 
-constexpr int kScoreWarpTma = 8;
-constexpr int kScoreWarpMma = 9;
-constexpr int kScoreThreadsTc = 320;  // 8 score warps (two per TMEM lane quarter), TMA warp, MMA warp
-constexpr int kScoreCompute = 256;
+// 16 score warps (four per TMEM lane quarter, each summing 64 of a unit's columns), TMA warp, MMA
+// warp.  The score warps are latency-bound (TMEM loads, exp chains, per-unit barriers), so four per
+// scheduler hide more of it than two did.
+constexpr int kScoreWarps = 16;
+constexpr int kScoreWarpTma = kScoreWarps;
+constexpr int kScoreWarpMma = kScoreWarps + 1;
+constexpr int kScoreThreadsTc = 32 * (kScoreWarps + 2);
+constexpr int kScoreCompute = 32 * kScoreWarps;
+constexpr int kScoreCols = kScoreWarps / 4 > 0 ? 256 / (kScoreWarps / 4) : 256;  // columns per score warp
 constexpr int kMaxCols = 256;  // columns of S^T per MMA group (window rows x heads)
 
 template <int D>
@@ -134,7 +139,7 @@ enum ScoreBar {
 // columns, K = D).  The window Q is loaded once per (segment, g, group); K
 // tiles and S buffers are double-buffered so the next MMA runs while the
 // score warps sum exp(s - lse) of the current one (warp w: lane quarter w % 4,
-// column half w / 4).
+// column group w / 4 of kScoreCols columns).
 template <int D>
 __global__ void __launch_bounds__(kScoreThreadsTc, 1) imp_score_tc_kernel(const __grid_constant__ ScoreArgs a) {
   using L = ScoreSmem<D>;
@@ -145,7 +150,7 @@ __global__ void __launch_bounds__(kScoreThreadsTc, 1) imp_score_tc_kernel(const 
   __shared__ int s_abort;
   __shared__ int s_tmem_busy;  // 1: tensor-core work could not be confirmed finished, TMEM is kept
   __shared__ __align__(16) float s_lse[kMaxCols];
-  __shared__ float s_key[128];
+  __shared__ float s_key[kScoreWarps / 4 - 1][128];
   __shared__ float s_red[4];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
@@ -318,13 +323,13 @@ __global__ void __launch_bounds__(kScoreThreadsTc, 1) imp_score_tc_kernel(const 
       const int32_t hn = min(hpg, group - it.gi * hpg), ncols = hn * B;
       if (!same_q(it, prev)) {
         // row normalisers of this window (log2 domain); window slots past the segment are masked
-        asm volatile("bar.sync 1, 256;" ::: "memory");
+        asm volatile("bar.sync 1, %0;" ::"n"(kScoreCompute) : "memory");
         if (tid < ncols) {
           const int32_t hh = tid / B, t = tid & (B - 1);
           const int32_t h = it.g * group + it.gi * hpg + hh;
           s_lse[tid] = t < W ? a.lse[(int64_t)h * a.N + c0 + wrow0 + t] * kLog2e : INFINITY;
         }
-        asm volatile("bar.sync 1, 256;" ::: "memory");
+        asm volatile("bar.sync 1, %0;" ::"n"(kScoreCompute) : "memory");
         prev = it;
       }
       const int slot = (int)(i & 1);
@@ -336,16 +341,16 @@ __global__ void __launch_bounds__(kScoreThreadsTc, 1) imp_score_tc_kernel(const 
       const bool open_chunk = it.c * 128 + 127 < n && it.c * 128 + 127 <= wrow0;
       if (live) {
         tc_fence_after();
-        // this warp's columns: [128 ch, 128 ch + 128) of the group's hn * B (a multiple of 16)
-        for (int32_t col0 = 128 * ch; col0 < min(128 * ch + 128, ncols); col0 += 64) {
-          float sv[64];
+        // this warp's columns: [kScoreCols ch, kScoreCols (ch + 1)) of the group's hn * B (a multiple of 16)
+        // (32 columns per TMEM load keeps the score warps within 96 registers)
+        for (int32_t col0 = kScoreCols * ch; col0 < min(kScoreCols * (ch + 1), ncols); col0 += 32) {
+          float sv[32];
           tmem_ld32(tl + slot * kMaxCols + col0, sv);
-          tmem_ld32(tl + slot * kMaxCols + col0 + 32, sv + 32);
           tmem_wait_ld();
-          if (open_chunk && col0 + 64 <= ncols) {
+          if (open_chunk && col0 + 32 <= ncols) {
             // no masks: packed (s * c - lse) pairs, four normalisers per shared-memory load
 #pragma unroll
-            for (int x = 0; x < 64; x += 4) {
+            for (int x = 0; x < 32; x += 4) {
               const float4 l4 = *reinterpret_cast<const float4 *>(&s_lse[col0 + x]);
               float y0, y1, y2, y3;
               ffma2(y0, y1, sv[x], sv[x + 1], a.scale_log2, a.scale_log2, -l4.x, -l4.y);
@@ -356,7 +361,7 @@ __global__ void __launch_bounds__(kScoreThreadsTc, 1) imp_score_tc_kernel(const 
             continue;
           }
 #pragma unroll
-          for (int x = 0; x < 64; x += 4) {
+          for (int x = 0; x < 32; x += 4) {
             float e[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
@@ -375,14 +380,16 @@ __global__ void __launch_bounds__(kScoreThreadsTc, 1) imp_score_tc_kernel(const 
       }
       mbar_arrive(bar(kSbSEmpty0 + slot));
       if (it.gi != ngroups - 1) continue;  // the unit's mass sums over all head groups
-      // unit done: key masses of both column halves, then per-block sums over the chunk's keys
+      // unit done: key masses of the column groups (summed in group order), then per-block sums over
+      // the chunk's keys
       float v = (acc0 + acc1) + (acc2 + acc3);
       acc0 = acc1 = acc2 = acc3 = 0.f;
-      asm volatile("bar.sync 1, 256;" ::: "memory");
-      if (ch == 1) s_key[key] = v;
-      asm volatile("bar.sync 1, 256;" ::: "memory");
+      asm volatile("bar.sync 1, %0;" ::"n"(kScoreCompute) : "memory");
+      if (ch > 0) s_key[ch - 1][key] = v;
+      asm volatile("bar.sync 1, %0;" ::"n"(kScoreCompute) : "memory");
       if (ch == 0) {
-        v += s_key[key];
+#pragma unroll
+        for (int g2 = 0; g2 < kScoreWarps / 4 - 1; ++g2) v += s_key[g2][key];
         const int32_t nb_seg = it.nbs;
         const int64_t pbase = (int64_t)it.bk0 + it.c * bpc;
         if (B <= 32) {
