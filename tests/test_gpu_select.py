@@ -469,6 +469,15 @@ def test_fused_single_segment_matches_the_separate_calls(L, B_, p, d_model, flag
     _check_selection(wl, bufs, flags)
 
 
+def test_fused_single_unscored_segment_keeps_everything():
+    """One segment that is not scored: the fused call scores nothing and keeps every token and row."""
+    wl = W.packed([333], 4, 2, 64, seed=91, block_size=64, top_p=0.5, d_model=64)
+    wl.seg_mask = np.array([0], np.uint8)
+    bufs = _fused_vs_separate(wl)
+    _check_selection(wl, bufs)
+    assert int(bufs.n_kept.item()) == 333
+
+
 def test_fused_path_with_unscored_and_empty_segments():
     wl = W.packed([0, 300, 1, 0, 700, 64, 17], 8, 2, 128, seed=61, block_size=32, top_p=0.8, d_model=512)
     wl.seg_mask = np.array([1, 1, 0, 1, 0, 1, 1], np.uint8)
