@@ -394,7 +394,7 @@ def select_copy_split(sel_ms, split, n_kept: int, d_model: int, hbm: float):
                    "[importance]; [unip_gather_tokens] minus [flush]"}
 
 
-def incremental_select_ms(di, bufs, flush, stream, reps: int = 10, trials: int = 5):
+def incremental_select_ms(di, bufs, flush, stream, reps: int = 10, trials: int = 9):
     """Device time of importance alone and the incremental time of Top-p + compaction in the step:
     CUDA-graph replays of [L2 flush, importance + selection + compaction (the fused call)] minus
     [L2 flush, importance], per step.  Returns (importance_ms, select_gather_ms, split): split is None
